@@ -1,0 +1,453 @@
+"""CPU oracle for ragged MLA prefill over a paged latent KV cache.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path (the CUDA library and its
+Python binding) imports or calls this module; only the tests, the smoke check
+and the benchmark's CPU baseline do.  It shares no code with the CUDA path.
+
+Everything is plain numpy in float64, written to be checked against the pages
+by eye, with a library matmul as the only borrowed step.  The pages are three
+API references from the Modular MAX kernel library:
+
+  * "mla_prefill_plan" -- the chunk plan (Args: buffer_row_offsets,
+    cache_offsets, buffer_lengths, input_row_offsets, buffer_token_size);
+  * "mla_prefill_decode_graph_bf16" -- the whole BF16 MLA layer (Args: q,
+    w_k, w_uk, w_uv, scale, buffer_row_offsets, cache_offsets, buffer_length;
+    Parameters: kv_input_fn, mask_str);
+  * "flare_mla_prefill_dispatch" -- prefill attention (Parameters: q_depth,
+    cache_depth, kv_num_heads, dtype, output_type; Args: k, v, k_rope,
+    valid_length, scale, cache_offsets).
+
+Readings taken where the pages are silent (each one is listed with its reason
+in the design notes of the repository):
+  * the plan packs all sequences' context tokens (cached first, then new, in
+    batch order) into consecutive chunks of ``buffer_token_size`` rows;
+  * a cache row is 512 latent values followed by the 64 k_rope values, and a
+    query row is 128 nope values followed by 64 rope values;
+  * the causal mask lets the new token ``i`` of sequence ``b`` (absolute
+    position ``cache_len_b + i``) see context positions ``j <= cache_len_b + i``;
+  * LSE is the natural log of the sum of exp of the scaled scores;
+  * K and V leave the up-projection in the storage dtype of the attention
+    operands (bf16 for the BF16 graph, e4m3 for the fp8 path), rounded to
+    nearest even, in the descale domain of the cache.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+R = 512        # kv_lora_rank: latent width
+DN = 128       # qk_nope_head_dim
+DR = 64        # qk_rope_head_dim
+DV = 128       # v_head_dim
+DQ = DN + DR   # q_depth, 192
+DC = R + DR    # cache_depth, 576
+
+# Device status codes shared by the plan and gather definitions.
+STATUS_OK = 0
+STATUS_TOO_MANY_CHUNKS = 1
+STATUS_BAD_OFFSETS = 2
+STATUS_BAD_PAGE = 3
+
+
+# --------------------------------------------------------------------------
+# Number formats (storage types named by flare_mla_prefill_dispatch, "dtype":
+# bfloat16 or float8_e4m3fn).  Decoders and encoders are written from the
+# format definitions, not taken from a library.
+# --------------------------------------------------------------------------
+
+def bf16_decode(bits: np.ndarray) -> np.ndarray:
+    """bfloat16 bit patterns (uint16) -> float64.  bf16 is the top half of an
+    IEEE binary32, so widening the bits by 16 zero bits gives the exact value."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def round_to_bf16(x: np.ndarray) -> np.ndarray:
+    """Round float64 values to the nearest bfloat16 value (ties to even) and
+    return them as float64.  bf16 keeps 8 significant bits; below the smallest
+    normal (2**-126) the quantum is fixed at 2**-133."""
+    x = np.asarray(x, dtype=np.float64)
+    _, e = np.frexp(x)                       # x = m * 2**e with 0.5 <= |m| < 1
+    e = np.maximum(e - 1, -126)              # exponent of the leading bit
+    quantum = np.ldexp(1.0, e - 7)
+    return np.rint(x / quantum) * quantum    # np.rint rounds half to even
+
+
+def bf16_encode(x: np.ndarray) -> np.ndarray:
+    """float64 -> bfloat16 bit patterns (uint16), round to nearest even."""
+    r = round_to_bf16(x).astype(np.float32)  # exact: r has 8 significant bits
+    return (r.view(np.uint32) >> 16).astype(np.uint16)
+
+
+# OCP 8-bit floating point, E4M3: 1 sign, 4 exponent (bias 7), 3 mantissa bits;
+# no infinities; S.1111.111 is NaN; largest finite value 448 = 1.75 * 2**8;
+# exponent field 0 holds subnormals m/8 * 2**-6.
+E4M3_MAX = 448.0
+
+
+def e4m3_decode(codes: np.ndarray) -> np.ndarray:
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    exp = (c >> 3) & 0xF
+    man = c & 0x7
+    normal = np.ldexp(1.0 + man / 8.0, exp - 7)
+    sub = np.ldexp(man / 8.0, -6)
+    val = np.where(exp == 0, sub, normal)
+    val = np.where((exp == 0xF) & (man == 0x7), np.nan, val)
+    return sign * val
+
+
+def round_to_e4m3(x: np.ndarray) -> np.ndarray:
+    """Round to the nearest E4M3 value, ties to even, saturating to +-448."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(x), E4M3_MAX)
+    _, e = np.frexp(a)
+    e = np.maximum(e - 1, -6)                # subnormal quantum is 2**-9
+    quantum = np.ldexp(1.0, e - 3)           # 4 significant bits
+    r = np.minimum(np.rint(a / quantum) * quantum, E4M3_MAX)
+    return np.copysign(r, x)
+
+
+def e4m3_encode(x: np.ndarray) -> np.ndarray:
+    """float64 -> E4M3 codes (uint8), round to nearest even, saturating."""
+    r = round_to_e4m3(x)
+    a = np.abs(r)
+    _, e = np.frexp(a)
+    e = e - 1
+    is_sub = a < 2.0 ** -6
+    exp_field = np.where(is_sub, 0, e + 7)
+    man = np.where(is_sub, a / 2.0 ** -9, (a / np.ldexp(1.0, e) - 1.0) * 8.0)
+    man = np.where(a == 0, 0, man)
+    exp_field = np.where(a == 0, 0, exp_field)
+    code = (exp_field.astype(np.int64) << 3) | np.rint(man).astype(np.int64)
+    code = code | np.where(np.signbit(r), 0x80, 0)
+    return code.astype(np.uint8)
+
+
+def decode(codes: np.ndarray, dtype: str) -> np.ndarray:
+    return bf16_decode(codes) if dtype == "bf16" else e4m3_decode(codes)
+
+
+def round_to(x: np.ndarray, dtype: str) -> np.ndarray:
+    return round_to_bf16(x) if dtype == "bf16" else round_to_e4m3(x)
+
+
+# --------------------------------------------------------------------------
+# (1) The chunk plan -- "mla_prefill_plan".
+# --------------------------------------------------------------------------
+
+def prefill_plan(input_row_offsets, cache_lengths, buffer_token_size: int, max_chunks: int):
+    """Chunk plan of a ragged batch through a buffer of ``buffer_token_size`` rows.
+
+    Follows the page's description: every sequence has cached tokens and new
+    tokens; the total tokens are divided into chunks of ``buffer_token_size``;
+    for each chunk the plan records, per sequence, where its rows start in the
+    buffer (``buffer_row_offsets [max_chunks, B+1]``) and where they start in
+    the cache (``cache_offsets [max_chunks, B]``), and the chunk's total valid
+    rows (``buffer_lengths [max_chunks]``, -1 for an unused chunk).
+
+    Returns (buffer_row_offsets, cache_offsets, buffer_lengths, status) as
+    int64 arrays and an int status (0 ok, 1 more chunks needed than
+    ``max_chunks``, 2 malformed ``input_row_offsets`` or total beyond int32).
+    """
+    iro = np.asarray(input_row_offsets, dtype=np.int64)
+    cache = np.asarray(cache_lengths, dtype=np.int64)
+    B = cache.shape[0]
+    S = int(buffer_token_size)
+    if S <= 0 or max_chunks < 0 or iro.shape[0] != B + 1:
+        raise ValueError("bad plan arguments")
+    status = STATUS_OK
+    new = iro[1:] - iro[:-1]
+    if B + 1 > 0 and (iro[0] != 0 or np.any(new < 0)):
+        status = STATUS_BAD_OFFSETS
+        new = np.maximum(new, 0)
+    total = cache + new                         # context tokens per sequence
+    # Each sequence's slice of the packed token order.
+    seq_start = np.zeros(B + 1, dtype=np.int64)
+    seq_start[1:] = np.cumsum(total)
+    tot = int(seq_start[B])
+    if tot >= 2 ** 31 and status == STATUS_OK:
+        status = STATUS_BAD_OFFSETS
+    needed = -(-tot // S)
+    if needed > max_chunks and status == STATUS_OK:
+        status = STATUS_TOO_MANY_CHUNKS
+
+    buffer_row_offsets = np.zeros((max_chunks, B + 1), dtype=np.int64)
+    cache_offsets = np.zeros((max_chunks, B), dtype=np.int64)
+    buffer_lengths = np.full(max_chunks, -1, dtype=np.int64)
+    for c in range(max_chunks):
+        win_lo, win_hi = c * S, (c + 1) * S     # this chunk's window of the packed order
+        rows = 0
+        for b in range(B):
+            lo = max(int(seq_start[b]), win_lo)
+            hi = min(int(seq_start[b + 1]), win_hi)
+            buffer_row_offsets[c, b] = rows
+            # Position (within sequence b) of its first token at or after the
+            # window start; L_b once the sequence is done, 0 before it starts.
+            cache_offsets[c, b] = min(max(win_lo - int(seq_start[b]), 0), int(total[b]))
+            rows += max(hi - lo, 0)
+        buffer_row_offsets[c, B] = rows
+        buffer_lengths[c] = rows if win_lo < tot else -1
+    return buffer_row_offsets, cache_offsets, buffer_lengths, status
+
+
+# --------------------------------------------------------------------------
+# (2) Latent gather -- "kv_input_fn" of mla_prefill_decode_graph_bf16 and the
+# k_rope operand of flare_mla_prefill_dispatch.
+# --------------------------------------------------------------------------
+
+def gather_latent(kv_cache_codes, page_table, page_size: int, plan, chunk: int):
+    """Copy chunk ``chunk``'s rows out of the paged cache.
+
+    For each sequence ``b`` and each of its ``n`` rows in the chunk, buffer row
+    ``buffer_row_offsets[chunk, b] + t`` receives the cache token at position
+    ``cache_offsets[chunk, b] + t`` of sequence ``b``, which lives in page
+    ``page_table[b, pos // page_size]`` at slot ``pos % page_size``.  The first
+    512 values go to ``c_kv_buf``, the last 64 to ``k_rope_buf``.  Bit copy:
+    the inputs are storage codes and so are the outputs.
+
+    Returns (c_kv_buf [n, 512], k_rope_buf [n, 64], status).
+    """
+    bro, co, bl, _ = plan
+    kv = np.asarray(kv_cache_codes)
+    pt = np.asarray(page_table, dtype=np.int64)
+    num_pages = kv.shape[0]
+    n = int(bl[chunk])
+    n = max(n, 0)
+    c_kv = np.zeros((n, R), dtype=kv.dtype)
+    k_rope = np.zeros((n, DR), dtype=kv.dtype)
+    status = STATUS_OK
+    B = bro.shape[1] - 1
+    for b in range(B):
+        r0, r1 = int(bro[chunk, b]), int(bro[chunk, b + 1])
+        for t in range(r1 - r0):
+            pos = int(co[chunk, b]) + t
+            slot_page = pos // page_size
+            if slot_page >= pt.shape[1] or pt[b, slot_page] < 0 or pt[b, slot_page] >= num_pages:
+                status = STATUS_BAD_PAGE
+                continue
+            row = kv[pt[b, slot_page], pos % page_size]
+            c_kv[r0 + t] = row[:R]
+            k_rope[r0 + t] = row[R:]
+    return c_kv, k_rope, status
+
+
+def context_latents(kv_cache_codes, page_table, page_size: int, total_lens):
+    """All context tokens of every sequence, in position order, straight from
+    the paged cache (no plan): a list of [L_b, 576] code arrays."""
+    kv = np.asarray(kv_cache_codes)
+    pt = np.asarray(page_table, dtype=np.int64)
+    out = []
+    for b, L in enumerate(total_lens):
+        pos = np.arange(int(L))
+        out.append(kv[pt[b, pos // page_size], pos % page_size])
+    return out
+
+
+# --------------------------------------------------------------------------
+# (3) Up-projection -- mla_prefill_decode_graph_bf16, Args w_k and w_uv.
+# --------------------------------------------------------------------------
+
+def upproject(c_kv, w_k, w_uv, heads=None, store: str | None = None, inv_scale: float = 1.0):
+    """Per-head K_nope and V from the latent.
+
+    ``c_kv`` [rows, 512], ``w_k`` [H*128, 512], ``w_uv`` [H, 128, 512], all
+    float64 real values.  For head h:  K_nope[:, h, :] = c_kv @ W_k,h^T with
+    W_k,h = w_k[h*128:(h+1)*128], and V[:, h, :] = c_kv @ w_uv[h]^T.
+    ``heads`` restricts the heads computed (the output keeps only those, in
+    order).  With ``store`` set, each result is multiplied by ``inv_scale``,
+    rounded to that storage type and multiplied back (the attention operands'
+    dtype and descale).
+    """
+    c = np.asarray(c_kv, dtype=np.float64)
+    H = w_uv.shape[0]
+    hs = range(H) if heads is None else heads
+    k = np.stack([c @ w_k[h * DN:(h + 1) * DN].T for h in hs], axis=1)
+    v = np.stack([c @ w_uv[h].T for h in hs], axis=1)
+    if store is not None:
+        k = round_to(k * inv_scale, store) / inv_scale
+        v = round_to(v * inv_scale, store) / inv_scale
+    return k, v
+
+
+# --------------------------------------------------------------------------
+# (4) Causal attention with q_depth 192 -- flare_mla_prefill_dispatch.
+# --------------------------------------------------------------------------
+
+def softmax_weights(s):
+    """Row softmax of a score matrix where -inf marks a masked entry.  Rows with
+    no visible entry get all-zero weights and LSE -inf."""
+    s = np.asarray(s, dtype=np.float64)
+    m = np.max(s, axis=-1, keepdims=True)
+    m_safe = np.where(np.isfinite(m), m, 0.0)
+    p = np.exp(s - m_safe)
+    l = np.sum(p, axis=-1, keepdims=True)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        w = np.where(l > 0, p / np.where(l > 0, l, 1.0), 0.0)
+        lse = np.where(l[..., 0] > 0, m_safe[..., 0] + np.log(np.where(l[..., 0] > 0, l[..., 0], 1.0)), -np.inf)
+    return w, lse
+
+
+def partial_attention(q_nope, q_rope, k_nope, k_rope, v, q_pos, k_pos, scale):
+    """Attention of query rows over one set of keys, causal by absolute position.
+
+    q_nope [n,128], q_rope [n,64], k_nope [m,128], k_rope [m,64], v [m,128];
+    q_pos [n], k_pos [m] absolute positions.  Score of query i and key j is
+    scale * (q_nope_i . k_nope_j + q_rope_i . k_rope_j), visible iff
+    k_pos[j] <= q_pos[i].  Returns (O [n,128] normalised, LSE [n]); a row with
+    no visible key has O = 0 and LSE = -inf.
+    """
+    s = scale * (q_nope @ k_nope.T + q_rope @ k_rope.T)
+    visible = np.asarray(k_pos)[None, :] <= np.asarray(q_pos)[:, None]
+    s = np.where(visible, s, -np.inf)
+    w, lse = softmax_weights(s)
+    return w @ v, lse
+
+
+def merge_partials(o_a, lse_a, o_b, lse_b):
+    """Combine two attention results over disjoint key sets: with
+    LSE = log(e^LSE_a + e^LSE_b), O = e^(LSE_a-LSE) O_a + e^(LSE_b-LSE) O_b."""
+    m = np.maximum(lse_a, lse_b)
+    m_safe = np.where(np.isfinite(m), m, 0.0)
+    ea = np.exp(lse_a - m_safe)
+    eb = np.exp(lse_b - m_safe)
+    tot = ea + eb
+    with np.errstate(divide="ignore", invalid="ignore"):
+        lse = np.where(tot > 0, m_safe + np.log(np.where(tot > 0, tot, 1.0)), -np.inf)
+        wa = np.where(tot > 0, ea / np.where(tot > 0, tot, 1.0), 0.0)
+        wb = np.where(tot > 0, eb / np.where(tot > 0, tot, 1.0), 0.0)
+    return wa[..., None] * o_a + wb[..., None] * o_b, lse
+
+
+def attention_reference(q, k_nope_ctx, k_rope_ctx, v_ctx, new_lens, cache_lens, scale,
+                        heads=None, rows=None):
+    """The definition, unchunked: for new token i of sequence b and head h,
+    softmax over every context position j <= cache_len_b + i of
+    scale * (q_nope . K_nope_h[j] + q_rope . k_rope[j]), applied to V_h.
+
+    q [T_q, H, 192] float64 (real values); per sequence b: k_nope_ctx[b]
+    [L_b, Hs, 128], k_rope_ctx[b] [L_b, 64], v_ctx[b] [L_b, Hs, 128] where Hs
+    indexes ``heads`` (all heads when None).  ``rows`` optionally lists, per
+    sequence, the new-token indices to evaluate.  Returns dicts keyed by
+    (b, head) with (token_indices, O [n,128], LSE [n]).
+    """
+    H = q.shape[1]
+    hs = list(range(H)) if heads is None else list(heads)
+    iro = np.concatenate([[0], np.cumsum(new_lens)]).astype(np.int64)
+    res = {}
+    for b in range(len(new_lens)):
+        n = int(new_lens[b])
+        idx = np.arange(n) if rows is None else np.asarray(rows[b], dtype=np.int64)
+        if idx.size == 0:
+            continue
+        L = int(cache_lens[b]) + n
+        q_pos = int(cache_lens[b]) + idx
+        k_pos = np.arange(L)
+        for hi, h in enumerate(hs):
+            qb = q[iro[b] + idx, h]
+            o, lse = partial_attention(qb[:, :DN], qb[:, DN:], k_nope_ctx[b][:, hi],
+                                       k_rope_ctx[b], v_ctx[b][:, hi], q_pos, k_pos, scale)
+            res[(b, h)] = (iro[b] + idx, o, lse)
+    return res
+
+
+def attention_absorbed(q, c_kv_ctx, k_rope_ctx, w_uk, w_uv, new_lens, cache_lens, scale,
+                       heads=None):
+    """Absorbed form (mla_prefill_decode_graph_bf16, Args w_uk and w_uv): the
+    nope query is projected into latent space by w_uk[h] [512,128], scored
+    against the latent c_kv directly, the softmax-weighted latent is projected
+    back by w_uv[h] [128,512].  Same result as up-projecting K and V first when
+    w_uk[h] = W_k,h^T."""
+    H = q.shape[1]
+    hs = list(range(H)) if heads is None else list(heads)
+    iro = np.concatenate([[0], np.cumsum(new_lens)]).astype(np.int64)
+    res = {}
+    for b in range(len(new_lens)):
+        n = int(new_lens[b])
+        if n == 0:
+            continue
+        L = int(cache_lens[b]) + n
+        q_pos = int(cache_lens[b]) + np.arange(n)
+        visible = np.arange(L)[None, :] <= q_pos[:, None]
+        for h in hs:
+            qb = q[iro[b]:iro[b + 1], h]
+            q_lat = qb[:, :DN] @ w_uk[h].T               # [n, 512]
+            s = scale * (q_lat @ c_kv_ctx[b].T + qb[:, DN:] @ k_rope_ctx[b].T)
+            w, lse = softmax_weights(np.where(visible, s, -np.inf))
+            o_lat = w @ c_kv_ctx[b]                      # [n, 512]
+            res[(b, h)] = (np.arange(iro[b], iro[b + 1]), o_lat @ w_uv[h].T, lse)
+    return res
+
+
+# --------------------------------------------------------------------------
+# The whole path, chunk by chunk, as the graph runs it.
+# --------------------------------------------------------------------------
+
+def mla_prefill(q_codes, kv_cache_codes, page_table, page_size, w_k_codes, w_uv_codes,
+                input_row_offsets, cache_lengths, buffer_token_size, max_chunks, scale,
+                dtype="bf16", q_scale=1.0, ckv_scale=1.0, w_scale=1.0,
+                heads=None, rows=None):
+    """Plan, then per chunk: gather, up-project, attend to the chunk's keys and
+    merge into the running (O, LSE) of every query row; finally O per row.
+
+    Inputs are storage codes (uint16 bf16 bits or uint8 e4m3 codes) plus
+    per-tensor descales (real = stored * scale).  K and V are held in the
+    storage dtype between the projection and the attention, in the cache's
+    descale domain.  ``heads``/``rows`` restrict the output to a sample.
+
+    Returns (out dict keyed by (b,h) -> (tokens, O [n,128], LSE [n]), plan).
+    """
+    plan = prefill_plan(input_row_offsets, cache_lengths, buffer_token_size, max_chunks)
+    bro, co, bl, status = plan
+    iro = np.asarray(input_row_offsets, dtype=np.int64)
+    cache = np.asarray(cache_lengths, dtype=np.int64)
+    new = iro[1:] - iro[:-1]
+    B = cache.shape[0]
+    q = decode(q_codes, dtype) * q_scale
+    H = q.shape[1]
+    hs = list(range(H)) if heads is None else list(heads)
+    w_k = decode(w_k_codes, dtype) * w_scale
+    w_uv = decode(w_uv_codes, dtype) * w_scale
+    sel = [np.arange(int(new[b])) if rows is None else np.asarray(rows[b], np.int64)
+           for b in range(B)]
+    acc = {}
+    for b in range(B):
+        for h in hs:
+            n = sel[b].size
+            acc[(b, h)] = (iro[b] + sel[b], np.zeros((n, DV)), np.full(n, -np.inf))
+    for c in range(max_chunks):
+        if bl[c] < 0:
+            continue
+        c_kv_codes, k_rope_codes, _ = gather_latent(kv_cache_codes, page_table, page_size, plan, c)
+        c_kv = decode(c_kv_codes, dtype) * ckv_scale
+        k_rope = decode(k_rope_codes, dtype) * ckv_scale
+        k_nope, v = upproject(c_kv, w_k, w_uv, heads=hs, store=dtype, inv_scale=1.0 / ckv_scale)
+        for b in range(B):
+            r0, r1 = int(bro[c, b]), int(bro[c, b + 1])
+            if r1 == r0 or sel[b].size == 0:
+                continue
+            k_pos = int(co[c, b]) + np.arange(r1 - r0)
+            q_pos = int(cache[b]) + sel[b]
+            for hi, h in enumerate(hs):
+                qb = q[iro[b] + sel[b], h]
+                o_c, lse_c = partial_attention(qb[:, :DN], qb[:, DN:], k_nope[r0:r1, hi],
+                                               k_rope[r0:r1], v[r0:r1, hi], q_pos, k_pos, scale)
+                tok, o_acc, lse_acc = acc[(b, h)]
+                o_new, lse_new = merge_partials(o_acc, lse_acc, o_c, lse_c)
+                acc[(b, h)] = (tok, o_new, lse_new)
+    return acc, plan
+
+
+def causal_pairs(new_lens, cache_lens) -> int:
+    """Number of visible (query, key) pairs: sum over b, i of cache_len_b + i + 1."""
+    tot = 0
+    for n, c in zip(new_lens, cache_lens):
+        n, c = int(n), int(c)
+        tot += n * c + n * (n + 1) // 2
+    return tot
+
+
+def attention_flops(new_lens, cache_lens, H) -> int:
+    """Causal-effective attention flops: 2*H*(128+64+128) per visible pair."""
+    return 2 * H * (DN + DR + DV) * causal_pairs(new_lens, cache_lens)

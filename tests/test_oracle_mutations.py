@@ -1,0 +1,105 @@
+"""Planted mistakes in the oracle (CPU only): each plausible slip -- an
+off-by-one mask, a dropped rope term, a wrong weight slice, a shifted cache
+offset, swapped merge weights -- must make at least one pin fail."""
+import os
+
+import numpy as np
+import pytest
+
+from oracle import mla_oracle as M
+import test_oracle_pins as P
+
+
+def _plant(monkeypatch, name, fn):
+    """Replace an oracle function in the module and in the package namespace."""
+    monkeypatch.setattr(M, name, fn)
+    if hasattr(P.O, name):
+        monkeypatch.setattr(P.O, name, fn)
+
+
+def _must_fail(*pins):
+    failed = 0
+    for pin in pins:
+        try:
+            pin()
+        except AssertionError:
+            failed += 1
+    assert failed > 0, "a planted mistake went unnoticed"
+
+
+def test_strict_causal_mask_is_caught(monkeypatch):
+    orig = M.partial_attention
+
+    def strict(q_nope, q_rope, k_nope, k_rope, v, q_pos, k_pos, scale):
+        return orig(q_nope, q_rope, k_nope, k_rope, v, np.asarray(q_pos) - 1, k_pos, scale)
+    _plant(monkeypatch, "partial_attention", strict)
+    _must_fail(P.test_attention_bruteforce_tiny, P.test_attention_closed_forms)
+
+
+def test_dropped_rope_term_is_caught(monkeypatch):
+    orig = M.partial_attention
+
+    def no_rope(q_nope, q_rope, k_nope, k_rope, v, q_pos, k_pos, scale):
+        return orig(q_nope, 0 * q_rope, k_nope, k_rope, v, q_pos, k_pos, scale)
+    _plant(monkeypatch, "partial_attention", no_rope)
+    _must_fail(P.test_attention_bruteforce_tiny)
+
+
+def test_wrong_weight_slice_is_caught(monkeypatch):
+    def bad(c_kv, w_k, w_uv, heads=None, store=None, inv_scale=1.0):
+        c = np.asarray(c_kv, dtype=np.float64)
+        H = w_uv.shape[0]
+        hs = range(H) if heads is None else heads
+        k = np.stack([c @ w_k[h::H][:M.DN].T for h in hs], axis=1)     # strided, not blocked
+        v = np.stack([c @ w_uv[h].T for h in hs], axis=1)
+        return k, v
+    _plant(monkeypatch, "upproject", bad)
+    _must_fail(P.test_upproject_bruteforce)
+
+
+def test_transposed_value_weight_is_caught(monkeypatch):
+    def bad(c_kv, w_k, w_uv, heads=None, store=None, inv_scale=1.0):
+        c = np.asarray(c_kv, dtype=np.float64)
+        H = w_uv.shape[0]
+        hs = range(H) if heads is None else heads
+        k = np.stack([c @ w_k[h * M.DN:(h + 1) * M.DN].T for h in hs], axis=1)
+        flat = w_uv.reshape(H * M.DV, M.R)
+        v = np.stack([c @ flat[h::H].T for h in hs], axis=1)           # heads interleaved
+        return k, v
+    _plant(monkeypatch, "upproject", bad)
+    _must_fail(P.test_upproject_bruteforce)
+
+
+def test_shifted_cache_offset_is_caught(monkeypatch):
+    orig = M.prefill_plan
+
+    def shifted(*a, **k):
+        bro, co, bl, st = orig(*a, **k)
+        co = co.copy()
+        co[1:] = np.maximum(co[1:] - 1, 0)
+        return bro, co, bl, st
+    _plant(monkeypatch, "prefill_plan", shifted)
+    golden = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+    _must_fail(lambda: P.test_plan_hand_worked_tiny_ragged(golden),
+               P.test_plan_matches_token_walk_random)
+
+
+def test_swapped_merge_weights_are_caught(monkeypatch):
+    orig = M.merge_partials
+
+    def swapped(o_a, lse_a, o_b, lse_b):
+        o, lse = orig(o_a, lse_a, o_b, lse_b)
+        o2, _ = orig(o_b, lse_a, o_a, lse_b)
+        return o2, lse
+    _plant(monkeypatch, "merge_partials", swapped)
+    _must_fail(P.test_merge_split_equals_one_shot,
+               lambda: P.test_chunked_pipeline_equals_unchunked(32))
+
+
+def test_unscaled_scores_are_caught(monkeypatch):
+    orig = M.partial_attention
+
+    def unscaled(q_nope, q_rope, k_nope, k_rope, v, q_pos, k_pos, scale):
+        return orig(q_nope, q_rope, k_nope, k_rope, v, q_pos, k_pos, 1.0)
+    _plant(monkeypatch, "partial_attention", unscaled)
+    _must_fail(P.test_attention_bruteforce_tiny, P.test_attention_closed_forms)
