@@ -1,0 +1,412 @@
+#!/usr/bin/env python3
+"""Benchmark of ragged MLA prefill over a paged latent KV cache on GB300.
+
+One step = one pass of the whole path over one batch: the chunk plan, then
+per chunk the paged gather, the K/V up-projection and the causal attention
+with LSE merge.  The default workload is the DeepSeek-V3-shaped prefill
+(B=1, 4096 new tokens, no cache, 128 heads, page size 128) that the
+tensor-peak target is quoted on.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...     (the CPU oracle, timed on host cores)
+
+Prints one JSON line.  `value` is causal-effective TFLOP/s of the whole step
+(attention flops counted once per visible query-key pair, 640*H per pair,
+plus the up-projection's 2*rows*512*2*H*128), with inputs resident on the
+device; `e2e` is the same metric through the fused C entry point with
+pinned-host inputs copied in and the output copied back inside the timed
+region.  `roofline` describes the attention kernel.  Under torchrun (N>1)
+every rank runs its own full replica (no collective) and rank 0 reports.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+# ncu traffic per attention launch for the default workload, from the committed
+# profile summary (None until a capture of the current kernel exists).
+ATTN_DRAM_BYTES_PER_LAUNCH = {}
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="v3_prefill")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    return ap.parse_args()
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def _flops(w, new, cache):
+    from workloads import KV_LORA_RANK
+    pairs = sum(int(n) * int(c) + int(n) * (int(n) + 1) // 2 for n, c in zip(new, cache))
+    attn = 2 * w.H * (128 + 64 + 128) * pairs
+    ctx = int(sum(int(n) + int(c) for n, c in zip(new, cache)))
+    up = 2 * ctx * KV_LORA_RANK * 2 * w.H * 128
+    return attn, up, pairs
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.dev = device_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.dev), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), float(parts[2]), parts[3:]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        busy = [r for r in rows if r[2] > 200.0] or rows
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in busy:
+            for n, v in zip(names, r[3][1:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[0] for r in busy), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(busy),
+                "power_w_max": max(r[2] for r in rows)}
+
+
+def _oracle_run(w, inp, codes, heads, rows=None):
+    """One timed oracle run over the given heads (and per-sequence query rows,
+    all when None).  Returns (seconds, flops the oracle computed): the
+    projection of every context row for those heads plus the causal attention
+    of the selected rows."""
+    import numpy as np
+    import oracle as O
+    new, cache = inp["new_lens"], inp["cache_lens"]
+    t = time.perf_counter()
+    O.mla_prefill(codes["q"], codes["kv_cache"], codes["page_table"], inp["page_size"],
+                  codes["w_k"], codes["w_uv"], codes["input_row_offsets"], codes["cache_lengths"],
+                  w.buffer_token_size, w.max_chunks, inp["scale"], dtype=w.dtype,
+                  q_scale=inp["q_scale"], ckv_scale=inp["ckv_scale"], w_scale=inp["w_scale"],
+                  heads=heads, rows=rows)
+    secs = time.perf_counter() - t
+    if rows is None:
+        pairs = sum(int(n) * int(c) + int(n) * (int(n) + 1) // 2 for n, c in zip(new, cache))
+    else:
+        pairs = sum(int(np.sum(int(c) + np.asarray(r) + 1)) for r, c in zip(rows, cache))
+    ctx = int(sum(int(n) + int(c) for n, c in zip(new, cache)))
+    flops = len(heads) * (2 * 320 * pairs + 2 * ctx * 512 * 256)
+    return secs, flops
+
+
+def _codes(inp):
+    import oracle as O
+    return {k: O.codes(inp[k]) for k in ("q", "kv_cache", "page_table", "w_k", "w_uv",
+                                         "input_row_offsets", "cache_lengths")}
+
+
+def _oracle_sample(w, inp, budget_s=15.0):
+    """The oracle over whole sequences for as many heads (spread over all H)
+    as fit in about `budget_s` seconds.  Returns (TFLOP/s, seconds, desc)."""
+    codes = _codes(inp)
+    secs, flops, heads = 0.0, 0, []
+    stride = max(1, w.H // 16)
+    for h in range(0, w.H, stride):
+        s, f = _oracle_run(w, inp, codes, [h])
+        secs += s
+        flops += f
+        heads.append(h)
+        if secs >= budget_s:
+            break
+    desc = (f"oracle (numpy float64) on the whole path for all {int(sum(inp['new_lens']))} query "
+            f"rows of {len(heads)} of {w.H} heads (every {stride}th from 0)")
+    return flops / secs / 1e12, secs, desc
+
+
+def _cores():
+    return os.cpu_count() or 1
+
+
+def run_reference(a):
+    import numpy as np
+    rank, world, _ = _dist()
+    if rank != 0:
+        return
+    from workloads import WORKLOADS, make_inputs
+    w = WORKLOADS[a.workload]
+    inp = make_inputs(w)
+    codes = _codes(inp)
+    rng = np.random.default_rng(0)
+
+    def sample(k):
+        h = (k * 37) % w.H
+        rows = [np.sort(rng.choice(int(n), size=min(256, int(n)), replace=False)) if n else
+                np.zeros(0, np.int64) for n in inp["new_lens"]]
+        return [h], rows
+
+    for k in range(a.warmup):
+        _oracle_run(w, inp, codes, *sample(k))
+    secs, flops = 0.0, 0
+    for k in range(a.steps):
+        s, f = _oracle_run(w, inp, codes, *sample(k))
+        secs += s
+        flops += f
+    value = flops / secs / 1e12
+    desc = ("oracle (numpy float64), whole path per step on one head (cycling over the heads) "
+            "for 256 random query rows per sequence; flops counted for exactly that work")
+    line = {
+        "impl": "reference", "metric": "MLA prefill TFLOP/s (causal-effective)", "value": value,
+        "unit": "TFLOP/s", "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": secs / a.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config(w, inp),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _config(w, inp):
+    return {"workload": w.name, "B": inp["B"], "new_tokens": int(sum(inp["new_lens"])),
+            "cache_tokens": int(sum(inp["cache_lens"])), "H": w.H, "q_depth": 192, "v_depth": 128,
+            "kv_lora_rank": 512, "page_size": w.page_size,
+            "buffer_token_size": w.buffer_token_size, "max_chunks": w.max_chunks,
+            "dtype": w.dtype,
+            "l2": "inputs larger than L2 (no flush): q, K/V buffers and weights exceed 129 MB"}
+
+
+def run_ours(a):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = _dist()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import mla_prefill_attention_plan_gb300 as mla
+    from mla_prefill_attention_plan_gb300 import build as B
+    B.build()
+    mla.load()
+    from workloads import WORKLOADS, make_inputs
+    w = WORKLOADS[a.workload]
+    inp = make_inputs(w)
+    H, T, Bsz = w.H, inp["T_q"], inp["B"]
+    S, mc = w.buffer_token_size, w.max_chunks
+    dt = mla.MLA_BF16 if w.dtype == "bf16" else mla.MLA_E4M3
+    elt = torch.bfloat16 if w.dtype == "bf16" else torch.float8_e4m3fn
+    attn_flops, up_flops, pairs = _flops(w, inp["new_lens"], inp["cache_lens"])
+    step_flops = attn_flops + up_flops
+
+    # device-resident inputs
+    d = {k: inp[k].to(dev) for k in ("q", "input_row_offsets", "cache_lengths", "kv_cache",
+                                     "page_table", "w_k", "w_uv")}
+    out = torch.empty(T, H, 128, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(T, H, dtype=torch.float32, device=dev)
+    bro = torch.empty(mc, Bsz + 1, dtype=torch.int32, device=dev)
+    co = torch.empty(mc, Bsz, dtype=torch.int32, device=dev)
+    bl = torch.empty(mc, dtype=torch.int32, device=dev)
+    ckv = torch.empty(S, 512, dtype=elt, device=dev)
+    krope = torch.empty(S, 64, dtype=elt, device=dev)
+    knope = torch.empty(S, H, 128, dtype=elt, device=dev)
+    vbuf = torch.empty(S, H, 128, dtype=elt, device=dev)
+    oacc = torch.empty(T, H, 128, dtype=torch.float32, device=dev) if mc > 1 else None
+    lacc = torch.empty(T, H, dtype=torch.float32, device=dev) if mc > 1 else None
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    kv_descale = inp["ckv_scale"] if w.dtype == "e4m3" else 1.0
+    kv_inv = 1.0 / inp["ckv_scale"] if w.dtype == "e4m3" else 1.0
+    launches_per_step = 1 + 3 * mc + (2 if Bsz > 4096 else 0)
+
+    def step(ev=None):
+        mla.check(mla.mla_prefill_plan(bro, co, bl, d["input_row_offsets"], d["cache_lengths"], Bsz,
+                                       mc, S, status, stream))
+        for ch in range(mc):
+            mla.check(mla.mla_gather_latent(ckv, krope, d["kv_cache"], d["page_table"],
+                                            inp["num_pages"], inp["page_size"], inp["max_pages"],
+                                            bro, co, bl, ch, Bsz, S, dt, status, stream))
+            mla.check(mla.mla_upproject(knope, vbuf, ckv, d["w_k"], d["w_uv"], bl, ch, S, H, dt,
+                                        inp["ckv_scale"], inp["w_scale"], kv_inv, stream))
+            if ev is not None:
+                ev[ch][0].record(stream)
+            mla.check(mla.mla_prefill_attention(out, lse, oacc, lacc, d["q"], knope, vbuf, krope,
+                                                d["input_row_offsets"], d["cache_lengths"], bro, co,
+                                                bl, ch, mc, Bsz, H, inp["max_prompt_len"], T, S,
+                                                inp["scale"], inp["q_scale"], kv_descale,
+                                                kv_descale, dt, status, stream))
+            if ev is not None:
+                ev[ch][1].record(stream)
+
+    for _ in range(max(3, a.warmup)):
+        step()
+    torch.cuda.synchronize()
+    assert status.item() == 0, mla.status_string(int(status.item()))
+
+    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+            for _ in range(mc)] for _ in range(a.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for k in range(a.steps):
+        step(evs[k])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / a.steps
+    attn_ms = sum(evs[k][ch][0].elapsed_time(evs[k][ch][1]) for k in range(a.steps) for ch in range(mc))
+    used_chunks = int((bl >= 0).sum().item())
+    attn_ms_per_launch = attn_ms / (a.steps * max(used_chunks, 1))
+    assert status.item() == 0, mla.status_string(int(status.item()))
+
+    # end to end: pinned host inputs in, result out, through the fused entry point
+    host = {k: inp[k].pin_memory() for k in ("q", "input_row_offsets", "cache_lengths", "kv_cache",
+                                             "page_table")}
+    out_host = torch.empty(T, H, 128, dtype=torch.bfloat16).pin_memory()
+    nbytes = mla.mla_prefill_workspace_bytes(Bsz, H, T, mc, S, dt)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        for k2, t in host.items():
+            d[k2].copy_(t, non_blocking=True)
+        mla.check(mla.mla_prefill(out, None, d["q"], d["input_row_offsets"], d["cache_lengths"],
+                                  d["kv_cache"], d["page_table"], inp["num_pages"], inp["page_size"],
+                                  inp["max_pages"], d["w_k"], d["w_uv"], Bsz, H, T,
+                                  inp["max_prompt_len"], S, mc, inp["scale"], inp["q_scale"],
+                                  inp["ckv_scale"], inp["w_scale"], dt, ws, nbytes, status, stream))
+        out_host.copy_(out, non_blocking=True)
+
+    e2e_steps = a.e2e_steps or max(3, min(a.steps, 50))
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    assert status.item() == 0, mla.status_string(int(status.item()))
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peaks, src = _peaks()
+    peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+    achieved = attn_flops / max(used_chunks, 1) / (attn_ms_per_launch * 1e-3) / 1e12
+    line = {
+        "metric": "MLA prefill TFLOP/s (causal-effective)",
+        "value": step_flops * world / (ms_per_step * 1e-3) / 1e12,
+        "unit": "TFLOP/s",
+        "n_gpus": world, "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic",
+        "config": dict(_config(w, inp), parallelism=f"replicas{world}" if world > 1 else "single"),
+        "attn_tflops": achieved,
+        "attn_ms_per_launch": attn_ms_per_launch,
+        "step_flops": {"attention": attn_flops, "upproject": up_flops, "visible_pairs": pairs},
+        "roofline": {"bound": "tensor", "kernel": "attn_kernel", "achieved": achieved,
+                     "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                     "peak_source": f"{src} bf16 dense, sustained (kernel timed inside a long step loop)",
+                     "traffic": ATTN_DRAM_BYTES_PER_LAUNCH.get(w.name)},
+        "e2e": {"value": step_flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "api": "mla_prefill"},
+        "gpu_launches": launches_per_step * a.steps,
+        "clocks": clk,
+    }
+    if not a.no_cpu_baseline:
+        v, secs, desc = _oracle_sample(w, inp, budget_s=15.0)
+        line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle",
+                                "sample": desc, "seconds": secs}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    a = _args()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_ours(a)
+
+
+if __name__ == "__main__":
+    main()

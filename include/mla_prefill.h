@@ -1,0 +1,236 @@
+/*
+ * mla_prefill.h -- C ABI of a GB300 (sm_103a) library for ragged-batch
+ * Multi-head Latent Attention (MLA) prefill over a paged latent KV cache.
+ *
+ * The path has four stages, each an entry point below, plus a fused entry
+ * point that runs them all:
+ *   1. mla_prefill_plan       -- chunk plan      ("mla_prefill_plan" page)
+ *   2. mla_gather_latent      -- paged gather    ("mla_prefill_decode_graph_bf16",
+ *                                                 Parameters: kv_input_fn)
+ *   3. mla_upproject          -- K/V projection  ("mla_prefill_decode_graph_bf16",
+ *                                                 Args: w_k, w_uv)
+ *   4. mla_prefill_attention  -- causal attention with LSE merge across chunks
+ *                                                ("flare_mla_prefill_dispatch")
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument is a DEVICE pointer owned by the caller, unless
+ *     stated otherwise.  The library allocates no memory.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream) and never synchronises.  A host return of
+ *     MLA_OK means the work was enqueued.
+ *   - Tensors are dense row-major with the leading dimensions written in the
+ *     comments.  Integer tables are uint32/int32 as on the pages.
+ *   - Geometry is fixed by the pages: q_depth 192 = 128 nope + 64 rope,
+ *     cache_depth 576 = 512 latent + 64 rope, v_depth 128, kv_num_heads 1.
+ *   - Element types (`dtype`): MLA_BF16 (bfloat16) or MLA_E4M3
+ *     (float8_e4m3fn).  Attention output is always bfloat16.
+ *   - Problems found on the device (plan overflow, bad offsets, bad page ids,
+ *     a pipeline wait that timed out) are written to the caller's
+ *     `int32_t* d_status` (first error wins; kernels never clear it; the
+ *     fused entry point clears it first).  `d_status` may be NULL.
+ *   - fp8 scales are descales: real value = stored value * scale.
+ */
+#ifndef MLA_PREFILL_H
+#define MLA_PREFILL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t mla_status_t;
+typedef void* mla_stream_t; /* cudaStream_t */
+
+/* Host return codes. */
+enum {
+  MLA_OK = 0,
+  MLA_ERR_ARG = -1,       /* null or misaligned (16 B) pointer, or a bad size */
+  MLA_ERR_GEOMETRY = -2,  /* head count / layout outside what the kernels support */
+  MLA_ERR_DTYPE = -3,     /* dtype not MLA_BF16 or MLA_E4M3 */
+  MLA_ERR_LAUNCH = -4,    /* the CUDA runtime refused a launch or a tensor map */
+  MLA_ERR_WORKSPACE = -5  /* workspace missing or smaller than mla_prefill_workspace_bytes */
+};
+
+/* Device status codes written to *d_status. */
+enum {
+  MLA_DEV_OK = 0,
+  MLA_DEV_TOO_MANY_CHUNKS = 1, /* the plan needs more than max_chunks rows (truncated) */
+  MLA_DEV_BAD_OFFSETS = 2,     /* input_row_offsets[0] != 0, decreasing, or total >= 2^31 */
+  MLA_DEV_BAD_PAGE = 3,        /* a page-table entry is negative or >= num_pages */
+  MLA_DEV_TIMEOUT = 4          /* a pipeline wait exceeded its limit; the kernel drained and exited */
+};
+
+enum { MLA_BF16 = 0, MLA_E4M3 = 1 };
+
+/* Human-readable text for a host or device status code (static storage). */
+const char* mla_status_string(int32_t code);
+
+/* ABI version of this header. */
+int32_t mla_abi_version(void);
+#define MLA_ABI_VERSION 1
+
+/*
+ * 1. Chunk plan.  Follows "mla_prefill_plan" (Args: buffer_row_offsets,
+ * cache_offsets, buffer_lengths, input_row_offsets, k_cache, buffer_token_size).
+ *
+ * Every sequence b has cache_lengths[b] cached tokens and
+ * input_row_offsets[b+1] - input_row_offsets[b] new tokens; its context is
+ * L_b = cached + new tokens, cached first.  All contexts are laid end to end in
+ * batch order and cut into consecutive chunks of buffer_token_size rows.  For
+ * chunk c (0 <= c < max_chunks):
+ *   buffer_row_offsets[c][b]  first buffer row of sequence b (b <= B; [c][B] = rows used)
+ *   cache_offsets[c][b]       first context position of sequence b in the chunk
+ *                             (L_b once b is finished, 0 before it starts)
+ *   buffer_lengths[c]         rows used, or -1 if the chunk is unused.
+ *
+ * buffer_row_offsets: [max_chunks][B+1] uint32, output
+ * cache_offsets:      [max_chunks][B]   uint32, output
+ * buffer_lengths:     [max_chunks]      int32,  output
+ * input_row_offsets:  [B+1] uint32 cumulative new-token offsets, starting at 0
+ * cache_lengths:      [B]   uint32 cached tokens per sequence (the page's k_cache lengths)
+ * Errors: host MLA_ERR_ARG for null pointers, B < 0, max_chunks < 1 or
+ * buffer_token_size == 0.  Device MLA_DEV_TOO_MANY_CHUNKS when more than
+ * max_chunks chunks are needed (the first max_chunks rows are still written),
+ * MLA_DEV_BAD_OFFSETS for malformed offsets (tables then unspecified).
+ */
+mla_status_t mla_prefill_plan(uint32_t* buffer_row_offsets, uint32_t* cache_offsets,
+                              int32_t* buffer_lengths, const uint32_t* input_row_offsets,
+                              const uint32_t* cache_lengths, int32_t batch_size,
+                              int32_t max_chunks, uint32_t buffer_token_size, int32_t* d_status,
+                              mla_stream_t stream);
+
+/*
+ * 2. Latent gather.  Follows "mla_prefill_decode_graph_bf16" (Parameters:
+ * kv_input_fn, the loader of KV latents [tot_seq_len, cache_head_dim]) and the
+ * k_rope operand of "flare_mla_prefill_dispatch" (Parameters: k_rope_t;
+ * Args: cache_offsets).
+ *
+ * For chunk `chunk` of the plan, every sequence b and t < n_cb (its rows in the
+ * chunk): buffer row buffer_row_offsets[chunk][b] + t receives the cache token
+ * at context position p = cache_offsets[chunk][b] + t of sequence b, stored in
+ * page page_table[b][p / page_size] at slot p % page_size.  Elements 0..511 of
+ * the 576-wide cache row go to c_kv_buf, 512..575 to k_rope_buf.  Bit copy.
+ * Buffer rows at and beyond buffer_lengths[chunk] are not written.  A chunk
+ * with buffer_lengths[chunk] == -1 does nothing.
+ *
+ * c_kv_buf:    [buffer_token_size][512] dtype, output
+ * k_rope_buf:  [buffer_token_size][64]  dtype, output
+ * kv_cache:    [num_pages][page_size][576] dtype
+ * page_table:  [B][max_pages_per_seq] int32 physical page ids
+ * buffer_row_offsets, cache_offsets, buffer_lengths: the plan tables (all chunks)
+ * Errors: host MLA_ERR_ARG / MLA_ERR_DTYPE; device MLA_DEV_BAD_PAGE for a page id
+ * outside [0, num_pages) or a position beyond max_pages_per_seq pages (row skipped).
+ */
+mla_status_t mla_gather_latent(void* c_kv_buf, void* k_rope_buf, const void* kv_cache,
+                               const int32_t* page_table, int32_t num_pages, int32_t page_size,
+                               int32_t max_pages_per_seq, const uint32_t* buffer_row_offsets,
+                               const uint32_t* cache_offsets, const int32_t* buffer_lengths,
+                               int32_t chunk, int32_t batch_size, uint32_t buffer_token_size,
+                               int32_t dtype, int32_t* d_status, mla_stream_t stream);
+
+/*
+ * 3. Up-projection.  Follows "mla_prefill_decode_graph_bf16" (Args: w_k
+ * [num_heads * qk_nope_head_dim, kv_latent_dim]; w_uv [num_heads, v_head_dim,
+ * kv_latent_dim]).
+ *
+ * For rows r < n (n = buffer_lengths[chunk], or buffer_token_size when
+ * buffer_lengths is NULL) and head h:
+ *   k_nope[r][h][:] = s * c_kv_buf[r][:] . w_k[h*128 + :][:]^T
+ *   v[r][h][:]      = s * c_kv_buf[r][:] . w_uv[h][:][:]^T
+ * with s = ckv_scale * w_scale * kv_out_inv_scale, fp32 accumulation, rounded
+ * to the storage dtype (nearest even; e4m3 saturates at +-448).  Rows from n
+ * up to the next multiple of 128 (within buffer_token_size) are written as 0.
+ *
+ * k_nope, v:  [buffer_token_size][num_heads][128] dtype, outputs
+ * c_kv_buf:   [buffer_token_size][512] dtype
+ * w_k:        [num_heads*128][512] dtype;  w_uv: [num_heads][128][512] dtype
+ * Errors: host MLA_ERR_ARG / MLA_ERR_DTYPE / MLA_ERR_GEOMETRY (num_heads < 1).
+ */
+mla_status_t mla_upproject(void* k_nope, void* v, const void* c_kv_buf, const void* w_k,
+                           const void* w_uv, const int32_t* buffer_lengths, int32_t chunk,
+                           uint32_t buffer_token_size, int32_t num_heads, int32_t dtype,
+                           float ckv_scale, float w_scale, float kv_out_inv_scale,
+                           mla_stream_t stream);
+
+/*
+ * 4. Prefill attention for one plan chunk.  Follows "flare_mla_prefill_dispatch"
+ * (Args: output [total_q_tokens, num_heads, v_depth]; q [total_q_tokens,
+ * num_heads, q_depth]; k, v (ragged K nope and V); k_rope [cache_len, 1,
+ * q_depth - depth]; valid_length (cumulative row offsets); max_prompt_len;
+ * scale; cache_offsets) with the causal mask of mla_prefill_decode_graph_bf16
+ * (Parameters: mask_str).
+ *
+ * New token i of sequence b sits at context position P = cache_lengths[b] + i.
+ * The chunk's keys of sequence b are buffer rows r in [buffer_row_offsets
+ * [chunk][b], buffer_row_offsets[chunk][b+1]) at positions j = cache_offsets
+ * [chunk][b] + (r - buffer_row_offsets[chunk][b]); key r is visible iff j <= P.
+ * Score = scale * q_scale * k_scale * (q[t][h][0:128] . k_nope[r][h] +
+ * q[t][h][128:192] . k_rope[r]); the chunk's softmax-weighted V (times v_scale)
+ * and log-sum-exp (natural log) are merged with the running fp32 result in
+ * o_acc / lse_acc.  In the chunk that holds position P the merged result is
+ * written to out (bf16) and lse; in earlier chunks it is kept in o_acc/lse_acc.
+ * Rows whose position lies before the chunk are left untouched.
+ *
+ * out:      [total_q_tokens][num_heads][128] bf16, output
+ * lse:      [total_q_tokens][num_heads] fp32 output, or NULL
+ * o_acc:    [total_q_tokens][num_heads][128] fp32 scratch, lse_acc [total_q_tokens]
+ *           [num_heads] fp32 scratch; both may be NULL only when max_chunks == 1.
+ *           They carry state from one chunk's call to the next.
+ * q:        [total_q_tokens][num_heads][192] dtype (128 nope, then 64 rope)
+ * k_nope, v:[buffer_token_size][num_heads][128] dtype; k_rope: [buffer_token_size][64]
+ * Rows of k_nope/k_rope beyond a sequence's keys are read but masked; rows of v
+ * beyond them are never used.
+ * max_prompt_len: largest new-token count of any sequence (sizes the grid).
+ * Errors: host MLA_ERR_ARG / MLA_ERR_DTYPE / MLA_ERR_GEOMETRY; device MLA_DEV_TIMEOUT.
+ */
+mla_status_t mla_prefill_attention(void* out, float* lse, float* o_acc, float* lse_acc,
+                                   const void* q, const void* k_nope, const void* v,
+                                   const void* k_rope, const uint32_t* input_row_offsets,
+                                   const uint32_t* cache_lengths,
+                                   const uint32_t* buffer_row_offsets,
+                                   const uint32_t* cache_offsets, const int32_t* buffer_lengths,
+                                   int32_t chunk, int32_t max_chunks, int32_t batch_size,
+                                   int32_t num_heads, int32_t max_prompt_len,
+                                   int32_t total_q_tokens, uint32_t buffer_token_size,
+                                   float scale, float q_scale, float k_scale, float v_scale,
+                                   int32_t dtype, int32_t* d_status, mla_stream_t stream);
+
+/*
+ * Workspace bytes needed by mla_prefill for these sizes (plan tables, the
+ * chunk's latent, k_rope, K and V buffers, and the fp32 merge state when
+ * max_chunks > 1).
+ */
+size_t mla_prefill_workspace_bytes(int32_t batch_size, int32_t num_heads,
+                                   int32_t total_q_tokens, int32_t max_chunks,
+                                   uint32_t buffer_token_size, int32_t dtype);
+
+/*
+ * Fused path: plan, then for every chunk c < max_chunks gather, up-project and
+ * attend, all enqueued on `stream` with no host synchronisation (chunks the
+ * plan leaves unused exit on the device).  Follows the prefill branch of
+ * "mla_prefill_decode_graph_bf16" with the tables of "mla_prefill_plan".
+ *
+ * out [total_q_tokens][num_heads][128] bf16 output; lse [total_q_tokens]
+ * [num_heads] fp32 output or NULL.  Inputs as in the stage entry points.  For
+ * e4m3, K and V are stored in e4m3 in the cache's descale domain (out scale
+ * 1/ckv_scale), so the attention uses k_scale = v_scale = ckv_scale.
+ * workspace: device memory of at least mla_prefill_workspace_bytes(...) bytes,
+ * 256-byte aligned.  *d_status is cleared first.
+ */
+mla_status_t mla_prefill(void* out, float* lse, const void* q, const uint32_t* input_row_offsets,
+                         const uint32_t* cache_lengths, const void* kv_cache,
+                         const int32_t* page_table, int32_t num_pages, int32_t page_size,
+                         int32_t max_pages_per_seq, const void* w_k, const void* w_uv,
+                         int32_t batch_size, int32_t num_heads, int32_t total_q_tokens,
+                         int32_t max_prompt_len, uint32_t buffer_token_size, int32_t max_chunks,
+                         float scale, float q_scale, float ckv_scale, float w_scale,
+                         int32_t dtype, void* workspace, size_t workspace_bytes,
+                         int32_t* d_status, mla_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_PREFILL_H */

@@ -1,0 +1,305 @@
+// C ABI of the library (declared in include/mla_prefill.h): argument checks,
+// tensor-map encoding, workspace layout and the fused chunk loop.  No entry
+// point allocates memory or synchronises the stream.
+#include <cstring>
+#include <mutex>
+
+#include "kernels.cuh"
+
+namespace mla {
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int elt_bytes(int32_t dtype) { return dtype == MLA_BF16 ? 2 : 1; }
+
+bool dtype_ok(int32_t dtype) { return dtype == MLA_BF16 || dtype == MLA_E4M3; }
+
+mla_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_LAUNCH; }
+
+// Workspace layout of the fused entry point.
+struct Layout {
+  size_t bro, co, bl, ckv, krope, knope, v, oacc, lseacc, total;
+};
+
+Layout layout(int B, int H, int T_q, int max_chunks, uint32_t S, int dtype) {
+  const size_t e = elt_bytes(dtype);
+  Layout L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = round_up(off + bytes, 256);
+    return at;
+  };
+  L.bro = take(sizeof(uint32_t) * size_t(max_chunks) * (B + 1));
+  L.co = take(sizeof(uint32_t) * size_t(max_chunks) * (B > 0 ? B : 1));
+  L.bl = take(sizeof(int32_t) * size_t(max_chunks));
+  L.ckv = take(size_t(S) * 512 * e);
+  L.krope = take(size_t(S) * 64 * e);
+  L.knope = take(size_t(S) * H * 128 * e);
+  L.v = take(size_t(S) * H * 128 * e);
+  const bool merge = max_chunks > 1;
+  L.oacc = take(merge ? size_t(T_q) * H * 128 * sizeof(float) : 0);
+  L.lseacc = take(merge ? size_t(T_q) * H * sizeof(float) : 0);
+  L.total = off;
+  return L;
+}
+
+}  // namespace
+
+bool encode_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, uint64_t inner,
+               uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr || inner == 0 || outer == 0) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_stride_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estride[2] = {1, 1};
+  return fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estride,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static int cache[64] = {0};
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (n <= 0) n = 1;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+const char* mla_status_string(int32_t code) {
+  switch (code) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_ARG: return "bad argument (null or misaligned pointer, or bad size)";
+    case MLA_ERR_GEOMETRY: return "unsupported geometry";
+    case MLA_ERR_DTYPE: return "unsupported dtype (bf16 or e4m3 only)";
+    case MLA_ERR_LAUNCH: return "CUDA launch or tensor-map error";
+    case MLA_ERR_WORKSPACE: return "workspace missing or too small";
+    case MLA_DEV_TOO_MANY_CHUNKS: return "device: plan needs more than max_chunks chunks";
+    case MLA_DEV_BAD_OFFSETS: return "device: malformed input_row_offsets or lengths";
+    case MLA_DEV_BAD_PAGE: return "device: page id out of range";
+    case MLA_DEV_TIMEOUT: return "device: pipeline wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int32_t mla_abi_version(void) { return MLA_ABI_VERSION; }
+
+mla_status_t mla_prefill_plan(uint32_t* buffer_row_offsets, uint32_t* cache_offsets,
+                              int32_t* buffer_lengths, const uint32_t* input_row_offsets,
+                              const uint32_t* cache_lengths, int32_t batch_size,
+                              int32_t max_chunks, uint32_t buffer_token_size, int32_t* d_status,
+                              mla_stream_t stream) {
+  if (!buffer_row_offsets || !buffer_lengths || !input_row_offsets || batch_size < 0 ||
+      max_chunks < 1 || buffer_token_size == 0)
+    return MLA_ERR_ARG;
+  if (batch_size > 0 && (!cache_offsets || !cache_lengths)) return MLA_ERR_ARG;
+  return from_cuda(launch_plan(buffer_row_offsets, cache_offsets, buffer_lengths, input_row_offsets,
+                               cache_lengths, batch_size, max_chunks, buffer_token_size, d_status,
+                               static_cast<cudaStream_t>(stream)));
+}
+
+mla_status_t mla_gather_latent(void* c_kv_buf, void* k_rope_buf, const void* kv_cache,
+                               const int32_t* page_table, int32_t num_pages, int32_t page_size,
+                               int32_t max_pages_per_seq, const uint32_t* buffer_row_offsets,
+                               const uint32_t* cache_offsets, const int32_t* buffer_lengths,
+                               int32_t chunk, int32_t batch_size, uint32_t buffer_token_size,
+                               int32_t dtype, int32_t* d_status, mla_stream_t stream) {
+  if (!dtype_ok(dtype)) return MLA_ERR_DTYPE;
+  if (!c_kv_buf || !k_rope_buf || !kv_cache || !page_table || !buffer_row_offsets ||
+      !cache_offsets || !buffer_lengths || !aligned16(c_kv_buf) || !aligned16(k_rope_buf) ||
+      !aligned16(kv_cache) || num_pages < 1 || page_size < 1 || max_pages_per_seq < 1 ||
+      chunk < 0 || batch_size < 1 || buffer_token_size == 0)
+    return MLA_ERR_ARG;
+  return from_cuda(launch_gather(c_kv_buf, k_rope_buf, kv_cache, page_table, num_pages, page_size,
+                                 max_pages_per_seq, buffer_row_offsets, cache_offsets,
+                                 buffer_lengths, chunk, batch_size, buffer_token_size,
+                                 elt_bytes(dtype), d_status, static_cast<cudaStream_t>(stream)));
+}
+
+mla_status_t mla_upproject(void* k_nope, void* v, const void* c_kv_buf, const void* w_k,
+                           const void* w_uv, const int32_t* buffer_lengths, int32_t chunk,
+                           uint32_t buffer_token_size, int32_t num_heads, int32_t dtype,
+                           float ckv_scale, float w_scale, float kv_out_inv_scale,
+                           mla_stream_t stream) {
+  if (!dtype_ok(dtype)) return MLA_ERR_DTYPE;
+  if (num_heads < 1) return MLA_ERR_GEOMETRY;
+  if (!k_nope || !v || !c_kv_buf || !w_k || !w_uv || !aligned16(k_nope) || !aligned16(v) ||
+      !aligned16(c_kv_buf) || !aligned16(w_k) || !aligned16(w_uv) || chunk < 0 ||
+      buffer_token_size == 0 || buffer_token_size > 0x7FFFFFFFu)
+    return MLA_ERR_ARG;
+  UpprojArgs a;
+  a.k_nope = k_nope;
+  a.v = v;
+  a.c_kv = c_kv_buf;
+  a.w_k = w_k;
+  a.w_uv = w_uv;
+  a.buffer_lengths = buffer_lengths;
+  a.chunk = chunk;
+  a.S = buffer_token_size;
+  a.H = num_heads;
+  a.dtype = dtype;
+  a.out_scale = ckv_scale * w_scale * kv_out_inv_scale;
+  a.status = nullptr;
+  return from_cuda(launch_upproject(a, static_cast<cudaStream_t>(stream)));
+}
+
+static mla_status_t attention_impl(void* out, float* lse, float* o_acc, float* lse_acc,
+                                   const void* q, const void* k_nope, const void* v,
+                                   const void* k_rope, const uint32_t* iro,
+                                   const uint32_t* cache_lengths, const uint32_t* bro,
+                                   const uint32_t* co, const int32_t* bl, int32_t chunk,
+                                   int32_t max_chunks, int32_t B, int32_t H,
+                                   int32_t max_prompt_len, int32_t T_q, uint32_t S, float scale,
+                                   float q_scale, float k_scale, float v_scale, int32_t dtype,
+                                   int32_t* d_status, cudaStream_t stream) {
+  if (!dtype_ok(dtype)) return MLA_ERR_DTYPE;
+  if (H < 1) return MLA_ERR_GEOMETRY;
+  if (!out || !q || !k_nope || !v || !k_rope || !iro || !cache_lengths || !bro || !co || !bl ||
+      !aligned16(out) || !aligned16(q) || !aligned16(k_nope) || !aligned16(v) ||
+      !aligned16(k_rope) || B < 1 || T_q < 0 || max_prompt_len < 0 || chunk < 0 ||
+      chunk >= max_chunks || S == 0 || S > 0x7FFFFFFFu)
+    return MLA_ERR_ARG;
+  if (max_chunks > 1 && (!o_acc || !lse_acc || !aligned16(o_acc))) return MLA_ERR_ARG;
+  if (T_q == 0 || max_prompt_len == 0) return MLA_OK;
+  if (dtype != MLA_BF16) return MLA_ERR_DTYPE;
+  AttnArgs a;
+  a.out = out;
+  a.lse = lse;
+  a.o_acc = o_acc;
+  a.lse_acc = lse_acc;
+  a.q = q;
+  a.k_nope = k_nope;
+  a.v = v;
+  a.k_rope = k_rope;
+  a.iro = iro;
+  a.cache_len = cache_lengths;
+  a.bro = bro;
+  a.co = co;
+  a.bl = bl;
+  a.chunk = chunk;
+  a.max_chunks = max_chunks;
+  a.B = B;
+  a.H = H;
+  a.max_prompt_len = max_prompt_len;
+  a.T_q = T_q;
+  a.S = S;
+  a.scale = scale * q_scale * k_scale;
+  a.v_scale = v_scale;
+  a.dtype = dtype;
+  a.status = d_status;
+  return from_cuda(launch_attention(a, stream));
+}
+
+mla_status_t mla_prefill_attention(void* out, float* lse, float* o_acc, float* lse_acc,
+                                   const void* q, const void* k_nope, const void* v,
+                                   const void* k_rope, const uint32_t* input_row_offsets,
+                                   const uint32_t* cache_lengths,
+                                   const uint32_t* buffer_row_offsets,
+                                   const uint32_t* cache_offsets, const int32_t* buffer_lengths,
+                                   int32_t chunk, int32_t max_chunks, int32_t batch_size,
+                                   int32_t num_heads, int32_t max_prompt_len,
+                                   int32_t total_q_tokens, uint32_t buffer_token_size,
+                                   float scale, float q_scale, float k_scale, float v_scale,
+                                   int32_t dtype, int32_t* d_status, mla_stream_t stream) {
+  return attention_impl(out, lse, o_acc, lse_acc, q, k_nope, v, k_rope, input_row_offsets,
+                        cache_lengths, buffer_row_offsets, cache_offsets, buffer_lengths, chunk,
+                        max_chunks, batch_size, num_heads, max_prompt_len, total_q_tokens,
+                        buffer_token_size, scale, q_scale, k_scale, v_scale, dtype, d_status,
+                        static_cast<cudaStream_t>(stream));
+}
+
+size_t mla_prefill_workspace_bytes(int32_t batch_size, int32_t num_heads, int32_t total_q_tokens,
+                                   int32_t max_chunks, uint32_t buffer_token_size, int32_t dtype) {
+  if (batch_size < 0 || num_heads < 1 || total_q_tokens < 0 || max_chunks < 1 ||
+      buffer_token_size == 0 || !dtype_ok(dtype))
+    return 0;
+  return layout(batch_size, num_heads, total_q_tokens, max_chunks, buffer_token_size, dtype).total;
+}
+
+mla_status_t mla_prefill(void* out, float* lse, const void* q, const uint32_t* input_row_offsets,
+                         const uint32_t* cache_lengths, const void* kv_cache,
+                         const int32_t* page_table, int32_t num_pages, int32_t page_size,
+                         int32_t max_pages_per_seq, const void* w_k, const void* w_uv,
+                         int32_t batch_size, int32_t num_heads, int32_t total_q_tokens,
+                         int32_t max_prompt_len, uint32_t buffer_token_size, int32_t max_chunks,
+                         float scale, float q_scale, float ckv_scale, float w_scale,
+                         int32_t dtype, void* workspace, size_t workspace_bytes,
+                         int32_t* d_status, mla_stream_t stream_) {
+  if (!dtype_ok(dtype)) return MLA_ERR_DTYPE;
+  if (num_heads < 1) return MLA_ERR_GEOMETRY;
+  if (!out || !q || !input_row_offsets || !cache_lengths || !kv_cache || !page_table || !w_k ||
+      !w_uv || batch_size < 1 || total_q_tokens < 0 || max_prompt_len < 0 || max_chunks < 1 ||
+      buffer_token_size == 0 || buffer_token_size > 0x7FFFFFFFu || num_pages < 1 ||
+      page_size < 1 || max_pages_per_seq < 1 || ckv_scale == 0.f)
+    return MLA_ERR_ARG;
+  const Layout L = layout(batch_size, num_heads, total_q_tokens, max_chunks, buffer_token_size, dtype);
+  if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return MLA_ERR_WORKSPACE;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* bro = reinterpret_cast<uint32_t*>(ws + L.bro);
+  uint32_t* co = reinterpret_cast<uint32_t*>(ws + L.co);
+  int32_t* bl = reinterpret_cast<int32_t*>(ws + L.bl);
+  float* oacc = max_chunks > 1 ? reinterpret_cast<float*>(ws + L.oacc) : nullptr;
+  float* lseacc = max_chunks > 1 ? reinterpret_cast<float*>(ws + L.lseacc) : nullptr;
+  if (d_status && cudaMemsetAsync(d_status, 0, sizeof(int32_t), stream) != cudaSuccess)
+    return MLA_ERR_LAUNCH;
+  mla_status_t st = mla_prefill_plan(bro, co, bl, input_row_offsets, cache_lengths, batch_size,
+                                     max_chunks, buffer_token_size, d_status, stream_);
+  if (st != MLA_OK) return st;
+  // fp8: K and V are stored in the cache's descale domain.
+  const float kv_inv = dtype == MLA_E4M3 ? 1.0f / ckv_scale : 1.0f;
+  const float kv_descale = dtype == MLA_E4M3 ? ckv_scale : 1.0f;
+  for (int c = 0; c < max_chunks; ++c) {
+    st = mla_gather_latent(ws + L.ckv, ws + L.krope, kv_cache, page_table, num_pages, page_size,
+                           max_pages_per_seq, bro, co, bl, c, batch_size, buffer_token_size,
+                           dtype, d_status, stream_);
+    if (st != MLA_OK) return st;
+    st = mla_upproject(ws + L.knope, ws + L.v, ws + L.ckv, w_k, w_uv, bl, c, buffer_token_size,
+                       num_heads, dtype, ckv_scale, w_scale, kv_inv, stream_);
+    if (st != MLA_OK) return st;
+    st = attention_impl(out, lse, oacc, lseacc, q, ws + L.knope, ws + L.v, ws + L.krope,
+                        input_row_offsets, cache_lengths, bro, co, bl, c, max_chunks, batch_size,
+                        num_heads, max_prompt_len, total_q_tokens, buffer_token_size, scale,
+                        q_scale, kv_descale, kv_descale, dtype, d_status, stream);
+    if (st != MLA_OK) return st;
+  }
+  return MLA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,506 @@
+// MLA prefill attention for one plan chunk ("flare_mla_prefill_dispatch":
+// q [tokens, H, 192], ragged k (nope) and v [rows, H, 128], k_rope [rows, 64]
+// shared by all heads, valid_length row offsets, scale, cache_offsets), with a
+// causal mask offset by each sequence's cache length and a log-sum-exp merge
+// of per-chunk results.
+//
+// Work item = (sequence b, 128-row query tile, head h).  Persistent CTAs (one
+// per SM) stride over the items, heaviest query tiles first.  Per CTA:
+//   warp 0      TMA producer: Q tile (3 x 16 KB), K tiles (nope 2 x 16 KB +
+//               rope 16 KB) and V tiles (2 x 16 KB), all 128-byte swizzled,
+//               into a 2-stage K ring and a 2-stage V ring.
+//   warp 1      TMEM owner (512 columns) and single-thread MMA issuer:
+//                 S_j = Q K_j^T   (M=128 queries, N=128 keys, K=192: 12 MMAs,
+//                                  A and B K-major in shared memory)
+//                 O  += P_j V_j   (M=128, N=128 dv, K=128 keys: 8 MMAs, A = P
+//                                  read from tensor memory, B = V MN-major)
+//               S is double-buffered (columns 0..255) so S_{j+1} runs while
+//               the softmax works on S_j; O is double-buffered across items
+//               (columns 256..511) so an item's epilogue overlaps the next.
+//   warps 2..5  softmax + epilogue, one thread per query row: tcgen05.ld the
+//               S row, scale (log2 domain), causal/ragged mask, row max, lazy
+//               rescale of O only when the max grows by more than 2^8, exp2,
+//               row sum, bf16 P written back over S in tensor memory; at the
+//               end O / l, then the LSE merge with earlier chunks (fp32
+//               scratch) or the final bf16 store.
+#include "kernels.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int BM = 128, BN = 128;
+constexpr int BLK = 128 * 128;                // one 128-row x 128-byte swizzled block
+constexpr int Q_BYTES = 3 * BLK;              // 192 bf16 columns
+constexpr int K_BYTES = 3 * BLK;              // nope 128 + rope 64
+constexpr int V_BYTES = 2 * BLK;              // 128 dv
+constexpr int NK = 2, NV = 2;
+constexpr int SMEM_Q = 0;
+constexpr int SMEM_K = SMEM_Q + Q_BYTES;
+constexpr int SMEM_V = SMEM_K + NK * K_BYTES;
+constexpr int SMEM_BAR = SMEM_V + NV * V_BYTES;   // 212992
+constexpr int SMEM_TOTAL = SMEM_BAR + 256 + 1024;
+constexpr int NUM_THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TM_S = 0;      // S/P buffers: columns 0..127, 128..255
+constexpr uint32_t TM_O = 256;    // O buffers: columns 256..383, 384..511
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kLn2 = 0.693147180559945309f;
+constexpr float kNegInf = -__builtin_huge_valf();
+
+constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, false, false);
+constexpr uint32_t IDESC_PV = idesc_bf16(BM, 128, false, true);
+
+struct Smem {
+  uint64_t q_full, q_empty;
+  uint64_t k_full[NK], k_empty[NK];
+  uint64_t v_full[NV], v_empty[NV];
+  uint64_t s_full[2], p_full[2];
+  uint64_t o_done, o_free[2];
+  uint64_t drain;
+  uint32_t tmem;
+  int abort;
+};
+static_assert(sizeof(Smem) <= 256, "barrier block");
+
+struct Params {
+  __nv_bfloat16* out;
+  float* lse;
+  float* o_acc;
+  float* lse_acc;
+  const uint32_t* iro;
+  const uint32_t* cache_len;
+  const uint32_t* bro;
+  const uint32_t* co;
+  const int32_t* bl;
+  int chunk, B, H, n_qtiles;
+  float scale_log2;   // softmax scale * descales * log2(e)
+  float v_scale;
+  int32_t* status;
+};
+
+// One work item, as every role sees it.
+struct Item {
+  int b, h;
+  int i0;        // first query row (within the sequence) of the tile
+  int nq;        // valid query rows in the tile
+  int q_row0;    // first query row in q / out
+  int kv_row0;   // first buffer row of the sequence's keys in this chunk
+  int n_cb;      // keys of the sequence in this chunk
+  int co;        // context position of the first of those keys
+  int cb;        // cached tokens of the sequence
+  int n_kv;      // 128-key tiles to visit (0: nothing to do)
+};
+
+__device__ __forceinline__ bool load_item(const Params& p, int idx, Item& it) {
+  it.h = idx % p.H;
+  const int pair = idx / p.H;
+  const int qt = p.n_qtiles - 1 - pair / p.B;   // heaviest query tiles first
+  it.b = pair % p.B;
+  const uint32_t* bro_c = p.bro + static_cast<size_t>(p.chunk) * (p.B + 1);
+  const int r0 = static_cast<int>(bro_c[it.b]);
+  it.n_cb = static_cast<int>(bro_c[it.b + 1]) - r0;
+  const int q0 = static_cast<int>(p.iro[it.b]);
+  const int new_b = static_cast<int>(p.iro[it.b + 1]) - q0;
+  it.i0 = qt * BM;
+  if (it.n_cb <= 0 || it.i0 >= new_b) return false;
+  it.nq = min(BM, new_b - it.i0);
+  it.q_row0 = q0 + it.i0;
+  it.kv_row0 = r0;
+  it.co = static_cast<int>(p.co[static_cast<size_t>(p.chunk) * p.B + it.b]);
+  it.cb = static_cast<int>(p.cache_len[it.b]);
+  // Keys visible to the tile's last row: relative key index <= last.
+  const long long last = static_cast<long long>(it.cb) + it.i0 + it.nq - 1 - it.co;
+  if (last < 0) return false;
+  const long long nkeys = min(static_cast<long long>(it.n_cb), last + 1);
+  it.n_kv = static_cast<int>((nkeys + BN - 1) / BN);
+  return true;
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    attn_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap kn_map,
+                const __grid_constant__ CUtensorMap kr_map, const __grid_constant__ CUtensorMap v_map,
+                const Params p, int total_items) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Smem* sh = reinterpret_cast<Smem*>(smem + SMEM_BAR);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (p.bl[p.chunk] <= 0) return;
+  if (p.status && *reinterpret_cast<volatile int32_t*>(p.status) == MLA_DEV_TIMEOUT) return;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&sh->q_full), 1);
+    mbar_init(smem_u32(&sh->q_empty), 1);
+    for (int i = 0; i < NK; ++i) {
+      mbar_init(smem_u32(&sh->k_full[i]), 1);
+      mbar_init(smem_u32(&sh->k_empty[i]), 1);
+    }
+    for (int i = 0; i < NV; ++i) {
+      mbar_init(smem_u32(&sh->v_full[i]), 1);
+      mbar_init(smem_u32(&sh->v_empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&sh->s_full[i]), 1);
+      mbar_init(smem_u32(&sh->p_full[i]), 4);
+      mbar_init(smem_u32(&sh->o_free[i]), 4);
+    }
+    mbar_init(smem_u32(&sh->o_done), 1);
+    mbar_init(smem_u32(&sh->drain), 1);
+    sh->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sh->tmem), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh->tmem;
+  volatile int* abort_flag = &sh->abort;
+  int32_t* status = p.status;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&q_map);
+      prefetch_tmap(&kn_map);
+      prefetch_tmap(&kr_map);
+      prefetch_tmap(&v_map);
+      uint32_t g = 0, it_n = 0;
+      int q_last = -1, k_last[NK] = {-1, -1}, v_last[NV] = {-1, -1};
+      bool ok = true;
+      for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
+        Item it;
+        if (!load_item(p, idx, it)) continue;
+        if (it_n > 0 && !(ok = mbar_wait(smem_u32(&sh->q_empty), (it_n - 1) & 1, status, abort_flag))) break;
+        const uint32_t qf = smem_u32(&sh->q_full);
+        mbar_expect_tx(qf, Q_BYTES);
+        for (int blk = 0; blk < 3; ++blk)
+          tma_load_2d(smem_u32(smem + SMEM_Q + blk * BLK), &q_map, qf, it.h * 192 + blk * 64, it.q_row0);
+        q_last = int(it_n & 1);
+        for (int j = 0; j < it.n_kv; ++j) {
+          const uint32_t gj = g + j;
+          const int row = it.kv_row0 + j * BN;
+          const int ks = gj % NK;
+          if (!(ok = mbar_wait(smem_u32(&sh->k_empty[ks]), ((gj / NK) & 1) ^ 1, status, abort_flag))) break;
+          const uint32_t kf = smem_u32(&sh->k_full[ks]);
+          mbar_expect_tx(kf, K_BYTES);
+          const uint32_t kdst = smem_u32(smem + SMEM_K + ks * K_BYTES);
+          tma_load_2d(kdst, &kn_map, kf, it.h * 128, row);
+          tma_load_2d(kdst + BLK, &kn_map, kf, it.h * 128 + 64, row);
+          tma_load_2d(kdst + 2 * BLK, &kr_map, kf, 0, row);
+          k_last[ks] = int((gj / NK) & 1);
+          const int vs = gj % NV;
+          if (!(ok = mbar_wait(smem_u32(&sh->v_empty[vs]), ((gj / NV) & 1) ^ 1, status, abort_flag))) break;
+          const uint32_t vf = smem_u32(&sh->v_full[vs]);
+          mbar_expect_tx(vf, V_BYTES);
+          const uint32_t vdst = smem_u32(smem + SMEM_V + vs * V_BYTES);
+          tma_load_2d(vdst, &v_map, vf, it.h * 128, row);
+          tma_load_2d(vdst + BLK, &v_map, vf, it.h * 128 + 64, row);
+          v_last[vs] = int((gj / NV) & 1);
+        }
+        g += it.n_kv;
+        ++it_n;
+      }
+      // Drain: every issued load lands before the CTA exits.
+      volatile int never = 0;
+      if (q_last >= 0) mbar_wait(smem_u32(&sh->q_full), uint32_t(q_last), status, &never);
+      for (int s = 0; s < NK; ++s)
+        if (k_last[s] >= 0) mbar_wait(smem_u32(&sh->k_full[s]), uint32_t(k_last[s]), status, &never);
+      for (int s = 0; s < NV; ++s)
+        if (v_last[s] >= 0) mbar_wait(smem_u32(&sh->v_full[s]), uint32_t(v_last[s]), status, &never);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t g = 0, it_n = 0;
+      bool ok = true;
+      const uint32_t q_s = smem_u32(smem + SMEM_Q);
+      for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
+        Item it;
+        if (!load_item(p, idx, it)) continue;
+        const uint32_t ob = it_n & 1;
+        if (!(ok = mbar_wait(smem_u32(&sh->q_full), it_n & 1, status, abort_flag))) break;
+        tc_fence_after();
+        // O += P_jj V_jj for the tile with global index gp (item-local jj).
+        auto issue_pv = [&](uint32_t gp, int jj) -> bool {
+          const uint32_t sb = gp & 1;
+          if (!mbar_wait(smem_u32(&sh->p_full[sb]), (gp >> 1) & 1, status, abort_flag)) return false;
+          if (jj == 0 && it_n >= 2 &&
+              !mbar_wait(smem_u32(&sh->o_free[ob]), ((it_n >> 1) & 1) ^ 1, status, abort_flag))
+            return false;
+          const int vs = gp % NV;
+          if (!mbar_wait(smem_u32(&sh->v_full[vs]), (gp / NV) & 1, status, abort_flag)) return false;
+          tc_fence_after();
+          const uint32_t v_s = smem_u32(smem + SMEM_V + vs * V_BYTES);
+          const uint32_t d = tmem + TM_O + ob * 128;
+          const uint32_t pa = tmem + TM_S + sb * 128;
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_f16_ts(d, pa + kk * 8, sdesc(v_s + kk * 2048, BLK, 1024), IDESC_PV, (jj > 0 || kk > 0));
+          tc_commit(smem_u32(&sh->v_empty[vs]));
+          tc_commit(smem_u32(&sh->o_done));
+          return true;
+        };
+        for (int j = 0; j < it.n_kv && ok; ++j) {
+          const uint32_t gj = g + j;
+          const uint32_t sb = gj & 1;
+          const int ks = gj % NK;
+          if (!(ok = mbar_wait(smem_u32(&sh->k_full[ks]), (gj / NK) & 1, status, abort_flag))) break;
+          tc_fence_after();
+          const uint32_t k_s = smem_u32(smem + SMEM_K + ks * K_BYTES);
+          const uint32_t d = tmem + TM_S + sb * 128;
+#pragma unroll
+          for (int kk = 0; kk < 12; ++kk) {
+            const uint32_t off = (kk >> 2) * BLK + (kk & 3) * 32;
+            mma_f16_ss(d, sdesc(q_s + off, 16, 1024), sdesc(k_s + off, 16, 1024), IDESC_QK, kk > 0);
+          }
+          tc_commit(smem_u32(&sh->k_empty[ks]));
+          tc_commit(smem_u32(&sh->s_full[sb]));
+          if (j == it.n_kv - 1) tc_commit(smem_u32(&sh->q_empty));
+          if (j > 0) ok = issue_pv(gj - 1, j - 1);
+        }
+        if (ok) ok = issue_pv(g + it.n_kv - 1, it.n_kv - 1);
+        g += it.n_kv;
+        ++it_n;
+      }
+      tc_commit(smem_u32(&sh->drain));
+      volatile int never = 0;
+      mbar_wait(smem_u32(&sh->drain), 0, status, &never);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int q4 = warp & 3;                 // TMEM lane quarter
+    const int row = q4 * 32 + lane;          // query row within the tile (= TMEM lane)
+    const uint32_t lane_off = uint32_t(q4 * 32) << 16;
+    uint32_t g = 0, it_n = 0;
+    bool ok = true;
+    for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
+      __syncwarp();  // rows that skipped the last epilogue rejoin before warp-collective work
+      Item it;
+      if (!load_item(p, idx, it)) continue;
+      const uint32_t ob = it_n & 1;
+      const long long qpos = static_cast<long long>(it.cb) + it.i0 + row;
+      // Relative key index kk is visible iff kk < lim_all.
+      const long long lim_all = min(static_cast<long long>(it.n_cb), qpos - it.co + 1);
+      float m_run = kNegInf, l_run = 0.f;
+      for (int j = 0; j < it.n_kv; ++j) {
+        const uint32_t gj = g + j;
+        const uint32_t sb = gj & 1;
+        if (!(ok = mbar_wait_warp(smem_u32(&sh->s_full[sb]), (gj >> 1) & 1, status, abort_flag))) break;
+        tc_fence_after();
+        float x[BN];
+        {
+          uint32_t r[32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            tmem_ld32(tmem + lane_off + TM_S + sb * 128 + c * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(r[i]);
+          }
+        }
+        const long long lim = lim_all - static_cast<long long>(j) * BN;
+        float mx = kNegInf;
+        if (lim < BN) {
+#pragma unroll
+          for (int k = 0; k < BN; ++k) {
+            x[k] = k < lim ? x[k] * p.scale_log2 : kNegInf;
+            mx = fmaxf(mx, x[k]);
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < BN; ++k) {
+            x[k] *= p.scale_log2;
+            mx = fmaxf(mx, x[k]);
+          }
+        }
+        const float m_new = fmaxf(m_run, mx);
+        const bool need = m_new > m_run + kRescaleThreshold;
+        const float f = need ? ex2(m_run - m_new) : 1.0f;   // m_run = -inf gives 0
+        if (need) m_run = m_new;
+        const float msub = m_run == kNegInf ? 0.f : m_run;
+        uint32_t pk[BN / 2];
+        float sum = 0.f;
+#pragma unroll
+        for (int k = 0; k < BN / 2; ++k) {
+          const float p0 = ex2(x[2 * k] - msub);
+          const float p1 = ex2(x[2 * k + 1] - msub);
+          sum += p0 + p1;
+          pk[k] = pack_bf16(p0, p1);
+        }
+        l_run = l_run * f + sum;
+        if (j == it.n_kv - 1 && it.n_cb - j * BN < BN) {
+          // The last tile reaches past the sequence's keys: those V rows may hold
+          // anything (even non-finite values), so zero them before P*V reads them.
+          const int vs = gj % NV;
+          if (!(ok = mbar_wait_warp(smem_u32(&sh->v_full[vs]), (gj / NV) & 1, status, abort_flag))) break;
+          if (j * BN + row >= it.n_cb) {
+            uint8_t* vrow = smem + SMEM_V + vs * V_BYTES + row * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              reinterpret_cast<uint4*>(vrow)[c] = make_uint4(0, 0, 0, 0);
+              reinterpret_cast<uint4*>(vrow + BLK)[c] = make_uint4(0, 0, 0, 0);
+            }
+          }
+          fence_async_smem();
+        }
+        tmem_st32(tmem + lane_off + TM_S + sb * 128, pk);
+        tmem_st32(tmem + lane_off + TM_S + sb * 128 + 32, pk + 32);
+        if (j > 0) {
+          // Observe every P*V completion in order (a parity wait cannot tell one
+          // phase behind from two).  P*V of the previous tile was issued before
+          // this tile's softmax began, so this rarely waits.  Then, if the row
+          // maximum grew by more than 2^8, rescale O in TMEM before P_j*V_j.
+          if (!(ok = mbar_wait_warp(smem_u32(&sh->o_done), (gj - 1) & 1, status, abort_flag))) break;
+          if (__any_sync(0xffffffffu, need)) {
+            tc_fence_after();
+            uint32_t r[32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const uint32_t ta = tmem + lane_off + TM_O + ob * 128 + c * 32;
+              tmem_ld32(ta, r);
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
+              tmem_st32(ta, r);
+            }
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sh->p_full[sb]));
+      }
+      if (!ok) break;
+      g += it.n_kv;
+      // ---------------------------------------------------------- epilogue
+      if (!(ok = mbar_wait_warp(smem_u32(&sh->o_done), (g - 1) & 1, status, abort_flag))) break;
+      tc_fence_after();
+      float o[128];
+      {
+        uint32_t r[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld32(tmem + lane_off + TM_O + ob * 128 + c * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[c * 32 + i] = __uint_as_float(r[i]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh->o_free[ob]));
+      ++it_n;
+      if (row >= it.nq || qpos < it.co) continue;   // padding row, or finished in an earlier chunk
+      const bool first = it.co == 0;
+      const bool final_chunk = qpos < static_cast<long long>(it.co) + it.n_cb;
+      // Without merge scratch (a one-chunk call) a row can only be finished
+      // here; anything else means the plan overflowed max_chunks.
+      if ((!first || !final_chunk) && (p.o_acc == nullptr || p.lse_acc == nullptr)) {
+        set_status(status, MLA_DEV_TOO_MANY_CHUNKS);
+        continue;
+      }
+      const size_t t = static_cast<size_t>(it.q_row0 + row);
+      const size_t th = t * p.H + it.h;
+      float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
+      float lse_c = l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2 : kNegInf;
+      float w_c = inv;     // weight of this chunk's unnormalised O
+      float w_a = 0.f;     // weight of the running result
+      float lse_tot = lse_c;
+      if (!first) {
+        const float lse_a = p.lse_acc[th];
+        const float mm = fmaxf(lse_a, lse_c);
+        const float ea = __expf(lse_a - mm), ec = __expf(lse_c - mm);
+        const float tot = ea + ec;
+        w_a = ea / tot;
+        w_c = inv * (ec / tot);
+        lse_tot = mm + __logf(tot);
+      }
+      const float4* oa = first ? nullptr : reinterpret_cast<const float4*>(p.o_acc + th * 128);
+      if (final_chunk) {
+        uint4* dst = reinterpret_cast<uint4*>(p.out + th * 128);
+        const float vs = p.v_scale;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          float y[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) y[i] = o[c * 8 + i] * w_c;
+          if (!first) {
+            const float4 a0 = oa[2 * c], a1 = oa[2 * c + 1];
+            y[0] += w_a * a0.x; y[1] += w_a * a0.y; y[2] += w_a * a0.z; y[3] += w_a * a0.w;
+            y[4] += w_a * a1.x; y[5] += w_a * a1.y; y[6] += w_a * a1.z; y[7] += w_a * a1.w;
+          }
+          dst[c] = make_uint4(pack_bf16(y[0] * vs, y[1] * vs), pack_bf16(y[2] * vs, y[3] * vs),
+                              pack_bf16(y[4] * vs, y[5] * vs), pack_bf16(y[6] * vs, y[7] * vs));
+        }
+        if (p.lse) p.lse[th] = lse_tot;
+      } else {
+        float4* dst = reinterpret_cast<float4*>(p.o_acc + th * 128);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          float4 y = make_float4(o[4 * c] * w_c, o[4 * c + 1] * w_c, o[4 * c + 2] * w_c, o[4 * c + 3] * w_c);
+          if (!first) {
+            const float4 a = oa[c];
+            y.x += w_a * a.x; y.y += w_a * a.y; y.z += w_a * a.z; y.w += w_a * a.w;
+          }
+          dst[c] = y;
+        }
+        p.lse_acc[th] = lse_tot;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
+  if (a.dtype != MLA_BF16) return cudaErrorNotSupported;
+  const uint64_t HN = static_cast<uint64_t>(a.H) * 128;
+  CUtensorMap q_map, kn_map, kr_map, v_map;
+  const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  bool ok = encode_2d(&q_map, a.q, dt, static_cast<uint64_t>(a.H) * 192, a.T_q,
+                      static_cast<uint64_t>(a.H) * 192 * 2, 64, BM, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            encode_2d(&kn_map, a.k_nope, dt, HN, a.S, HN * 2, 64, BN, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            encode_2d(&kr_map, a.k_rope, dt, 64, a.S, 128, 64, BN, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            encode_2d(&v_map, a.v, dt, HN, a.S, HN * 2, 64, BN, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!ok) return cudaErrorInvalidValue;
+  Params p;
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.lse = a.lse;
+  p.o_acc = a.o_acc;
+  p.lse_acc = a.lse_acc;
+  p.iro = a.iro;
+  p.cache_len = a.cache_len;
+  p.bro = a.bro;
+  p.co = a.co;
+  p.bl = a.bl;
+  p.chunk = a.chunk;
+  p.B = a.B;
+  p.H = a.H;
+  p.n_qtiles = (a.max_prompt_len + BM - 1) / BM;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.v_scale = a.v_scale;
+  p.status = a.status;
+  const long long total = static_cast<long long>(p.n_qtiles) * a.B * a.H;
+  if (total <= 0) return cudaSuccess;
+  const int grid = total < sm_count() ? static_cast<int>(total) : sm_count();
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
+    attr = true;
+  }
+  attn_kernel<<<grid, NUM_THREADS, SMEM_TOTAL, stream>>>(q_map, kn_map, kr_map, v_map, p,
+                                                        static_cast<int>(total));
+  return cudaGetLastError();
+}
+
+}  // namespace mla

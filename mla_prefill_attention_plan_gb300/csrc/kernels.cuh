@@ -1,0 +1,72 @@
+// Internal launchers of the sm_103a kernels (host side).  The public C ABI in
+// mla_prefill.h validates arguments and calls these.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sm100.cuh"
+
+namespace mla {
+
+cudaError_t launch_plan(uint32_t* bro, uint32_t* co, int32_t* bl, const uint32_t* iro,
+                        const uint32_t* cache_len, int B, int max_chunks, uint32_t S,
+                        int32_t* status, cudaStream_t stream);
+
+cudaError_t launch_gather(void* c_kv_buf, void* k_rope_buf, const void* kv_cache,
+                          const int32_t* page_table, int num_pages, int page_size, int max_pages,
+                          const uint32_t* bro, const uint32_t* co, const int32_t* bl, int chunk,
+                          int B, uint32_t S, int elt_bytes, int32_t* status, cudaStream_t stream);
+
+struct UpprojArgs {
+  void* k_nope;
+  void* v;
+  const void* c_kv;
+  const void* w_k;
+  const void* w_uv;
+  const int32_t* buffer_lengths;
+  int chunk;
+  uint32_t S;
+  int H;
+  int dtype;
+  float out_scale;
+  int32_t* status;
+};
+cudaError_t launch_upproject(const UpprojArgs& a, cudaStream_t stream);
+
+struct AttnArgs {
+  void* out;
+  float* lse;
+  float* o_acc;
+  float* lse_acc;
+  const void* q;
+  const void* k_nope;
+  const void* v;
+  const void* k_rope;
+  const uint32_t* iro;
+  const uint32_t* cache_len;
+  const uint32_t* bro;
+  const uint32_t* co;
+  const int32_t* bl;
+  int chunk;
+  int max_chunks;
+  int B;
+  int H;
+  int max_prompt_len;
+  int T_q;
+  uint32_t S;
+  float scale;  // softmax scale times the q and k descales
+  float v_scale;
+  int dtype;
+  int32_t* status;
+};
+cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream);
+
+// Tensor-map encoder and device properties (abi.cu).
+bool encode_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, uint64_t inner,
+               uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle swizzle);
+int sm_count();
+
+}  // namespace mla

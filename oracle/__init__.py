@@ -6,7 +6,8 @@ leg may import this package.  The CUDA library and its binding never do.
 import numpy as np
 
 from .mla_oracle import *  # noqa: F401,F403
-from .mla_oracle import (attention_reference, attention_absorbed, context_latents,  # noqa: F401
+from .mla_oracle import (attention_over_chunks, attention_reference, attention_absorbed,  # noqa: F401
+                         context_latents,
                          decode, gather_latent, merge_partials, mla_prefill,
                          partial_attention, prefill_plan, upproject)
 

@@ -384,31 +384,25 @@ def attention_absorbed(q, c_kv_ctx, k_rope_ctx, w_uk, w_uv, new_lens, cache_lens
 # The whole path, chunk by chunk, as the graph runs it.
 # --------------------------------------------------------------------------
 
-def mla_prefill(q_codes, kv_cache_codes, page_table, page_size, w_k_codes, w_uv_codes,
-                input_row_offsets, cache_lengths, buffer_token_size, max_chunks, scale,
-                dtype="bf16", q_scale=1.0, ckv_scale=1.0, w_scale=1.0,
-                heads=None, rows=None):
-    """Plan, then per chunk: gather, up-project, attend to the chunk's keys and
-    merge into the running (O, LSE) of every query row; finally O per row.
+def attention_over_chunks(q, operands, plan, input_row_offsets, cache_lengths, scale,
+                          heads=None, rows=None):
+    """Chunk by chunk, as the prefill graph runs it: for every used chunk c of
+    the plan, each sequence's new tokens attend to the sequence's keys in the
+    chunk (buffer rows buffer_row_offsets[c,b] .. [c,b+1], at context positions
+    cache_offsets[c,b] onward), and the result is merged into the running
+    (O, LSE) of every query row.
 
-    Inputs are storage codes (uint16 bf16 bits or uint8 e4m3 codes) plus
-    per-tensor descales (real = stored * scale).  K and V are held in the
-    storage dtype between the projection and the attention, in the cache's
-    descale domain.  ``heads``/``rows`` restrict the output to a sample.
-
-    Returns (out dict keyed by (b,h) -> (tokens, O [n,128], LSE [n]), plan).
+    q [T_q, H, 192] real values; ``operands(c)`` returns the chunk's buffers
+    (k_nope [n, Hs, 128], k_rope [n, 64], v [n, Hs, 128]) as real values, Hs
+    indexing ``heads``.  Returns a dict keyed by (b, h) -> (tokens, O, LSE).
     """
-    plan = prefill_plan(input_row_offsets, cache_lengths, buffer_token_size, max_chunks)
-    bro, co, bl, status = plan
+    bro, co, bl, _ = plan
     iro = np.asarray(input_row_offsets, dtype=np.int64)
     cache = np.asarray(cache_lengths, dtype=np.int64)
     new = iro[1:] - iro[:-1]
     B = cache.shape[0]
-    q = decode(q_codes, dtype) * q_scale
     H = q.shape[1]
     hs = list(range(H)) if heads is None else list(heads)
-    w_k = decode(w_k_codes, dtype) * w_scale
-    w_uv = decode(w_uv_codes, dtype) * w_scale
     sel = [np.arange(int(new[b])) if rows is None else np.asarray(rows[b], np.int64)
            for b in range(B)]
     acc = {}
@@ -416,13 +410,10 @@ def mla_prefill(q_codes, kv_cache_codes, page_table, page_size, w_k_codes, w_uv_
         for h in hs:
             n = sel[b].size
             acc[(b, h)] = (iro[b] + sel[b], np.zeros((n, DV)), np.full(n, -np.inf))
-    for c in range(max_chunks):
+    for c in range(bl.shape[0]):
         if bl[c] < 0:
             continue
-        c_kv_codes, k_rope_codes, _ = gather_latent(kv_cache_codes, page_table, page_size, plan, c)
-        c_kv = decode(c_kv_codes, dtype) * ckv_scale
-        k_rope = decode(k_rope_codes, dtype) * ckv_scale
-        k_nope, v = upproject(c_kv, w_k, w_uv, heads=hs, store=dtype, inv_scale=1.0 / ckv_scale)
+        k_nope, k_rope, v = operands(c)
         for b in range(B):
             r0, r1 = int(bro[c, b]), int(bro[c, b + 1])
             if r1 == r0 or sel[b].size == 0:
@@ -436,6 +427,39 @@ def mla_prefill(q_codes, kv_cache_codes, page_table, page_size, w_k_codes, w_uv_
                 tok, o_acc, lse_acc = acc[(b, h)]
                 o_new, lse_new = merge_partials(o_acc, lse_acc, o_c, lse_c)
                 acc[(b, h)] = (tok, o_new, lse_new)
+    return acc
+
+
+def mla_prefill(q_codes, kv_cache_codes, page_table, page_size, w_k_codes, w_uv_codes,
+                input_row_offsets, cache_lengths, buffer_token_size, max_chunks, scale,
+                dtype="bf16", q_scale=1.0, ckv_scale=1.0, w_scale=1.0,
+                heads=None, rows=None):
+    """The whole path: plan, then per chunk gather, up-project and attend,
+    merging chunk results by LSE (``attention_over_chunks``).
+
+    Inputs are storage codes (uint16 bf16 bits or uint8 e4m3 codes) plus
+    per-tensor descales (real = stored * scale).  K and V are held in the
+    storage dtype between the projection and the attention, in the cache's
+    descale domain.  ``heads``/``rows`` restrict the output to a sample.
+
+    Returns (out dict keyed by (b,h) -> (tokens, O [n,128], LSE [n]), plan).
+    """
+    plan = prefill_plan(input_row_offsets, cache_lengths, buffer_token_size, max_chunks)
+    q = decode(q_codes, dtype) * q_scale
+    H = q.shape[1]
+    hs = list(range(H)) if heads is None else list(heads)
+    w_k = decode(w_k_codes, dtype) * w_scale
+    w_uv = decode(w_uv_codes, dtype) * w_scale
+
+    def operands(c):
+        c_kv_codes, k_rope_codes, _ = gather_latent(kv_cache_codes, page_table, page_size, plan, c)
+        c_kv = decode(c_kv_codes, dtype) * ckv_scale
+        k_rope = decode(k_rope_codes, dtype) * ckv_scale
+        k_nope, v = upproject(c_kv, w_k, w_uv, heads=hs, store=dtype, inv_scale=1.0 / ckv_scale)
+        return k_nope, k_rope, v
+
+    acc = attention_over_chunks(q, operands, plan, input_row_offsets, cache_lengths, scale,
+                                heads=hs, rows=rows)
     return acc, plan
 
 

@@ -1,0 +1,413 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle on the
+same seeded inputs.  Plan and gather must match bit for bit; the projection
+within bf16 (or e4m3) rounding; attention within max-abs 2e-2 / mean-rel 1e-2
+for bf16 (6e-2 / 3e-2 for e4m3), mean-rel = sum|gpu-ref| / sum|ref|."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import mla_prefill_attention_plan_gb300 as mla
+import oracle as O
+from oracle import mla_oracle as M
+from workloads import WORKLOADS, lengths, make_attention_operands, make_inputs, scaled
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+TOL = {"bf16": (2e-2, 1e-2), "e4m3": (6e-2, 3e-2)}
+LSE_TOL = 5e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from mla_prefill_attention_plan_gb300 import build
+    build.build()
+    mla.load()
+    assert torch.cuda.is_available()
+
+
+def _dt(w):
+    return mla.MLA_BF16 if w.dtype == "bf16" else mla.MLA_E4M3
+
+
+def _i32(a):
+    return torch.as_tensor(np.asarray(a, dtype=np.int64).astype(np.int32)).to(DEV)
+
+
+def gpu_plan(iro, cache, S, max_chunks):
+    B = len(cache)
+    bro = torch.full((max_chunks, B + 1), -7, dtype=torch.int32, device=DEV)
+    co = torch.full((max_chunks, max(B, 1)), -7, dtype=torch.int32, device=DEV)
+    bl = torch.full((max_chunks,), -7, dtype=torch.int32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    mla.check(mla.mla_prefill_plan(bro, co, bl, _i32(iro), _i32(cache) if B else _i32([0]), B,
+                                   max_chunks, S, st))
+    torch.cuda.synchronize()
+    return (bro.cpu().numpy().astype(np.int64), co.cpu().numpy()[:, :B].astype(np.int64),
+            bl.cpu().numpy().astype(np.int64), int(st.item()))
+
+
+def _assert_plan_equal(iro, cache, S, mc):
+    g = gpu_plan(iro, cache, S, mc)
+    o = O.prefill_plan(iro, cache, S, mc)
+    assert g[3] == o[3]
+    if o[3] in (0, M.STATUS_TOO_MANY_CHUNKS):
+        np.testing.assert_array_equal(g[0], o[0])
+        np.testing.assert_array_equal(g[1], o[1])
+        np.testing.assert_array_equal(g[2], o[2])
+
+
+# ----------------------------------------------------------------------------- plan
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_plan_workloads_bit_exact(name):
+    w = WORKLOADS[name]
+    new, cache = lengths(w)
+    iro = np.concatenate([[0], np.cumsum(new)])
+    _assert_plan_equal(iro, cache, w.buffer_token_size, w.max_chunks)
+
+
+def test_plan_random_fuzz():
+    rng = np.random.default_rng(5)
+    for _ in range(150):
+        B = int(rng.integers(1, 60))
+        new = rng.integers(0, 300, B)
+        cache = rng.integers(0, 300, B)
+        S = int(rng.integers(1, 700))
+        need = -(-int((new + cache).sum()) // S)
+        mc = max(1, need + int(rng.integers(-2, 3)))
+        _assert_plan_equal(np.concatenate([[0], np.cumsum(new)]), cache, S, mc)
+
+
+@pytest.mark.parametrize("B", [4096, 4097, 20000])
+def test_plan_many_sequences(B):
+    rng = np.random.default_rng(B)
+    new = rng.integers(0, 64, B)
+    cache = rng.integers(0, 64, B)
+    S = 20000
+    need = -(-int((new + cache).sum()) // S)
+    _assert_plan_equal(np.concatenate([[0], np.cumsum(new)]), cache, S, need + 1)
+
+
+def test_plan_status_codes():
+    assert gpu_plan([0, 10], [0], 4, 2)[3] == mla.MLA_DEV_TOO_MANY_CHUNKS
+    _assert_plan_equal([0, 10], [0], 4, 2)          # truncated rows still written
+    assert gpu_plan([1, 3], [0], 4, 2)[3] == mla.MLA_DEV_BAD_OFFSETS
+    assert gpu_plan([0, 5, 3], [0, 0], 4, 4)[3] == mla.MLA_DEV_BAD_OFFSETS
+    bro, co, bl, st = gpu_plan([0, 0, 0], [0, 0], 8, 3)
+    assert st == 0 and list(bl) == [-1, -1, -1]
+
+
+# ----------------------------------------------------------------------------- gather
+
+def _gather_case(w, **kw):
+    inp = make_inputs(w, **kw)
+    c = {k: O.codes(inp[k]) for k in ("kv_cache", "page_table", "input_row_offsets", "cache_lengths")}
+    plan = O.prefill_plan(c["input_row_offsets"], c["cache_lengths"], w.buffer_token_size, w.max_chunks)
+    S = w.buffer_token_size
+    B = inp["B"]
+    g = gpu_plan(c["input_row_offsets"], c["cache_lengths"], S, w.max_chunks)
+    tdt = inp["kv_cache"].dtype
+    kv = inp["kv_cache"].to(DEV)
+    pt = inp["page_table"].to(DEV)
+    bro = torch.as_tensor(g[0].astype(np.int32)).to(DEV)
+    co = torch.as_tensor(g[1].astype(np.int32)).to(DEV)
+    bl = torch.as_tensor(g[2].astype(np.int32)).to(DEV)
+    for ch in range(w.max_chunks):
+        ckv = torch.full((S, 512), 0.5, dtype=torch.float32).to(tdt).to(DEV)
+        kr = torch.full((S, 64), 0.5, dtype=torch.float32).to(tdt).to(DEV)
+        st = torch.zeros(1, dtype=torch.int32, device=DEV)
+        mla.check(mla.mla_gather_latent(ckv, kr, kv, pt, inp["num_pages"], inp["page_size"],
+                                        inp["max_pages"], bro, co, bl, ch, B, S, _dt(w), st))
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        o_ckv, o_kr, ost = O.gather_latent(c["kv_cache"], c["page_table"], inp["page_size"], plan, ch)
+        assert ost == 0
+        n = max(int(plan[2][ch]), 0)
+        g_ckv, g_kr = O.codes(ckv.cpu()), O.codes(kr.cpu())
+        np.testing.assert_array_equal(g_ckv[:n], o_ckv)
+        np.testing.assert_array_equal(g_kr[:n], o_kr)
+        # rows past the chunk's length are left untouched
+        sentinel = O.codes(torch.full((1,), 0.5).to(tdt))[0]
+        assert np.all(g_ckv[n:] == sentinel) and np.all(g_kr[n:] == sentinel)
+
+
+def test_gather_tiny_ragged():
+    _gather_case(WORKLOADS["tiny_ragged"])
+
+
+def test_gather_shuffled_pages_multi_chunk():
+    w = scaled(WORKLOADS["ragged_chunked_cache"], H=1, buffer_token_size=1000, max_chunks=16,
+               new_range=(1, 500), cache_range=(0, 900), page_size=16)
+    _gather_case(w)
+
+
+def test_gather_e4m3():
+    w = scaled(WORKLOADS["longctx_fp8"], H=1, new_lens=(300,), cache_lens=(200,),
+               buffer_token_size=192, max_chunks=3, page_size=64)
+    _gather_case(w)
+
+
+def test_gather_bad_page_reports_status():
+    w = WORKLOADS["tiny_ragged"]
+    inp = make_inputs(w)
+    pt = inp["page_table"].clone()
+    pt[1, 2] = inp["num_pages"] + 5
+    g = gpu_plan(O.codes(inp["input_row_offsets"]), O.codes(inp["cache_lengths"]), 32, 4)
+    ckv = torch.zeros(32, 512, dtype=torch.bfloat16, device=DEV)
+    kr = torch.zeros(32, 64, dtype=torch.bfloat16, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    tabs = [torch.as_tensor(x.astype(np.int32)).to(DEV) for x in g[:3]]
+    for ch in range(4):
+        mla.check(mla.mla_gather_latent(ckv, kr, inp["kv_cache"].to(DEV), pt.to(DEV),
+                                        inp["num_pages"], 16, inp["max_pages"], *tabs, ch, 2, 32,
+                                        mla.MLA_BF16, st))
+    torch.cuda.synchronize()
+    assert st.item() == mla.MLA_DEV_BAD_PAGE
+
+
+# ----------------------------------------------------------------------------- up-projection
+
+@pytest.mark.parametrize("dtype,H,rows,S", [("bf16", 4, 89, 96), ("bf16", 3, 300, 320),
+                                            ("bf16", 16, 1000, 1024), ("e4m3", 4, 200, 256)])
+def test_upproject(dtype, H, rows, S):
+    w = scaled(WORKLOADS["tiny_ragged" if dtype == "bf16" else "longctx_fp8"], H=H)
+    gen = torch.Generator().manual_seed(H * 1000 + rows)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float8_e4m3fn
+    ckv = torch.randn(S, 512, generator=gen).to(tdt)
+    wstd, wsc = (1 / math.sqrt(512), 1.0) if dtype == "bf16" else (1.0, 1 / math.sqrt(512))
+    wk = (torch.randn(H * 128, 512, generator=gen) * wstd).to(tdt)
+    wuv = (torch.randn(H, 128, 512, generator=gen) * wstd).to(tdt)
+    kn = torch.full((S, H, 128), 3.0).to(tdt).to(DEV)
+    vv = torch.full((S, H, 128), 3.0).to(tdt).to(DEV)
+    bl = torch.tensor([rows], dtype=torch.int32, device=DEV)
+    mla.check(mla.mla_upproject(kn, vv, ckv.to(DEV), wk.to(DEV), wuv.to(DEV), bl, 0, S, H,
+                                mla.MLA_BF16 if dtype == "bf16" else mla.MLA_E4M3, 1.0, wsc, 1.0))
+    torch.cuda.synchronize()
+    rk, rv = O.upproject(O.decode(O.codes(ckv), dtype)[:rows], O.decode(O.codes(wk), dtype) * wsc,
+                         O.decode(O.codes(wuv), dtype) * wsc)
+    gk = kn.float().cpu().double().numpy()
+    gv = vv.float().cpu().double().numpy()
+    if dtype == "bf16":
+        bound = lambda ref: 2.0 ** -8 * np.abs(ref) + 1e-3
+    else:
+        bound = lambda ref: 2.0 ** -3 * np.abs(ref) + 2.0 ** -8
+    assert np.all(np.abs(gk[:rows] - rk) <= bound(rk))
+    assert np.all(np.abs(gv[:rows] - rv) <= bound(rv))
+    pad = min(S, -(-rows // 128) * 128)
+    assert np.all(gk[rows:pad] == 0) and np.all(gv[rows:pad] == 0)   # zero-filled tile tail
+    assert np.all(gk[pad:] == 3.0) and np.all(gv[pad:] == 3.0)       # untouched beyond it
+
+
+# ----------------------------------------------------------------------------- attention
+
+def _compare(out, ref, dtype, lse=None):
+    tol_abs, tol_rel = TOL[dtype]
+    max_abs, num, den, lse_err = 0.0, 0.0, 0.0, 0.0
+    out = out.float().cpu().double().numpy()
+    lse_np = None if lse is None else lse.cpu().double().numpy()
+    for (b, h), (tok, o, l) in ref.items():
+        if tok.size == 0:
+            continue
+        g = out[tok, h]
+        assert np.all(np.isfinite(g))
+        d = np.abs(g - o)
+        max_abs = max(max_abs, float(d.max()))
+        num += float(d.sum())
+        den += float(np.abs(o).sum())
+        if lse_np is not None:
+            lse_err = max(lse_err, float(np.abs(lse_np[tok, h] - l).max()))
+    mean_rel = num / max(den, 1e-30)
+    assert max_abs <= tol_abs, (max_abs, mean_rel)
+    assert mean_rel <= tol_rel, (max_abs, mean_rel)
+    assert lse_err <= LSE_TOL, lse_err
+    return max_abs, mean_rel
+
+
+def test_attention_stage_multi_chunk():
+    """Attention alone over seeded K/V buffers, chunk by chunk, with the merge
+    scratch carried between calls."""
+    w = WORKLOADS["tiny_ragged"]
+    inp = make_inputs(w)
+    c = {k: O.codes(inp[k]) for k in ("q", "input_row_offsets", "cache_lengths")}
+    S, mc, B, H, T = w.buffer_token_size, w.max_chunks, inp["B"], w.H, inp["T_q"]
+    plan = O.prefill_plan(c["input_row_offsets"], c["cache_lengths"], S, mc)
+    g = gpu_plan(c["input_row_offsets"], c["cache_lengths"], S, mc)
+    tabs = [torch.as_tensor(x.astype(np.int32)).to(DEV) for x in g[:3]]
+    ops = [make_attention_operands(w, S, seed_offset=11 + ch) for ch in range(mc)]
+    out = torch.full((T, H, 128), float("nan"), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(T, H, dtype=torch.float32, device=DEV)
+    oacc = torch.empty(T, H, 128, dtype=torch.float32, device=DEV)
+    lacc = torch.empty(T, H, dtype=torch.float32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    q = inp["q"].to(DEV)
+    for ch in range(mc):
+        kn, vv, kr = (t.to(DEV) for t in ops[ch])
+        mla.check(mla.mla_prefill_attention(out, lse, oacc, lacc, q, kn, vv, kr,
+                                            inp["input_row_offsets"].to(DEV),
+                                            inp["cache_lengths"].to(DEV), *tabs, ch, mc, B, H,
+                                            inp["max_prompt_len"], T, S, inp["scale"], d_status=st))
+    torch.cuda.synchronize()
+    assert st.item() == 0
+
+    def operands(ch):
+        kn, vv, kr = ops[ch]
+        return (O.decode(O.codes(kn), "bf16"), O.decode(O.codes(kr), "bf16"),
+                O.decode(O.codes(vv), "bf16"))
+    ref = O.attention_over_chunks(O.decode(c["q"], "bf16"), operands, plan,
+                                  c["input_row_offsets"], c["cache_lengths"], inp["scale"])
+    _compare(out, ref, "bf16", lse)
+
+
+def run_fused(inp, S=None, max_chunks=None, lse=True):
+    w = inp["workload"]
+    S = S or w.buffer_token_size
+    mc = max_chunks or w.max_chunks
+    B, H, T = inp["B"], w.H, inp["T_q"]
+    dt = _dt(w)
+    out = torch.full((T, H, 128), float("nan"), dtype=torch.bfloat16, device=DEV)
+    lse_t = torch.empty(T, H, dtype=torch.float32, device=DEV) if lse else None
+    nbytes = mla.mla_prefill_workspace_bytes(B, H, T, mc, S, dt)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    st = torch.full((1,), 99, dtype=torch.int32, device=DEV)
+    mla.check(mla.mla_prefill(out, lse_t, inp["q"].to(DEV), inp["input_row_offsets"].to(DEV),
+                              inp["cache_lengths"].to(DEV), inp["kv_cache"].to(DEV),
+                              inp["page_table"].to(DEV), inp["num_pages"], inp["page_size"],
+                              inp["max_pages"], inp["w_k"].to(DEV), inp["w_uv"].to(DEV), B, H, T,
+                              inp["max_prompt_len"], S, mc, inp["scale"], inp["q_scale"],
+                              inp["ckv_scale"], inp["w_scale"], dt, ws, nbytes, st))
+    torch.cuda.synchronize()
+    assert st.item() == 0, mla.status_string(int(st.item()))
+    return out, lse_t
+
+
+def oracle_fused(inp, S=None, max_chunks=None, heads=None, rows=None):
+    w = inp["workload"]
+    c = {k: O.codes(inp[k]) for k in ("q", "kv_cache", "page_table", "w_k", "w_uv",
+                                      "input_row_offsets", "cache_lengths")}
+    ref, _ = O.mla_prefill(c["q"], c["kv_cache"], c["page_table"], inp["page_size"], c["w_k"],
+                           c["w_uv"], c["input_row_offsets"], c["cache_lengths"],
+                           S or w.buffer_token_size, max_chunks or w.max_chunks, inp["scale"],
+                           dtype=w.dtype, q_scale=inp["q_scale"], ckv_scale=inp["ckv_scale"],
+                           w_scale=inp["w_scale"], heads=heads, rows=rows)
+    return ref
+
+
+def _sample_rows(new_lens, cache_lens, S, k, seed):
+    """First, last, tile-edge and chunk-edge rows plus random ones, per sequence."""
+    rng = np.random.default_rng(seed)
+    out = []
+    start = 0
+    for n, cb in zip(new_lens, cache_lens):
+        n, cb = int(n), int(cb)
+        cand = {0, n - 1, min(127, n - 1), min(128, n - 1), n // 2}
+        # rows whose position sits on a chunk boundary of the packed order
+        for edge in range((start // S + 1) * S, start + cb + n, S):
+            i = edge - start - cb
+            for d in (-1, 0, 1):
+                if 0 <= i + d < n:
+                    cand.add(i + d)
+        cand |= set(rng.integers(0, n, size=k).tolist()) if n > 0 else set()
+        out.append(np.array(sorted(x for x in cand if 0 <= x < n), dtype=np.int64))
+        start += cb + n
+    return out
+
+
+def test_fused_tiny_ragged_all_rows():
+    inp = make_inputs(WORKLOADS["tiny_ragged"])
+    out, lse = run_fused(inp)
+    _compare(out, oracle_fused(inp), "bf16", lse)
+
+
+@pytest.mark.parametrize("S", [7, 64, 200])
+def test_fused_buffer_size_invariance(S):
+    """Different buffer sizes cut the context differently; the result is the same."""
+    w = WORKLOADS["tiny_ragged"]
+    inp = make_inputs(w)
+    mc = -(-89 // S)
+    out, lse = run_fused(inp, S=S, max_chunks=mc)
+    _compare(out, oracle_fused(inp, S=S, max_chunks=mc), "bf16", lse)
+    out_ref, _ = run_fused(inp)
+    assert (out.float() - out_ref.float()).abs().max().item() <= 2e-2
+
+
+def test_fused_v2lite_shape_small_heads():
+    inp = make_inputs(scaled(WORKLOADS["v2lite_prefill"], H=2))
+    out, lse = run_fused(inp)
+    rows = _sample_rows(inp["new_lens"], inp["cache_lens"], 4096, 40, 1)
+    _compare(out, oracle_fused(inp, rows=rows), "bf16", lse)
+
+
+def test_fused_v3_full_length_small_heads():
+    inp = make_inputs(scaled(WORKLOADS["v3_prefill"], H=2))
+    out, lse = run_fused(inp)
+    rows = _sample_rows(inp["new_lens"], inp["cache_lens"], 4096, 60, 2)
+    _compare(out, oracle_fused(inp, rows=rows), "bf16", lse)
+
+
+def test_fused_ragged_chunked_small_heads():
+    w = scaled(WORKLOADS["ragged_chunked_cache"], H=2)
+    inp = make_inputs(w)
+    out, lse = run_fused(inp)
+    rows = _sample_rows(inp["new_lens"], inp["cache_lens"], w.buffer_token_size, 24, 3)
+    _compare(out, oracle_fused(inp, rows=rows), "bf16", lse)
+
+
+def test_fused_edge_cases():
+    # an empty sequence, a cache-only sequence, a single token, a tile-edge length,
+    # a buffer smaller than one sequence
+    w = scaled(WORKLOADS["tiny_ragged"], H=3, page_size=8, buffer_token_size=50, max_chunks=12)
+    new, cache = (0, 1, 129, 0, 5), (0, 0, 17, 30, 70)
+    inp = make_inputs(w, new_lens=new, cache_lens=cache)
+    mc = -(-sum(a + b for a, b in zip(new, cache)) // 50)
+    out, lse = run_fused(inp, max_chunks=mc)
+    _compare(out, oracle_fused(inp, max_chunks=mc), "bf16", lse)
+
+
+def test_fused_sequence_alone_equals_in_batch():
+    w = scaled(WORKLOADS["ragged_chunked_cache"], H=2, B=3, buffer_token_size=256,
+               new_range=(100, 300), cache_range=(0, 400))
+    inp = make_inputs(w)
+    mc = -(-int((inp["new_lens"] + inp["cache_lens"]).sum()) // 256)
+    out, _ = run_fused(inp, max_chunks=mc)
+    b = 1
+    alone = make_inputs(scaled(w, B=1), new_lens=[inp["new_lens"][b]], cache_lens=[inp["cache_lens"][b]])
+    # same sequence content: copy its q rows, pages and weights
+    iro = inp["input_row_offsets"].numpy()
+    alone["q"] = inp["q"][iro[b]:iro[b + 1]].clone()
+    pages = inp["page_table"][b]
+    pages = pages[pages >= 0]
+    alone["kv_cache"] = inp["kv_cache"][pages.long()].clone()
+    alone["page_table"] = torch.arange(len(pages), dtype=torch.int32)[None, :]
+    alone["num_pages"], alone["max_pages"] = len(pages), len(pages)
+    alone["w_k"], alone["w_uv"] = inp["w_k"], inp["w_uv"]
+    mc1 = -(-int(inp["new_lens"][b] + inp["cache_lens"][b]) // 256)
+    out1, _ = run_fused(alone, max_chunks=mc1)
+    d = (out[iro[b]:iro[b + 1]].float() - out1.float()).abs().max().item()
+    assert d <= 2e-2
+
+
+@pytest.mark.parametrize("name", ["v2lite_prefill", "v3_prefill", "ragged_chunked_cache"])
+def test_fused_full_size_sampled(name):
+    """Full sizes, the launch configuration the benchmark times; the oracle
+    checks a sample of heads and rows."""
+    w = WORKLOADS[name]
+    inp = make_inputs(w)
+    out, lse = run_fused(inp)
+    heads = [0, w.H // 2 + 1, w.H - 1]
+    rows = _sample_rows(inp["new_lens"], inp["cache_lens"], w.buffer_token_size, 12, 4)
+    _compare(out, oracle_fused(inp, heads=heads, rows=rows), "bf16", lse)
+    assert torch.isfinite(out.float()).all()
+
+
+def test_fused_is_deterministic():
+    """No atomics in the arithmetic: repeated calls agree bit for bit (a
+    pipeline race shows up here first)."""
+    inp = make_inputs(scaled(WORKLOADS["ragged_chunked_cache"], H=2, B=4, buffer_token_size=2048,
+                             new_range=(100, 900), cache_range=(0, 1500)))
+    mc = -(-int((inp["new_lens"] + inp["cache_lens"]).sum()) // 2048)
+    outs = [run_fused(inp, max_chunks=mc) for _ in range(4)]
+    for o, l in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0][0].view(torch.int16))
+        assert torch.equal(l, outs[0][1])
