@@ -45,6 +45,7 @@ def _args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
     return ap.parse_args()
 
 
@@ -324,43 +325,50 @@ def run_ours(a):
     attn_ms_per_launch = attn_ms / (a.steps * max(used_chunks, 1))
     assert status.item() == 0, mla.status_string(int(status.item()))
 
-    # end to end: pinned host inputs in, result out, through the fused entry point
-    host = {k: inp[k].pin_memory() for k in ("q", "input_row_offsets", "cache_lengths", "kv_cache",
-                                             "page_table")}
-    out_host = torch.empty(T, H, 128, dtype=torch.bfloat16).pin_memory()
-    nbytes = mla.mla_prefill_workspace_bytes(Bsz, H, T, mc, S, dt)
-    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = out_host.numel() * out_host.element_size()
+    # End to end through the fused entry point: pinned host inputs copied in,
+    # the result copied back, every step.
+    e2e = None
+    if not a.no_e2e:
+        host = {k: inp[k].pin_memory() for k in ("q", "input_row_offsets", "cache_lengths",
+                                                 "kv_cache", "page_table")}
+        out_host = torch.empty(T, H, 128, dtype=torch.bfloat16).pin_memory()
+        nbytes = mla.mla_prefill_workspace_bytes(Bsz, H, T, mc, S, dt)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_host.numel() * out_host.element_size()
 
-    def e2e_step():
-        for k2, t in host.items():
-            d[k2].copy_(t, non_blocking=True)
-        mla.check(mla.mla_prefill(out, None, d["q"], d["input_row_offsets"], d["cache_lengths"],
-                                  d["kv_cache"], d["page_table"], inp["num_pages"], inp["page_size"],
-                                  inp["max_pages"], d["w_k"], d["w_uv"], Bsz, H, T,
-                                  inp["max_prompt_len"], S, mc, inp["scale"], inp["q_scale"],
-                                  inp["ckv_scale"], inp["w_scale"], dt, ws, nbytes, status, stream))
-        out_host.copy_(out, non_blocking=True)
+        def e2e_step():
+            for k2, t in host.items():
+                d[k2].copy_(t, non_blocking=True)
+            mla.check(mla.mla_prefill(out, None, d["q"], d["input_row_offsets"], d["cache_lengths"],
+                                      d["kv_cache"], d["page_table"], inp["num_pages"],
+                                      inp["page_size"], inp["max_pages"], d["w_k"], d["w_uv"], Bsz, H,
+                                      T, inp["max_prompt_len"], S, mc, inp["scale"], inp["q_scale"],
+                                      inp["ckv_scale"], inp["w_scale"], dt, ws, nbytes, status,
+                                      stream))
+            out_host.copy_(out, non_blocking=True)
 
-    e2e_steps = a.e2e_steps or max(3, min(a.steps, 50))
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        dist.barrier()
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    assert status.item() == 0, mla.status_string(int(status.item()))
+        e2e_steps = a.e2e_steps or max(3, min(a.steps, 50))
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            dist.barrier()
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / e2e_steps
+        if world > 1:
+            tt = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e2e_ms = float(tt.item())
+        assert status.item() == 0, mla.status_string(int(status.item()))
+        e2e = {"value": step_flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "ms_per_step": e2e_ms, "steps": e2e_steps, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "api": "mla_prefill"}
 
     if rank != 0:
         if world > 1:
@@ -385,9 +393,7 @@ def run_ours(a):
                      "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                      "peak_source": f"{src} bf16 dense, sustained (kernel timed inside a long step loop)",
                      "traffic": ATTN_DRAM_BYTES_PER_LAUNCH.get(w.name)},
-        "e2e": {"value": step_flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "api": "mla_prefill"},
+        "e2e": e2e,
         "gpu_launches": launches_per_step * a.steps,
         "clocks": clk,
     }

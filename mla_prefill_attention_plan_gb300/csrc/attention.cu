@@ -5,24 +5,31 @@
 // of per-chunk results.
 //
 // Work item = (sequence b, 128-row query tile, head h).  Persistent CTAs (one
-// per SM) stride over the items, heaviest query tiles first.  Per CTA:
-//   warp 0      TMA producer: Q tile (3 x 16 KB), K tiles (nope 2 x 16 KB +
-//               rope 16 KB) and V tiles (2 x 16 KB), all 128-byte swizzled,
-//               into a 2-stage K ring and a 2-stage V ring.
+// per SM) stride over the items: heads in groups (so the CTAs in flight share
+// a few heads' K/V in L2), heaviest query tiles first within a group.
+//
+//   warp 0      TMA producer: the Q tile (3 x 16 KB) into shared memory, K
+//               tiles (nope 2 x 16 KB + rope 16 KB) and V tiles (2 x 16 KB),
+//               all 128-byte swizzled, into 2-stage K and V rings.
 //   warp 1      TMEM owner (512 columns) and single-thread MMA issuer:
-//                 S_j = Q K_j^T   (M=128 queries, N=128 keys, K=192: 12 MMAs,
-//                                  A and B K-major in shared memory)
-//                 O  += P_j V_j   (M=128, N=128 dv, K=128 keys: 8 MMAs, A = P
-//                                  read from tensor memory, B = V MN-major)
-//               S is double-buffered (columns 0..255) so S_{j+1} runs while
-//               the softmax works on S_j; O is double-buffered across items
-//               (columns 256..511) so an item's epilogue overlaps the next.
-//   warps 2..5  softmax + epilogue, one thread per query row: tcgen05.ld the
-//               S row, scale (log2 domain), causal/ragged mask, row max, lazy
-//               rescale of O only when the max grows by more than 2^8, exp2,
-//               row sum, bf16 P written back over S in tensor memory; at the
-//               end O / l, then the LSE merge with earlier chunks (fp32
-//               scratch) or the final bf16 store.
+//                 S_j = Q K_j^T   M=128 queries, N=128 keys, K=192 as 12 MMAs;
+//                                 A = Q read from tensor memory, B = K (K-major)
+//                 O  += P_j V_j   M=128, N=128 (dv), K=128 keys as 8 MMAs;
+//                                 A = P read from tensor memory, B = V (MN-major)
+//               Keeping both A operands in TMEM leaves shared-memory bandwidth
+//               to the K/V operands and the TMA writes.
+//   warps 2..5  one thread per query row.  Copy the item's Q row from shared
+//               memory into TMEM; per key tile: tcgen05.ld the S row, mask the
+//               boundary tiles, row max, exp2 of s*scale*log2(e) - m with packed
+//               f32x2 FMAs, row sum, bf16 P written back over S; O rescaled in
+//               TMEM only when the row max grows by more than 2^8.  After the
+//               last tile the next item's Q goes into TMEM (so its first MMAs
+//               overlap this epilogue), then O / l, the natural-log LSE, and the
+//               merge with earlier chunks (fp32 scratch) or the bf16 store.
+//
+// TMEM columns: S/P buffers 0..127 and 128..255, O 256..383, Q 384..479.
+#include <algorithm>
+
 #include "kernels.cuh"
 
 namespace mla {
@@ -42,7 +49,8 @@ constexpr int SMEM_TOTAL = SMEM_BAR + 256 + 1024;
 constexpr int NUM_THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_S = 0;      // S/P buffers: columns 0..127, 128..255
-constexpr uint32_t TM_O = 256;    // O buffers: columns 256..383, 384..511
+constexpr uint32_t TM_O = 256;    // O: columns 256..383
+constexpr uint32_t TM_Q = 384;    // Q (bf16 pairs): columns 384..479
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr float kNegInf = -__builtin_huge_valf();
@@ -51,11 +59,11 @@ constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, false, false);
 constexpr uint32_t IDESC_PV = idesc_bf16(BM, 128, false, true);
 
 struct Smem {
-  uint64_t q_full, q_empty;
+  uint64_t q_full, q_empty, q_ready;
   uint64_t k_full[NK], k_empty[NK];
   uint64_t v_full[NV], v_empty[NV];
   uint64_t s_full[2], p_full[2];
-  uint64_t o_done, o_free[2];
+  uint64_t o_done, o_free;
   uint64_t drain;
   uint32_t tmem;
   int abort;
@@ -72,7 +80,7 @@ struct Params {
   const uint32_t* bro;
   const uint32_t* co;
   const int32_t* bl;
-  int chunk, B, H, n_qtiles;
+  int chunk, B, H, n_qtiles, head_group;
   float scale_log2;   // softmax scale * descales * log2(e)
   float v_scale;
   int32_t* status;
@@ -91,9 +99,17 @@ struct Item {
   int n_kv;      // 128-key tiles to visit (0: nothing to do)
 };
 
+// Item order: heads in groups of `head_group`; within a group, query tiles
+// heaviest first, and the group's heads side by side.  The CTAs in flight then
+// share the K/V of a few heads in L2 instead of streaming every head's K/V.
 __device__ __forceinline__ bool load_item(const Params& p, int idx, Item& it) {
-  it.h = idx % p.H;
-  const int pair = idx / p.H;
+  const int n_pairs = p.n_qtiles * p.B;
+  const int per_group = p.head_group * n_pairs;
+  const int grp = idx / per_group;
+  const int r = idx - grp * per_group;
+  const int hg = min(p.head_group, p.H - grp * p.head_group);   // heads in this group
+  const int pair = r / hg;
+  it.h = grp * p.head_group + (r - pair * hg);
   const int qt = p.n_qtiles - 1 - pair / p.B;   // heaviest query tiles first
   it.b = pair % p.B;
   const uint32_t* bro_c = p.bro + static_cast<size_t>(p.chunk) * (p.B + 1);
@@ -116,6 +132,13 @@ __device__ __forceinline__ bool load_item(const Params& p, int idx, Item& it) {
   return true;
 }
 
+// First item with work at or after `idx` (stepping by the grid size).
+__device__ __forceinline__ bool next_item(const Params& p, int& idx, int total, Item& it) {
+  for (; idx < total; idx += gridDim.x)
+    if (load_item(p, idx, it)) return true;
+  return false;
+}
+
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap kn_map,
                 const __grid_constant__ CUtensorMap kr_map, const __grid_constant__ CUtensorMap v_map,
@@ -130,7 +153,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&sh->q_full), 1);
-    mbar_init(smem_u32(&sh->q_empty), 1);
+    mbar_init(smem_u32(&sh->q_empty), 4);
+    mbar_init(smem_u32(&sh->q_ready), 4);
     for (int i = 0; i < NK; ++i) {
       mbar_init(smem_u32(&sh->k_full[i]), 1);
       mbar_init(smem_u32(&sh->k_empty[i]), 1);
@@ -142,9 +166,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&sh->s_full[i]), 1);
       mbar_init(smem_u32(&sh->p_full[i]), 4);
-      mbar_init(smem_u32(&sh->o_free[i]), 4);
     }
     mbar_init(smem_u32(&sh->o_done), 1);
+    mbar_init(smem_u32(&sh->o_free), 4);
     mbar_init(smem_u32(&sh->drain), 1);
     sh->abort = 0;
     fence_mbar_init();
@@ -170,9 +194,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t g = 0, it_n = 0;
       int q_last = -1, k_last[NK] = {-1, -1}, v_last[NV] = {-1, -1};
       bool ok = true;
-      for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
-        Item it;
-        if (!load_item(p, idx, it)) continue;
+      Item it;
+      for (int idx = blockIdx.x; ok && next_item(p, idx, total_items, it); idx += gridDim.x) {
+        // The shared-memory Q buffer is free once the previous item's Q is in TMEM.
         if (it_n > 0 && !(ok = mbar_wait(smem_u32(&sh->q_empty), (it_n - 1) & 1, status, abort_flag))) break;
         const uint32_t qf = smem_u32(&sh->q_full);
         mbar_expect_tx(qf, Q_BYTES);
@@ -216,29 +240,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       uint32_t g = 0, it_n = 0;
       bool ok = true;
-      const uint32_t q_s = smem_u32(smem + SMEM_Q);
-      for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
-        Item it;
-        if (!load_item(p, idx, it)) continue;
-        const uint32_t ob = it_n & 1;
-        if (!(ok = mbar_wait(smem_u32(&sh->q_full), it_n & 1, status, abort_flag))) break;
+      const uint32_t q_t = tmem + TM_Q;
+      const uint32_t o_t = tmem + TM_O;
+      Item it;
+      for (int idx = blockIdx.x; ok && next_item(p, idx, total_items, it); idx += gridDim.x) {
+        if (!(ok = mbar_wait(smem_u32(&sh->q_ready), it_n & 1, status, abort_flag))) break;
         tc_fence_after();
         // O += P_jj V_jj for the tile with global index gp (item-local jj).
         auto issue_pv = [&](uint32_t gp, int jj) -> bool {
           const uint32_t sb = gp & 1;
           if (!mbar_wait(smem_u32(&sh->p_full[sb]), (gp >> 1) & 1, status, abort_flag)) return false;
-          if (jj == 0 && it_n >= 2 &&
-              !mbar_wait(smem_u32(&sh->o_free[ob]), ((it_n >> 1) & 1) ^ 1, status, abort_flag))
+          // The previous item's epilogue must have read O before it is overwritten.
+          if (jj == 0 && it_n >= 1 &&
+              !mbar_wait(smem_u32(&sh->o_free), (it_n - 1) & 1, status, abort_flag))
             return false;
           const int vs = gp % NV;
           if (!mbar_wait(smem_u32(&sh->v_full[vs]), (gp / NV) & 1, status, abort_flag)) return false;
           tc_fence_after();
           const uint32_t v_s = smem_u32(smem + SMEM_V + vs * V_BYTES);
-          const uint32_t d = tmem + TM_O + ob * 128;
           const uint32_t pa = tmem + TM_S + sb * 128;
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
-            mma_f16_ts(d, pa + kk * 8, sdesc(v_s + kk * 2048, BLK, 1024), IDESC_PV, (jj > 0 || kk > 0));
+            mma_f16_ts(o_t, pa + kk * 8, sdesc(v_s + kk * 2048, BLK, 1024), IDESC_PV, (jj > 0 || kk > 0));
           tc_commit(smem_u32(&sh->v_empty[vs]));
           tc_commit(smem_u32(&sh->o_done));
           return true;
@@ -254,11 +277,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int kk = 0; kk < 12; ++kk) {
             const uint32_t off = (kk >> 2) * BLK + (kk & 3) * 32;
-            mma_f16_ss(d, sdesc(q_s + off, 16, 1024), sdesc(k_s + off, 16, 1024), IDESC_QK, kk > 0);
+            mma_f16_ts(d, q_t + kk * 8, sdesc(k_s + off, 16, 1024), IDESC_QK, kk > 0);
           }
           tc_commit(smem_u32(&sh->k_empty[ks]));
           tc_commit(smem_u32(&sh->s_full[sb]));
-          if (j == it.n_kv - 1) tc_commit(smem_u32(&sh->q_empty));
           if (j > 0) ok = issue_pv(gj - 1, j - 1);
         }
         if (ok) ok = issue_pv(g + it.n_kv - 1, it.n_kv - 1);
@@ -274,13 +296,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int q4 = warp & 3;                 // TMEM lane quarter
     const int row = q4 * 32 + lane;          // query row within the tile (= TMEM lane)
     const uint32_t lane_off = uint32_t(q4 * 32) << 16;
+    const float sl2 = p.scale_log2;
+    const float2 sl2v = make_float2(sl2, sl2);
     uint32_t g = 0, it_n = 0;
     bool ok = true;
-    for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
-      __syncwarp();  // rows that skipped the last epilogue rejoin before warp-collective work
-      Item it;
-      if (!load_item(p, idx, it)) continue;
-      const uint32_t ob = it_n & 1;
+
+    // Item n's Q row: shared memory (after its TMA) -> registers -> TMEM, then
+    // release the shared buffer and tell the MMA warp.
+    auto stage_q = [&](uint32_t n) -> bool {
+      if (!mbar_wait_warp(smem_u32(&sh->q_full), n & 1, status, abort_flag)) return false;
+      uint32_t v[96];
+      const uint8_t* qs = smem + SMEM_Q + row * 128;
+#pragma unroll
+      for (int j = 0; j < 24; ++j) {
+        const uint4 x = *reinterpret_cast<const uint4*>(qs + (j >> 3) * BLK + (((j & 7) ^ (row & 7)) << 4));
+        v[4 * j] = x.x; v[4 * j + 1] = x.y; v[4 * j + 2] = x.z; v[4 * j + 3] = x.w;
+      }
+      tmem_st32(tmem + lane_off + TM_Q, v);
+      tmem_st32(tmem + lane_off + TM_Q + 32, v + 32);
+      tmem_st32(tmem + lane_off + TM_Q + 64, v + 64);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&sh->q_empty));
+        mbar_arrive(smem_u32(&sh->q_ready));
+      }
+      return true;
+    };
+
+    int idx = blockIdx.x;
+    Item it;
+    bool have = next_item(p, idx, total_items, it);
+    if (have) ok = stage_q(0);
+    while (have && ok) {
       const long long qpos = static_cast<long long>(it.cb) + it.i0 + row;
       // Relative key index kk is visible iff kk < lim_all.
       const long long lim_all = min(static_cast<long long>(it.n_cb), qpos - it.co + 1);
@@ -290,47 +339,49 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t sb = gj & 1;
         if (!(ok = mbar_wait_warp(smem_u32(&sh->s_full[sb]), (gj >> 1) & 1, status, abort_flag))) break;
         tc_fence_after();
+        // Raw scores of this row: four TMEM loads in flight, one wait.
         float x[BN];
-        {
-          uint32_t r[32];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            tmem_ld32(tmem + lane_off + TM_S + sb * 128 + c * 32, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(r[i]);
-          }
-        }
+        for (int c = 0; c < 4; ++c)
+          tmem_ld32(tmem + lane_off + TM_S + sb * 128 + c * 32,
+                    *reinterpret_cast<uint32_t(*)[32]>(reinterpret_cast<uint32_t*>(x) + c * 32));
+        tmem_ld_wait();
         const long long lim = lim_all - static_cast<long long>(j) * BN;
-        float mx = kNegInf;
         if (lim < BN) {
 #pragma unroll
-          for (int k = 0; k < BN; ++k) {
-            x[k] = k < lim ? x[k] * p.scale_log2 : kNegInf;
-            mx = fmaxf(mx, x[k]);
-          }
-        } else {
-#pragma unroll
-          for (int k = 0; k < BN; ++k) {
-            x[k] *= p.scale_log2;
-            mx = fmaxf(mx, x[k]);
-          }
+          for (int k = 0; k < BN; ++k) x[k] = k < lim ? x[k] : kNegInf;
         }
-        const float m_new = fmaxf(m_run, mx);
+        // Row maximum: 3-input max over 8 independent chains.
+        float mx8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = fmax3(x[i], x[8 + i], x[16 + i]);
+#pragma unroll
+        for (int k = 24; k < BN; k += 16)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], x[k + i], x[k + 8 + i]);
+        const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                               fmaxf(mx8[6], mx8[7]));
+        // Scores enter exp2 as s * scale*log2(e) - m (scale > 0, so the max
+        // commutes with the scaling).
+        const float m_new = fmaxf(m_run, mx * sl2);
         const bool need = m_new > m_run + kRescaleThreshold;
         const float f = need ? ex2(m_run - m_new) : 1.0f;   // m_run = -inf gives 0
         if (need) m_run = m_new;
         const float msub = m_run == kNegInf ? 0.f : m_run;
+        const float2 negm = make_float2(-msub, -msub);
         uint32_t pk[BN / 2];
-        float sum = 0.f;
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
 #pragma unroll
         for (int k = 0; k < BN / 2; ++k) {
-          const float p0 = ex2(x[2 * k] - msub);
-          const float p1 = ex2(x[2 * k + 1] - msub);
-          sum += p0 + p1;
-          pk[k] = pack_bf16(p0, p1);
+          const float2 t = __ffma2_rn(make_float2(x[2 * k], x[2 * k + 1]), sl2v, negm);
+          const float2 e = make_float2(ex2(t.x), ex2(t.y));
+          acc[k & 3] = __fadd2_rn(acc[k & 3], e);
+          pk[k] = pack_bf16(e.x, e.y);
         }
-        l_run = l_run * f + sum;
+        const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
+        const float2 a = __fadd2_rn(a01, a23);
+        l_run = l_run * f + (a.x + a.y);
         if (j == it.n_kv - 1 && it.n_cb - j * BN < BN) {
           // The last tile reaches past the sequence's keys: those V rows may hold
           // anything (even non-finite values), so zero them before P*V reads them.
@@ -359,7 +410,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t r[32];
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-              const uint32_t ta = tmem + lane_off + TM_O + ob * 128 + c * 32;
+              const uint32_t ta = tmem + lane_off + TM_O + c * 32;
               tmem_ld32(ta, r);
               tmem_ld_wait();
 #pragma unroll
@@ -375,37 +426,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       if (!ok) break;
       g += it.n_kv;
+      // All of this item's S MMAs are done (the last one was waited for), so
+      // its Q can be replaced: stage the next item's Q now, letting that
+      // item's first MMAs run under this epilogue.
+      int nidx = idx + gridDim.x;
+      Item nx;
+      const bool have_next = next_item(p, nidx, total_items, nx);
+      if (have_next && !(ok = stage_q(it_n + 1))) break;
       // ---------------------------------------------------------- epilogue
       if (!(ok = mbar_wait_warp(smem_u32(&sh->o_done), (g - 1) & 1, status, abort_flag))) break;
       tc_fence_after();
       float o[128];
-      {
-        uint32_t r[32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          tmem_ld32(tmem + lane_off + TM_O + ob * 128 + c * 32, r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[c * 32 + i] = __uint_as_float(r[i]);
-        }
-      }
+      for (int c = 0; c < 4; ++c)
+        tmem_ld32(tmem + lane_off + TM_O + c * 32,
+                  *reinterpret_cast<uint32_t(*)[32]>(reinterpret_cast<uint32_t*>(o) + c * 32));
+      tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh->o_free[ob]));
+      if (lane == 0) mbar_arrive(smem_u32(&sh->o_free));
+      const Item cur = it;
+      it = nx;
+      idx = nidx;
+      have = have_next;
       ++it_n;
-      if (row >= it.nq || qpos < it.co) continue;   // padding row, or finished in an earlier chunk
-      const bool first = it.co == 0;
-      const bool final_chunk = qpos < static_cast<long long>(it.co) + it.n_cb;
+      if (row >= cur.nq || qpos < cur.co) continue;   // padding row, or finished in an earlier chunk
+      const bool first = cur.co == 0;
+      const bool final_chunk = qpos < static_cast<long long>(cur.co) + cur.n_cb;
       // Without merge scratch (a one-chunk call) a row can only be finished
       // here; anything else means the plan overflowed max_chunks.
       if ((!first || !final_chunk) && (p.o_acc == nullptr || p.lse_acc == nullptr)) {
         set_status(status, MLA_DEV_TOO_MANY_CHUNKS);
         continue;
       }
-      const size_t t = static_cast<size_t>(it.q_row0 + row);
-      const size_t th = t * p.H + it.h;
-      float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
-      float lse_c = l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2 : kNegInf;
+      const size_t t = static_cast<size_t>(cur.q_row0 + row);
+      const size_t th = t * p.H + cur.h;
+      const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
+      const float lse_c = l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2 : kNegInf;
       float w_c = inv;     // weight of this chunk's unnormalised O
       float w_a = 0.f;     // weight of the running result
       float lse_tot = lse_c;
@@ -487,6 +544,9 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   p.B = a.B;
   p.H = a.H;
   p.n_qtiles = (a.max_prompt_len + BM - 1) / BM;
+  // Heads per group: about 32 MB of K_nope + V (S rows x 512 B per head) in L2.
+  p.head_group = static_cast<int>(std::max<uint64_t>(1, (32ull << 20) / (static_cast<uint64_t>(a.S) * 512)));
+  if (p.head_group > a.H) p.head_group = a.H;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.v_scale = a.v_scale;
   p.status = a.status;
