@@ -198,6 +198,44 @@ mla_status_t mla_prefill_attention(void* out, float* lse, float* o_acc, float* l
                                    int32_t dtype, int32_t* d_status, mla_stream_t stream);
 
 /*
+ * Prefill attention for one plan chunk without caller scratch.  The pages have
+ * no counterpart to this entry point.
+ *
+ * Same arguments and results as mla_prefill_attention, minus o_acc and lse_acc:
+ * the fp32 state carried from one chunk's call to the next lives in a fixed
+ * array inside this library (MLA_NOALLOC_MAX_ROWS rows of 129 floats, about
+ * 16.9 MB, held on every GPU that loads the library until the process exits).
+ * It exists for callers that cannot allocate device memory: code running
+ * inside a host framework that owns the whole device memory pool and offers no
+ * allocator, and loops that must not call cudaMalloc because it synchronises
+ * the device.  This function allocates nothing and calls no allocating routine.
+ *
+ * - total_q_tokens * num_heads must be <= MLA_NOALLOC_MAX_ROWS; larger calls
+ *   return MLA_ERR_WORKSPACE (use mla_prefill_attention with caller scratch).
+ * - The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.  Failure of the lookup returns MLA_ERR_LAUNCH.
+ * - All calls share the one array and it keeps the last call's contents.  A
+ *   multi-chunk sequence of calls (chunk 0, 1, ...) relies on that; calls from
+ *   different sequences that overlap on the GPU (other streams, other threads)
+ *   race on the array.  Nothing in it needs to start at zero.
+ */
+#define MLA_NOALLOC_MAX_ROWS 32768
+mla_status_t mla_prefill_attention_noalloc(void* out, float* lse, const void* q,
+                                           const void* k_nope, const void* v, const void* k_rope,
+                                           const uint32_t* input_row_offsets,
+                                           const uint32_t* cache_lengths,
+                                           const uint32_t* buffer_row_offsets,
+                                           const uint32_t* cache_offsets,
+                                           const int32_t* buffer_lengths, int32_t chunk,
+                                           int32_t max_chunks, int32_t batch_size,
+                                           int32_t num_heads, int32_t max_prompt_len,
+                                           int32_t total_q_tokens, uint32_t buffer_token_size,
+                                           float scale, float q_scale, float k_scale,
+                                           float v_scale, int32_t dtype, int32_t* d_status,
+                                           mla_stream_t stream);
+
+/*
  * Workspace bytes needed by mla_prefill for these sizes (plan tables, the
  * chunk's latent, k_rope, K and V buffers, and the fp32 merge state when
  * max_chunks > 1).

@@ -46,6 +46,9 @@ SIGNATURES = {
     "mla_upproject": (_I, [_P, _P, _P, _P, _P, _P, _I, _U, _I, _I, _F, _F, _F, _P]),
     "mla_prefill_attention": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                    _I, _I, _I, _I, _I, _I, _U, _F, _F, _F, _F, _I, _P, _P]),
+    "mla_prefill_attention_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                           _I, _I, _I, _I, _I, _I, _U, _F, _F, _F, _F, _I, _P,
+                                           _P]),
     "mla_prefill_workspace_bytes": (_Z, [_I, _I, _I, _I, _U, _I]),
     "mla_prefill": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _I, _I, _I, _U, _I,
                          _F, _F, _F, _F, _I, _P, _Z, _P, _P]),
@@ -139,6 +142,26 @@ def mla_prefill_attention(out, lse, o_acc, lse_acc, q, k_nope, v, k_rope, input_
     return load().mla_prefill_attention(
         _ptr(out), _ptr(lse), _ptr(o_acc), _ptr(lse_acc), _ptr(q), _ptr(k_nope), _ptr(v),
         _ptr(k_rope), _ptr(input_row_offsets), _ptr(cache_lengths), _ptr(buffer_row_offsets),
+        _ptr(cache_offsets), _ptr(buffer_lengths), chunk, max_chunks, batch_size, num_heads,
+        max_prompt_len, total_q_tokens, buffer_token_size, scale, q_scale, k_scale, v_scale,
+        dtype, _ptr(d_status), _stream(stream))
+
+
+MLA_NOALLOC_MAX_ROWS = 32768
+
+
+def mla_prefill_attention_noalloc(out, lse, q, k_nope, v, k_rope, input_row_offsets,
+                                  cache_lengths, buffer_row_offsets, cache_offsets,
+                                  buffer_lengths, chunk, max_chunks, batch_size, num_heads,
+                                  max_prompt_len, total_q_tokens, buffer_token_size, scale,
+                                  q_scale=1.0, k_scale=1.0, v_scale=1.0, dtype=MLA_BF16,
+                                  d_status=None, stream=None) -> int:
+    """mla_prefill_attention without caller scratch: the cross-chunk merge
+    state lives in a fixed array inside the library, for callers that cannot
+    allocate device memory.  See include/mla_prefill.h for the limits."""
+    return load().mla_prefill_attention_noalloc(
+        _ptr(out), _ptr(lse), _ptr(q), _ptr(k_nope), _ptr(v), _ptr(k_rope),
+        _ptr(input_row_offsets), _ptr(cache_lengths), _ptr(buffer_row_offsets),
         _ptr(cache_offsets), _ptr(buffer_lengths), chunk, max_chunks, batch_size, num_heads,
         max_prompt_len, total_q_tokens, buffer_token_size, scale, q_scale, k_scale, v_scale,
         dtype, _ptr(d_status), _stream(stream))
