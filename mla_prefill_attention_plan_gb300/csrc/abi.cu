@@ -196,7 +196,6 @@ static mla_status_t attention_impl(void* out, float* lse, float* o_acc, float* l
     return MLA_ERR_ARG;
   if (max_chunks > 1 && (!o_acc || !lse_acc || !aligned16(o_acc))) return MLA_ERR_ARG;
   if (T_q == 0 || max_prompt_len == 0) return MLA_OK;
-  if (dtype != MLA_BF16) return MLA_ERR_DTYPE;
   AttnArgs a;
   a.out = out;
   a.lse = lse;
