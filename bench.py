@@ -31,9 +31,10 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-# ncu traffic per attention launch for the default workload, from the committed
-# profile summary (None until a capture of the current kernel exists).
-ATTN_DRAM_BYTES_PER_LAUNCH = {}
+# DRAM bytes (read + write) per attention launch from one ncu capture of the
+# current kernel (profiles/attn_kernel_v3_prefill.md); absent for workloads
+# without a capture.
+ATTN_DRAM_BYTES_PER_LAUNCH = {"v3_prefill": 493_838_848 + 119_783_680}
 
 
 def _args():
@@ -46,6 +47,9 @@ def _args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
+    ap.add_argument("--stage", default=None, choices=["plan", "gather"],
+                    help="time one HBM-bound stage alone on its stress shape")
+    ap.add_argument("--batch", type=int, default=None, help="sequences for --stage")
     return ap.parse_args()
 
 
@@ -406,8 +410,93 @@ def run_ours(a):
         dist.destroy_process_group()
 
 
+def run_stage(a):
+    """One HBM-bound stage alone on a stress shape, L2 flushed before every
+    timed launch (a 512 MB write), CUDA events around each launch."""
+    import numpy as np
+    import torch
+    import mla_prefill_attention_plan_gb300 as mla
+    from mla_prefill_attention_plan_gb300 import build as B
+    B.build()
+    mla.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    peaks, src = _peaks()
+    rng = np.random.default_rng(0)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    if a.stage == "plan":
+        Bsz = a.batch or (1 << 22)
+        mc = 4
+        new = rng.integers(0, 64, Bsz)
+        cache = rng.integers(0, 64, Bsz)
+        S = int(-(-int((new + cache).sum()) // mc))
+        iro = torch.as_tensor(np.concatenate([[0], np.cumsum(new)]).astype(np.int32), device=dev)
+        cl = torch.as_tensor(cache.astype(np.int32), device=dev)
+        bro = torch.empty(mc, Bsz + 1, dtype=torch.int32, device=dev)
+        co = torch.empty(mc, Bsz, dtype=torch.int32, device=dev)
+        bl = torch.empty(mc, dtype=torch.int32, device=dev)
+        nbytes = 4 * (2 * Bsz + 1) + 4 * mc * (2 * Bsz + 2)
+        launch = lambda: mla.check(mla.mla_prefill_plan(bro, co, bl, iro, cl, Bsz, mc, S, st, stream))
+        kernels = "plan_tile_sums + plan_tile_write + row-0 memset" if Bsz > 4096 else "plan_one_cta"
+        desc = {"workload": "plan_stress", "B": Bsz, "max_chunks": mc, "buffer_token_size": S,
+                "new_tokens": "U[0,63]", "cache_tokens": "U[0,63]"}
+    else:
+        Bsz = a.batch or 64
+        L = 8192
+        ps = 128
+        pages = Bsz * L // ps
+        perm = torch.as_tensor(rng.permutation(pages).astype(np.int32), device=dev)
+        pt = perm.view(Bsz, L // ps)
+        kv = torch.randn(pages, ps, 576, device=dev).to(torch.bfloat16)
+        S = Bsz * L
+        iro = torch.zeros(Bsz + 1, dtype=torch.int32, device=dev)
+        cl = torch.full((Bsz,), L, dtype=torch.int32, device=dev)
+        bro = torch.empty(1, Bsz + 1, dtype=torch.int32, device=dev)
+        co = torch.empty(1, Bsz, dtype=torch.int32, device=dev)
+        bl = torch.empty(1, dtype=torch.int32, device=dev)
+        mla.check(mla.mla_prefill_plan(bro, co, bl, iro, cl, Bsz, 1, S, st, stream))
+        ckv = torch.empty(S, 512, dtype=torch.bfloat16, device=dev)
+        kr = torch.empty(S, 64, dtype=torch.bfloat16, device=dev)
+        nbytes = 2 * S * 576 * 2 + 4 * Bsz * (L // ps)
+        launch = lambda: mla.check(mla.mla_gather_latent(ckv, kr, kv, pt, pages, ps, L // ps, bro, co,
+                                                         bl, 0, Bsz, S, mla.MLA_BF16, st, stream))
+        kernels = "gather_kernel<2>"
+        desc = {"workload": "gather_stress", "B": Bsz, "cached_tokens_per_seq": L, "page_size": ps,
+                "pages": "shuffled", "dtype": "bf16"}
+    for _ in range(max(3, a.warmup)):
+        launch()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(a.steps):
+        flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        launch()
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    assert st.item() == 0, mla.status_string(int(st.item()))
+    ms = statistics.median(times)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peak = peaks["hbm_gbs"]
+    line = {"metric": f"{a.stage} algorithmic GB/s", "value": gbs, "unit": "GB/s", "n_gpus": 1,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms, "ms_min": min(times),
+            "higher_is_better": True, "dtype": "int32" if a.stage == "plan" else "bf16",
+            "data": "synthetic", "config": dict(desc, l2="flushed before every timed launch"),
+            "roofline": {"bound": "hbm", "kernel": kernels, "achieved": gbs, "peak": peak,
+                         "unit": "GB/s", "frac": gbs / peak, "traffic": None,
+                         "peak_source": f"{src} copy bandwidth (burst)",
+                         "algorithmic_bytes": nbytes}}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     a = _args()
+    if a.stage is not None:
+        run_stage(a)
+        return
     if a.impl == "reference":
         run_reference(a)
     else:

@@ -7,10 +7,8 @@
 //   buffer_lengths[c]        = c*S < TOT ? min(S, TOT - c*S) : -1
 // so the whole plan is one prefix sum followed by independent writes.
 //
-// Small batches run in one CTA (warp-shuffle scan + a scan of warp totals).
-// Large batches run in two passes over many CTAs; the per-CTA totals of the
-// first pass are parked in row 0 of cache_offsets (which the plan defines to
-// be all zeros) and that row is cleared at the end.
+// Small batches run in one CTA (warp-shuffle scan + a scan of warp totals);
+// large batches run in three passes over tiles (described below).
 #include "kernels.cuh"
 
 namespace mla {
@@ -18,8 +16,7 @@ namespace mla {
 namespace {
 
 constexpr int kThreads = 1024;
-constexpr int kItems = 4;                    // sequences per thread in the multi-CTA pass
-constexpr int kTile = kThreads * kItems;     // sequences per CTA in the multi-CTA pass
+constexpr int kOneCtaMax = 4096;             // largest batch planned by a single CTA
 
 __device__ __forceinline__ uint64_t clamp_u64(int64_t v, int64_t hi) {
   return static_cast<uint64_t>(v < 0 ? 0 : (v > hi ? hi : v));
@@ -117,62 +114,126 @@ __global__ void __launch_bounds__(kThreads) plan_one_cta(uint32_t* bro, uint32_t
   write_tail(bro, bl, B, max_chunks, S, carry, s_bad, status);
 }
 
-// Pass 1 of the multi-CTA plan: per-CTA totals into cache_offsets row 0.
-__global__ void __launch_bounds__(kThreads) plan_tile_sums(uint32_t* co_row0, const uint32_t* iro,
-                                                           const uint32_t* cache_len, int B) {
-  __shared__ uint64_t warp_tot[32];
-  int bad = 0;
-  uint64_t v = 0;
-  const int base = blockIdx.x * kTile;
-#pragma unroll
-  for (int k = 0; k < kItems; ++k) {
-    const int b = base + k * kThreads + threadIdx.x;
-    if (b < B) v += ctx_len(iro, cache_len, b, bad);
-  }
-  uint64_t total;
-  block_scan(v, warp_tot, total);
-  // Totals fit in 32 bits whenever the whole batch is below 2^31 tokens (larger
-  // batches are rejected by pass 2); saturate so an oversize tile still shows.
-  if (threadIdx.x == 0) co_row0[blockIdx.x] = total > 0xFFFFFFFFull ? 0xFFFFFFFFu : uint32_t(total);
+// Large batches: three passes over tiles of 4096 sequences (256 threads, each
+// lane of a warp owning 16 sequences strided by 32, so every load and store of
+// a warp is one coalesced 128-byte access).
+//   pass 1  per-tile total of the context lengths, parked in the tile's own
+//           first entry of cache_offsets row 0 (that row is zero by definition
+//           and is rewritten by pass 3);
+//   pass 2  one CTA turns the parked totals into exclusive tile prefixes in
+//           place and writes buffer_lengths, the [c][B] column and the status;
+//   pass 3  every tile reads its own prefix, scans its sequences with warp
+//           shuffles and writes its part of every table row (row 0 of
+//           cache_offsets comes out zero, overwriting the parked value).
+constexpr int kWThreads = 256;
+constexpr int kWPerLane = 16;
+constexpr int kWTile = kWThreads * kWPerLane;   // 4096
+
+__device__ __forceinline__ int tile_elem(int base, int warp, int lane, int k) {
+  return base + warp * (32 * kWPerLane) + k * 32 + lane;
 }
 
-// Pass 2: every CTA adds up the totals of the CTAs before it, scans its own
-// tile and writes every table entry except cache_offsets row 0.
-__global__ void __launch_bounds__(kThreads) plan_tile_write(uint32_t* bro, uint32_t* co, int32_t* bl,
-                                                            const uint32_t* iro,
-                                                            const uint32_t* cache_len, int B,
-                                                            int max_chunks, uint32_t S,
-                                                            int32_t* status) {
+__global__ void __launch_bounds__(kWThreads) plan_tile_sums(uint32_t* co_row0, const uint32_t* iro,
+                                                            const uint32_t* cache_len, int B) {
+  __shared__ uint64_t warp_sum[kWThreads / 32];
+  const int base = blockIdx.x * kWTile;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint64_t v = 0;
+#pragma unroll
+  for (int k = 0; k < kWPerLane; ++k) {
+    const int e = tile_elem(base, warp, lane, k);
+    if (e < B) v += cache_len[e];
+  }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) v += __shfl_down_sync(0xffffffffu, v, d);
+  if (lane == 0) warp_sum[warp] = v;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint64_t t = 0;
+    for (int w = 0; w < kWThreads / 32; ++w) t += warp_sum[w];
+    // New tokens of the tile telescope to a difference of two offsets (a
+    // decreasing pair is reported by pass 3; clamp so the sum stays sane).
+    const int end = min(base + kWTile, B);
+    const uint32_t a = iro[base], e = iro[end];
+    t += e >= a ? (e - a) : 0;
+    co_row0[base] = t > 0xFFFFFFFFull ? 0xFFFFFFFFu : static_cast<uint32_t>(t);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) plan_tile_scan(uint32_t* bro, uint32_t* co_row0,
+                                                           int32_t* bl, const uint32_t* iro, int B,
+                                                           int max_chunks, uint32_t S,
+                                                           int32_t* status) {
   __shared__ uint64_t warp_tot[32];
-  __shared__ int s_bad;
-  const int ntiles = gridDim.x;
-  // Sum of the tile totals before this CTA, and of all of them.
-  uint64_t before = 0, all = 0;
-  for (int t = threadIdx.x; t < ntiles; t += kThreads) {
-    const uint64_t s = co[t];
-    all += s;
-    if (t < static_cast<int>(blockIdx.x)) before += s;
+  const int ntiles = (B + kWTile - 1) / kWTile;
+  uint64_t carry = 0;
+  for (int t0 = 0; t0 < ntiles; t0 += kThreads) {
+    const int t = t0 + threadIdx.x;
+    const uint64_t v = t < ntiles ? co_row0[static_cast<size_t>(t) * kWTile] : 0;
+    uint64_t round_total;
+    const uint64_t incl = block_scan(v, warp_tot, round_total);
+    if (t < ntiles) {
+      const uint64_t excl = carry + incl - v;
+      co_row0[static_cast<size_t>(t) * kWTile] = excl > 0xFFFFFFFFull ? 0xFFFFFFFFu : uint32_t(excl);
+    }
+    carry += round_total;
   }
-  uint64_t before_sum, all_sum;
-  block_scan(before, warp_tot, before_sum);
-  block_scan(all, warp_tot, all_sum);
-  if (threadIdx.x == 0) s_bad = iro[0] != 0 ? 1 : 0;
-  __syncthreads();
+  write_tail(bro, bl, B, max_chunks, S, carry, iro[0] != 0, status);
+}
+
+__global__ void __launch_bounds__(kWThreads) plan_tile_write(uint32_t* bro, uint32_t* co, const uint32_t* iro,
+                                                             const uint32_t* cache_len, int B,
+                                                             int max_chunks, uint32_t S,
+                                                             int32_t* status) {
+  __shared__ uint64_t warp_sum[kWThreads / 32];
+  __shared__ uint64_t tile_prefix;
+  const int base = blockIdx.x * kWTile;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) tile_prefix = co[base];   // parked by pass 2
+  uint32_t L[kWPerLane];
   int bad = 0;
-  uint64_t carry = before_sum;
-  const int base = blockIdx.x * kTile;
-  for (int k = 0; k < kItems; ++k) {
-    const int b = base + k * kThreads + threadIdx.x;
-    const uint64_t L = b < B ? ctx_len(iro, cache_len, b, bad) : 0;
-    uint64_t tile_total;
-    const uint64_t incl = block_scan(L, warp_tot, tile_total);
-    if (b < B) write_seq(bro, co, B, max_chunks, S, b, carry + incl - L, L, true);
-    carry += tile_total;
+  uint64_t mine = 0;
+#pragma unroll
+  for (int k = 0; k < kWPerLane; ++k) {
+    const int e = tile_elem(base, warp, lane, k);
+    uint32_t l = 0;
+    if (e < B) {
+      const uint32_t a = iro[e], n = iro[e + 1];
+      if (n < a) bad = 1;
+      l = cache_len[e] + (n >= a ? n - a : 0u);
+    }
+    L[k] = l;
+    mine += l;
   }
-  if (bad) atomicOr(&s_bad, 1);
-  __syncthreads();
-  if (blockIdx.x == 0) write_tail(bro, bl, B, max_chunks, S, all_sum, s_bad, status);
-  else if (s_bad && threadIdx.x == 0) set_status(status, MLA_DEV_BAD_OFFSETS);
+  uint64_t wsum = mine;
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, d);
+  if (lane == 0) warp_sum[warp] = wsum;
+  __syncthreads();   // also orders every read of the parked prefix before row 0 is rewritten
+  uint64_t carry = tile_prefix;
+  for (int w = 0; w < warp; ++w) carry += warp_sum[w];
+#pragma unroll
+  for (int k = 0; k < kWPerLane; ++k) {
+    const int e = tile_elem(base, warp, lane, k);
+    uint64_t incl = L[k];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const uint64_t n = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += n;
+    }
+    const uint64_t excl = carry + incl - L[k];
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+    if (e < B) {
+      for (int c = 0; c < max_chunks; ++c) {
+        const int64_t lo = static_cast<int64_t>(c) * S;
+        bro[static_cast<size_t>(c) * (B + 1) + e] =
+            static_cast<uint32_t>(clamp_u64(static_cast<int64_t>(excl) - lo, S));
+        co[static_cast<size_t>(c) * B + e] =
+            static_cast<uint32_t>(clamp_u64(lo - static_cast<int64_t>(excl), static_cast<int64_t>(L[k])));
+      }
+    }
+  }
+  if (bad) set_status(status, MLA_DEV_BAD_OFFSETS);
 }
 
 }  // namespace
@@ -180,19 +241,15 @@ __global__ void __launch_bounds__(kThreads) plan_tile_write(uint32_t* bro, uint3
 cudaError_t launch_plan(uint32_t* bro, uint32_t* co, int32_t* bl, const uint32_t* iro,
                         const uint32_t* cache_len, int B, int max_chunks, uint32_t S,
                         int32_t* status, cudaStream_t stream) {
-  if (B <= kTile) {
+  if (B <= kOneCtaMax) {
     plan_one_cta<<<1, kThreads, 0, stream>>>(bro, co, bl, iro, cache_len, B, max_chunks, S, status);
     return cudaGetLastError();
   }
-  const int ntiles = (B + kTile - 1) / kTile;
-  plan_tile_sums<<<ntiles, kThreads, 0, stream>>>(co, iro, cache_len, B);
-  plan_tile_write<<<ntiles, kThreads, 0, stream>>>(bro, co, bl, iro, cache_len, B, max_chunks, S,
-                                                   status);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  // Row 0 of cache_offsets is all zeros by definition (chunk 0 starts every
-  // sequence at position 0); it held the tile totals until now.
-  return cudaMemsetAsync(co, 0, sizeof(uint32_t) * static_cast<size_t>(B), stream);
+  const int ntiles = (B + kWTile - 1) / kWTile;
+  plan_tile_sums<<<ntiles, kWThreads, 0, stream>>>(co, iro, cache_len, B);
+  plan_tile_scan<<<1, kThreads, 0, stream>>>(bro, co, bl, iro, B, max_chunks, S, status);
+  plan_tile_write<<<ntiles, kWThreads, 0, stream>>>(bro, co, iro, cache_len, B, max_chunks, S, status);
+  return cudaGetLastError();
 }
 
 }  // namespace mla
