@@ -300,59 +300,69 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the loop and waits; one elected lane issues.
+    {
       uint32_t g = 0, it_n = 0;
       bool ok = true;
       const uint32_t q_t = tmem + TM_Q;
       const uint32_t o_t = tmem + TM_O;
       Item it;
       for (int idx = blockIdx.x; ok && next_item(p, idx, total_items, it); idx += gridDim.x) {
-        if (!(ok = mbar_wait(smem_u32(&sh->q_ready), it_n & 1, status, abort_flag))) break;
+        if (!(ok = mbar_wait_warp(smem_u32(&sh->q_ready), it_n & 1, status, abort_flag))) break;
         tc_fence_after();
         // O += P_jj V_jj for the tile with global index gp (item-local jj).
         auto issue_pv = [&](uint32_t gp, int jj) -> bool {
           const uint32_t sb = gp & 1;
-          if (!mbar_wait(smem_u32(&sh->p_full[sb]), (gp >> 1) & 1, status, abort_flag)) return false;
+          if (!mbar_wait_warp(smem_u32(&sh->p_full[sb]), (gp >> 1) & 1, status, abort_flag)) return false;
           // The previous item's epilogue must have read O before it is overwritten.
           if (jj == 0 && it_n >= 1 &&
-              !mbar_wait(smem_u32(&sh->o_free), (it_n - 1) & 1, status, abort_flag))
+              !mbar_wait_warp(smem_u32(&sh->o_free), (it_n - 1) & 1, status, abort_flag))
             return false;
           const int vs = gp % NV;
-          if (!mbar_wait(smem_u32(&sh->v_full[vs]), (gp / NV) & 1, status, abort_flag)) return false;
+          if (!mbar_wait_warp(smem_u32(&sh->v_full[vs]), (gp / NV) & 1, status, abort_flag)) return false;
           tc_fence_after();
-          const uint32_t v_s = smem_u32(smem + SMEM_V + vs * V_BYTES);
-          const uint32_t pa = tmem + TM_S + sb * 128;
+          if (elect_one()) {
+            const uint32_t v_s = smem_u32(smem + SMEM_V + vs * V_BYTES);
+            const uint32_t pa = tmem + TM_S + sb * 128;
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            mma_f16_ts(o_t, pa + kk * 8, sdesc(v_s + kk * 2048, BLK, 1024), IDESC_PV, (jj > 0 || kk > 0));
-          tc_commit(smem_u32(&sh->v_empty[vs]));
-          tc_commit(smem_u32(&sh->o_done));
+            for (int kk = 0; kk < BN / 16; ++kk)
+              mma_f16_ts(o_t, pa + kk * 8, sdesc(v_s + kk * 2048, BLK, 1024), IDESC_PV, (jj > 0 || kk > 0));
+            tc_commit(smem_u32(&sh->v_empty[vs]));
+            tc_commit(smem_u32(&sh->o_done));
+          }
+          __syncwarp();
           return true;
         };
         for (int j = 0; j < it.n_kv && ok; ++j) {
           const uint32_t gj = g + j;
           const uint32_t sb = gj & 1;
           const int ks = gj % NK;
-          if (!(ok = mbar_wait(smem_u32(&sh->k_full[ks]), (gj / NK) & 1, status, abort_flag))) break;
+          if (!(ok = mbar_wait_warp(smem_u32(&sh->k_full[ks]), (gj / NK) & 1, status, abort_flag))) break;
           tc_fence_after();
-          const uint32_t k_s = smem_u32(smem + SMEM_K + ks * K_BYTES);
-          const uint32_t d = tmem + TM_S + sb * 128;
+          if (elect_one()) {
+            const uint32_t k_s = smem_u32(smem + SMEM_K + ks * K_BYTES);
+            const uint32_t d = tmem + TM_S + sb * 128;
 #pragma unroll
-          for (int kk = 0; kk < 12; ++kk) {
-            const uint32_t off = (kk >> 2) * BLK + (kk & 3) * 32;
-            mma_f16_ts(d, q_t + kk * 8, sdesc(k_s + off, 16, 1024), IDESC_QK, kk > 0);
+            for (int kk = 0; kk < 12; ++kk) {
+              const uint32_t off = (kk >> 2) * BLK + (kk & 3) * 32;
+              mma_f16_ts(d, q_t + kk * 8, sdesc(k_s + off, 16, 1024), IDESC_QK, kk > 0);
+            }
+            tc_commit(smem_u32(&sh->k_empty[ks]));
+            tc_commit(smem_u32(&sh->s_full[sb]));
           }
-          tc_commit(smem_u32(&sh->k_empty[ks]));
-          tc_commit(smem_u32(&sh->s_full[sb]));
+          __syncwarp();
           if (j > 0) ok = issue_pv(gj - 1, j - 1);
         }
         if (ok) ok = issue_pv(g + it.n_kv - 1, it.n_kv - 1);
         g += it.n_kv;
         ++it_n;
       }
-      tc_commit(smem_u32(&sh->drain));
-      volatile int never = 0;
-      mbar_wait(smem_u32(&sh->drain), 0, status, &never);
+      if (elect_one()) {
+        tc_commit(smem_u32(&sh->drain));
+        volatile int never = 0;
+        mbar_wait(smem_u32(&sh->drain), 0, status, &never);
+      }
+      __syncwarp();
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
@@ -643,58 +653,68 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the loop and waits; one elected lane issues.
+    {
       uint32_t g = 0, it_n = 0;
       bool ok = true;
       const uint32_t q_s = smem_u32(smem + F8_SMEM_Q);
       const uint32_t o_t = tmem + TM_O;
       Item it;
       for (int idx = blockIdx.x; ok && next_item(p, idx, total_items, it); idx += gridDim.x) {
-        if (!(ok = mbar_wait(smem_u32(&sh->q_full), it_n & 1, status, abort_flag))) break;
+        if (!(ok = mbar_wait_warp(smem_u32(&sh->q_full), it_n & 1, status, abort_flag))) break;
         tc_fence_after();
         // O += P_jj V_jj; p_full also means the f16 copy of V_jj is in place.
         auto issue_pv = [&](uint32_t gp, int jj) -> bool {
           const uint32_t sb = gp & 1;
-          if (!mbar_wait(smem_u32(&sh->p_full[sb]), (gp >> 1) & 1, status, abort_flag)) return false;
+          if (!mbar_wait_warp(smem_u32(&sh->p_full[sb]), (gp >> 1) & 1, status, abort_flag)) return false;
           if (jj == 0 && it_n >= 1 &&
-              !mbar_wait(smem_u32(&sh->o_free), (it_n - 1) & 1, status, abort_flag))
+              !mbar_wait_warp(smem_u32(&sh->o_free), (it_n - 1) & 1, status, abort_flag))
             return false;
           tc_fence_after();
-          const uint32_t v_s = smem_u32(smem + F8_SMEM_V16 + (gp % NV) * V16_BYTES);
-          const uint32_t pa = tmem + TM_S + sb * 128;
+          if (elect_one()) {
+            const uint32_t v_s = smem_u32(smem + F8_SMEM_V16 + (gp % NV) * V16_BYTES);
+            const uint32_t pa = tmem + TM_S + sb * 128;
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            mma_f16_ts(o_t, pa + kk * 8, sdesc(v_s + kk * 2048, BLK, 1024), IDESC_PV16, (jj > 0 || kk > 0));
-          tc_commit(smem_u32(&sh->o_done));
+            for (int kk = 0; kk < BN / 16; ++kk)
+              mma_f16_ts(o_t, pa + kk * 8, sdesc(v_s + kk * 2048, BLK, 1024), IDESC_PV16, (jj > 0 || kk > 0));
+            tc_commit(smem_u32(&sh->o_done));
+          }
+          __syncwarp();
           return true;
         };
         for (int j = 0; j < it.n_kv && ok; ++j) {
           const uint32_t gj = g + j;
           const uint32_t sb = gj & 1;
           const int ks = gj % NK;
-          if (!(ok = mbar_wait(smem_u32(&sh->k_full[ks]), (gj / NK) & 1, status, abort_flag))) break;
+          if (!(ok = mbar_wait_warp(smem_u32(&sh->k_full[ks]), (gj / NK) & 1, status, abort_flag))) break;
           tc_fence_after();
-          const uint32_t k_s = smem_u32(smem + F8_SMEM_K + ks * K8_BYTES);
-          const uint32_t d = tmem + TM_S + sb * 128;
+          if (elect_one()) {
+            const uint32_t k_s = smem_u32(smem + F8_SMEM_K + ks * K8_BYTES);
+            const uint32_t d = tmem + TM_S + sb * 128;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)   // nope: 128 B per row, 32 e4m3 per MMA
-            mma_f8_ss(d, sdesc(q_s + kk * 32, 16, 1024), sdesc(k_s + kk * 32, 16, 1024), IDESC_QK8, kk > 0);
+            for (int kk = 0; kk < 4; ++kk)   // nope: 128 B per row, 32 e4m3 per MMA
+              mma_f8_ss(d, sdesc(q_s + kk * 32, 16, 1024), sdesc(k_s + kk * 32, 16, 1024), IDESC_QK8, kk > 0);
 #pragma unroll
-          for (int kk = 0; kk < 2; ++kk)   // rope: 64 B per row
-            mma_f8_ss(d, sdesc(q_s + Q8_NOPE + kk * 32, 16, 512, kSwizzle64),
-                      sdesc(k_s + Q8_NOPE + kk * 32, 16, 512, kSwizzle64), IDESC_QK8, 1);
-          tc_commit(smem_u32(&sh->k_empty[ks]));
-          tc_commit(smem_u32(&sh->s_full[sb]));
-          if (j == it.n_kv - 1) tc_commit(smem_u32(&sh->q_empty));
+            for (int kk = 0; kk < 2; ++kk)   // rope: 64 B per row
+              mma_f8_ss(d, sdesc(q_s + Q8_NOPE + kk * 32, 16, 512, kSwizzle64),
+                        sdesc(k_s + Q8_NOPE + kk * 32, 16, 512, kSwizzle64), IDESC_QK8, 1);
+            tc_commit(smem_u32(&sh->k_empty[ks]));
+            tc_commit(smem_u32(&sh->s_full[sb]));
+            if (j == it.n_kv - 1) tc_commit(smem_u32(&sh->q_empty));
+          }
+          __syncwarp();
           if (j > 0) ok = issue_pv(gj - 1, j - 1);
         }
         if (ok) ok = issue_pv(g + it.n_kv - 1, it.n_kv - 1);
         g += it.n_kv;
         ++it_n;
       }
-      tc_commit(smem_u32(&sh->drain));
-      volatile int never = 0;
-      mbar_wait(smem_u32(&sh->drain), 0, status, &never);
+      if (elect_one()) {
+        tc_commit(smem_u32(&sh->drain));
+        volatile int never = 0;
+        mbar_wait(smem_u32(&sh->drain), 0, status, &never);
+      }
+      __syncwarp();
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue

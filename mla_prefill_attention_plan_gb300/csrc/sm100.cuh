@@ -86,6 +86,17 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, in
   return __all_sync(0xffffffffu, ok);
 }
 
+// One lane of a converged warp (elect.sync).  Issuing tcgen05.mma from an
+// elected lane of a warp that runs the loop together keeps the descriptors on
+// the uniform datapath; a lone lane in a divergent branch issues far slower.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.b32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
