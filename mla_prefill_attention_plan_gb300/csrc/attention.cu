@@ -8,9 +8,10 @@
 // per SM) stride over the items: heads in groups (so the CTAs in flight share
 // a few heads' K/V in L2), heaviest query tiles first within a group.
 //
-//   warp 0      TMA producer: the Q tile (3 x 16 KB) into shared memory, K
-//               tiles (nope 2 x 16 KB + rope 16 KB) and V tiles (2 x 16 KB),
-//               all 128-byte swizzled, into 2-stage K and V rings.
+//   warp 0      TMA producer of the Q tile (3 x 16 KB) and the K tiles (nope
+//               2 x 16 KB + rope 16 KB), 128-byte swizzled, 2-stage K ring.
+//   warp 6      TMA producer of the V tiles (2 x 16 KB), 2-stage V ring; kept
+//               apart from K so K tiles run ahead of the V stages' release.
 //   warp 1      TMEM owner (512 columns) and single-thread MMA issuer:
 //                 S_j = Q K_j^T   M=128 queries, N=128 keys, K=192 as 12 MMAs;
 //                                 A = Q read from tensor memory, B = K (K-major)
@@ -46,7 +47,7 @@ constexpr int SMEM_K = SMEM_Q + Q_BYTES;
 constexpr int SMEM_V = SMEM_K + NK * K_BYTES;
 constexpr int SMEM_BAR = SMEM_V + NV * V_BYTES;   // 212992
 constexpr int SMEM_TOTAL = SMEM_BAR + 256 + 1024;
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 224;   // 7 warps: Q/K producer, MMA, 4 softmax, V producer
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_S = 0;      // S/P buffers: columns 0..127, 128..255
 constexpr uint32_t TM_O = 256;    // O: columns 256..383
@@ -63,7 +64,7 @@ struct Smem {
   uint64_t k_full[NK], k_empty[NK];
   uint64_t v_full[NV], v_empty[NV];
   uint64_t s_full[2], p_full[2];
-  uint64_t o_done, o_free;
+  uint64_t o_done[2], o_free;   // o_done[t & 1] completes when P*V of tile t does
   uint64_t drain;
   uint32_t tmem;
   int abort;
@@ -230,7 +231,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(smem_u32(&sh->s_full[i]), 1);
       mbar_init(smem_u32(&sh->p_full[i]), 4);
     }
-    mbar_init(smem_u32(&sh->o_done), 1);
+    mbar_init(smem_u32(&sh->o_done[0]), 1);
+    mbar_init(smem_u32(&sh->o_done[1]), 1);
     mbar_init(smem_u32(&sh->o_free), 4);
     mbar_init(smem_u32(&sh->drain), 1);
     sh->abort = 0;
@@ -248,59 +250,95 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   int32_t* status = p.status;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    // ------------------------------------------------------------ Q and K producer
+    // The whole warp runs the loop and waits; one elected lane issues copies.
+    if (elect_one()) {
       prefetch_tmap(&q_map);
       prefetch_tmap(&kn_map);
       prefetch_tmap(&kr_map);
-      prefetch_tmap(&v_map);
-      uint32_t g = 0, it_n = 0;
-      int q_last = -1, k_last[NK] = {-1, -1}, v_last[NV] = {-1, -1};
-      bool ok = true;
-      Item it;
-      for (int idx = blockIdx.x; ok && next_item(p, idx, total_items, it); idx += gridDim.x) {
-        // The shared-memory Q buffer is free once the previous item's Q is in TMEM.
-        if (it_n > 0 && !(ok = mbar_wait(smem_u32(&sh->q_empty), (it_n - 1) & 1, status, abort_flag))) break;
+    }
+    __syncwarp();
+    uint32_t g = 0, it_n = 0;
+    int q_last = -1, k_last[NK] = {-1, -1};
+    bool ok = true;
+    Item it;
+    for (int idx = blockIdx.x; ok && next_item(p, idx, total_items, it); idx += gridDim.x) {
+      // The shared-memory Q buffer is free once the previous item's Q is in TMEM.
+      if (it_n > 0 && !(ok = mbar_wait_warp(smem_u32(&sh->q_empty), (it_n - 1) & 1, status, abort_flag))) break;
+      if (elect_one()) {
         const uint32_t qf = smem_u32(&sh->q_full);
         mbar_expect_tx(qf, Q_BYTES);
         for (int blk = 0; blk < 3; ++blk)
           tma_load_2d(smem_u32(smem + SMEM_Q + blk * BLK), &q_map, qf, it.h * 192 + blk * 64, it.q_row0);
-        q_last = int(it_n & 1);
-        for (int j = 0; j < it.n_kv; ++j) {
-          const uint32_t gj = g + j;
-          const int row = it.kv_row0 + j * BN;
-          const int ks = gj % NK;
-          if (!(ok = mbar_wait(smem_u32(&sh->k_empty[ks]), ((gj / NK) & 1) ^ 1, status, abort_flag))) break;
+      }
+      __syncwarp();
+      q_last = int(it_n & 1);
+      for (int j = 0; j < it.n_kv; ++j) {
+        const uint32_t gj = g + j;
+        const int row = it.kv_row0 + j * BN;
+        const int ks = gj % NK;
+        // K stage ks is free once S_{gj-2} (same stage, same S buffer) has
+        // completed: s_full[ks] doubles as the stage's release.
+        if (gj >= NK && !(ok = mbar_wait_warp(smem_u32(&sh->s_full[ks]), ((gj - NK) / NK) & 1, status, abort_flag))) break;
+        if (elect_one()) {
           const uint32_t kf = smem_u32(&sh->k_full[ks]);
           mbar_expect_tx(kf, K_BYTES);
           const uint32_t kdst = smem_u32(smem + SMEM_K + ks * K_BYTES);
           tma_load_2d(kdst, &kn_map, kf, it.h * 128, row);
           tma_load_2d(kdst + BLK, &kn_map, kf, it.h * 128 + 64, row);
           tma_load_2d(kdst + 2 * BLK, &kr_map, kf, 0, row);
-          k_last[ks] = int((gj / NK) & 1);
-          const int vs = gj % NV;
-          if (!(ok = mbar_wait(smem_u32(&sh->v_empty[vs]), ((gj / NV) & 1) ^ 1, status, abort_flag))) break;
+        }
+        __syncwarp();
+        k_last[ks] = int((gj / NK) & 1);
+      }
+      g += it.n_kv;
+      ++it_n;
+    }
+    // Drain: every issued load lands before the CTA exits.
+    volatile int never = 0;
+    if (q_last >= 0) mbar_wait_warp(smem_u32(&sh->q_full), uint32_t(q_last), status, &never);
+    for (int s = 0; s < NK; ++s)
+      if (k_last[s] >= 0) mbar_wait_warp(smem_u32(&sh->k_full[s]), uint32_t(k_last[s]), status, &never);
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ V producer
+    // Separate from K so that K tiles run ahead of the V stages' release.
+    if (elect_one()) prefetch_tmap(&v_map);
+    __syncwarp();
+    uint32_t g = 0;
+    int v_last[NV] = {-1, -1};
+    bool ok = true;
+    Item it;
+    for (int idx = blockIdx.x; ok && next_item(p, idx, total_items, it); idx += gridDim.x) {
+      for (int j = 0; j < it.n_kv; ++j) {
+        const uint32_t gj = g + j;
+        const int row = it.kv_row0 + j * BN;
+        const int vs = gj % NV;
+        // V stage vs is free once P*V of tile gj-2 (same stage) has completed.
+        // o_done[gj & 1] completes once per P*V of that parity; a P*V two
+        // ahead on it would need this very V tile, so it cannot run ahead.
+        if (gj >= NV && !(ok = mbar_wait_warp(smem_u32(&sh->o_done[gj & 1]), ((gj - NV) >> 1) & 1, status, abort_flag))) break;
+        if (elect_one()) {
           const uint32_t vf = smem_u32(&sh->v_full[vs]);
           mbar_expect_tx(vf, V_BYTES);
           const uint32_t vdst = smem_u32(smem + SMEM_V + vs * V_BYTES);
           tma_load_2d(vdst, &v_map, vf, it.h * 128, row);
           tma_load_2d(vdst + BLK, &v_map, vf, it.h * 128 + 64, row);
-          v_last[vs] = int((gj / NV) & 1);
         }
-        g += it.n_kv;
-        ++it_n;
+        __syncwarp();
+        v_last[vs] = int((gj / NV) & 1);
       }
-      // Drain: every issued load lands before the CTA exits.
-      volatile int never = 0;
-      if (q_last >= 0) mbar_wait(smem_u32(&sh->q_full), uint32_t(q_last), status, &never);
-      for (int s = 0; s < NK; ++s)
-        if (k_last[s] >= 0) mbar_wait(smem_u32(&sh->k_full[s]), uint32_t(k_last[s]), status, &never);
-      for (int s = 0; s < NV; ++s)
-        if (v_last[s] >= 0) mbar_wait(smem_u32(&sh->v_full[s]), uint32_t(v_last[s]), status, &never);
+      g += it.n_kv;
     }
+    volatile int never = 0;
+    for (int s = 0; s < NV; ++s)
+      if (v_last[s] >= 0) mbar_wait_warp(smem_u32(&sh->v_full[s]), uint32_t(v_last[s]), status, &never);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // The whole warp runs the loop and waits; one elected lane issues.
+    // The whole warp runs the loop; one elected lane (lane 0) issues.  The
+    // tensor pipe queues only a few MMAs, so any pause between two groups of
+    // MMAs is a bubble: while the elected lane issues a group it already
+    // probes (non-blocking) the barriers the next group depends on, and the
+    // warp blocks on a barrier only when that probe found it incomplete.
     {
       uint32_t g = 0, it_n = 0;
       bool ok = true;
@@ -309,52 +347,76 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       Item it;
       for (int idx = blockIdx.x; ok && next_item(p, idx, total_items, it); idx += gridDim.x) {
         if (!(ok = mbar_wait_warp(smem_u32(&sh->q_ready), it_n & 1, status, abort_flag))) break;
-        tc_fence_after();
-        // O += P_jj V_jj for the tile with global index gp (item-local jj).
-        auto issue_pv = [&](uint32_t gp, int jj) -> bool {
-          const uint32_t sb = gp & 1;
-          if (!mbar_wait_warp(smem_u32(&sh->p_full[sb]), (gp >> 1) & 1, status, abort_flag)) return false;
-          // The previous item's epilogue must have read O before it is overwritten.
-          if (jj == 0 && it_n >= 1 &&
-              !mbar_wait_warp(smem_u32(&sh->o_free), (it_n - 1) & 1, status, abort_flag))
-            return false;
-          const int vs = gp % NV;
-          if (!mbar_wait_warp(smem_u32(&sh->v_full[vs]), (gp / NV) & 1, status, abort_flag)) return false;
-          tc_fence_after();
-          if (elect_one()) {
-            const uint32_t v_s = smem_u32(smem + SMEM_V + vs * V_BYTES);
-            const uint32_t pa = tmem + TM_S + sb * 128;
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-              mma_f16_ts(o_t, pa + kk * 8, sdesc(v_s + kk * 2048, BLK, 1024), IDESC_PV, (jj > 0 || kk > 0));
-            tc_commit(smem_u32(&sh->v_empty[vs]));
-            tc_commit(smem_u32(&sh->o_done));
-          }
-          __syncwarp();
-          return true;
-        };
-        for (int j = 0; j < it.n_kv && ok; ++j) {
+        const int n = it.n_kv;
+        // S_j = Q K_j^T into S buffer j % 2 (it last held P_{j-2}, whose P*V
+        // was issued earlier; tcgen05 MMAs execute in issue order).  While
+        // issuing, probe what P_pj * V_pj needs; returns that probe's result.
+        auto issue_s = [&](int j, int pj, bool& ready) -> bool {
           const uint32_t gj = g + j;
-          const uint32_t sb = gj & 1;
           const int ks = gj % NK;
-          if (!(ok = mbar_wait_warp(smem_u32(&sh->k_full[ks]), (gj / NK) & 1, status, abort_flag))) break;
+          if (!ready && !mbar_wait_warp(smem_u32(&sh->k_full[ks]), (gj / NK) & 1, status, abort_flag)) return false;
           tc_fence_after();
+          uint32_t next_ready = 0;
           if (elect_one()) {
             const uint32_t k_s = smem_u32(smem + SMEM_K + ks * K_BYTES);
-            const uint32_t d = tmem + TM_S + sb * 128;
+            const uint32_t d = tmem + TM_S + (gj & 1) * 128;
 #pragma unroll
             for (int kk = 0; kk < 12; ++kk) {
               const uint32_t off = (kk >> 2) * BLK + (kk & 3) * 32;
               mma_f16_ts(d, q_t + kk * 8, sdesc(k_s + off, 16, 1024), IDESC_QK, kk > 0);
+              if (kk == 5 && pj >= 0) {
+                const uint32_t gp = g + pj;
+                next_ready = mbar_test(smem_u32(&sh->p_full[gp & 1]), (gp >> 1) & 1) &&
+                             mbar_test(smem_u32(&sh->v_full[gp % NV]), (gp / NV) & 1);
+              }
             }
-            tc_commit(smem_u32(&sh->k_empty[ks]));
-            tc_commit(smem_u32(&sh->s_full[sb]));
+            tc_commit(smem_u32(&sh->s_full[gj & 1]));
           }
-          __syncwarp();
-          if (j > 0) ok = issue_pv(gj - 1, j - 1);
+          ready = __shfl_sync(0xffffffffu, next_ready, 0) != 0;
+          return true;
+        };
+        // O += P_j V_j; while issuing, probe K_{sj} for the S that follows.
+        auto issue_pv = [&](int j, int sj, bool& ready) -> bool {
+          const uint32_t gp = g + j;
+          const int vs = gp % NV;
+          if (!ready) {
+            if (!mbar_wait_warp(smem_u32(&sh->p_full[gp & 1]), (gp >> 1) & 1, status, abort_flag)) return false;
+            if (!mbar_wait_warp(smem_u32(&sh->v_full[vs]), (gp / NV) & 1, status, abort_flag)) return false;
+          }
+          // The previous item's epilogue must have read O before it is overwritten.
+          if (j == 0 && it_n >= 1 &&
+              !mbar_wait_warp(smem_u32(&sh->o_free), (it_n - 1) & 1, status, abort_flag))
+            return false;
+          tc_fence_after();
+          uint32_t next_ready = 0;
+          if (elect_one()) {
+            const uint32_t v_s = smem_u32(smem + SMEM_V + vs * V_BYTES);
+            const uint32_t pa = tmem + TM_S + (gp & 1) * 128;
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk) {
+              mma_f16_ts(o_t, pa + kk * 8, sdesc(v_s + kk * 2048, BLK, 1024), IDESC_PV, (j > 0 || kk > 0));
+              if (kk == 3 && sj >= 0) {
+                const uint32_t gs = g + sj;
+                next_ready = mbar_test(smem_u32(&sh->k_full[gs % NK]), (gs / NK) & 1);
+              }
+            }
+            tc_commit(smem_u32(&sh->o_done[gp & 1]));
+          }
+          ready = __shfl_sync(0xffffffffu, next_ready, 0) != 0;
+          return true;
+        };
+        // Two S tiles ahead; then each P_j*V_j as soon as P_j is ready,
+        // followed by S_{j+2}.
+        bool ready = false;
+        ok = issue_s(0, -1, ready);
+        ready = false;
+        if (ok && n > 1) ok = issue_s(1, 0, ready);
+        for (int j = 0; j < n && ok; ++j) {
+          const int sj = j + 2 < n ? j + 2 : -1;
+          ok = issue_pv(j, sj, ready);
+          if (ok && sj >= 0) ok = issue_s(sj, j + 1 < n ? j + 1 : -1, ready);
         }
-        if (ok) ok = issue_pv(g + it.n_kv - 1, it.n_kv - 1);
-        g += it.n_kv;
+        g += n;
         ++it_n;
       }
       if (elect_one()) {
@@ -364,7 +426,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       __syncwarp();
     }
-  } else {
+  } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------ softmax + epilogue
     const int q4 = warp & 3;                 // TMEM lane quarter
     const int row = q4 * 32 + lane;          // query row within the tile (= TMEM lane)
@@ -477,7 +539,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // phase behind from two).  P*V of the previous tile was issued before
           // this tile's softmax began, so this rarely waits.  Then, if the row
           // maximum grew by more than 2^8, rescale O in TMEM before P_j*V_j.
-          if (!(ok = mbar_wait_warp(smem_u32(&sh->o_done), (gj - 1) & 1, status, abort_flag))) break;
+          if (!(ok = mbar_wait_warp(smem_u32(&sh->o_done[(gj - 1) & 1]), ((gj - 1) >> 1) & 1, status, abort_flag))) break;
           if (__any_sync(0xffffffffu, need)) {
             tc_fence_after();
             uint32_t r[32];
@@ -507,7 +569,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const bool have_next = next_item(p, nidx, total_items, nx);
       if (have_next && !(ok = stage_q(it_n + 1))) break;
       // ---------------------------------------------------------- epilogue
-      if (!(ok = mbar_wait_warp(smem_u32(&sh->o_done), (g - 1) & 1, status, abort_flag))) break;
+      if (!(ok = mbar_wait_warp(smem_u32(&sh->o_done[(g - 1) & 1]), ((g - 1) >> 1) & 1, status, abort_flag))) break;
       tc_fence_after();
       float o[128];
 #pragma unroll
@@ -587,7 +649,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(smem_u32(&sh->s_full[i]), 1);
       mbar_init(smem_u32(&sh->p_full[i]), 4);
     }
-    mbar_init(smem_u32(&sh->o_done), 1);
+    mbar_init(smem_u32(&sh->o_done[0]), 1);
+    mbar_init(smem_u32(&sh->o_done[1]), 1);
     mbar_init(smem_u32(&sh->o_free), 4);
     mbar_init(smem_u32(&sh->drain), 1);
     sh->abort = 0;
@@ -605,52 +668,77 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   int32_t* status = p.status;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    // ------------------------------------------------------------ Q and K producer
+    if (elect_one()) {
       prefetch_tmap(&qn_map);
       prefetch_tmap(&qr_map);
       prefetch_tmap(&kn_map);
       prefetch_tmap(&kr_map);
-      prefetch_tmap(&v_map);
-      uint32_t g = 0, it_n = 0;
-      int q_last = -1, k_last[NK] = {-1, -1}, v_last[NV] = {-1, -1};
-      bool ok = true;
-      Item it;
-      for (int idx = blockIdx.x; ok && next_item(p, idx, total_items, it); idx += gridDim.x) {
-        if (it_n > 0 && !(ok = mbar_wait(smem_u32(&sh->q_empty), (it_n - 1) & 1, status, abort_flag))) break;
+    }
+    __syncwarp();
+    uint32_t g = 0, it_n = 0;
+    int q_last = -1, k_last[NK] = {-1, -1};
+    bool ok = true;
+    Item it;
+    for (int idx = blockIdx.x; ok && next_item(p, idx, total_items, it); idx += gridDim.x) {
+      if (it_n > 0 && !(ok = mbar_wait_warp(smem_u32(&sh->q_empty), (it_n - 1) & 1, status, abort_flag))) break;
+      if (elect_one()) {
         const uint32_t qf = smem_u32(&sh->q_full);
         mbar_expect_tx(qf, Q8_BYTES);
         tma_load_2d(smem_u32(smem + F8_SMEM_Q), &qn_map, qf, it.h * 192, it.q_row0);
         tma_load_2d(smem_u32(smem + F8_SMEM_Q + Q8_NOPE), &qr_map, qf, it.h * 192 + 128, it.q_row0);
-        q_last = int(it_n & 1);
-        for (int j = 0; j < it.n_kv; ++j) {
-          const uint32_t gj = g + j;
-          const int row = it.kv_row0 + j * BN;
-          const int ks = gj % NK;
-          if (!(ok = mbar_wait(smem_u32(&sh->k_empty[ks]), ((gj / NK) & 1) ^ 1, status, abort_flag))) break;
+      }
+      __syncwarp();
+      q_last = int(it_n & 1);
+      for (int j = 0; j < it.n_kv; ++j) {
+        const uint32_t gj = g + j;
+        const int row = it.kv_row0 + j * BN;
+        const int ks = gj % NK;
+        if (!(ok = mbar_wait_warp(smem_u32(&sh->k_empty[ks]), ((gj / NK) & 1) ^ 1, status, abort_flag))) break;
+        if (elect_one()) {
           const uint32_t kf = smem_u32(&sh->k_full[ks]);
           mbar_expect_tx(kf, K8_BYTES);
           const uint32_t kdst = smem_u32(smem + F8_SMEM_K + ks * K8_BYTES);
           tma_load_2d(kdst, &kn_map, kf, it.h * 128, row);
           tma_load_2d(kdst + Q8_NOPE, &kr_map, kf, 0, row);
-          k_last[ks] = int((gj / NK) & 1);
-          const int vs = gj % NV;
-          if (!(ok = mbar_wait(smem_u32(&sh->v_empty[vs]), ((gj / NV) & 1) ^ 1, status, abort_flag))) break;
+        }
+        __syncwarp();
+        k_last[ks] = int((gj / NK) & 1);
+      }
+      g += it.n_kv;
+      ++it_n;
+    }
+    volatile int never = 0;
+    if (q_last >= 0) mbar_wait_warp(smem_u32(&sh->q_full), uint32_t(q_last), status, &never);
+    for (int s = 0; s < NK; ++s)
+      if (k_last[s] >= 0) mbar_wait_warp(smem_u32(&sh->k_full[s]), uint32_t(k_last[s]), status, &never);
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ V producer (e4m3 tiles)
+    if (elect_one()) prefetch_tmap(&v_map);
+    __syncwarp();
+    uint32_t g = 0;
+    int v_last[NV] = {-1, -1};
+    bool ok = true;
+    Item it;
+    for (int idx = blockIdx.x; ok && next_item(p, idx, total_items, it); idx += gridDim.x) {
+      for (int j = 0; j < it.n_kv; ++j) {
+        const uint32_t gj = g + j;
+        const int row = it.kv_row0 + j * BN;
+        const int vs = gj % NV;
+        if (!(ok = mbar_wait_warp(smem_u32(&sh->v_empty[vs]), ((gj / NV) & 1) ^ 1, status, abort_flag))) break;
+        if (elect_one()) {
           const uint32_t vf = smem_u32(&sh->v_full[vs]);
           mbar_expect_tx(vf, V8_BYTES);
           tma_load_2d(smem_u32(smem + F8_SMEM_V8 + vs * V8_BYTES), &v_map, vf, it.h * 128, row);
-          v_last[vs] = int((gj / NV) & 1);
         }
-        g += it.n_kv;
-        ++it_n;
+        __syncwarp();
+        v_last[vs] = int((gj / NV) & 1);
       }
-      volatile int never = 0;
-      if (q_last >= 0) mbar_wait(smem_u32(&sh->q_full), uint32_t(q_last), status, &never);
-      for (int s = 0; s < NK; ++s)
-        if (k_last[s] >= 0) mbar_wait(smem_u32(&sh->k_full[s]), uint32_t(k_last[s]), status, &never);
-      for (int s = 0; s < NV; ++s)
-        if (v_last[s] >= 0) mbar_wait(smem_u32(&sh->v_full[s]), uint32_t(v_last[s]), status, &never);
+      g += it.n_kv;
     }
+    volatile int never = 0;
+    for (int s = 0; s < NV; ++s)
+      if (v_last[s] >= 0) mbar_wait_warp(smem_u32(&sh->v_full[s]), uint32_t(v_last[s]), status, &never);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs the loop and waits; one elected lane issues.
@@ -677,16 +765,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk)
               mma_f16_ts(o_t, pa + kk * 8, sdesc(v_s + kk * 2048, BLK, 1024), IDESC_PV16, (jj > 0 || kk > 0));
-            tc_commit(smem_u32(&sh->o_done));
+            tc_commit(smem_u32(&sh->o_done[gp & 1]));
           }
           __syncwarp();
           return true;
         };
-        for (int j = 0; j < it.n_kv && ok; ++j) {
+        auto issue_s = [&](int j) -> bool {
           const uint32_t gj = g + j;
           const uint32_t sb = gj & 1;
           const int ks = gj % NK;
-          if (!(ok = mbar_wait_warp(smem_u32(&sh->k_full[ks]), (gj / NK) & 1, status, abort_flag))) break;
+          if (!mbar_wait_warp(smem_u32(&sh->k_full[ks]), (gj / NK) & 1, status, abort_flag)) return false;
           tc_fence_after();
           if (elect_one()) {
             const uint32_t k_s = smem_u32(smem + F8_SMEM_K + ks * K8_BYTES);
@@ -703,9 +791,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (j == it.n_kv - 1) tc_commit(smem_u32(&sh->q_empty));
           }
           __syncwarp();
-          if (j > 0) ok = issue_pv(gj - 1, j - 1);
+          return true;
+        };
+        ok = issue_s(0);
+        if (ok && it.n_kv > 1) ok = issue_s(1);
+        for (int j = 0; j < it.n_kv && ok; ++j) {
+          ok = issue_pv(g + j, j);
+          if (ok && j + 2 < it.n_kv) ok = issue_s(j + 2);
         }
-        if (ok) ok = issue_pv(g + it.n_kv - 1, it.n_kv - 1);
         g += it.n_kv;
         ++it_n;
       }
@@ -716,7 +809,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       __syncwarp();
     }
-  } else {
+  } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------ softmax + epilogue
     const int q4 = warp & 3;
     const int row = q4 * 32 + lane;          // query row (TMEM lane), and key row for V widening
@@ -808,7 +901,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tmem_st32(tmem + lane_off + TM_S + sb * 128, pk);
         tmem_st32(tmem + lane_off + TM_S + sb * 128 + 32, pk + 32);
         if (j > 0) {
-          if (!(ok = mbar_wait_warp(smem_u32(&sh->o_done), (gj - 1) & 1, status, abort_flag))) break;
+          if (!(ok = mbar_wait_warp(smem_u32(&sh->o_done[(gj - 1) & 1]), ((gj - 1) >> 1) & 1, status, abort_flag))) break;
           if (__any_sync(0xffffffffu, need)) {
             tc_fence_after();
             uint32_t r[32];
@@ -830,7 +923,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       if (!ok) break;
       g += it.n_kv;
-      if (!(ok = mbar_wait_warp(smem_u32(&sh->o_done), (g - 1) & 1, status, abort_flag))) break;
+      if (!(ok = mbar_wait_warp(smem_u32(&sh->o_done[(g - 1) & 1]), ((g - 1) >> 1) & 1, status, abort_flag))) break;
       tc_fence_after();
       float o[128];
 #pragma unroll

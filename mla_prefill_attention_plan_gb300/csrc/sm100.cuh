@@ -57,6 +57,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return done != 0;
 }
+// Non-blocking check that the phase of parity `parity` has completed.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
 // Wait for the phase of parity `parity` to complete.  False on timeout (the
 // timeout is recorded in *status and in the CTA's abort flag).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* status,
