@@ -284,9 +284,12 @@ def run_ours(a):
             mla.check(mla.mla_gather_latent(ckv, krope, d["kv_cache"], d["page_table"],
                                             inp["num_pages"], inp["page_size"], inp["max_pages"],
                                             bro, co, bl, ch, Bsz, S, dt, status, stream))
+            if ev is not None:
+                ev[ch][2].record(stream)
             mla.check(mla.mla_upproject(knope, vbuf, ckv, d["w_k"], d["w_uv"], bl, ch, S, H, dt,
                                         inp["ckv_scale"], inp["w_scale"], kv_inv, stream))
             if ev is not None:
+                ev[ch][3].record(stream)
                 ev[ch][0].record(stream)
             mla.check(mla.mla_prefill_attention(out, lse, oacc, lacc, d["q"], knope, vbuf, krope,
                                                 d["input_row_offsets"], d["cache_lengths"], bro, co,
@@ -301,7 +304,7 @@ def run_ours(a):
     torch.cuda.synchronize()
     assert status.item() == 0, mla.status_string(int(status.item()))
 
-    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)]
             for _ in range(mc)] for _ in range(a.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
@@ -327,6 +330,7 @@ def run_ours(a):
     attn_ms = sum(evs[k][ch][0].elapsed_time(evs[k][ch][1]) for k in range(a.steps) for ch in range(mc))
     used_chunks = int((bl >= 0).sum().item())
     attn_ms_per_launch = attn_ms / (a.steps * max(used_chunks, 1))
+    up_ms = sum(evs[k][ch][2].elapsed_time(evs[k][ch][3]) for k in range(a.steps) for ch in range(mc))
     assert status.item() == 0, mla.status_string(int(status.item()))
 
     # End to end through the fused entry point: pinned host inputs copied in,
@@ -392,6 +396,8 @@ def run_ours(a):
         "config": dict(_config(w, inp), parallelism=f"replicas{world}" if world > 1 else "single"),
         "attn_tflops": achieved,
         "attn_ms_per_launch": attn_ms_per_launch,
+        "upproj_tflops": up_flops / (up_ms / a.steps * 1e-3) / 1e12,
+        "upproj_ms_per_step": up_ms / a.steps,
         "step_flops": {"attention": attn_flops, "upproject": up_flops, "visible_pairs": pairs},
         "roofline": {"bound": "tensor", "kernel": "attn_kernel", "achieved": achieved,
                      "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,

@@ -334,98 +334,71 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (v_last[s] >= 0) mbar_wait_warp(smem_u32(&sh->v_full[s]), uint32_t(v_last[s]), status, &never);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // The whole warp runs the loop; one elected lane (lane 0) issues.  The
-    // tensor pipe queues only a few MMAs, so any pause between two groups of
-    // MMAs is a bubble: while the elected lane issues a group it already
-    // probes (non-blocking) the barriers the next group depends on, and the
-    // warp blocks on a barrier only when that probe found it incomplete.
-    {
+    // One elected lane runs the whole loop, waits included, and the warp
+    // reconverges only at the end.  Reconverging a warp whose lane has MMAs in
+    // flight stalls it until most of them have executed, and a wait that then
+    // follows leaves the tensor pipe idle; a lone elected lane goes straight
+    // from one MMA group to the next wait and back.
+    if (elect_one()) {
       uint32_t g = 0, it_n = 0;
-      bool ok = true;
       const uint32_t q_t = tmem + TM_Q;
       const uint32_t o_t = tmem + TM_O;
       Item it;
-      for (int idx = blockIdx.x; ok && next_item(p, idx, total_items, it); idx += gridDim.x) {
-        if (!(ok = mbar_wait_warp(smem_u32(&sh->q_ready), it_n & 1, status, abort_flag))) break;
+      for (int idx = blockIdx.x; next_item(p, idx, total_items, it); idx += gridDim.x) {
+        if (!mbar_wait(smem_u32(&sh->q_ready), it_n & 1, status, abort_flag)) break;
         const int n = it.n_kv;
         // S_j = Q K_j^T into S buffer j % 2 (it last held P_{j-2}, whose P*V
-        // was issued earlier; tcgen05 MMAs execute in issue order).  While
-        // issuing, probe what P_pj * V_pj needs; returns that probe's result.
-        auto issue_s = [&](int j, int pj, bool& ready) -> bool {
+        // was issued earlier; tcgen05 MMAs execute in issue order).
+        auto issue_s = [&](int j) -> bool {
           const uint32_t gj = g + j;
           const int ks = gj % NK;
-          if (!ready && !mbar_wait_warp(smem_u32(&sh->k_full[ks]), (gj / NK) & 1, status, abort_flag)) return false;
+          if (!mbar_wait(smem_u32(&sh->k_full[ks]), (gj / NK) & 1, status, abort_flag)) return false;
           tc_fence_after();
-          uint32_t next_ready = 0;
-          if (elect_one()) {
-            const uint32_t k_s = smem_u32(smem + SMEM_K + ks * K_BYTES);
-            const uint32_t d = tmem + TM_S + (gj & 1) * 128;
+          const uint32_t k_s = smem_u32(smem + SMEM_K + ks * K_BYTES);
+          const uint32_t d = tmem + TM_S + (gj & 1) * 128;
 #pragma unroll
-            for (int kk = 0; kk < 12; ++kk) {
-              const uint32_t off = (kk >> 2) * BLK + (kk & 3) * 32;
-              mma_f16_ts(d, q_t + kk * 8, sdesc(k_s + off, 16, 1024), IDESC_QK, kk > 0);
-              if (kk == 5 && pj >= 0) {
-                const uint32_t gp = g + pj;
-                next_ready = mbar_test(smem_u32(&sh->p_full[gp & 1]), (gp >> 1) & 1) &&
-                             mbar_test(smem_u32(&sh->v_full[gp % NV]), (gp / NV) & 1);
-              }
-            }
-            tc_commit(smem_u32(&sh->s_full[gj & 1]));
+          for (int kk = 0; kk < 12; ++kk) {
+            const uint32_t off = (kk >> 2) * BLK + (kk & 3) * 32;
+            mma_f16_ts(d, q_t + kk * 8, sdesc(k_s + off, 16, 1024), IDESC_QK, kk > 0);
           }
-          ready = __shfl_sync(0xffffffffu, next_ready, 0) != 0;
+          tc_commit(smem_u32(&sh->s_full[gj & 1]));
           return true;
         };
-        // O += P_j V_j; while issuing, probe K_{sj} for the S that follows.
-        auto issue_pv = [&](int j, int sj, bool& ready) -> bool {
+        // O += P_j V_j.
+        auto issue_pv = [&](int j) -> bool {
           const uint32_t gp = g + j;
           const int vs = gp % NV;
-          if (!ready) {
-            if (!mbar_wait_warp(smem_u32(&sh->p_full[gp & 1]), (gp >> 1) & 1, status, abort_flag)) return false;
-            if (!mbar_wait_warp(smem_u32(&sh->v_full[vs]), (gp / NV) & 1, status, abort_flag)) return false;
-          }
+          if (!mbar_wait(smem_u32(&sh->p_full[gp & 1]), (gp >> 1) & 1, status, abort_flag)) return false;
+          if (!mbar_wait(smem_u32(&sh->v_full[vs]), (gp / NV) & 1, status, abort_flag)) return false;
           // The previous item's epilogue must have read O before it is overwritten.
-          if (j == 0 && it_n >= 1 &&
-              !mbar_wait_warp(smem_u32(&sh->o_free), (it_n - 1) & 1, status, abort_flag))
+          if (j == 0 && it_n >= 1 && !mbar_wait(smem_u32(&sh->o_free), (it_n - 1) & 1, status, abort_flag))
             return false;
           tc_fence_after();
-          uint32_t next_ready = 0;
-          if (elect_one()) {
-            const uint32_t v_s = smem_u32(smem + SMEM_V + vs * V_BYTES);
-            const uint32_t pa = tmem + TM_S + (gp & 1) * 128;
+          const uint32_t v_s = smem_u32(smem + SMEM_V + vs * V_BYTES);
+          const uint32_t pa = tmem + TM_S + (gp & 1) * 128;
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk) {
-              mma_f16_ts(o_t, pa + kk * 8, sdesc(v_s + kk * 2048, BLK, 1024), IDESC_PV, (j > 0 || kk > 0));
-              if (kk == 3 && sj >= 0) {
-                const uint32_t gs = g + sj;
-                next_ready = mbar_test(smem_u32(&sh->k_full[gs % NK]), (gs / NK) & 1);
-              }
-            }
-            tc_commit(smem_u32(&sh->o_done[gp & 1]));
-          }
-          ready = __shfl_sync(0xffffffffu, next_ready, 0) != 0;
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_f16_ts(o_t, pa + kk * 8, sdesc(v_s + kk * 2048, BLK, 1024), IDESC_PV, (j > 0 || kk > 0));
+          tc_commit(smem_u32(&sh->o_done[gp & 1]));
           return true;
         };
         // Two S tiles ahead; then each P_j*V_j as soon as P_j is ready,
         // followed by S_{j+2}.
-        bool ready = false;
-        ok = issue_s(0, -1, ready);
-        ready = false;
-        if (ok && n > 1) ok = issue_s(1, 0, ready);
+        bool ok = issue_s(0);
+        if (ok && n > 1) ok = issue_s(1);
         for (int j = 0; j < n && ok; ++j) {
-          const int sj = j + 2 < n ? j + 2 : -1;
-          ok = issue_pv(j, sj, ready);
-          if (ok && sj >= 0) ok = issue_s(sj, j + 1 < n ? j + 1 : -1, ready);
+          ok = issue_pv(j);
+          if (ok && j + 2 < n) ok = issue_s(j + 2);
         }
+        if (!ok) break;
         g += n;
         ++it_n;
       }
-      if (elect_one()) {
-        tc_commit(smem_u32(&sh->drain));
-        volatile int never = 0;
-        mbar_wait(smem_u32(&sh->drain), 0, status, &never);
-      }
-      __syncwarp();
+      tc_commit(smem_u32(&sh->drain));
+      volatile int never = 0;
+      mbar_wait(smem_u32(&sh->drain), 0, status, &never);
     }
+    __syncwarp();
   } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------ softmax + epilogue
     const int q4 = warp & 3;                 // TMEM lane quarter
@@ -741,56 +714,50 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (v_last[s] >= 0) mbar_wait_warp(smem_u32(&sh->v_full[s]), uint32_t(v_last[s]), status, &never);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // The whole warp runs the loop and waits; one elected lane issues.
-    {
+    // One elected lane runs the whole loop, waits included (as in the bf16
+    // kernel: the warp reconverges only at the end).
+    if (elect_one()) {
       uint32_t g = 0, it_n = 0;
       bool ok = true;
       const uint32_t q_s = smem_u32(smem + F8_SMEM_Q);
       const uint32_t o_t = tmem + TM_O;
       Item it;
       for (int idx = blockIdx.x; ok && next_item(p, idx, total_items, it); idx += gridDim.x) {
-        if (!(ok = mbar_wait_warp(smem_u32(&sh->q_full), it_n & 1, status, abort_flag))) break;
+        if (!(ok = mbar_wait(smem_u32(&sh->q_full), it_n & 1, status, abort_flag))) break;
         tc_fence_after();
         // O += P_jj V_jj; p_full also means the f16 copy of V_jj is in place.
         auto issue_pv = [&](uint32_t gp, int jj) -> bool {
           const uint32_t sb = gp & 1;
-          if (!mbar_wait_warp(smem_u32(&sh->p_full[sb]), (gp >> 1) & 1, status, abort_flag)) return false;
-          if (jj == 0 && it_n >= 1 &&
-              !mbar_wait_warp(smem_u32(&sh->o_free), (it_n - 1) & 1, status, abort_flag))
+          if (!mbar_wait(smem_u32(&sh->p_full[sb]), (gp >> 1) & 1, status, abort_flag)) return false;
+          if (jj == 0 && it_n >= 1 && !mbar_wait(smem_u32(&sh->o_free), (it_n - 1) & 1, status, abort_flag))
             return false;
           tc_fence_after();
-          if (elect_one()) {
-            const uint32_t v_s = smem_u32(smem + F8_SMEM_V16 + (gp % NV) * V16_BYTES);
-            const uint32_t pa = tmem + TM_S + sb * 128;
+          const uint32_t v_s = smem_u32(smem + F8_SMEM_V16 + (gp % NV) * V16_BYTES);
+          const uint32_t pa = tmem + TM_S + sb * 128;
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-              mma_f16_ts(o_t, pa + kk * 8, sdesc(v_s + kk * 2048, BLK, 1024), IDESC_PV16, (jj > 0 || kk > 0));
-            tc_commit(smem_u32(&sh->o_done[gp & 1]));
-          }
-          __syncwarp();
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_f16_ts(o_t, pa + kk * 8, sdesc(v_s + kk * 2048, BLK, 1024), IDESC_PV16, (jj > 0 || kk > 0));
+          tc_commit(smem_u32(&sh->o_done[gp & 1]));
           return true;
         };
         auto issue_s = [&](int j) -> bool {
           const uint32_t gj = g + j;
           const uint32_t sb = gj & 1;
           const int ks = gj % NK;
-          if (!mbar_wait_warp(smem_u32(&sh->k_full[ks]), (gj / NK) & 1, status, abort_flag)) return false;
+          if (!mbar_wait(smem_u32(&sh->k_full[ks]), (gj / NK) & 1, status, abort_flag)) return false;
           tc_fence_after();
-          if (elect_one()) {
-            const uint32_t k_s = smem_u32(smem + F8_SMEM_K + ks * K8_BYTES);
-            const uint32_t d = tmem + TM_S + sb * 128;
+          const uint32_t k_s = smem_u32(smem + F8_SMEM_K + ks * K8_BYTES);
+          const uint32_t d = tmem + TM_S + sb * 128;
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)   // nope: 128 B per row, 32 e4m3 per MMA
-              mma_f8_ss(d, sdesc(q_s + kk * 32, 16, 1024), sdesc(k_s + kk * 32, 16, 1024), IDESC_QK8, kk > 0);
+          for (int kk = 0; kk < 4; ++kk)   // nope: 128 B per row, 32 e4m3 per MMA
+            mma_f8_ss(d, sdesc(q_s + kk * 32, 16, 1024), sdesc(k_s + kk * 32, 16, 1024), IDESC_QK8, kk > 0);
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk)   // rope: 64 B per row
-              mma_f8_ss(d, sdesc(q_s + Q8_NOPE + kk * 32, 16, 512, kSwizzle64),
-                        sdesc(k_s + Q8_NOPE + kk * 32, 16, 512, kSwizzle64), IDESC_QK8, 1);
-            tc_commit(smem_u32(&sh->k_empty[ks]));
-            tc_commit(smem_u32(&sh->s_full[sb]));
-            if (j == it.n_kv - 1) tc_commit(smem_u32(&sh->q_empty));
-          }
-          __syncwarp();
+          for (int kk = 0; kk < 2; ++kk)   // rope: 64 B per row
+            mma_f8_ss(d, sdesc(q_s + Q8_NOPE + kk * 32, 16, 512, kSwizzle64),
+                      sdesc(k_s + Q8_NOPE + kk * 32, 16, 512, kSwizzle64), IDESC_QK8, 1);
+          tc_commit(smem_u32(&sh->k_empty[ks]));
+          tc_commit(smem_u32(&sh->s_full[sb]));
+          if (j == it.n_kv - 1) tc_commit(smem_u32(&sh->q_empty));
           return true;
         };
         ok = issue_s(0);
@@ -802,13 +769,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         g += it.n_kv;
         ++it_n;
       }
-      if (elect_one()) {
-        tc_commit(smem_u32(&sh->drain));
-        volatile int never = 0;
-        mbar_wait(smem_u32(&sh->drain), 0, status, &never);
-      }
-      __syncwarp();
+      tc_commit(smem_u32(&sh->drain));
+      volatile int never = 0;
+      mbar_wait(smem_u32(&sh->drain), 0, status, &never);
     }
+    __syncwarp();
   } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------ softmax + epilogue
     const int q4 = warp & 3;

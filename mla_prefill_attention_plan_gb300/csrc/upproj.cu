@@ -129,20 +129,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (last_ph[s] >= 0) mbar_wait(smem_u32(&sh->full[s]), uint32_t(last_ph[s]), status, &never);
     }
   } else if (warp == 1) {
-    // The whole warp runs the loop and waits; one elected lane issues.
-    int stage = 0;
-    uint32_t phase = 0;
-    int tl = 0;
-    bool ok = true;
-    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++tl) {
-      const int acc = tl & 1;
-      if (!(ok = mbar_wait_warp(smem_u32(&sh->tempty[acc]), ((tl >> 1) & 1) ^ 1, status, abort_flag))) break;
-      tc_fence_after();
-      const uint32_t d = tmem + acc * BN;
-      for (int kb = 0; kb < KB; ++kb) {
-        if (!(ok = mbar_wait_warp(smem_u32(&sh->full[stage]), phase, status, abort_flag))) break;
+    // One elected lane runs the whole loop, waits included; the warp
+    // reconverges only at the end (a warp that reconverges while its lane has
+    // MMAs in flight stalls until most of them have executed, and the next
+    // wait then leaves the tensor pipe idle).
+    if (elect_one()) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int tl = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++tl) {
+        const int acc = tl & 1;
+        if (!(ok = mbar_wait(smem_u32(&sh->tempty[acc]), ((tl >> 1) & 1) ^ 1, status, abort_flag))) break;
         tc_fence_after();
-        if (elect_one()) {
+        const uint32_t d = tmem + acc * BN;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!(ok = mbar_wait(smem_u32(&sh->full[stage]), phase, status, abort_flag))) break;
+          tc_fence_after();
           const uint32_t a = smem_u32(smem + SMEM_A + stage * A_BYTES);
           const uint32_t b = smem_u32(smem + SMEM_B + stage * B_BYTES);
 #pragma unroll
@@ -153,17 +156,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             else mma_f8_ss(d, ad, bd, IDESC, (kb | k) != 0);
           }
           tc_commit(smem_u32(&sh->empty[stage]));
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
-        __syncwarp();
-        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        if (ok) tc_commit(smem_u32(&sh->tfull[acc]));
       }
-      if (ok) {
-        if (elect_one()) tc_commit(smem_u32(&sh->tfull[acc]));
-        __syncwarp();
-      }
-    }
-    // Drain: every MMA issued so far completes before TMEM is released.
-    if (elect_one()) {
+      // Drain: every MMA issued so far completes before TMEM is released.
       tc_commit(smem_u32(&sh->drain));
       volatile int never = 0;
       mbar_wait(smem_u32(&sh->drain), 0, status, &never);
