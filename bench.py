@@ -34,7 +34,7 @@ sys.path.insert(0, ROOT)
 # DRAM bytes (read + write) per attention launch from one ncu capture of the
 # current kernel (profiles/attn_kernel_v3_prefill.md); absent for workloads
 # without a capture.
-ATTN_DRAM_BYTES_PER_LAUNCH = {}
+ATTN_DRAM_BYTES_PER_LAUNCH = {"v3_prefill": 496_654_592 + 119_747_840}
 
 
 def _args():
