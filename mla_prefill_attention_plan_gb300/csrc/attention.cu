@@ -30,13 +30,14 @@
 //
 // TMEM columns: S/P buffers 0..127 and 128..255, O 256..383, Q 384..479.
 #include <algorithm>
+#include <cstdlib>
+#include <cstring>
 
-#include "kernels.cuh"
+#include "attn_common.cuh"
 
 namespace mla {
 namespace {
 
-constexpr int BM = 128, BN = 128;
 constexpr int BLK = 128 * 128;                // one 128-row x 128-byte swizzled block
 constexpr int Q_BYTES = 3 * BLK;              // 192 bf16 columns
 constexpr int K_BYTES = 3 * BLK;              // nope 128 + rope 64
@@ -52,10 +53,6 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_S = 0;      // S/P buffers: columns 0..127, 128..255
 constexpr uint32_t TM_O = 256;    // O: columns 256..383
 constexpr uint32_t TM_Q = 384;    // Q (bf16 pairs): columns 384..479
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr float kLn2 = 0.693147180559945309f;
-constexpr float kNegInf = -__builtin_huge_valf();
-
 constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, false, false);
 constexpr uint32_t IDESC_PV = idesc_bf16(BM, 128, false, true);
 
@@ -71,35 +68,6 @@ struct Smem {
 };
 static_assert(sizeof(Smem) <= 256, "barrier block");
 
-struct Params {
-  __nv_bfloat16* out;
-  float* lse;
-  float* o_acc;
-  float* lse_acc;
-  const uint32_t* iro;
-  const uint32_t* cache_len;
-  const uint32_t* bro;
-  const uint32_t* co;
-  const int32_t* bl;
-  int chunk, B, H, n_qtiles, head_group;
-  float scale_log2;   // softmax scale * descales * log2(e)
-  float v_scale;
-  int32_t* status;
-};
-
-// One work item, as every role sees it.
-struct Item {
-  int b, h;
-  int i0;        // first query row (within the sequence) of the tile
-  int nq;        // valid query rows in the tile
-  int q_row0;    // first query row in q / out
-  int kv_row0;   // first buffer row of the sequence's keys in this chunk
-  int n_cb;      // keys of the sequence in this chunk
-  int co;        // context position of the first of those keys
-  int cb;        // cached tokens of the sequence
-  int n_kv;      // 128-key tiles to visit (0: nothing to do)
-};
-
 // Item order: heads in groups of `head_group`; within a group, query tiles
 // heaviest first, and the group's heads side by side.  The CTAs in flight then
 // share the K/V of a few heads in L2 instead of streaming every head's K/V.
@@ -110,27 +78,9 @@ __device__ __forceinline__ bool load_item(const Params& p, int idx, Item& it) {
   const int r = idx - grp * per_group;
   const int hg = min(p.head_group, p.H - grp * p.head_group);   // heads in this group
   const int pair = r / hg;
-  it.h = grp * p.head_group + (r - pair * hg);
+  const int h = grp * p.head_group + (r - pair * hg);
   const int qt = p.n_qtiles - 1 - pair / p.B;   // heaviest query tiles first
-  it.b = pair % p.B;
-  const uint32_t* bro_c = p.bro + static_cast<size_t>(p.chunk) * (p.B + 1);
-  const int r0 = static_cast<int>(bro_c[it.b]);
-  it.n_cb = static_cast<int>(bro_c[it.b + 1]) - r0;
-  const int q0 = static_cast<int>(p.iro[it.b]);
-  const int new_b = static_cast<int>(p.iro[it.b + 1]) - q0;
-  it.i0 = qt * BM;
-  if (it.n_cb <= 0 || it.i0 >= new_b) return false;
-  it.nq = min(BM, new_b - it.i0);
-  it.q_row0 = q0 + it.i0;
-  it.kv_row0 = r0;
-  it.co = static_cast<int>(p.co[static_cast<size_t>(p.chunk) * p.B + it.b]);
-  it.cb = static_cast<int>(p.cache_len[it.b]);
-  // Keys visible to the tile's last row: relative key index <= last.
-  const long long last = static_cast<long long>(it.cb) + it.i0 + it.nq - 1 - it.co;
-  if (last < 0) return false;
-  const long long nkeys = min(static_cast<long long>(it.n_cb), last + 1);
-  it.n_kv = static_cast<int>((nkeys + BN - 1) / BN);
-  return true;
+  return tile_item(p, pair % p.B, h, qt, it);
 }
 
 // First item with work at or after `idx` (stepping by the grid size).
@@ -138,69 +88,6 @@ __device__ __forceinline__ bool next_item(const Params& p, int& idx, int total, 
   for (; idx < total; idx += gridDim.x)
     if (load_item(p, idx, it)) return true;
   return false;
-}
-
-// Epilogue of one query row: O / l, this chunk's natural-log LSE, merge with
-// the running result of earlier chunks, then either the final bf16 row (the
-// chunk that holds the row's own position) or the fp32 running state.
-__device__ __forceinline__ void store_row(const Params& p, const Item& cur, int row, long long qpos,
-                                          float m_run, float l_run, const float (&o)[128]) {
-  if (row >= cur.nq || qpos < cur.co) return;   // padding row, or finished in an earlier chunk
-  const bool first = cur.co == 0;
-  const bool final_chunk = qpos < static_cast<long long>(cur.co) + cur.n_cb;
-  // Without merge scratch (a one-chunk call) a row can only be finished here;
-  // anything else means the plan overflowed max_chunks.
-  if ((!first || !final_chunk) && (p.o_acc == nullptr || p.lse_acc == nullptr)) {
-    set_status(p.status, MLA_DEV_TOO_MANY_CHUNKS);
-    return;
-  }
-  const size_t t = static_cast<size_t>(cur.q_row0 + row);
-  const size_t th = t * p.H + cur.h;
-  const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
-  const float lse_c = l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2 : kNegInf;
-  float w_c = inv;     // weight of this chunk's unnormalised O
-  float w_a = 0.f;     // weight of the running result
-  float lse_tot = lse_c;
-  if (!first) {
-    const float lse_a = p.lse_acc[th];
-    const float mm = fmaxf(lse_a, lse_c);
-    const float ea = __expf(lse_a - mm), ec = __expf(lse_c - mm);
-    const float tot = ea + ec;
-    w_a = ea / tot;
-    w_c = inv * (ec / tot);
-    lse_tot = mm + __logf(tot);
-  }
-  const float4* oa = first ? nullptr : reinterpret_cast<const float4*>(p.o_acc + th * 128);
-  if (final_chunk) {
-    uint4* dst = reinterpret_cast<uint4*>(p.out + th * 128);
-    const float vs = p.v_scale;
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      float y[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) y[i] = o[c * 8 + i] * w_c;
-      if (!first) {
-        const float4 a0 = oa[2 * c], a1 = oa[2 * c + 1];
-        y[0] += w_a * a0.x; y[1] += w_a * a0.y; y[2] += w_a * a0.z; y[3] += w_a * a0.w;
-        y[4] += w_a * a1.x; y[5] += w_a * a1.y; y[6] += w_a * a1.z; y[7] += w_a * a1.w;
-      }
-      dst[c] = make_uint4(pack_bf16(y[0] * vs, y[1] * vs), pack_bf16(y[2] * vs, y[3] * vs),
-                          pack_bf16(y[4] * vs, y[5] * vs), pack_bf16(y[6] * vs, y[7] * vs));
-    }
-    if (p.lse) p.lse[th] = lse_tot;
-  } else {
-    float4* dst = reinterpret_cast<float4*>(p.o_acc + th * 128);
-#pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      float4 y = make_float4(o[4 * c] * w_c, o[4 * c + 1] * w_c, o[4 * c + 2] * w_c, o[4 * c + 3] * w_c);
-      if (!first) {
-        const float4 a = oa[c];
-        y.x += w_a * a.x; y.y += w_a * a.y; y.z += w_a * a.z; y.w += w_a * a.w;
-      }
-      dst[c] = y;
-    }
-    p.lse_acc[th] = lse_tot;
-  }
 }
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -507,13 +394,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tmem_st32(tmem + lane_off + TM_S + sb * 128, pk);
         tmem_st32(tmem + lane_off + TM_S + sb * 128 + 32, pk + 32);
-        if (j > 0) {
-          // Observe every P*V completion in order (a parity wait cannot tell one
-          // phase behind from two).  P*V of the previous tile was issued before
-          // this tile's softmax began, so this rarely waits.  Then, if the row
-          // maximum grew by more than 2^8, rescale O in TMEM before P_j*V_j.
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+          // The row maximum grew by more than 2^8: rescale O in TMEM once P*V
+          // of the previous tile has completed, before P_j*V_j.  Otherwise P_j
+          // goes out without that wait.  (The wait cannot alias a later phase:
+          // the next P*V on the same barrier needs a P this warp has not
+          // produced yet.)
           if (!(ok = mbar_wait_warp(smem_u32(&sh->o_done[(gj - 1) & 1]), ((gj - 1) >> 1) & 1, status, abort_flag))) break;
-          if (__any_sync(0xffffffffu, need)) {
+          {
             tc_fence_after();
             uint32_t r[32];
 #pragma unroll
@@ -836,9 +724,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         {
           // Widen V_j (key row `row`) from e4m3 to f16 into the MN-major f16
           // buffer; rows past the sequence's keys become zeros.  The f16 buffer
-          // was last read by P*V two tiles ago, whose completion this thread
-          // has already observed.
+          // was last read by P*V two tiles ago: within the item, wait for it
+          // (it ran before S_j in the tensor pipe, so this returns at once);
+          // for the first two tiles it belonged to the previous item, whose
+          // last P*V this warp waited for in that item's epilogue.
           const int vs = gj % NV;
+          if (j >= 2 && !(ok = mbar_wait_warp(smem_u32(&sh->o_done[gj & 1]), ((gj - 2) >> 1) & 1, status, abort_flag))) break;
           if (!(ok = mbar_wait_warp(smem_u32(&sh->v_full[vs]), (gj / NV) & 1, status, abort_flag))) break;
           const uint8_t* src = smem + F8_SMEM_V8 + vs * V8_BYTES + row * 128;
           uint8_t* dst = smem + F8_SMEM_V16 + vs * V16_BYTES + row * 128;
@@ -865,9 +756,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tmem_st32(tmem + lane_off + TM_S + sb * 128, pk);
         tmem_st32(tmem + lane_off + TM_S + sb * 128 + 32, pk + 32);
-        if (j > 0) {
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+          // Rescale O once P*V of the previous tile has completed (as in the
+          // bf16 kernel, only when the row maximum grew by more than 2^8).
           if (!(ok = mbar_wait_warp(smem_u32(&sh->o_done[(gj - 1) & 1]), ((gj - 1) >> 1) & 1, status, abort_flag))) break;
-          if (__any_sync(0xffffffffu, need)) {
+          {
             tc_fence_after();
             uint32_t r[32];
 #pragma unroll
@@ -914,8 +807,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 }  // namespace
 
+// MLA_ATTENTION_KERNEL=single|pair picks the bf16 kernel (default: the two-SM
+// pair kernel where the device can run it).
+static bool use_pair_kernel() {
+  const char* v = std::getenv("MLA_ATTENTION_KERNEL");
+  if (v != nullptr && std::strcmp(v, "single") == 0) return false;
+  return attention_pair_available();
+}
+
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   const bool e4m3 = a.dtype == MLA_E4M3;
+  if (!e4m3 && use_pair_kernel()) return launch_attention_pair(a, stream);
   const uint64_t HN = static_cast<uint64_t>(a.H) * 128;
   const uint64_t QW = static_cast<uint64_t>(a.H) * 192;
   CUtensorMap maps[5];

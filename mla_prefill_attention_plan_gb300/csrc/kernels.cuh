@@ -62,6 +62,10 @@ struct AttnArgs {
   int32_t* status;
 };
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream);
+// bf16 attention on two-SM pairs (cta_group::2 clusters); false / an error
+// when the device cannot keep a two-CTA cluster of the kernel resident.
+bool attention_pair_available();
+cudaError_t launch_attention_pair(const AttnArgs& a, cudaStream_t stream);
 
 // Tensor-map encoder and device properties (abi.cu).
 bool encode_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, uint64_t inner,
