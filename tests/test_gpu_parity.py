@@ -27,6 +27,14 @@ def _built():
     assert torch.cuda.is_available()
 
 
+@pytest.fixture(params=["pair", "single"])
+def bf16_kernel(request, monkeypatch):
+    """Both bf16 attention kernels: the two-SM pair kernel (the default) and
+    the one-SM kernel, selected through MLA_ATTENTION_KERNEL."""
+    monkeypatch.setenv("MLA_ATTENTION_KERNEL", request.param)
+    return request.param
+
+
 def _dt(w):
     return mla.MLA_BF16 if w.dtype == "bf16" else mla.MLA_E4M3
 
@@ -260,7 +268,7 @@ def _attention_stage(w, seed_base=11):
     return _compare(out, ref, dt, lse)
 
 
-def test_attention_stage_multi_chunk():
+def test_attention_stage_multi_chunk(bf16_kernel):
     _attention_stage(WORKLOADS["tiny_ragged"])
 
 
@@ -330,14 +338,14 @@ def _sample_rows(new_lens, cache_lens, S, k, seed):
     return out
 
 
-def test_fused_tiny_ragged_all_rows():
+def test_fused_tiny_ragged_all_rows(bf16_kernel):
     inp = make_inputs(WORKLOADS["tiny_ragged"])
     out, lse = run_fused(inp)
     _compare(out, oracle_fused(inp), "bf16", lse)
 
 
 @pytest.mark.parametrize("S", [7, 64, 200])
-def test_fused_buffer_size_invariance(S):
+def test_fused_buffer_size_invariance(S, bf16_kernel):
     """Different buffer sizes cut the context differently; the result is the same."""
     w = WORKLOADS["tiny_ragged"]
     inp = make_inputs(w)
@@ -348,21 +356,21 @@ def test_fused_buffer_size_invariance(S):
     assert (out.float() - out_ref.float()).abs().max().item() <= 2e-2
 
 
-def test_fused_v2lite_shape_small_heads():
+def test_fused_v2lite_shape_small_heads(bf16_kernel):
     inp = make_inputs(scaled(WORKLOADS["v2lite_prefill"], H=2))
     out, lse = run_fused(inp)
     rows = _sample_rows(inp["new_lens"], inp["cache_lens"], 4096, 40, 1)
     _compare(out, oracle_fused(inp, rows=rows), "bf16", lse)
 
 
-def test_fused_v3_full_length_small_heads():
+def test_fused_v3_full_length_small_heads(bf16_kernel):
     inp = make_inputs(scaled(WORKLOADS["v3_prefill"], H=2))
     out, lse = run_fused(inp)
     rows = _sample_rows(inp["new_lens"], inp["cache_lens"], 4096, 60, 2)
     _compare(out, oracle_fused(inp, rows=rows), "bf16", lse)
 
 
-def test_fused_ragged_chunked_small_heads():
+def test_fused_ragged_chunked_small_heads(bf16_kernel):
     w = scaled(WORKLOADS["ragged_chunked_cache"], H=2)
     inp = make_inputs(w)
     out, lse = run_fused(inp)
@@ -370,7 +378,7 @@ def test_fused_ragged_chunked_small_heads():
     _compare(out, oracle_fused(inp, rows=rows), "bf16", lse)
 
 
-def test_fused_edge_cases():
+def test_fused_edge_cases(bf16_kernel):
     # an empty sequence, a cache-only sequence, a single token, a tile-edge length,
     # a buffer smaller than one sequence
     w = scaled(WORKLOADS["tiny_ragged"], H=3, page_size=8, buffer_token_size=50, max_chunks=12)
@@ -381,7 +389,19 @@ def test_fused_edge_cases():
     _compare(out, oracle_fused(inp, max_chunks=mc), "bf16", lse)
 
 
-def test_fused_sequence_alone_equals_in_batch():
+def test_fused_pair_boundaries(bf16_kernel):
+    """Query-tile pairs with an odd tile count (the second tile of the last pair
+    is empty), one-tile sequences, and chunk cuts that leave one tile of a
+    pair with no visible keys of a chunk while its partner has some."""
+    w = scaled(WORKLOADS["tiny_ragged"], H=3, page_size=16, buffer_token_size=384, max_chunks=8)
+    new, cache = (300, 129, 1, 257, 640), (0, 500, 37, 130, 90)
+    inp = make_inputs(w, new_lens=new, cache_lens=cache)
+    mc = -(-sum(a + b for a, b in zip(new, cache)) // 384)
+    out, lse = run_fused(inp, max_chunks=mc)
+    _compare(out, oracle_fused(inp, max_chunks=mc), "bf16", lse)
+
+
+def test_fused_sequence_alone_equals_in_batch(bf16_kernel):
     w = scaled(WORKLOADS["ragged_chunked_cache"], H=2, B=3, buffer_token_size=256,
                new_range=(100, 300), cache_range=(0, 400))
     inp = make_inputs(w)
@@ -414,10 +434,12 @@ def test_fused_e4m3_full_length_small_heads():
 
 @pytest.mark.parametrize("name", ["v2lite_prefill", "v3_prefill", "ragged_chunked_cache",
                                   "longctx_fp8"])
-def test_fused_full_size_sampled(name):
+def test_fused_full_size_sampled(name, bf16_kernel):
     """Full sizes, the launch configuration the benchmark times; the oracle
     checks a sample of heads and rows."""
     w = WORKLOADS[name]
+    if w.dtype != "bf16" and bf16_kernel != "pair":
+        pytest.skip("one e4m3 kernel")
     inp = make_inputs(w)
     out, lse = run_fused(inp)
     heads = [0, w.H // 2 + 1, w.H - 1]
@@ -426,7 +448,7 @@ def test_fused_full_size_sampled(name):
     assert torch.isfinite(out.float()).all()
 
 
-def test_fused_is_deterministic():
+def test_fused_is_deterministic(bf16_kernel):
     """No atomics in the arithmetic: repeated calls agree bit for bit (a
     pipeline race shows up here first)."""
     inp = make_inputs(scaled(WORKLOADS["ragged_chunked_cache"], H=2, B=4, buffer_token_size=2048,
