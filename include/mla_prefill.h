@@ -72,6 +72,16 @@ int32_t mla_abi_version(void);
 #define MLA_ABI_VERSION 1
 
 /*
+ * Which attention kernel mla_prefill_attention / mla_prefill will launch for
+ * `dtype` on the current CUDA device: "pair" (bf16 on two-SM clusters, the
+ * default where the device can keep such a cluster resident), "single" (bf16,
+ * one SM per work item; also chosen by setting the environment variable
+ * MLA_ATTENTION_KERNEL=single) or "e4m3".  Static storage; NULL for an unknown
+ * dtype.  The pages have no counterpart: this is an introspection call.
+ */
+const char* mla_attention_kernel(int32_t dtype);
+
+/*
  * 1. Chunk plan.  Follows "mla_prefill_plan" (Args: buffer_row_offsets,
  * cache_offsets, buffer_lengths, input_row_offsets, k_cache, buffer_token_size).
  *

@@ -41,6 +41,7 @@ _Z = ctypes.c_size_t
 SIGNATURES = {
     "mla_status_string": (ctypes.c_char_p, [_I]),
     "mla_abi_version": (_I, []),
+    "mla_attention_kernel": (ctypes.c_char_p, [_I]),
     "mla_prefill_plan": (_I, [_P, _P, _P, _P, _P, _I, _I, _U, _P, _P]),
     "mla_gather_latent": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _I, _I, _U, _I, _P, _P]),
     "mla_upproject": (_I, [_P, _P, _P, _P, _P, _P, _I, _U, _I, _I, _F, _F, _F, _P]),
@@ -105,6 +106,12 @@ def check(code: int) -> None:
 
 def mla_abi_version() -> int:
     return load().mla_abi_version()
+
+
+def mla_attention_kernel(dtype) -> str:
+    """Which attention kernel a call with `dtype` launches on the current device."""
+    r = load().mla_attention_kernel(dtype)
+    return r.decode() if r is not None else None
 
 
 def mla_prefill_plan(buffer_row_offsets, cache_offsets, buffer_lengths, input_row_offsets,

@@ -119,6 +119,12 @@ const char* mla_status_string(int32_t code) {
 
 int32_t mla_abi_version(void) { return MLA_ABI_VERSION; }
 
+const char* mla_attention_kernel(int32_t dtype) {
+  if (dtype == MLA_E4M3) return "e4m3";
+  if (dtype != MLA_BF16) return nullptr;
+  return mla::attention_uses_pair() ? "pair" : "single";
+}
+
 mla_status_t mla_prefill_plan(uint32_t* buffer_row_offsets, uint32_t* cache_offsets,
                               int32_t* buffer_lengths, const uint32_t* input_row_offsets,
                               const uint32_t* cache_lengths, int32_t batch_size,

@@ -809,7 +809,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 // MLA_ATTENTION_KERNEL=single|pair picks the bf16 kernel (default: the two-SM
 // pair kernel where the device can run it).
-static bool use_pair_kernel() {
+bool attention_uses_pair() {
   const char* v = std::getenv("MLA_ATTENTION_KERNEL");
   if (v != nullptr && std::strcmp(v, "single") == 0) return false;
   return attention_pair_available();
@@ -817,7 +817,7 @@ static bool use_pair_kernel() {
 
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   const bool e4m3 = a.dtype == MLA_E4M3;
-  if (!e4m3 && use_pair_kernel()) return launch_attention_pair(a, stream);
+  if (!e4m3 && attention_uses_pair()) return launch_attention_pair(a, stream);
   const uint64_t HN = static_cast<uint64_t>(a.H) * 128;
   const uint64_t QW = static_cast<uint64_t>(a.H) * 192;
   CUtensorMap maps[5];

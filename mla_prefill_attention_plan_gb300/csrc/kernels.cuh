@@ -65,6 +65,9 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream);
 // bf16 attention on two-SM pairs (cta_group::2 clusters); false / an error
 // when the device cannot keep a two-CTA cluster of the kernel resident.
 bool attention_pair_available();
+// The bf16 kernel launch_attention picks (MLA_ATTENTION_KERNEL=single forces
+// the one-SM kernel).
+bool attention_uses_pair();
 cudaError_t launch_attention_pair(const AttnArgs& a, cudaStream_t stream);
 
 // Tensor-map encoder and device properties (abi.cu).

@@ -45,6 +45,9 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_abi_version_and_strings(lib):
     assert mla.mla_abi_version() == 1
+    # dtype-only answers need no device
+    assert mla.mla_attention_kernel(mla.MLA_E4M3) == "e4m3"
+    assert mla.mla_attention_kernel(7) is None
     assert "workspace" in mla.status_string(mla.MLA_ERR_WORKSPACE)
     assert "timed out" in mla.status_string(mla.MLA_DEV_TIMEOUT)
 

@@ -32,6 +32,8 @@ def bf16_kernel(request, monkeypatch):
     """Both bf16 attention kernels: the two-SM pair kernel (the default) and
     the one-SM kernel, selected through MLA_ATTENTION_KERNEL."""
     monkeypatch.setenv("MLA_ATTENTION_KERNEL", request.param)
+    # No silent fallback: on a GB300 the pair kernel must be the one that runs.
+    assert mla.mla_attention_kernel(mla.MLA_BF16) == request.param
     return request.param
 
 
