@@ -32,9 +32,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 # DRAM bytes (read + write) per attention launch from one ncu capture of the
-# current kernel (profiles/attn_kernel_v3_prefill.md); absent for workloads
-# without a capture.
-ATTN_DRAM_BYTES_PER_LAUNCH = {"v3_prefill": 496_654_592 + 119_747_840}
+# current kernel, keyed by (workload, kernel) (profiles/attn_*_v3_prefill.md);
+# absent where the kernel has changed since its capture.
+ATTN_DRAM_BYTES_PER_LAUNCH = {("v3_prefill", "attn_pair_kernel"): 483_606_272 + 118_548_992}
+# CUDA kernel name of each attention variant the library reports.
+ATTN_KERNEL_NAMES = {"pair": "attn_pair_kernel", "single": "attn_kernel", "e4m3": "attn_kernel_e4m3"}
 
 
 def _args():
@@ -276,6 +278,7 @@ def run_ours(a):
     kv_descale = inp["ckv_scale"] if w.dtype == "e4m3" else 1.0
     kv_inv = 1.0 / inp["ckv_scale"] if w.dtype == "e4m3" else 1.0
     launches_per_step = 1 + 3 * mc + (2 if Bsz > 4096 else 0)
+    attn_kernel_name = ATTN_KERNEL_NAMES[mla.mla_attention_kernel(dt)]
 
     def step(ev=None):
         mla.check(mla.mla_prefill_plan(bro, co, bl, d["input_row_offsets"], d["cache_lengths"], Bsz,
@@ -427,10 +430,10 @@ def run_ours(a):
         "upproj_tflops": up_flops / (up_ms / a.steps * 1e-3) / 1e12,
         "upproj_ms_per_step": up_ms / a.steps,
         "step_flops": {"attention": attn_flops, "upproject": up_flops, "visible_pairs": pairs},
-        "roofline": {"bound": "tensor", "kernel": "attn_kernel", "achieved": achieved,
+        "roofline": {"bound": "tensor", "kernel": attn_kernel_name, "achieved": achieved,
                      "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                      "peak_source": f"{src} bf16 dense, sustained (kernel timed inside a long step loop)",
-                     "traffic": ATTN_DRAM_BYTES_PER_LAUNCH.get(w.name)},
+                     "traffic": ATTN_DRAM_BYTES_PER_LAUNCH.get((w.name, attn_kernel_name))},
         "e2e": e2e,
         "gpu_launches": launches_per_step * a.steps,
         "clocks": clk,
