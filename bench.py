@@ -488,7 +488,7 @@ def run_stage(a):
         bl = torch.empty(mc, dtype=torch.int32, device=dev)
         nbytes = 4 * (2 * Bsz + 1) + 4 * mc * (2 * Bsz + 2)
         launch = lambda: mla.check(mla.mla_prefill_plan(bro, co, bl, iro, cl, Bsz, mc, S, st, stream))
-        kernels = "plan_tile_sums + plan_tile_write + row-0 memset" if Bsz > 4096 else "plan_one_cta"
+        kernels = "plan_tile_sums + plan_tile_scan + plan_tile_write" if Bsz > 4096 else "plan_one_cta"
         desc = {"workload": "plan_stress", "B": Bsz, "max_chunks": mc, "buffer_token_size": S,
                 "new_tokens": "U[0,63]", "cache_tokens": "U[0,63]"}
     else:

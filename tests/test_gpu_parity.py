@@ -90,14 +90,44 @@ def test_plan_random_fuzz():
         _assert_plan_equal(np.concatenate([[0], np.cumsum(new)]), cache, S, mc)
 
 
-@pytest.mark.parametrize("B", [4096, 4097, 20000])
+@pytest.mark.parametrize("B", [4096, 4097, 20000, 300000])
 def test_plan_many_sequences(B):
+    """Multi-tile plans (tiles of 4096 sequences); 300000 sequences make 74 tiles."""
     rng = np.random.default_rng(B)
     new = rng.integers(0, 64, B)
     cache = rng.integers(0, 64, B)
-    S = 20000
+    S = max(20000, int((new + cache).sum()) // 3)
     need = -(-int((new + cache).sum()) // S)
     _assert_plan_equal(np.concatenate([[0], np.cumsum(new)]), cache, S, need + 1)
+
+
+def test_plan_unaligned_tables():
+    """Tables and inputs 4 bytes off a 16-byte boundary (the plan takes any
+    4-byte aligned pointers): same tables."""
+    rng = np.random.default_rng(5)
+    B = 70000
+    new, cache = rng.integers(0, 64, B), rng.integers(0, 64, B)
+    iro = np.concatenate([[0], np.cumsum(new)])
+    S = int((new + cache).sum()) // 3 + 1
+    mc = 4
+    def shifted(n, fill):
+        t = torch.full((n + 1,), fill, dtype=torch.int32, device=DEV)
+        return t, t.data_ptr() + 4
+    bro_t, bro_p = shifted(mc * (B + 1), -7)
+    co_t, co_p = shifted(mc * B, -7)
+    bl = torch.full((mc,), -7, dtype=torch.int32, device=DEV)
+    iro_t, iro_p = shifted(B + 1, 0)
+    iro_t[1:] = _i32(iro)
+    cl_t, cl_p = shifted(B, 0)
+    cl_t[1:] = _i32(cache)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    mla.check(mla.mla_prefill_plan(bro_p, co_p, bl, iro_p, cl_p, B, mc, S, st))
+    torch.cuda.synchronize()
+    o = O.prefill_plan(iro, cache, S, mc)
+    assert int(st.item()) == o[3] == 0
+    np.testing.assert_array_equal(bro_t[1:].cpu().numpy().reshape(mc, B + 1), o[0])
+    np.testing.assert_array_equal(co_t[1:].cpu().numpy().reshape(mc, B), o[1])
+    np.testing.assert_array_equal(bl.cpu().numpy(), o[2])
 
 
 def test_plan_status_codes():
