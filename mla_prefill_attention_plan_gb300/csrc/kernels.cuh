@@ -34,6 +34,11 @@ struct UpprojArgs {
   int32_t* status;
 };
 cudaError_t launch_upproject(const UpprojArgs& a, cudaStream_t stream);
+// The same GEMM on two-SM pairs (cta_group::2 clusters, 256 x 256 tiles);
+// launch_upproject uses it where the device can keep such a cluster resident
+// unless MLA_UPPROJ_KERNEL=single.
+bool upproject_pair_available(int dtype);
+cudaError_t launch_upproject_pair(const UpprojArgs& a, cudaStream_t stream);
 
 struct AttnArgs {
   void* out;

@@ -17,6 +17,9 @@
 //               scale, round to the storage type, stage 32x128 B in shared
 //               memory and TMA-store it; the second accumulator lets the next
 //               tile's MMAs run under this epilogue.
+#include <cstdlib>
+#include <cstring>
+
 #include "kernels.cuh"
 
 namespace mla {
@@ -248,6 +251,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }  // namespace
 
 cudaError_t launch_upproject(const UpprojArgs& a, cudaStream_t stream) {
+  const char* pick = std::getenv("MLA_UPPROJ_KERNEL");
+  if (!(pick != nullptr && std::strcmp(pick, "single") == 0) && upproject_pair_available(a.dtype))
+    return launch_upproject_pair(a, stream);
   const int elt = a.dtype == MLA_BF16 ? 2 : 1;
   const CUtensorMapDataType dt =
       elt == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;

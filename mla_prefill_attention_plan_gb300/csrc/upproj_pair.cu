@@ -1,0 +1,328 @@
+// Up-projection on pairs of SMs ("mla_prefill_decode_graph_bf16", Args: w_k,
+// w_uv): the GEMM  [rows, 512] x [512, 2*H*128]  of upproj.cu (N axis = the
+// 128-wide head blocks of w_k then of w_uv), with 256 x 256 output tiles
+// computed by a cluster of two CTAs through two-SM MMAs (cta_group::2,
+// M = 256).  CTA r holds rows [128r, 128r + 128) of the tile's A and D, and
+// B rows (N) [128r, 128r + 128) of the tile: each SM loads 32 KB per k-block
+// for 128 x 256 x k of tensor work, against 48 KB in the one-SM kernel, whose
+// L2 -> SM stream (~94 B/clk per SM at the tensor rate) exceeds what L2
+// delivers to every SM at once (~72 B/clk).
+//
+//   warp 0      TMA producer: own A rows and own B half per k-block, 6-stage ring.
+//   warp 1      both CTAs: TMEM allocation (512 columns, pair form).
+//               CTA 0: one elected lane issues the pair MMAs (M=256, N=256)
+//               into one of two 256-column accumulators and commits to the
+//               barriers of both CTAs.  CTA 1: one elected lane relays "my
+//               k-block landed" to CTA 0's ring barriers.
+//   warps 2..5  epilogue of the CTA's own 128 rows, as in upproj.cu; "this
+//               accumulator has been read" goes to CTA 0.
+#include <mutex>
+
+#include "kernels.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int UBM = 128, UBN = 256, UBKB = 128;   // rows per CTA, tile cols, k-block bytes
+constexpr int USTAGES = 6;
+constexpr int UA_BYTES = UBM * UBKB;              // 16 KB: own A rows
+constexpr int UB_BYTES = (UBN / 2) * UBKB;        // 16 KB: own half of B
+constexpr int UEPI_BYTES = 32 * 128;
+constexpr int U_SMEM_A = 0;
+constexpr int U_SMEM_B = U_SMEM_A + USTAGES * UA_BYTES;
+constexpr int U_SMEM_EPI = U_SMEM_B + USTAGES * UB_BYTES;          // 196608
+constexpr int U_SMEM_BAR = U_SMEM_EPI + 4 * 2 * UEPI_BYTES;        // 229376
+constexpr int U_SMEM_TOTAL = U_SMEM_BAR + 256 + 1024;
+constexpr int U_THREADS = 192;
+constexpr uint32_t U_TMEM_COLS = 512;
+constexpr uint16_t kPairMask = 3;
+
+struct PairGemmSmem {
+  uint64_t full[USTAGES];    // CTA 0: own bytes + the relay; CTA 1: own bytes
+  uint64_t empty[USTAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];        // CTA 0: both CTAs' epilogues (8 warps)
+  uint64_t drain;
+  uint32_t tmem;
+  int abort;
+};
+static_assert(sizeof(PairGemmSmem) <= 256, "barrier block");
+
+template <int ELT>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(U_THREADS, 1)
+    upproj_pair_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap wk_map,
+                       const __grid_constant__ CUtensorMap wuv_map,
+                       const __grid_constant__ CUtensorMap k_out_map,
+                       const __grid_constant__ CUtensorMap v_out_map, const int32_t* buffer_lengths,
+                       int chunk, int S, int H, float out_scale, int32_t* status) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  PairGemmSmem* sh = reinterpret_cast<PairGemmSmem*>(smem + U_SMEM_BAR);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const int pair_id = blockIdx.x >> 1;
+  const int n_pairs = gridDim.x >> 1;
+
+  // Both CTAs of a pair read the same row count, so they return together.
+  int rows = buffer_lengths ? buffer_lengths[chunk] : S;
+  if (rows <= 0) return;
+  if (rows > S) rows = S;
+  const int num_m = (rows + 2 * UBM - 1) / (2 * UBM);   // 256-row pair tiles
+  const int num_tiles = num_m * H;                      // N: 2*H*128 / 256
+  constexpr int KB = 512 * ELT / UBKB;                  // k-blocks: 8 (bf16) or 4 (e4m3)
+  constexpr int KSTEP = 32;                             // bytes of one MMA's K
+  constexpr uint32_t IDESC = ELT == 2 ? idesc_bf16(2 * UBM, UBN, false, false) : idesc_e4m3(2 * UBM, UBN, false, false);
+
+  if (threadIdx.x == 0) {
+    const uint32_t lead = rank == 0 ? 1u : 0u;
+    for (int s = 0; s < USTAGES; ++s) {
+      mbar_init(smem_u32(&sh->full[s]), 1 + lead);
+      mbar_init(smem_u32(&sh->empty[s]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&sh->tfull[i]), 1);
+      mbar_init(smem_u32(&sh->tempty[i]), 8);
+    }
+    mbar_init(smem_u32(&sh->drain), 1);
+    sh->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(&sh->tmem), U_TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = sh->tmem;
+  volatile int* abort_flag = &sh->abort;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tmap(&a_map);
+      prefetch_tmap(&wk_map);
+      prefetch_tmap(&wuv_map);
+      int stage = 0;
+      uint32_t phase = 0;
+      int last_ph[USTAGES];
+      for (int s = 0; s < USTAGES; ++s) last_ph[s] = -1;
+      for (int t = pair_id; t < num_tiles && !*abort_flag; t += n_pairs) {
+        const int m0 = (t % num_m) * 2 * UBM + static_cast<int>(rank) * UBM;
+        const int nt = t / num_m;
+        const int hf = 2 * nt + static_cast<int>(rank);   // this CTA's 128-wide block of N
+        const CUtensorMap* wmap = hf < H ? &wk_map : &wuv_map;
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!(ok = mbar_wait(smem_u32(&sh->empty[stage]), phase ^ 1, status, abort_flag))) break;
+          const uint32_t full = smem_u32(&sh->full[stage]);
+          mbar_expect_tx(full, UA_BYTES + UB_BYTES);
+          const int x = kb * (UBKB / ELT);
+          tma_load_2d(smem_u32(smem + U_SMEM_A + stage * UA_BYTES), &a_map, full, x, m0);
+          tma_load_2d(smem_u32(smem + U_SMEM_B + stage * UB_BYTES), wmap, full, x, (hf % H) * 128);
+          last_ph[stage] = int(phase);
+          if (++stage == USTAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+      }
+      volatile int never = 0;
+      for (int s = 0; s < USTAGES; ++s)
+        if (last_ph[s] >= 0) mbar_wait(smem_u32(&sh->full[s]), uint32_t(last_ph[s]), status, &never);
+    }
+  } else if (warp == 1) {
+    if (rank == 0) {
+      // One elected lane runs the whole issue loop (no reconvergence while
+      // MMAs are in flight).
+      if (elect_one()) {
+        int stage = 0;
+        uint32_t phase = 0;
+        int tl = 0;
+        bool ok = true;
+        for (int t = pair_id; t < num_tiles && ok; t += n_pairs, ++tl) {
+          const int acc = tl & 1;
+          if (!(ok = mbar_wait(smem_u32(&sh->tempty[acc]), ((tl >> 1) & 1) ^ 1, status, abort_flag))) break;
+          tc_fence_after();
+          const uint32_t d = tmem + acc * UBN;
+          for (int kb = 0; kb < KB; ++kb) {
+            if (!(ok = mbar_wait(smem_u32(&sh->full[stage]), phase, status, abort_flag))) break;
+            tc_fence_after();
+            const uint32_t a = smem_u32(smem + U_SMEM_A + stage * UA_BYTES);
+            const uint32_t b = smem_u32(smem + U_SMEM_B + stage * UB_BYTES);
+#pragma unroll
+            for (int k = 0; k < UBKB / KSTEP; ++k) {
+              const uint64_t ad = sdesc(a + k * KSTEP, 16, 1024);
+              const uint64_t bd = sdesc(b + k * KSTEP, 16, 1024);
+              if (ELT == 2) mma_f16_ss_pair(d, ad, bd, IDESC, (kb | k) != 0);
+              else mma_f8_ss_pair(d, ad, bd, IDESC, (kb | k) != 0);
+            }
+            tc_commit_pair(smem_u32(&sh->empty[stage]), kPairMask);
+            if (++stage == USTAGES) { stage = 0; phase ^= 1; }
+          }
+          if (ok) tc_commit_pair(smem_u32(&sh->tfull[acc]), kPairMask);
+        }
+        tc_commit_pair(smem_u32(&sh->drain), 1);
+        volatile int never = 0;
+        mbar_wait(smem_u32(&sh->drain), 0, status, &never);
+      }
+      __syncwarp();
+    } else {
+      // Relay: CTA 1's k-blocks to CTA 0's ring, in order.
+      if (elect_one()) {
+        const uint32_t full0 = cluster_addr(smem_u32(&sh->full[0]), 0);
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int t = pair_id; t < num_tiles && ok; t += n_pairs) {
+          for (int kb = 0; kb < KB; ++kb) {
+            if (!(ok = mbar_wait(smem_u32(&sh->full[stage]), phase, status, abort_flag))) break;
+            mbar_arrive_cluster(full0 + stage * 8);
+            if (++stage == USTAGES) { stage = 0; phase ^= 1; }
+          }
+        }
+      }
+      __syncwarp();
+    }
+  } else {
+    // Epilogue warps 2..5: TMEM lane quarter q = warp % 4 holds rows 32q..32q+31.
+    const int q = warp & 3;
+    const uint32_t lane_off = uint32_t(q * 32) << 16;
+    const uint32_t tempty0 = cluster_addr(smem_u32(&sh->tempty[0]), 0);
+    uint8_t* stage_buf = smem + U_SMEM_EPI + (warp - 2) * 2 * UEPI_BYTES;
+    int buf = 0;
+    int tl = 0;
+    for (int t = pair_id; t < num_tiles; t += n_pairs, ++tl) {
+      const int acc = tl & 1;
+      if (!mbar_wait_warp(smem_u32(&sh->tfull[acc]), (tl >> 1) & 1, status, abort_flag)) break;
+      tc_fence_after();
+      const int m0 = (t % num_m) * 2 * UBM + static_cast<int>(rank) * UBM;
+      const int nt = t / num_m;
+      const bool row_ok = m0 + q * 32 + lane < rows;
+      constexpr int SEG_COLS = 128 / ELT;      // columns per 128-byte staging row
+      constexpr int NSEG = UBN / SEG_COLS;     // 4 (bf16) or 2 (e4m3)
+#pragma unroll 1
+      for (int seg = 0; seg < NSEG; ++seg) {
+        uint32_t packed[32];
+#pragma unroll
+        for (int part = 0; part < SEG_COLS / 32; ++part) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_off + acc * UBN + seg * SEG_COLS + part * 32, r);
+          tmem_ld_wait();
+          if (ELT == 2) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              packed[part * 16 + i] = row_ok ? pack_bf16(__uint_as_float(r[2 * i]) * out_scale,
+                                                         __uint_as_float(r[2 * i + 1]) * out_scale)
+                                             : 0u;
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const uint32_t lo = pack_e4m3(__uint_as_float(r[4 * i]) * out_scale,
+                                            __uint_as_float(r[4 * i + 1]) * out_scale);
+              const uint32_t hi = pack_e4m3(__uint_as_float(r[4 * i + 2]) * out_scale,
+                                            __uint_as_float(r[4 * i + 3]) * out_scale);
+              packed[part * 8 + i] = row_ok ? (lo | (hi << 16)) : 0u;
+            }
+          }
+        }
+        if (seg == NSEG - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(tempty0 + acc * 8);
+        }
+        if (lane == 0) bulk_wait_read<1>();
+        __syncwarp();
+        uint8_t* sb = stage_buf + buf * UEPI_BYTES;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(sb + lane * 128 + ((c ^ (lane & 7)) * 16)) =
+              make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int col = seg * SEG_COLS;          // within the 256-wide tile
+          const int hf = 2 * nt + col / 128;       // 128-wide block of N
+          const CUtensorMap* omap = hf < H ? &k_out_map : &v_out_map;
+          tma_store_2d(omap, smem_u32(sb), (hf % H) * 128 + (col % 128), m0 + q * 32);
+          bulk_commit();
+        }
+        buf ^= 1;
+      }
+    }
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // neither CTA frees TMEM or leaves while the pair still uses it
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, U_TMEM_COLS);
+  }
+}
+
+template <int ELT>
+int pair_gemm_clusters(int device) {
+  static std::mutex mu;
+  static int cached[64];
+  static bool done[64];
+  std::lock_guard<std::mutex> lock(mu);
+  if (device < 0 || device >= 64) return 0;
+  if (!done[device]) {
+    cudaFuncSetAttribute(upproj_pair_kernel<ELT>, cudaFuncAttributeMaxDynamicSharedMemorySize, U_SMEM_TOTAL);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(U_THREADS);
+    cfg.dynamicSmemBytes = U_SMEM_TOTAL;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, upproj_pair_kernel<ELT>, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+    cached[device] = n;
+    done[device] = true;
+  }
+  return cached[device];
+}
+
+}  // namespace
+
+bool upproject_pair_available(int dtype) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  return (dtype == MLA_BF16 ? pair_gemm_clusters<2>(dev) : pair_gemm_clusters<1>(dev)) > 0;
+}
+
+cudaError_t launch_upproject_pair(const UpprojArgs& a, cudaStream_t stream) {
+  const int elt = a.dtype == MLA_BF16 ? 2 : 1;
+  const CUtensorMapDataType dt =
+      elt == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const uint32_t box_k = UBKB / elt;
+  const uint64_t HN = static_cast<uint64_t>(a.H) * 128;
+  CUtensorMap a_map, wk_map, wuv_map, k_map, v_map;
+  const bool ok =
+      encode_2d(&a_map, a.c_kv, dt, 512, a.S, 512ull * elt, box_k, UBM, CU_TENSOR_MAP_SWIZZLE_128B) &&
+      encode_2d(&wk_map, a.w_k, dt, 512, HN, 512ull * elt, box_k, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
+      encode_2d(&wuv_map, a.w_uv, dt, 512, HN, 512ull * elt, box_k, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
+      encode_2d(&k_map, a.k_nope, dt, HN, a.S, HN * elt, box_k, 32, CU_TENSOR_MAP_SWIZZLE_128B) &&
+      encode_2d(&v_map, a.v, dt, HN, a.S, HN * elt, box_k, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!ok) return cudaErrorInvalidValue;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const int clusters = elt == 2 ? pair_gemm_clusters<2>(dev) : pair_gemm_clusters<1>(dev);
+  if (clusters <= 0) return cudaErrorInvalidConfiguration;
+  // Upper bound on pair tiles (the device reads the chunk's real row count).
+  const long long max_tiles = static_cast<long long>((a.S + 2 * UBM - 1) / (2 * UBM)) * a.H;
+  const int grid = 2 * static_cast<int>(max_tiles < clusters ? max_tiles : clusters);
+  if (elt == 2)
+    upproj_pair_kernel<2><<<grid, U_THREADS, U_SMEM_TOTAL, stream>>>(a_map, wk_map, wuv_map, k_map, v_map,
+                                                                    a.buffer_lengths, a.chunk, int(a.S), a.H,
+                                                                    a.out_scale, a.status);
+  else
+    upproj_pair_kernel<1><<<grid, U_THREADS, U_SMEM_TOTAL, stream>>>(a_map, wk_map, wuv_map, k_map, v_map,
+                                                                    a.buffer_lengths, a.chunk, int(a.S), a.H,
+                                                                    a.out_scale, a.status);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -37,6 +37,13 @@ def bf16_kernel(request, monkeypatch):
     return request.param
 
 
+@pytest.fixture(params=["pair", "single"])
+def upproj_kernel(request, monkeypatch):
+    """Both up-projection GEMMs: two-SM pairs (the default) and one SM per tile."""
+    monkeypatch.setenv("MLA_UPPROJ_KERNEL", request.param)
+    return request.param
+
+
 def _dt(w):
     return mla.MLA_BF16 if w.dtype == "bf16" else mla.MLA_E4M3
 
@@ -211,7 +218,7 @@ def test_gather_bad_page_reports_status():
 
 @pytest.mark.parametrize("dtype,H,rows,S", [("bf16", 4, 89, 96), ("bf16", 3, 300, 320),
                                             ("bf16", 16, 1000, 1024), ("e4m3", 4, 200, 256)])
-def test_upproject(dtype, H, rows, S):
+def test_upproject(dtype, H, rows, S, upproj_kernel):
     w = scaled(WORKLOADS["tiny_ragged" if dtype == "bf16" else "longctx_fp8"], H=H)
     gen = torch.Generator().manual_seed(H * 1000 + rows)
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float8_e4m3fn
