@@ -36,7 +36,7 @@ sys.path.insert(0, ROOT)
 # absent where the kernel has changed since its capture.
 ATTN_DRAM_BYTES_PER_LAUNCH = {("v3_prefill", "attn_pair_kernel"): 483_606_272 + 118_548_992}
 # CUDA kernel name of each attention variant the library reports.
-ATTN_KERNEL_NAMES = {"pair": "attn_pair_kernel", "single": "attn_kernel", "e4m3": "attn_kernel_e4m3"}
+ATTN_KERNEL_NAMES = {"pair": "attn_pair_kernel", "single": "attn_kernel", "e4m3": "attn_pair_kernel_e4m3"}
 
 
 def _args():
@@ -270,7 +270,8 @@ def run_ours(a):
     ckv = torch.empty(S, 512, dtype=elt, device=dev)
     krope = torch.empty(S, 64, dtype=elt, device=dev)
     knope = torch.empty(S, H, 128, dtype=elt, device=dev)
-    vbuf = torch.empty(S, H, 128, dtype=elt, device=dev)
+    # V: bf16, or f16 holding the e4m3-rounded values for e4m3
+    vbuf = torch.empty(S, H, 128, dtype=torch.bfloat16 if w.dtype == "bf16" else torch.float16, device=dev)
     oacc = torch.empty(T, H, 128, dtype=torch.float32, device=dev) if mc > 1 else None
     lacc = torch.empty(T, H, dtype=torch.float32, device=dev) if mc > 1 else None
     status = torch.zeros(1, dtype=torch.int32, device=dev)

@@ -76,7 +76,8 @@ int32_t mla_abi_version(void);
  * `dtype` on the current CUDA device: "pair" (bf16 on two-SM clusters, the
  * default where the device can keep such a cluster resident), "single" (bf16,
  * one SM per work item; also chosen by setting the environment variable
- * MLA_ATTENTION_KERNEL=single) or "e4m3".  Static storage; NULL for an unknown
+ * MLA_ATTENTION_KERNEL=single) or "e4m3" (two-SM clusters; the only e4m3
+ * kernel, an error where the device cannot run it).  Static storage; NULL for an unknown
  * dtype.  The pages have no counterpart: this is an introspection call.
  */
 const char* mla_attention_kernel(int32_t dtype);
@@ -153,7 +154,12 @@ mla_status_t mla_gather_latent(void* c_kv_buf, void* k_rope_buf, const void* kv_
  * to the storage dtype (nearest even; e4m3 saturates at +-448).  Rows from n
  * up to the next multiple of 128 (within buffer_token_size) are written as 0.
  *
- * k_nope, v:  [buffer_token_size][num_heads][128] dtype, outputs
+ * k_nope:     [buffer_token_size][num_heads][128] dtype, output
+ * v:          [buffer_token_size][num_heads][128] output: bf16 for MLA_BF16; for
+ *             MLA_E4M3, f16 holding the e4m3-rounded values (exactly the e4m3
+ *             result, stored 2 bytes wide so that the attention's P*V runs on
+ *             f16 operands with no widening; the pages have no counterpart for
+ *             this storage choice)
  * c_kv_buf:   [buffer_token_size][512] dtype
  * w_k:        [num_heads*128][512] dtype;  w_uv: [num_heads][128][512] dtype
  * Errors: host MLA_ERR_ARG / MLA_ERR_DTYPE / MLA_ERR_GEOMETRY (num_heads < 1).
@@ -189,7 +195,9 @@ mla_status_t mla_upproject(void* k_nope, void* v, const void* c_kv_buf, const vo
  *           [num_heads] fp32 scratch; both may be NULL only when max_chunks == 1.
  *           They carry state from one chunk's call to the next.
  * q:        [total_q_tokens][num_heads][192] dtype (128 nope, then 64 rope)
- * k_nope, v:[buffer_token_size][num_heads][128] dtype; k_rope: [buffer_token_size][64]
+ * k_nope:   [buffer_token_size][num_heads][128] dtype; k_rope: [buffer_token_size][64]
+ * v:        [buffer_token_size][num_heads][128] bf16, or f16 for MLA_E4M3 (the
+ *           e4m3-rounded values mla_upproject writes)
  * Rows of k_nope/k_rope beyond a sequence's keys are read but masked; rows of v
  * beyond them are never used.
  * max_prompt_len: largest new-token count of any sequence (sizes the grid).

@@ -59,7 +59,7 @@ Layout layout(int B, int H, int T_q, int max_chunks, uint32_t S, int dtype) {
   L.ckv = take(size_t(S) * 512 * e);
   L.krope = take(size_t(S) * 64 * e);
   L.knope = take(size_t(S) * H * 128 * e);
-  L.v = take(size_t(S) * H * 128 * e);
+  L.v = take(size_t(S) * H * 128 * 2);   // bf16, or f16 holding e4m3-rounded values
   const bool merge = max_chunks > 1;
   L.oacc = take(merge ? size_t(T_q) * H * 128 * sizeof(float) : 0);
   L.lseacc = take(merge ? size_t(T_q) * H * sizeof(float) : 0);

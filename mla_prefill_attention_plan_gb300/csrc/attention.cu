@@ -458,353 +458,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-// ---------------------------------------------------------------------------
-// e4m3 inputs ("flare_mla_prefill_dispatch", Parameters: dtype float8_e4m3fn,
-// output_type bfloat16).  Q*K^T runs on e4m3 operands (kind::f8f6f4, both
-// K-major in shared memory: the 128-byte nope part with a 128-byte swizzle, the
-// 64-byte rope part with a 64-byte swizzle).  P*V runs in f16: the softmax warps
-// widen each V tile from e4m3 to f16 (exact) into a second shared buffer, which
-// also zeroes key rows past the sequence, and write P as f16 into TMEM, so the
-// P*V MMA uses the same MN-major 16-bit V layout as the bf16 kernel.
-// TMEM columns: S/P buffers 0..127 and 128..255, O 256..383.
-constexpr int Q8_NOPE = 128 * 128;                 // [128 rows][128 B], 128-byte swizzle
-constexpr int Q8_BYTES = Q8_NOPE + 128 * 64;       // + [128 rows][64 B], 64-byte swizzle
-constexpr int K8_BYTES = Q8_BYTES;
-constexpr int V8_BYTES = 128 * 128;                // [128 keys][128 dv] e4m3
-constexpr int V16_BYTES = 2 * BLK;                 // [2 dv blocks][128 keys][64 dv] f16
-constexpr int F8_SMEM_Q = 0;
-constexpr int F8_SMEM_K = F8_SMEM_Q + Q8_BYTES;
-constexpr int F8_SMEM_V8 = F8_SMEM_K + NK * K8_BYTES;
-constexpr int F8_SMEM_V16 = F8_SMEM_V8 + NV * V8_BYTES;
-constexpr int F8_SMEM_BAR = F8_SMEM_V16 + NV * V16_BYTES;   // 172032
-constexpr int F8_SMEM_TOTAL = F8_SMEM_BAR + 256 + 1024;
-static_assert(F8_SMEM_K % 1024 == 0 && F8_SMEM_V8 % 1024 == 0 && F8_SMEM_V16 % 1024 == 0, "align");
-
-constexpr uint32_t IDESC_QK8 = idesc_e4m3(BM, BN, false, false);
-constexpr uint32_t IDESC_PV16 = idesc_f16(BM, 128, false, true);
-
-__global__ void __launch_bounds__(NUM_THREADS, 1)
-    attn_kernel_e4m3(const __grid_constant__ CUtensorMap qn_map, const __grid_constant__ CUtensorMap qr_map,
-                     const __grid_constant__ CUtensorMap kn_map, const __grid_constant__ CUtensorMap kr_map,
-                     const __grid_constant__ CUtensorMap v_map, const Params p, int total_items) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Smem* sh = reinterpret_cast<Smem*>(smem + F8_SMEM_BAR);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  if (p.bl[p.chunk] <= 0) return;
-  if (p.status && *reinterpret_cast<volatile int32_t*>(p.status) == MLA_DEV_TIMEOUT) return;
-
-  if (threadIdx.x == 0) {
-    mbar_init(smem_u32(&sh->q_full), 1);
-    mbar_init(smem_u32(&sh->q_empty), 1);
-    for (int i = 0; i < NK; ++i) {
-      mbar_init(smem_u32(&sh->k_full[i]), 1);
-      mbar_init(smem_u32(&sh->k_empty[i]), 1);
-    }
-    for (int i = 0; i < NV; ++i) {
-      mbar_init(smem_u32(&sh->v_full[i]), 1);
-      mbar_init(smem_u32(&sh->v_empty[i]), 4);   // released by the four softmax warps
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&sh->s_full[i]), 1);
-      mbar_init(smem_u32(&sh->p_full[i]), 4);
-    }
-    mbar_init(smem_u32(&sh->o_done[0]), 1);
-    mbar_init(smem_u32(&sh->o_done[1]), 1);
-    mbar_init(smem_u32(&sh->o_free), 4);
-    mbar_init(smem_u32(&sh->drain), 1);
-    sh->abort = 0;
-    fence_mbar_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(&sh->tmem), TMEM_COLS);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = sh->tmem;
-  volatile int* abort_flag = &sh->abort;
-  int32_t* status = p.status;
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ Q and K producer
-    if (elect_one()) {
-      prefetch_tmap(&qn_map);
-      prefetch_tmap(&qr_map);
-      prefetch_tmap(&kn_map);
-      prefetch_tmap(&kr_map);
-    }
-    __syncwarp();
-    uint32_t g = 0, it_n = 0;
-    int q_last = -1, k_last[NK] = {-1, -1};
-    bool ok = true;
-    Item it;
-    for (int idx = blockIdx.x; ok && next_item(p, idx, total_items, it); idx += gridDim.x) {
-      if (it_n > 0 && !(ok = mbar_wait_warp(smem_u32(&sh->q_empty), (it_n - 1) & 1, status, abort_flag))) break;
-      if (elect_one()) {
-        const uint32_t qf = smem_u32(&sh->q_full);
-        mbar_expect_tx(qf, Q8_BYTES);
-        tma_load_2d(smem_u32(smem + F8_SMEM_Q), &qn_map, qf, it.h * 192, it.q_row0);
-        tma_load_2d(smem_u32(smem + F8_SMEM_Q + Q8_NOPE), &qr_map, qf, it.h * 192 + 128, it.q_row0);
-      }
-      __syncwarp();
-      q_last = int(it_n & 1);
-      for (int j = 0; j < it.n_kv; ++j) {
-        const uint32_t gj = g + j;
-        const int row = it.kv_row0 + j * BN;
-        const int ks = gj % NK;
-        if (!(ok = mbar_wait_warp(smem_u32(&sh->k_empty[ks]), ((gj / NK) & 1) ^ 1, status, abort_flag))) break;
-        if (elect_one()) {
-          const uint32_t kf = smem_u32(&sh->k_full[ks]);
-          mbar_expect_tx(kf, K8_BYTES);
-          const uint32_t kdst = smem_u32(smem + F8_SMEM_K + ks * K8_BYTES);
-          tma_load_2d(kdst, &kn_map, kf, it.h * 128, row);
-          tma_load_2d(kdst + Q8_NOPE, &kr_map, kf, 0, row);
-        }
-        __syncwarp();
-        k_last[ks] = int((gj / NK) & 1);
-      }
-      g += it.n_kv;
-      ++it_n;
-    }
-    volatile int never = 0;
-    if (q_last >= 0) mbar_wait_warp(smem_u32(&sh->q_full), uint32_t(q_last), status, &never);
-    for (int s = 0; s < NK; ++s)
-      if (k_last[s] >= 0) mbar_wait_warp(smem_u32(&sh->k_full[s]), uint32_t(k_last[s]), status, &never);
-  } else if (warp == 6) {
-    // ------------------------------------------------------------ V producer (e4m3 tiles)
-    if (elect_one()) prefetch_tmap(&v_map);
-    __syncwarp();
-    uint32_t g = 0;
-    int v_last[NV] = {-1, -1};
-    bool ok = true;
-    Item it;
-    for (int idx = blockIdx.x; ok && next_item(p, idx, total_items, it); idx += gridDim.x) {
-      for (int j = 0; j < it.n_kv; ++j) {
-        const uint32_t gj = g + j;
-        const int row = it.kv_row0 + j * BN;
-        const int vs = gj % NV;
-        if (!(ok = mbar_wait_warp(smem_u32(&sh->v_empty[vs]), ((gj / NV) & 1) ^ 1, status, abort_flag))) break;
-        if (elect_one()) {
-          const uint32_t vf = smem_u32(&sh->v_full[vs]);
-          mbar_expect_tx(vf, V8_BYTES);
-          tma_load_2d(smem_u32(smem + F8_SMEM_V8 + vs * V8_BYTES), &v_map, vf, it.h * 128, row);
-        }
-        __syncwarp();
-        v_last[vs] = int((gj / NV) & 1);
-      }
-      g += it.n_kv;
-    }
-    volatile int never = 0;
-    for (int s = 0; s < NV; ++s)
-      if (v_last[s] >= 0) mbar_wait_warp(smem_u32(&sh->v_full[s]), uint32_t(v_last[s]), status, &never);
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // One elected lane runs the whole loop, waits included (as in the bf16
-    // kernel: the warp reconverges only at the end).
-    if (elect_one()) {
-      uint32_t g = 0, it_n = 0;
-      bool ok = true;
-      const uint32_t q_s = smem_u32(smem + F8_SMEM_Q);
-      const uint32_t o_t = tmem + TM_O;
-      Item it;
-      for (int idx = blockIdx.x; ok && next_item(p, idx, total_items, it); idx += gridDim.x) {
-        if (!(ok = mbar_wait(smem_u32(&sh->q_full), it_n & 1, status, abort_flag))) break;
-        tc_fence_after();
-        // O += P_jj V_jj; p_full also means the f16 copy of V_jj is in place.
-        auto issue_pv = [&](uint32_t gp, int jj) -> bool {
-          const uint32_t sb = gp & 1;
-          if (!mbar_wait(smem_u32(&sh->p_full[sb]), (gp >> 1) & 1, status, abort_flag)) return false;
-          if (jj == 0 && it_n >= 1 && !mbar_wait(smem_u32(&sh->o_free), (it_n - 1) & 1, status, abort_flag))
-            return false;
-          tc_fence_after();
-          const uint32_t v_s = smem_u32(smem + F8_SMEM_V16 + (gp % NV) * V16_BYTES);
-          const uint32_t pa = tmem + TM_S + sb * 128;
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            mma_f16_ts(o_t, pa + kk * 8, sdesc(v_s + kk * 2048, BLK, 1024), IDESC_PV16, (jj > 0 || kk > 0));
-          tc_commit(smem_u32(&sh->o_done[gp & 1]));
-          return true;
-        };
-        auto issue_s = [&](int j) -> bool {
-          const uint32_t gj = g + j;
-          const uint32_t sb = gj & 1;
-          const int ks = gj % NK;
-          if (!mbar_wait(smem_u32(&sh->k_full[ks]), (gj / NK) & 1, status, abort_flag)) return false;
-          tc_fence_after();
-          const uint32_t k_s = smem_u32(smem + F8_SMEM_K + ks * K8_BYTES);
-          const uint32_t d = tmem + TM_S + sb * 128;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)   // nope: 128 B per row, 32 e4m3 per MMA
-            mma_f8_ss(d, sdesc(q_s + kk * 32, 16, 1024), sdesc(k_s + kk * 32, 16, 1024), IDESC_QK8, kk > 0);
-#pragma unroll
-          for (int kk = 0; kk < 2; ++kk)   // rope: 64 B per row
-            mma_f8_ss(d, sdesc(q_s + Q8_NOPE + kk * 32, 16, 512, kSwizzle64),
-                      sdesc(k_s + Q8_NOPE + kk * 32, 16, 512, kSwizzle64), IDESC_QK8, 1);
-          tc_commit(smem_u32(&sh->k_empty[ks]));
-          tc_commit(smem_u32(&sh->s_full[sb]));
-          if (j == it.n_kv - 1) tc_commit(smem_u32(&sh->q_empty));
-          return true;
-        };
-        ok = issue_s(0);
-        if (ok && it.n_kv > 1) ok = issue_s(1);
-        for (int j = 0; j < it.n_kv && ok; ++j) {
-          ok = issue_pv(g + j, j);
-          if (ok && j + 2 < it.n_kv) ok = issue_s(j + 2);
-        }
-        g += it.n_kv;
-        ++it_n;
-      }
-      tc_commit(smem_u32(&sh->drain));
-      volatile int never = 0;
-      mbar_wait(smem_u32(&sh->drain), 0, status, &never);
-    }
-    __syncwarp();
-  } else if (warp >= 2 && warp <= 5) {
-    // ------------------------------------------------------------ softmax + epilogue
-    const int q4 = warp & 3;
-    const int row = q4 * 32 + lane;          // query row (TMEM lane), and key row for V widening
-    const uint32_t lane_off = uint32_t(q4 * 32) << 16;
-    const float sl2 = p.scale_log2;
-    const float2 sl2v = make_float2(sl2, sl2);
-    uint32_t g = 0, it_n = 0;
-    bool ok = true;
-    Item it;
-    for (int idx = blockIdx.x; ok && next_item(p, idx, total_items, it); idx += gridDim.x) {
-      __syncwarp();
-      const long long qpos = static_cast<long long>(it.cb) + it.i0 + row;
-      const long long lim_all = min(static_cast<long long>(it.n_cb), qpos - it.co + 1);
-      float m_run = kNegInf, l_run = 0.f;
-      for (int j = 0; j < it.n_kv; ++j) {
-        const uint32_t gj = g + j;
-        const uint32_t sb = gj & 1;
-        if (!(ok = mbar_wait_warp(smem_u32(&sh->s_full[sb]), (gj >> 1) & 1, status, abort_flag))) break;
-        tc_fence_after();
-        float x[BN];
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          tmem_ld32(tmem + lane_off + TM_S + sb * 128 + c * 32,
-                    *reinterpret_cast<uint32_t(*)[32]>(reinterpret_cast<uint32_t*>(x) + c * 32));
-        tmem_ld_wait();
-        const long long lim = lim_all - static_cast<long long>(j) * BN;
-        if (lim < BN) {
-#pragma unroll
-          for (int k = 0; k < BN; ++k) x[k] = k < lim ? x[k] : kNegInf;
-        }
-        float mx8[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx8[i] = fmax3(x[i], x[8 + i], x[16 + i]);
-#pragma unroll
-        for (int k = 24; k < BN; k += 16)
-#pragma unroll
-          for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], x[k + i], x[k + 8 + i]);
-        const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
-                               fmaxf(mx8[6], mx8[7]));
-        const float m_new = fmaxf(m_run, mx * sl2);
-        const bool need = m_new > m_run + kRescaleThreshold;
-        const float f = need ? ex2(m_run - m_new) : 1.0f;
-        if (need) m_run = m_new;
-        const float msub = m_run == kNegInf ? 0.f : m_run;
-        const float2 negm = make_float2(-msub, -msub);
-        uint32_t pk[BN / 2];
-        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                         make_float2(0.f, 0.f)};
-#pragma unroll
-        for (int k = 0; k < BN / 2; ++k) {
-          const float2 t = __ffma2_rn(make_float2(x[2 * k], x[2 * k + 1]), sl2v, negm);
-          const float2 e = make_float2(ex2(t.x), ex2(t.y));
-          acc[k & 3] = __fadd2_rn(acc[k & 3], e);
-          pk[k] = pack_f16(e.x, e.y);
-        }
-        const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
-        const float2 a = __fadd2_rn(a01, a23);
-        l_run = l_run * f + (a.x + a.y);
-        {
-          // Widen V_j (key row `row`) from e4m3 to f16 into the MN-major f16
-          // buffer; rows past the sequence's keys become zeros.  The f16 buffer
-          // was last read by P*V two tiles ago: within the item, wait for it
-          // (it ran before S_j in the tensor pipe, so this returns at once);
-          // for the first two tiles it belonged to the previous item, whose
-          // last P*V this warp waited for in that item's epilogue.
-          const int vs = gj % NV;
-          if (j >= 2 && !(ok = mbar_wait_warp(smem_u32(&sh->o_done[gj & 1]), ((gj - 2) >> 1) & 1, status, abort_flag))) break;
-          if (!(ok = mbar_wait_warp(smem_u32(&sh->v_full[vs]), (gj / NV) & 1, status, abort_flag))) break;
-          const uint8_t* src = smem + F8_SMEM_V8 + vs * V8_BYTES + row * 128;
-          uint8_t* dst = smem + F8_SMEM_V16 + vs * V16_BYTES + row * 128;
-          const bool valid = j * BN + row < it.n_cb;
-          const int sw = row & 7;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {       // 16 dv values per 16-byte e4m3 chunk
-            uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
-            if (valid) {
-              const uint4 v8 = *reinterpret_cast<const uint4*>(src + ((c ^ sw) << 4));
-              lo = make_uint4(e4m3x2_to_f16x2(uint16_t(v8.x)), e4m3x2_to_f16x2(uint16_t(v8.x >> 16)),
-                              e4m3x2_to_f16x2(uint16_t(v8.y)), e4m3x2_to_f16x2(uint16_t(v8.y >> 16)));
-              hi = make_uint4(e4m3x2_to_f16x2(uint16_t(v8.z)), e4m3x2_to_f16x2(uint16_t(v8.z >> 16)),
-                              e4m3x2_to_f16x2(uint16_t(v8.w)), e4m3x2_to_f16x2(uint16_t(v8.w >> 16)));
-            }
-            uint8_t* blk = dst + (c >> 2) * BLK;     // dv 0..63 or 64..127
-            const int c16 = 2 * (c & 3);             // first f16 chunk of these 16 values
-            *reinterpret_cast<uint4*>(blk + ((c16 ^ sw) << 4)) = lo;
-            *reinterpret_cast<uint4*>(blk + (((c16 + 1) ^ sw) << 4)) = hi;
-          }
-          fence_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&sh->v_empty[vs]));
-        }
-        tmem_st32(tmem + lane_off + TM_S + sb * 128, pk);
-        tmem_st32(tmem + lane_off + TM_S + sb * 128 + 32, pk + 32);
-        if (j > 0 && __any_sync(0xffffffffu, need)) {
-          // Rescale O once P*V of the previous tile has completed (as in the
-          // bf16 kernel, only when the row maximum grew by more than 2^8).
-          if (!(ok = mbar_wait_warp(smem_u32(&sh->o_done[(gj - 1) & 1]), ((gj - 1) >> 1) & 1, status, abort_flag))) break;
-          {
-            tc_fence_after();
-            uint32_t r[32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const uint32_t ta = tmem + lane_off + TM_O + c * 32;
-              tmem_ld32(ta, r);
-              tmem_ld_wait();
-#pragma unroll
-              for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
-              tmem_st32(ta, r);
-            }
-          }
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sh->p_full[sb]));
-      }
-      if (!ok) break;
-      g += it.n_kv;
-      if (!(ok = mbar_wait_warp(smem_u32(&sh->o_done[(g - 1) & 1]), ((g - 1) >> 1) & 1, status, abort_flag))) break;
-      tc_fence_after();
-      float o[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        tmem_ld32(tmem + lane_off + TM_O + c * 32,
-                  *reinterpret_cast<uint32_t(*)[32]>(reinterpret_cast<uint32_t*>(o) + c * 32));
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh->o_free));
-      ++it_n;
-      store_row(p, it, row, qpos, m_run, l_run, o);
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
-  }
-}
-
 }  // namespace
 
 // MLA_ATTENTION_KERNEL=single|pair picks the bf16 kernel (default: the two-SM
@@ -816,26 +469,16 @@ bool attention_uses_pair() {
 }
 
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
-  const bool e4m3 = a.dtype == MLA_E4M3;
-  if (!e4m3 && attention_uses_pair()) return launch_attention_pair(a, stream);
+  if (a.dtype == MLA_E4M3) return launch_attention_pair_e4m3(a, stream);
+  if (attention_uses_pair()) return launch_attention_pair(a, stream);
   const uint64_t HN = static_cast<uint64_t>(a.H) * 128;
   const uint64_t QW = static_cast<uint64_t>(a.H) * 192;
-  CUtensorMap maps[5];
-  bool ok;
-  if (!e4m3) {
-    const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    ok = encode_2d(&maps[0], a.q, dt, QW, a.T_q, QW * 2, 64, BM, CU_TENSOR_MAP_SWIZZLE_128B) &&
-         encode_2d(&maps[1], a.k_nope, dt, HN, a.S, HN * 2, 64, BN, CU_TENSOR_MAP_SWIZZLE_128B) &&
-         encode_2d(&maps[2], a.k_rope, dt, 64, a.S, 128, 64, BN, CU_TENSOR_MAP_SWIZZLE_128B) &&
-         encode_2d(&maps[3], a.v, dt, HN, a.S, HN * 2, 64, BN, CU_TENSOR_MAP_SWIZZLE_128B);
-  } else {
-    const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_UINT8;
-    ok = encode_2d(&maps[0], a.q, dt, QW, a.T_q, QW, 128, BM, CU_TENSOR_MAP_SWIZZLE_128B) &&
-         encode_2d(&maps[1], a.q, dt, QW, a.T_q, QW, 64, BM, CU_TENSOR_MAP_SWIZZLE_64B) &&
-         encode_2d(&maps[2], a.k_nope, dt, HN, a.S, HN, 128, BN, CU_TENSOR_MAP_SWIZZLE_128B) &&
-         encode_2d(&maps[3], a.k_rope, dt, 64, a.S, 64, 64, BN, CU_TENSOR_MAP_SWIZZLE_64B) &&
-         encode_2d(&maps[4], a.v, dt, HN, a.S, HN, 128, BN, CU_TENSOR_MAP_SWIZZLE_128B);
-  }
+  const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUtensorMap maps[4];
+  const bool ok = encode_2d(&maps[0], a.q, dt, QW, a.T_q, QW * 2, 64, BM, CU_TENSOR_MAP_SWIZZLE_128B) &&
+                  encode_2d(&maps[1], a.k_nope, dt, HN, a.S, HN * 2, 64, BN, CU_TENSOR_MAP_SWIZZLE_128B) &&
+                  encode_2d(&maps[2], a.k_rope, dt, 64, a.S, 128, 64, BN, CU_TENSOR_MAP_SWIZZLE_128B) &&
+                  encode_2d(&maps[3], a.v, dt, HN, a.S, HN * 2, 64, BN, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return cudaErrorInvalidValue;
   Params p;
   p.out = static_cast<__nv_bfloat16*>(a.out);
@@ -860,23 +503,9 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   const long long total = static_cast<long long>(p.n_qtiles) * a.B * a.H;
   if (total <= 0) return cudaSuccess;
   const int grid = total < sm_count() ? static_cast<int>(total) : sm_count();
-  if (!e4m3) {
-    static bool attr = false;
-    if (!attr) {
-      cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
-      attr = true;
-    }
-    attn_kernel<<<grid, NUM_THREADS, SMEM_TOTAL, stream>>>(maps[0], maps[1], maps[2], maps[3], p,
-                                                          static_cast<int>(total));
-  } else {
-    static bool attr8 = false;
-    if (!attr8) {
-      cudaFuncSetAttribute(attn_kernel_e4m3, cudaFuncAttributeMaxDynamicSharedMemorySize, F8_SMEM_TOTAL);
-      attr8 = true;
-    }
-    attn_kernel_e4m3<<<grid, NUM_THREADS, F8_SMEM_TOTAL, stream>>>(maps[0], maps[1], maps[2], maps[3],
-                                                                  maps[4], p, static_cast<int>(total));
-  }
+  cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
+  attn_kernel<<<grid, NUM_THREADS, SMEM_TOTAL, stream>>>(maps[0], maps[1], maps[2], maps[3], p,
+                                                        static_cast<int>(total));
   return cudaGetLastError();
 }
 

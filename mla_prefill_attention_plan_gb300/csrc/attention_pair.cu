@@ -495,30 +495,461 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// e4m3 inputs.  The same pair schedule; Q and K are e4m3 and S = Q K^T runs as
+// kind::f8f6f4 pair MMAs with both operands in shared memory (Q double
+// buffered, since the MMAs read it there: nope part 128-byte swizzled, rope
+// part 64-byte swizzled); V arrives as f16 holding the e4m3-rounded values
+// (written so by the up-projection), and P is f16, so P V is a kind::f16 pair
+// MMA with no widening in this kernel.
+constexpr int EQN_BYTES = 128 * 128;            // Q nope: 128 rows x 128 B
+constexpr int EQ_BYTES = EQN_BYTES + 128 * 64;  // + rope: 128 rows x 64 B
+constexpr int EKN_BYTES = 64 * 128;             // K nope half: 64 keys x 128 B
+constexpr int EK_BYTES = EKN_BYTES + 64 * 64;   // + rope: 64 keys x 64 B
+constexpr int E_SMEM_Q = 0;                                  // 2 slots
+constexpr int E_SMEM_K = E_SMEM_Q + 2 * EQ_BYTES;
+constexpr int E_SMEM_V = E_SMEM_K + PNK * EK_BYTES;          // f16 halves, as in the bf16 kernel
+constexpr int E_SMEM_BAR = E_SMEM_V + PNV * PV_BYTES;        // 163840
+constexpr int E_SMEM_TOTAL = E_SMEM_BAR + 256 + 1024;
+constexpr uint32_t IDESC_QK8P = idesc_e4m3(256, 128, false, false);
+constexpr uint32_t IDESC_PV16P = idesc_f16(256, 128, false, true);
+static_assert(EQ_BYTES % 1024 == 0 && EK_BYTES % 1024 == 0 && E_SMEM_V % 1024 == 0, "swizzle alignment");
+
+struct PairSmem8 {
+  uint64_t q_full[2];         // own Q landed in slot n & 1
+  uint64_t q_free[2];         // slot free: the item's last S MMA completed
+  uint64_t q_ready;           // CTA 0: both CTAs' Q landed (8 warps)
+  uint64_t k_full[PNK], k_empty[PNK];
+  uint64_t v_full[PNV], v_empty[PNV];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_done[2];
+  uint64_t o_free;
+  uint64_t drain;
+  uint32_t tmem;
+  int abort;
+};
+static_assert(sizeof(PairSmem8) <= 256, "barrier block");
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
+    attn_pair_kernel_e4m3(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap qr_map,
+                          const __grid_constant__ CUtensorMap kn_map, const __grid_constant__ CUtensorMap kr_map,
+                          const __grid_constant__ CUtensorMap v_map, const Params p, int total_items) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  PairSmem8* sh = reinterpret_cast<PairSmem8*>(smem + E_SMEM_BAR);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const int pair_id = blockIdx.x >> 1;
+  const int n_pairs = gridDim.x >> 1;
+
+  // Both CTAs of a pair see the same chunk length, so they return together.
+  if (p.bl[p.chunk] <= 0) return;
+
+  if (threadIdx.x == 0) {
+    const uint32_t lead = rank == 0 ? 1u : 0u;
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&sh->q_full[i]), 1);
+      mbar_init(smem_u32(&sh->q_free[i]), 1);
+    }
+    mbar_init(smem_u32(&sh->q_ready), 8);
+    for (int i = 0; i < PNK; ++i) {
+      mbar_init(smem_u32(&sh->k_full[i]), 1 + lead);   // CTA 0: own bytes + the relay
+      mbar_init(smem_u32(&sh->k_empty[i]), 1);
+    }
+    for (int i = 0; i < PNV; ++i) {
+      mbar_init(smem_u32(&sh->v_full[i]), 1 + lead);
+      mbar_init(smem_u32(&sh->v_empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&sh->s_full[i]), 1);
+      mbar_init(smem_u32(&sh->p_full[i]), 8);
+      mbar_init(smem_u32(&sh->o_done[i]), 1);
+    }
+    mbar_init(smem_u32(&sh->o_free), 8);
+    mbar_init(smem_u32(&sh->drain), 1);
+    sh->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(&sh->tmem), P_TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();   // barriers of both CTAs initialised, TMEM allocated
+  tc_fence_after();
+  const uint32_t tmem = sh->tmem;
+  volatile int* abort_flag = &sh->abort;
+  int32_t* status = p.status;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ Q and K producer
+    if (elect_one()) {
+      prefetch_tmap(&q_map);
+      prefetch_tmap(&qr_map);
+      prefetch_tmap(&kn_map);
+      prefetch_tmap(&kr_map);
+    }
+    __syncwarp();
+    uint32_t g = 0, it_n = 0;
+    int q_last[2] = {-1, -1}, k_last[PNK] = {-1, -1, -1, -1};
+    bool ok = true;
+    PairItem it;
+    for (int idx = pair_id; ok && next_pair(p, idx, n_pairs, total_items, rank, it); idx += n_pairs) {
+      // Q slot it_n & 1 is free once item it_n - 2's last S MMA completed
+      // (the MMAs read Q from shared memory).
+      const int qs = it_n & 1;
+      if (it_n > 1 &&
+          !(ok = mbar_wait_cluster_warp(smem_u32(&sh->q_free[qs]), ((it_n - 2) >> 1) & 1, status, abort_flag)))
+        break;
+      if (elect_one()) {
+        const uint32_t qf = smem_u32(&sh->q_full[qs]);
+        const uint32_t qd = smem_u32(smem + E_SMEM_Q + qs * EQ_BYTES);
+        mbar_expect_tx(qf, EQ_BYTES);
+        tma_load_2d(qd, &q_map, qf, it.own.h * 192, it.own.q_row0);              // nope: 128 B a row
+        tma_load_2d(qd + EQN_BYTES, &qr_map, qf, it.own.h * 192 + 128, it.own.q_row0);   // rope: 64 B
+      }
+      __syncwarp();
+      q_last[qs] = int((it_n >> 1) & 1);
+      for (int j = 0; j < it.n_kv; ++j) {
+        const uint32_t gj = g + j;
+        const int row = it.own.kv_row0 + j * BN + static_cast<int>(rank) * 64;
+        const int ks = gj % PNK;
+        if (gj >= PNK &&
+            !(ok = mbar_wait_cluster_warp(smem_u32(&sh->k_empty[ks]), ((gj / PNK) & 1) ^ 1, status, abort_flag)))
+          break;
+        if (elect_one()) {
+          const uint32_t kf = smem_u32(&sh->k_full[ks]);
+          mbar_expect_tx(kf, EK_BYTES);
+          const uint32_t kdst = smem_u32(smem + E_SMEM_K + ks * EK_BYTES);
+          tma_load_2d(kdst, &kn_map, kf, it.own.h * 128, row);      // nope: 64 keys x 128 B
+          tma_load_2d(kdst + EKN_BYTES, &kr_map, kf, 0, row);      // rope: 64 keys x 64 B
+        }
+        __syncwarp();
+        k_last[ks] = int((gj / PNK) & 1);
+      }
+      g += it.n_kv;
+      ++it_n;
+    }
+    // Drain: every issued load lands before the CTA leaves.  (In CTA 0 the
+    // K barriers also count the relay's arrival, so wait on the bytes only
+    // through the phases this warp started: a bounded wait either way.)
+    volatile int never = 0;
+    for (int s = 0; s < 2; ++s)
+      if (q_last[s] >= 0) mbar_wait_warp(smem_u32(&sh->q_full[s]), uint32_t(q_last[s]), status, &never);
+    for (int s = 0; s < PNK; ++s)
+      if (k_last[s] >= 0) mbar_wait_cluster_warp(smem_u32(&sh->k_full[s]), uint32_t(k_last[s]), status, &never);
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ V producer
+    if (elect_one()) prefetch_tmap(&v_map);
+    __syncwarp();
+    uint32_t g = 0;
+    int v_last[PNV] = {-1, -1, -1, -1};
+    bool ok = true;
+    PairItem it;
+    for (int idx = pair_id; ok && next_pair(p, idx, n_pairs, total_items, rank, it); idx += n_pairs) {
+      for (int j = 0; j < it.n_kv; ++j) {
+        const uint32_t gj = g + j;
+        const int row = it.own.kv_row0 + j * BN;
+        const int vs = gj % PNV;
+        if (gj >= PNV &&
+            !(ok = mbar_wait_cluster_warp(smem_u32(&sh->v_empty[vs]), ((gj / PNV) & 1) ^ 1, status, abort_flag)))
+          break;
+        if (elect_one()) {
+          const uint32_t vf = smem_u32(&sh->v_full[vs]);
+          mbar_expect_tx(vf, PV_BYTES);
+          tma_load_2d(smem_u32(smem + E_SMEM_V + vs * PV_BYTES), &v_map, vf,
+                      it.own.h * 128 + static_cast<int>(rank) * 64, row);
+        }
+        __syncwarp();
+        v_last[vs] = int((gj / PNV) & 1);
+      }
+      g += it.n_kv;
+    }
+    volatile int never = 0;
+    for (int s = 0; s < PNV; ++s)
+      if (v_last[s] >= 0) mbar_wait_cluster_warp(smem_u32(&sh->v_full[s]), uint32_t(v_last[s]), status, &never);
+  } else if (warp == 1) {
+    if (rank == 0) {
+      // ---------------------------------------------------------- pair MMA issuer
+      // One elected lane runs the whole loop (no reconvergence while MMAs are
+      // in flight); every commit goes to the barrier in both CTAs.
+      if (elect_one()) {
+        uint32_t g = 0, it_n = 0;
+        const uint32_t o_t = tmem + P_TM_O;
+        PairItem it;
+        for (int idx = pair_id; next_pair(p, idx, n_pairs, total_items, rank, it); idx += n_pairs) {
+          if (!mbar_wait_cluster(smem_u32(&sh->q_ready), it_n & 1, status, abort_flag)) break;
+          const int n = it.n_kv;
+          auto issue_s = [&](int j) -> bool {
+            const uint32_t gj = g + j;
+            const int ks = gj % PNK;
+            if (!mbar_wait_cluster(smem_u32(&sh->k_full[ks]), (gj / PNK) & 1, status, abort_flag)) return false;
+            tc_fence_after();
+            const uint32_t k_s = smem_u32(smem + E_SMEM_K + ks * EK_BYTES);
+            const uint32_t q_s = smem_u32(smem + E_SMEM_Q + (it_n & 1) * EQ_BYTES);
+            const uint32_t d = tmem + P_TM_S + (gj & 1) * 128;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)   // nope: 128 B a row, 32 e4m3 per MMA
+              mma_f8_ss_pair(d, sdesc(q_s + kk * 32, 16, 1024), sdesc(k_s + kk * 32, 16, 1024), IDESC_QK8P, kk > 0);
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk)   // rope: 64 B a row
+              mma_f8_ss_pair(d, sdesc(q_s + EQN_BYTES + kk * 32, 16, 512, kSwizzle64),
+                             sdesc(k_s + EKN_BYTES + kk * 32, 16, 512, kSwizzle64), IDESC_QK8P, 1);
+            tc_commit_pair(smem_u32(&sh->s_full[gj & 1]), kBoth);
+            tc_commit_pair(smem_u32(&sh->k_empty[ks]), kBoth);
+            if (j == it.n_kv - 1) tc_commit_pair(smem_u32(&sh->q_free[it_n & 1]), kBoth);
+            return true;
+          };
+          auto issue_pv = [&](int j) -> bool {
+            const uint32_t gp = g + j;
+            const int vs = gp % PNV;
+            if (!mbar_wait_cluster(smem_u32(&sh->p_full[gp & 1]), (gp >> 1) & 1, status, abort_flag)) return false;
+            if (!mbar_wait_cluster(smem_u32(&sh->v_full[vs]), (gp / PNV) & 1, status, abort_flag)) return false;
+            if (j == 0 && it_n >= 1 &&
+                !mbar_wait_cluster(smem_u32(&sh->o_free), (it_n - 1) & 1, status, abort_flag))
+              return false;
+            tc_fence_after();
+            const uint32_t v_s = smem_u32(smem + E_SMEM_V + vs * PV_BYTES);
+            const uint32_t pa = tmem + P_TM_S + (gp & 1) * 128;
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+              mma_f16_ts_pair(o_t, pa + kk * 8, sdesc(v_s + kk * 2048, PBLK, 1024), IDESC_PV16P, (j > 0 || kk > 0));
+            tc_commit_pair(smem_u32(&sh->o_done[gp & 1]), kBoth);
+            tc_commit_pair(smem_u32(&sh->v_empty[vs]), kBoth);
+            return true;
+          };
+          bool ok = issue_s(0);
+          if (ok && n > 1) ok = issue_s(1);
+          for (int j = 0; j < n && ok; ++j) {
+            ok = issue_pv(j);
+            if (ok && j + 2 < n) ok = issue_s(j + 2);
+          }
+          if (!ok) break;
+          g += n;
+          ++it_n;
+        }
+        tc_commit_pair(smem_u32(&sh->drain), 1);
+        volatile int never = 0;
+        mbar_wait(smem_u32(&sh->drain), 0, status, &never);
+      }
+      __syncwarp();
+    } else {
+      // ---------------------------------------------------------- relay (CTA 1)
+      // Forward "my half of K_j / V_j has landed" to CTA 0's ring barriers in
+      // the order CTA 0's MMAs consume them: K_0, K_1, then V_j, K_{j+2}.
+      if (elect_one()) {
+        const uint32_t k_full0 = cluster_addr(smem_u32(&sh->k_full[0]), 0);
+        const uint32_t v_full0 = cluster_addr(smem_u32(&sh->v_full[0]), 0);
+        uint32_t g = 0;
+        PairItem it;
+        auto relay_k = [&](uint32_t gj) -> bool {
+          const int ks = gj % PNK;
+          if (!mbar_wait(smem_u32(&sh->k_full[ks]), (gj / PNK) & 1, status, abort_flag)) return false;
+          mbar_arrive_cluster(k_full0 + ks * 8);
+          return true;
+        };
+        auto relay_v = [&](uint32_t gj) -> bool {
+          const int vs = gj % PNV;
+          if (!mbar_wait(smem_u32(&sh->v_full[vs]), (gj / PNV) & 1, status, abort_flag)) return false;
+          mbar_arrive_cluster(v_full0 + vs * 8);
+          return true;
+        };
+        for (int idx = pair_id; next_pair(p, idx, n_pairs, total_items, rank, it); idx += n_pairs) {
+          const int n = it.n_kv;
+          bool ok = relay_k(g);
+          if (ok && n > 1) ok = relay_k(g + 1);
+          for (int j = 0; j < n && ok; ++j) {
+            ok = relay_v(g + j);
+            if (ok && j + 2 < n) ok = relay_k(g + j + 2);
+          }
+          if (!ok) break;
+          g += n;
+        }
+      }
+      __syncwarp();
+    }
+  } else if (warp >= 2 && warp <= 5) {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int q4 = warp & 3;
+    const int row = q4 * 32 + lane;
+    const uint32_t lane_off = uint32_t(q4 * 32) << 16;
+    const float sl2 = p.scale_log2;
+    const float2 sl2v = make_float2(sl2, sl2);
+    const uint32_t q_ready0 = cluster_addr(smem_u32(&sh->q_ready), 0);
+    const uint32_t p_full0 = cluster_addr(smem_u32(&sh->p_full[0]), 0);
+    const uint32_t o_free0 = cluster_addr(smem_u32(&sh->o_free), 0);
+    uint32_t g = 0, it_n = 0;
+    bool ok = true;
+
+    // Item n's Q (read by the MMAs from shared memory) has landed in this CTA.
+    auto stage_q = [&](uint32_t n) -> bool {
+      if (!mbar_wait_warp(smem_u32(&sh->q_full[n & 1]), (n >> 1) & 1, status, abort_flag)) return false;
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(q_ready0);
+      return true;
+    };
+
+    int idx = pair_id;
+    PairItem it;
+    bool have = next_pair(p, idx, n_pairs, total_items, rank, it);
+    if (have) ok = stage_q(0);
+    while (have && ok) {
+      const Item& own = it.own;
+      const long long qpos = static_cast<long long>(own.cb) + own.i0 + row;
+      const long long lim_all = min(static_cast<long long>(own.n_cb), qpos - own.co + 1);
+      float m_run = kNegInf, l_run = 0.f;
+      for (int j = 0; j < it.n_kv; ++j) {
+        const uint32_t gj = g + j;
+        const uint32_t sb = gj & 1;
+        if (!(ok = mbar_wait_cluster_warp(smem_u32(&sh->s_full[sb]), (gj >> 1) & 1, status, abort_flag))) break;
+        tc_fence_after();
+        float x[BN];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          tmem_ld32(tmem + lane_off + P_TM_S + sb * 128 + c * 32,
+                    *reinterpret_cast<uint32_t(*)[32]>(reinterpret_cast<uint32_t*>(x) + c * 32));
+        tmem_ld_wait();
+        const long long lim = lim_all - static_cast<long long>(j) * BN;
+        if (lim < BN) {
+#pragma unroll
+          for (int k = 0; k < BN; ++k) x[k] = k < lim ? x[k] : kNegInf;
+        }
+        float mx8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = fmax3(x[i], x[8 + i], x[16 + i]);
+#pragma unroll
+        for (int k = 24; k < BN; k += 16)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], x[k + i], x[k + 8 + i]);
+        const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                               fmaxf(mx8[6], mx8[7]));
+        const float m_new = fmaxf(m_run, mx * sl2);
+        const bool need = m_new > m_run + kRescaleThreshold;
+        const float f = need ? ex2(m_run - m_new) : 1.0f;
+        if (need) m_run = m_new;
+        const float msub = m_run == kNegInf ? 0.f : m_run;
+        const float2 negm = make_float2(-msub, -msub);
+        uint32_t pk[BN / 2];
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int k = 0; k < BN / 2; ++k) {
+          const float2 t = __ffma2_rn(make_float2(x[2 * k], x[2 * k + 1]), sl2v, negm);
+          const float2 e = make_float2(ex2(t.x), ex2(t.y));
+          acc[k & 3] = __fadd2_rn(acc[k & 3], e);
+          pk[k] = pack_f16(e.x, e.y);
+        }
+        const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
+        const float2 a = __fadd2_rn(a01, a23);
+        l_run = l_run * f + (a.x + a.y);
+        if (j == it.n_kv - 1 && own.n_cb - j * BN < BN) {
+          // Keys past the sequence in the last tile: zero this CTA's half of
+          // those V rows (stale or non-finite) before P*V reads them.
+          const int vs = gj % PNV;
+          if (!(ok = mbar_wait_cluster_warp(smem_u32(&sh->v_full[vs]), (gj / PNV) & 1, status, abort_flag))) break;
+          if (j * BN + row >= own.n_cb) {
+            uint8_t* vrow = smem + E_SMEM_V + vs * PV_BYTES + row * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) reinterpret_cast<uint4*>(vrow)[c] = make_uint4(0, 0, 0, 0);
+          }
+          fence_async_smem();
+        }
+        tmem_st32(tmem + lane_off + P_TM_S + sb * 128, pk);
+        tmem_st32(tmem + lane_off + P_TM_S + sb * 128 + 32, pk + 32);
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+          // Rescale O only when the row maximum grew by more than 2^8, once P*V
+          // of the previous tile has completed.
+          if (!(ok = mbar_wait_cluster_warp(smem_u32(&sh->o_done[(gj - 1) & 1]), ((gj - 1) >> 1) & 1, status,
+                                            abort_flag)))
+            break;
+          {
+            tc_fence_after();
+            uint32_t r[32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const uint32_t ta = tmem + lane_off + P_TM_O + c * 32;
+              tmem_ld32(ta, r);
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
+              tmem_st32(ta, r);
+            }
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(p_full0 + sb * 8);
+      }
+      if (!ok) break;
+      g += it.n_kv;
+      int nidx = idx + n_pairs;
+      PairItem nx;
+      const bool have_next = next_pair(p, nidx, n_pairs, total_items, rank, nx);
+      if (have_next && !(ok = stage_q(it_n + 1))) break;
+      // ---------------------------------------------------------- epilogue
+      if (!(ok = mbar_wait_cluster_warp(smem_u32(&sh->o_done[(g - 1) & 1]), ((g - 1) >> 1) & 1, status,
+                                        abort_flag)))
+        break;
+      tc_fence_after();
+      float o[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        tmem_ld32(tmem + lane_off + P_TM_O + c * 32,
+                  *reinterpret_cast<uint32_t(*)[32]>(reinterpret_cast<uint32_t*>(o) + c * 32));
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(o_free0);
+      const Item cur = it.own;
+      it = nx;
+      idx = nidx;
+      have = have_next;
+      ++it_n;
+      store_row(p, cur, row, qpos, m_run, l_run, o);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // neither CTA frees TMEM or leaves while the pair still uses it
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, P_TMEM_COLS);
+  }
+}
+
 }  // namespace
 
-// Two-CTA clusters that can be resident at once (0 if none).
-static int pair_clusters(int device) {
+// Two-CTA clusters of `kernel` (with `smem` bytes) that can be resident at
+// once, per device (0 if none).
+template <typename Kernel>
+static int pair_clusters_of(Kernel kernel, int smem, int device, int slot) {
   static std::mutex mu;
-  static int cached[64];
-  static bool done[64];
+  static int cached[2][64];
+  static bool done[2][64];
   std::lock_guard<std::mutex> lock(mu);
   if (device < 0 || device >= 64) return 0;
-  if (!done[device]) {
-    cudaFuncSetAttribute(attn_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_TOTAL);
+  if (!done[slot][device]) {
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2);
     cfg.blockDim = dim3(P_THREADS);
-    cfg.dynamicSmemBytes = P_SMEM_TOTAL;
+    cfg.dynamicSmemBytes = smem;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, attn_pair_kernel, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
       cudaGetLastError();
       n = 0;
     }
-    cached[device] = n;
-    done[device] = true;
+    cached[slot][device] = n;
+    done[slot][device] = true;
   }
-  return cached[device];
+  return cached[slot][device];
+}
+static int pair_clusters(int device) { return pair_clusters_of(attn_pair_kernel, P_SMEM_TOTAL, device, 0); }
+static int pair_clusters_e4m3(int device) {
+  return pair_clusters_of(attn_pair_kernel_e4m3, E_SMEM_TOTAL, device, 1);
 }
 
 bool attention_pair_available() {
@@ -566,6 +997,52 @@ cudaError_t launch_attention_pair(const AttnArgs& a, cudaStream_t stream) {
   const int grid = 2 * static_cast<int>(total < clusters ? total : clusters);
   attn_pair_kernel<<<grid, P_THREADS, P_SMEM_TOTAL, stream>>>(maps[0], maps[1], maps[2], maps[3], p,
                                                              static_cast<int>(total));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attention_pair_e4m3(const AttnArgs& a, cudaStream_t stream) {
+  const uint64_t HN = static_cast<uint64_t>(a.H) * 128;
+  const uint64_t QW = static_cast<uint64_t>(a.H) * 192;
+  const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  CUtensorMap maps[5];
+  const bool ok =
+      encode_2d(&maps[0], a.q, u8, QW, a.T_q, QW, 128, BM, CU_TENSOR_MAP_SWIZZLE_128B) &&    // Q nope
+      encode_2d(&maps[1], a.q, u8, QW, a.T_q, QW, 64, BM, CU_TENSOR_MAP_SWIZZLE_64B) &&      // Q rope
+      encode_2d(&maps[2], a.k_nope, u8, HN, a.S, HN, 128, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+      encode_2d(&maps[3], a.k_rope, u8, 64, a.S, 64, 64, 64, CU_TENSOR_MAP_SWIZZLE_64B) &&
+      encode_2d(&maps[4], a.v, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, HN, a.S, HN * 2, 64, BN,
+                CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!ok) return cudaErrorInvalidValue;
+  Params p;
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.lse = a.lse;
+  p.o_acc = a.o_acc;
+  p.lse_acc = a.lse_acc;
+  p.iro = a.iro;
+  p.cache_len = a.cache_len;
+  p.bro = a.bro;
+  p.co = a.co;
+  p.bl = a.bl;
+  p.chunk = a.chunk;
+  p.B = a.B;
+  p.H = a.H;
+  p.n_qtiles = (a.max_prompt_len + BM - 1) / BM;
+  // Heads per group: about 32 MB of K_nope (e4m3) + V (f16) in L2.
+  p.head_group = static_cast<int>(std::max<uint64_t>(1, (32ull << 20) / (static_cast<uint64_t>(a.S) * 384)));
+  if (p.head_group > a.H) p.head_group = a.H;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.v_scale = a.v_scale;
+  p.status = a.status;
+  const long long total = static_cast<long long>((p.n_qtiles + 1) / 2) * a.B * a.H;
+  if (total <= 0) return cudaSuccess;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const int clusters = pair_clusters_e4m3(dev);
+  if (clusters <= 0) return cudaErrorInvalidConfiguration;
+  const int grid = 2 * static_cast<int>(total < clusters ? total : clusters);
+  attn_pair_kernel_e4m3<<<grid, P_THREADS, E_SMEM_TOTAL, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4],
+                                                                  p, static_cast<int>(total));
   return cudaGetLastError();
 }
 

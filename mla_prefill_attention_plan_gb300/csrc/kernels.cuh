@@ -74,6 +74,9 @@ bool attention_pair_available();
 // the one-SM kernel).
 bool attention_uses_pair();
 cudaError_t launch_attention_pair(const AttnArgs& a, cudaStream_t stream);
+// e4m3 Q / K with V as f16 holding e4m3-rounded values (as mla_upproject
+// writes it), on two-SM pairs; the only e4m3 attention kernel.
+cudaError_t launch_attention_pair_e4m3(const AttnArgs& a, cudaStream_t stream);
 
 // Tensor-map encoder and device properties (abi.cu).
 bool encode_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, uint64_t inner,

@@ -183,15 +183,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int m0 = (t % num_m) * BM;
       const int nt = t / num_m;
       const bool row_ok = m0 + q * 32 + lane < rows;
-      constexpr int SEG_COLS = 128 / ELT;      // columns per 128-byte staging row
-      constexpr int NSEG = BN / SEG_COLS;      // 4 (bf16) or 2 (e4m3)
+      // Segments of one 128-byte staging row each: bf16, 64 columns; e4m3, a
+      // whole 128-column head of K (e4m3) or half a head of V (64 columns as
+      // f16 holding the e4m3-rounded values, the operand the attention's P*V
+      // reads without widening).
 #pragma unroll 1
-      for (int seg = 0; seg < NSEG; ++seg) {
+      for (int seg = 0; seg < 4; ++seg) {
+        const int blk = seg >> 1;
+        const int hf = 2 * nt + blk;             // 128-wide block of N
+        const bool k_blk = hf < H;
+        if (ELT == 1 && k_blk && (seg & 1)) continue;   // e4m3 K head: one segment
+        const int col = (ELT == 1 && k_blk) ? blk * 128 : seg * 64;   // within the 256-wide tile
+        const int ncols = (ELT == 1 && k_blk) ? 128 : 64;
         uint32_t packed[32];
 #pragma unroll
-        for (int part = 0; part < SEG_COLS / 32; ++part) {
+        for (int part = 0; part < 4; ++part) {
+          if (part * 32 >= ncols) break;
           uint32_t r[32];
-          tmem_ld32(tmem + lane_off + acc * BN + seg * SEG_COLS + part * 32, r);
+          tmem_ld32(tmem + lane_off + acc * BN + col + part * 32, r);
           tmem_ld_wait();
           if (ELT == 2) {
 #pragma unroll
@@ -199,7 +208,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               packed[part * 16 + i] = row_ok ? pack_bf16(__uint_as_float(r[2 * i]) * out_scale,
                                                          __uint_as_float(r[2 * i + 1]) * out_scale)
                                              : 0u;
-          } else {
+          } else if (k_blk) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const uint32_t lo = pack_e4m3(__uint_as_float(r[4 * i]) * out_scale,
@@ -208,9 +217,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                             __uint_as_float(r[4 * i + 3]) * out_scale);
               packed[part * 8 + i] = row_ok ? (lo | (hi << 16)) : 0u;
             }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              packed[part * 16 + i] =
+                  row_ok ? e4m3x2_to_f16x2(pack_e4m3(__uint_as_float(r[2 * i]) * out_scale,
+                                                     __uint_as_float(r[2 * i + 1]) * out_scale))
+                         : 0u;
           }
         }
-        if (seg == NSEG - 1) {
+        const bool last = seg == 3 || (ELT == 1 && seg == 2 && 2 * nt + 1 < H);
+        if (last) {
           // All of this accumulator has been read: hand it back to the MMA warp.
           tc_fence_before();
           __syncwarp();
@@ -227,9 +244,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         fence_async_smem();
         __syncwarp();
         if (lane == 0) {
-          const int col = seg * SEG_COLS;          // within the 256-wide tile
-          const int hf = 2 * nt + col / 128;       // 128-wide block of N
-          const CUtensorMap* omap = hf < H ? &k_out_map : &v_out_map;
+          const CUtensorMap* omap = k_blk ? &k_out_map : &v_out_map;
           tma_store_2d(omap, smem_u32(sb), (hf % H) * 128 + (col % 128), m0 + q * 32);
           bulk_commit();
         }
@@ -264,7 +279,8 @@ cudaError_t launch_upproject(const UpprojArgs& a, cudaStream_t stream) {
             encode_2d(&wk_map, a.w_k, dt, 512, HN, 512ull * elt, box_k, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
             encode_2d(&wuv_map, a.w_uv, dt, 512, HN, 512ull * elt, box_k, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
             encode_2d(&k_map, a.k_nope, dt, HN, a.S, HN * elt, box_k, 32, CU_TENSOR_MAP_SWIZZLE_128B) &&
-            encode_2d(&v_map, a.v, dt, HN, a.S, HN * elt, box_k, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+            encode_2d(&v_map, a.v, elt == 2 ? dt : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, HN, a.S, HN * 2, 64, 32,
+                      CU_TENSOR_MAP_SWIZZLE_128B);   // V: bf16, or f16 holding e4m3-rounded values
   if (!ok) return cudaErrorInvalidValue;
   // Upper bound on tiles (the device reads the chunk's real row count).
   const int max_tiles = static_cast<int>((a.S + BM - 1) / BM) * a.H;

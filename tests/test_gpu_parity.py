@@ -227,7 +227,7 @@ def test_upproject(dtype, H, rows, S, upproj_kernel):
     wk = (torch.randn(H * 128, 512, generator=gen) * wstd).to(tdt)
     wuv = (torch.randn(H, 128, 512, generator=gen) * wstd).to(tdt)
     kn = torch.full((S, H, 128), 3.0).to(tdt).to(DEV)
-    vv = torch.full((S, H, 128), 3.0).to(tdt).to(DEV)
+    vv = torch.full((S, H, 128), 3.0).to(torch.bfloat16 if dtype == "bf16" else torch.float16).to(DEV)
     bl = torch.tensor([rows], dtype=torch.int32, device=DEV)
     mla.check(mla.mla_upproject(kn, vv, ckv.to(DEV), wk.to(DEV), wuv.to(DEV), bl, 0, S, H,
                                 mla.MLA_BF16 if dtype == "bf16" else mla.MLA_E4M3, 1.0, wsc, 1.0))
@@ -242,6 +242,9 @@ def test_upproject(dtype, H, rows, S, upproj_kernel):
         bound = lambda ref: 2.0 ** -3 * np.abs(ref) + 2.0 ** -8
     assert np.all(np.abs(gk[:rows] - rk) <= bound(rk))
     assert np.all(np.abs(gv[:rows] - rv) <= bound(rv))
+    if dtype == "e4m3":
+        # V is stored as f16 but must hold exactly the e4m3-rounded values
+        assert np.array_equal(gv[:rows], O.round_to_e4m3(gv[:rows]))
     pad = min(S, -(-rows // 128) * 128)
     assert np.all(gk[rows:pad] == 0) and np.all(gv[rows:pad] == 0)   # zero-filled tile tail
     assert np.all(gk[pad:] == 3.0) and np.all(gv[pad:] == 3.0)       # untouched beyond it
@@ -301,7 +304,9 @@ def _attention_stage(w, seed_base=11):
 
     def operands(ch):
         kn, vv, kr = ops[ch]
-        return (O.decode(O.codes(kn), dt), O.decode(O.codes(kr), dt), O.decode(O.codes(vv), dt))
+        # V of the e4m3 path is float16 holding e4m3 values: read it exactly
+        v64 = vv.double().numpy() if dt == "e4m3" else O.decode(O.codes(vv), dt)
+        return (O.decode(O.codes(kn), dt), O.decode(O.codes(kr), dt), v64)
     ref = O.attention_over_chunks(O.decode(c["q"], dt), operands, plan,
                                   c["input_row_offsets"], c["cache_lengths"], inp["scale"])
     return _compare(out, ref, dt, lse)

@@ -169,10 +169,14 @@ def make_inputs(w: Workload, with_w_uk: bool = False, new_lens=None, cache_lens=
 
 def make_attention_operands(w: Workload, rows: int, seed_offset: int = 7):
     """Direct K_nope / V / k_rope buffers ([rows,H,128], [rows,H,128], [rows,64]),
-    N(0,1) in the workload's dtype, for testing the attention stage on its own."""
+    N(0,1) in the workload's dtype, for testing the attention stage on its own.
+    For e4m3, V is stored as float16 holding the e4m3-rounded values (the
+    layout the up-projection writes for the attention)."""
     gen = torch.Generator().manual_seed(w.seed + seed_offset)
     k_nope = _to_storage(_normal(gen, (rows, w.H, QK_NOPE)), w.dtype)
     v = _to_storage(_normal(gen, (rows, w.H, V_DIM)), w.dtype)
+    if w.dtype == "e4m3":
+        v = v.to(torch.float16)   # exact
     k_rope = _to_storage(_normal(gen, (rows, QK_ROPE)), w.dtype)
     return k_nope, v, k_rope
 
