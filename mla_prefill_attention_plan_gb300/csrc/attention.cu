@@ -448,6 +448,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ++it_n;
       store_row(p, cur, row, qpos, m_run, l_run, o);
     }
+    // The completion of the P*V before the last (the other o_done barrier)
+    // has arrived too: no asynchronous arrival may reach a CTA that has left.
+    if (ok && g >= 2)
+      mbar_wait_warp(smem_u32(&sh->o_done[(g - 2) & 1]), ((g - 2) >> 1) & 1, status, abort_flag);
   }
 
   tc_fence_before();

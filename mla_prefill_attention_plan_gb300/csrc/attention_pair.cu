@@ -203,6 +203,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     if (q_last >= 0) mbar_wait_warp(smem_u32(&sh->q_full), uint32_t(q_last), status, &never);
     for (int s = 0; s < PNK; ++s)
       if (k_last[s] >= 0) mbar_wait_cluster_warp(smem_u32(&sh->k_full[s]), uint32_t(k_last[s]), status, &never);
+    // ... and every stage release the pair MMAs multicast to this CTA has
+    // arrived: an asynchronous arrival must not reach a CTA that has left.
+    for (int s = 0; s < PNK; ++s)
+      if (k_last[s] >= 0) mbar_wait_cluster_warp(smem_u32(&sh->k_empty[s]), uint32_t(k_last[s]), status, abort_flag);
   } else if (warp == 6) {
     // ------------------------------------------------------------ V producer
     if (elect_one()) prefetch_tmap(&v_map);
@@ -233,6 +237,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     volatile int never = 0;
     for (int s = 0; s < PNV; ++s)
       if (v_last[s] >= 0) mbar_wait_cluster_warp(smem_u32(&sh->v_full[s]), uint32_t(v_last[s]), status, &never);
+    for (int s = 0; s < PNV; ++s)
+      if (v_last[s] >= 0) mbar_wait_cluster_warp(smem_u32(&sh->v_empty[s]), uint32_t(v_last[s]), status, abort_flag);
   } else if (warp == 1) {
     if (rank == 0) {
       // ---------------------------------------------------------- pair MMA issuer
@@ -484,6 +490,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
       ++it_n;
       store_row(p, cur, row, qpos, m_run, l_run, o);
     }
+    // The completion of the P*V before the last (the other o_done barrier)
+    // has arrived too: no asynchronous arrival may reach a CTA that has left.
+    if (ok && g >= 2)
+      mbar_wait_cluster_warp(smem_u32(&sh->o_done[(g - 2) & 1]), ((g - 2) >> 1) & 1, status, abort_flag);
   }
 
   tc_fence_before();
@@ -639,6 +649,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
       if (q_last[s] >= 0) mbar_wait_warp(smem_u32(&sh->q_full[s]), uint32_t(q_last[s]), status, &never);
     for (int s = 0; s < PNK; ++s)
       if (k_last[s] >= 0) mbar_wait_cluster_warp(smem_u32(&sh->k_full[s]), uint32_t(k_last[s]), status, &never);
+    // ... and every slot and stage release the pair MMAs multicast to this CTA
+    // has arrived: an asynchronous arrival must not reach a CTA that has left.
+    for (int s = 0; s < 2; ++s)
+      if (q_last[s] >= 0) mbar_wait_cluster_warp(smem_u32(&sh->q_free[s]), uint32_t(q_last[s]), status, abort_flag);
+    for (int s = 0; s < PNK; ++s)
+      if (k_last[s] >= 0) mbar_wait_cluster_warp(smem_u32(&sh->k_empty[s]), uint32_t(k_last[s]), status, abort_flag);
   } else if (warp == 6) {
     // ------------------------------------------------------------ V producer
     if (elect_one()) prefetch_tmap(&v_map);
@@ -669,6 +685,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     volatile int never = 0;
     for (int s = 0; s < PNV; ++s)
       if (v_last[s] >= 0) mbar_wait_cluster_warp(smem_u32(&sh->v_full[s]), uint32_t(v_last[s]), status, &never);
+    for (int s = 0; s < PNV; ++s)
+      if (v_last[s] >= 0) mbar_wait_cluster_warp(smem_u32(&sh->v_empty[s]), uint32_t(v_last[s]), status, abort_flag);
   } else if (warp == 1) {
     if (rank == 0) {
       // ---------------------------------------------------------- pair MMA issuer
@@ -909,6 +927,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
       ++it_n;
       store_row(p, cur, row, qpos, m_run, l_run, o);
     }
+    // The completion of the P*V before the last (the other o_done barrier)
+    // has arrived too: no asynchronous arrival may reach a CTA that has left.
+    if (ok && g >= 2)
+      mbar_wait_cluster_warp(smem_u32(&sh->o_done[(g - 2) & 1]), ((g - 2) >> 1) & 1, status, abort_flag);
   }
 
   tc_fence_before();

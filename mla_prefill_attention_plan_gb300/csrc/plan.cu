@@ -8,7 +8,8 @@
 // so the whole plan is one prefix sum followed by independent writes.
 //
 // Small batches run in one CTA (warp-shuffle scan + a scan of warp totals);
-// large batches run in three passes over tiles (described below).
+// large batches run in two passes over tiles (described below).
+
 #include "kernels.cuh"
 
 namespace mla {
@@ -114,126 +115,184 @@ __global__ void __launch_bounds__(kThreads) plan_one_cta(uint32_t* bro, uint32_t
   write_tail(bro, bl, B, max_chunks, S, carry, s_bad, status);
 }
 
-// Large batches: three passes over tiles of 4096 sequences (256 threads, each
-// lane of a warp owning 16 sequences strided by 32, so every load and store of
-// a warp is one coalesced 128-byte access).
-//   pass 1  per-tile total of the context lengths, parked in the tile's own
-//           first entry of cache_offsets row 0 (that row is zero by definition
-//           and is rewritten by pass 3);
-//   pass 2  one CTA turns the parked totals into exclusive tile prefixes in
-//           place and writes buffer_lengths, the [c][B] column and the status;
-//   pass 3  every tile reads its own prefix, scans its sequences with warp
-//           shuffles and writes its part of every table row (row 0 of
-//           cache_offsets comes out zero, overwriting the parked value).
-constexpr int kWThreads = 256;
-constexpr int kWPerLane = 16;
-constexpr int kWTile = kWThreads * kWPerLane;   // 4096
+// Large batches: two passes over tiles of 2048 sequences (256 threads, each
+// lane of a warp owning 8 sequences strided by 32, so every load and store of
+// a warp is one coalesced 128-byte access), with no CTA waiting for another:
+//   pass A (plan_tile_totals)  each tile's total context length, stored in
+//                              cache_offsets row 0, word 1 + t;
+//   pass B (plan_tile_tables)  loads and scans its own sequences in registers
+//                              (overlapping pass A: it is a programmatic
+//                              dependent launch and waits for pass A only
+//                              before it reads the totals), adds the totals of
+//                              the tiles before it, and writes every table row
+//                              chunk by chunk.
+// Row 0 of cache_offsets is zero by definition, so it holds the scratch:
+// word 0 counts finished pass-B tiles (zeroed by pass A), words 1..ntiles the
+// tile totals (saturated to 32 bits).  No pass-B tile writes its row-0 entries
+// there; the last pass-B tile to finish zeroes them, so row 0 ends all zero as
+// the closed form says.  With TOT < 2^31 (anything larger is reported as bad
+// offsets) every prefix fits in 32 bits, and so does the table arithmetic.
+constexpr int kSThreads = 256;
+constexpr int kSWarps = kSThreads / 32;
+constexpr int kSPerLane = 8;
+constexpr int kSTile = kSThreads * kSPerLane;   // 2048
 
-__device__ __forceinline__ int tile_elem(int base, int warp, int lane, int k) {
-  return base + warp * (32 * kWPerLane) + k * 32 + lane;
+__device__ __forceinline__ uint32_t sat32(uint64_t v) {
+  return v > 0xFFFFFFFFull ? 0xFFFFFFFFu : static_cast<uint32_t>(v);
 }
 
-__global__ void __launch_bounds__(kWThreads) plan_tile_sums(uint32_t* co_row0, const uint32_t* iro,
-                                                            const uint32_t* cache_len, int B) {
-  __shared__ uint64_t warp_sum[kWThreads / 32];
-  const int base = blockIdx.x * kWTile;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+__device__ __forceinline__ uint64_t warp_sum64(uint64_t v) {
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+  return v;
+}
+
+// Block-wide sum of one 64-bit value per thread (every thread gets it).
+__device__ __forceinline__ uint64_t block_sum64(uint64_t v, uint64_t* red) {
+  v = warp_sum64(v);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  uint64_t s = 0;
+#pragma unroll
+  for (int w = 0; w < kSWarps; ++w) s += red[w];
+  return s;
+}
+
+__global__ void __launch_bounds__(kSThreads) plan_tile_totals(uint32_t* co, const uint32_t* iro,
+                                                              const uint32_t* cache_len, int B) {
+  __shared__ uint64_t red[kSWarps];
+  // Let pass B's CTAs start their own loads while this pass runs.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int t = blockIdx.x;
+  const int base = t * kSTile;
   uint64_t v = 0;
 #pragma unroll
-  for (int k = 0; k < kWPerLane; ++k) {
-    const int e = tile_elem(base, warp, lane, k);
+  for (int k = 0; k < kSPerLane; ++k) {
+    const int e = base + k * kSThreads + static_cast<int>(threadIdx.x);
     if (e < B) v += cache_len[e];
   }
-#pragma unroll
-  for (int d = 16; d > 0; d >>= 1) v += __shfl_down_sync(0xffffffffu, v, d);
-  if (lane == 0) warp_sum[warp] = v;
-  __syncthreads();
+  const uint64_t tot = block_sum64(v, red);
   if (threadIdx.x == 0) {
-    uint64_t t = 0;
-    for (int w = 0; w < kWThreads / 32; ++w) t += warp_sum[w];
     // New tokens of the tile telescope to a difference of two offsets (a
-    // decreasing pair is reported by pass 3; clamp so the sum stays sane).
-    const int end = min(base + kWTile, B);
-    const uint32_t a = iro[base], e = iro[end];
-    t += e >= a ? (e - a) : 0;
-    co_row0[base] = t > 0xFFFFFFFFull ? 0xFFFFFFFFu : static_cast<uint32_t>(t);
+    // decreasing pair is reported by pass B).
+    const uint32_t a = iro[base], e = iro[min(base + kSTile, B)];
+    co[1 + t] = sat32(tot + (e >= a ? e - a : 0u));
+    if (t == 0) co[0] = 0u;
   }
 }
 
-__global__ void __launch_bounds__(kThreads) plan_tile_scan(uint32_t* bro, uint32_t* co_row0,
-                                                           int32_t* bl, const uint32_t* iro, int B,
-                                                           int max_chunks, uint32_t S,
-                                                           int32_t* status) {
-  __shared__ uint64_t warp_tot[32];
-  const int ntiles = (B + kWTile - 1) / kWTile;
-  uint64_t carry = 0;
-  for (int t0 = 0; t0 < ntiles; t0 += kThreads) {
-    const int t = t0 + threadIdx.x;
-    const uint64_t v = t < ntiles ? co_row0[static_cast<size_t>(t) * kWTile] : 0;
-    uint64_t round_total;
-    const uint64_t incl = block_scan(v, warp_tot, round_total);
-    if (t < ntiles) {
-      const uint64_t excl = carry + incl - v;
-      co_row0[static_cast<size_t>(t) * kWTile] = excl > 0xFFFFFFFFull ? 0xFFFFFFFFu : uint32_t(excl);
-    }
-    carry += round_total;
-  }
-  write_tail(bro, bl, B, max_chunks, S, carry, iro[0] != 0, status);
-}
-
-__global__ void __launch_bounds__(kWThreads) plan_tile_write(uint32_t* bro, uint32_t* co, const uint32_t* iro,
-                                                             const uint32_t* cache_len, int B,
-                                                             int max_chunks, uint32_t S,
-                                                             int32_t* status) {
-  __shared__ uint64_t warp_sum[kWThreads / 32];
-  __shared__ uint64_t tile_prefix;
-  const int base = blockIdx.x * kWTile;
+__global__ void __launch_bounds__(kSThreads, 5) plan_tile_tables(uint32_t* bro, uint32_t* co, int32_t* bl,
+                                                                 const uint32_t* iro,
+                                                                 const uint32_t* cache_len, int B,
+                                                                 int ntiles, int max_chunks, uint32_t S,
+                                                                 int32_t* status) {
+  __shared__ uint32_t warp_tot[kSWarps];
+  __shared__ uint64_t red[kSWarps];
+  __shared__ int s_last, s_bad;
+  const int t = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) tile_prefix = co[base];   // parked by pass 2
-  uint32_t L[kWPerLane];
+  const int e0 = t * kSTile + warp * (32 * kSPerLane) + lane;   // this thread's first sequence
+  const int nk = B > e0 ? min(kSPerLane, (B - e0 + 31) / 32) : 0;
+  const uint32_t n_scratch = 1u + static_cast<uint32_t>(ntiles);
+  if (threadIdx.x == 0) s_bad = 0;
+
+  // Context lengths and the warp-local exclusive scan of each 32-wide group.
+  uint32_t L[kSPerLane], ex[kSPerLane];
+  uint32_t run = 0;
   int bad = 0;
-  uint64_t mine = 0;
 #pragma unroll
-  for (int k = 0; k < kWPerLane; ++k) {
-    const int e = tile_elem(base, warp, lane, k);
+  for (int k = 0; k < kSPerLane; ++k) {
+    const int e = e0 + k * 32;
     uint32_t l = 0;
     if (e < B) {
       const uint32_t a = iro[e], n = iro[e + 1];
-      if (n < a) bad = 1;
-      l = cache_len[e] + (n >= a ? n - a : 0u);
+      const uint64_t l64 = static_cast<uint64_t>(cache_len[e]) + (n >= a ? n - a : 0u);
+      bad |= (n < a) | (l64 >= (1ull << 31));
+      l = static_cast<uint32_t>(l64);
     }
     L[k] = l;
-    mine += l;
-  }
-  uint64_t wsum = mine;
-#pragma unroll
-  for (int d = 16; d > 0; d >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, d);
-  if (lane == 0) warp_sum[warp] = wsum;
-  __syncthreads();   // also orders every read of the parked prefix before row 0 is rewritten
-  uint64_t carry = tile_prefix;
-  for (int w = 0; w < warp; ++w) carry += warp_sum[w];
-#pragma unroll
-  for (int k = 0; k < kWPerLane; ++k) {
-    const int e = tile_elem(base, warp, lane, k);
-    uint64_t incl = L[k];
+    uint32_t incl = l;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-      const uint64_t n = __shfl_up_sync(0xffffffffu, incl, d);
-      if (lane >= d) incl += n;
+      const uint32_t v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
     }
-    const uint64_t excl = carry + incl - L[k];
-    carry += __shfl_sync(0xffffffffu, incl, 31);
-    if (e < B) {
-      for (int c = 0; c < max_chunks; ++c) {
-        const int64_t lo = static_cast<int64_t>(c) * S;
-        bro[static_cast<size_t>(c) * (B + 1) + e] =
-            static_cast<uint32_t>(clamp_u64(static_cast<int64_t>(excl) - lo, S));
-        co[static_cast<size_t>(c) * B + e] =
-            static_cast<uint32_t>(clamp_u64(lo - static_cast<int64_t>(excl), static_cast<int64_t>(L[k])));
-      }
+    ex[k] = run + incl - l;
+    run += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) warp_tot[warp] = run;
+  if (bad) s_bad = 1;
+
+  // Pass A has completed (and its writes are visible) past this point.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  uint64_t pv = 0;
+#pragma unroll 8
+  for (int j = threadIdx.x; j < t; j += kSThreads) pv += __ldcg(co + 1 + j);
+  const uint64_t prefix = block_sum64(pv, red);   // (its barrier also publishes warp_tot)
+
+  if (t == ntiles - 1 && warp == 0) {
+    // The last tile knows the total: the [c][B] column, buffer_lengths and
+    // the status (2^31 tokens or more reads as bad offsets).
+    const uint64_t tot = prefix + __ldcg(co + 1 + t);
+    const bool bad_all = iro[0] != 0 || tot >= (1ull << 31);
+    for (int c = lane; c < max_chunks; c += 32) {
+      const int64_t lo = static_cast<int64_t>(c) * S;
+      const int64_t rest = static_cast<int64_t>(tot) - lo;
+      bro[static_cast<size_t>(c) * (B + 1) + B] = static_cast<uint32_t>(clamp_u64(rest, S));
+      bl[c] = rest > 0 ? static_cast<int32_t>(rest < S ? rest : S) : -1;
+    }
+    if (lane == 0) {
+      const uint64_t needed = (tot + S - 1) / S;
+      if (bad_all)
+        set_status(status, MLA_DEV_BAD_OFFSETS);
+      else if (needed > static_cast<uint64_t>(max_chunks))
+        set_status(status, MLA_DEV_TOO_MANY_CHUNKS);
     }
   }
-  if (bad) set_status(status, MLA_DEV_BAD_OFFSETS);
+  if (threadIdx.x == 0 && (s_bad || prefix >= (1ull << 31))) set_status(status, MLA_DEV_BAD_OFFSETS);
+
+  // Every table row, chunk by chunk: with m = max(P_b, c*S),
+  //   buffer_row_offsets = min(m - c*S, S),  cache_offsets = min(m - P_b, L_b).
+  uint32_t off = static_cast<uint32_t>(prefix);
+  for (int w = 0; w < warp; ++w) off += warp_tot[w];
+#pragma unroll
+  for (int k = 0; k < kSPerLane; ++k) ex[k] += off;
+  uint32_t* br = bro + e0;
+  uint32_t* cr = co + e0;
+#pragma unroll
+  for (int k = 0; k < kSPerLane; ++k) {
+    if (k < nk) {
+      br[32 * k] = min(ex[k], S);
+      if (static_cast<uint32_t>(e0 + 32 * k) >= n_scratch) cr[32 * k] = 0u;
+    }
+  }
+  uint64_t lo64 = S;
+  for (int c = 1; c < max_chunks; ++c) {
+    br += B + 1;
+    cr += B;
+    const uint32_t lo = sat32(lo64);
+#pragma unroll
+    for (int k = 0; k < kSPerLane; ++k) {
+      if (k < nk) {
+        const uint32_t m = max(ex[k], lo);
+        br[32 * k] = min(m - lo, S);
+        cr[32 * k] = min(m - ex[k], L[k]);
+      }
+    }
+    lo64 += S;
+  }
+
+  // The last tile to finish zeroes the scratch (row 0 of cache_offsets).
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(co, 1u) == static_cast<uint32_t>(ntiles - 1);
+  }
+  __syncthreads();
+  if (s_last) {
+    __threadfence();
+    for (uint32_t i = threadIdx.x; i < n_scratch; i += kSThreads) co[i] = 0u;
+  }
 }
 
 }  // namespace
@@ -245,11 +304,23 @@ cudaError_t launch_plan(uint32_t* bro, uint32_t* co, int32_t* bl, const uint32_t
     plan_one_cta<<<1, kThreads, 0, stream>>>(bro, co, bl, iro, cache_len, B, max_chunks, S, status);
     return cudaGetLastError();
   }
-  const int ntiles = (B + kWTile - 1) / kWTile;
-  plan_tile_sums<<<ntiles, kWThreads, 0, stream>>>(co, iro, cache_len, B);
-  plan_tile_scan<<<1, kThreads, 0, stream>>>(bro, co, bl, iro, B, max_chunks, S, status);
-  plan_tile_write<<<ntiles, kWThreads, 0, stream>>>(bro, co, iro, cache_len, B, max_chunks, S, status);
-  return cudaGetLastError();
+  const int ntiles = (B + kSTile - 1) / kSTile;
+  plan_tile_totals<<<ntiles, kSThreads, 0, stream>>>(co, iro, cache_len, B);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  // Pass B as a programmatic dependent launch of pass A.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ntiles);
+  cfg.blockDim = dim3(kSThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, plan_tile_tables, bro, co, bl, iro, cache_len, B, ntiles, max_chunks, S,
+                            status);
 }
 
 }  // namespace mla

@@ -130,6 +130,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       volatile int never = 0;
       for (int s = 0; s < STAGES; ++s)
         if (last_ph[s] >= 0) mbar_wait(smem_u32(&sh->full[s]), uint32_t(last_ph[s]), status, &never);
+      // ... and every stage release the MMAs committed to this CTA has
+      // arrived: an asynchronous arrival must not reach a CTA that has left.
+      for (int s = 0; s < STAGES; ++s)
+        if (last_ph[s] >= 0) mbar_wait(smem_u32(&sh->empty[s]), uint32_t(last_ph[s]), status, abort_flag);
     }
   } else if (warp == 1) {
     // One elected lane runs the whole loop, waits included; the warp

@@ -99,13 +99,54 @@ def test_plan_random_fuzz():
 
 @pytest.mark.parametrize("B", [4096, 4097, 20000, 300000])
 def test_plan_many_sequences(B):
-    """Multi-tile plans (tiles of 4096 sequences); 300000 sequences make 74 tiles."""
+    """Multi-tile plans (tiles of 2048 sequences); 300000 sequences make 147 tiles."""
     rng = np.random.default_rng(B)
     new = rng.integers(0, 64, B)
     cache = rng.integers(0, 64, B)
     S = max(20000, int((new + cache).sum()) // 3)
     need = -(-int((new + cache).sum()) // S)
     _assert_plan_equal(np.concatenate([[0], np.cumsum(new)]), cache, S, need + 1)
+
+
+def test_plan_many_tiles_garbage_tables():
+    """600000 sequences (293 tiles of 2048), with the tables full of garbage
+    beforehand (row 0 of cache_offsets holds scratch during
+    the call and must come out zero); called twice on the same buffers."""
+    rng = np.random.default_rng(41)
+    B = 600_000
+    new, cache = rng.integers(0, 64, B), rng.integers(0, 64, B)
+    iro = np.concatenate([[0], np.cumsum(new)])
+    S = int((new + cache).sum()) // 2 + 1
+    mc = 3
+    o = O.prefill_plan(iro, cache, S, mc)
+    bro = torch.full((mc, B + 1), -7, dtype=torch.int32, device=DEV)
+    co = torch.full((mc, B), -7, dtype=torch.int32, device=DEV)
+    bl = torch.full((mc,), -7, dtype=torch.int32, device=DEV)
+    iro_d, cl_d = _i32(iro).to(DEV), _i32(cache).to(DEV)
+    for _ in range(2):
+        st = torch.zeros(1, dtype=torch.int32, device=DEV)
+        mla.check(mla.mla_prefill_plan(bro, co, bl, iro_d, cl_d, B, mc, S, st))
+        torch.cuda.synchronize()
+        assert int(st.item()) == o[3] == 0
+        np.testing.assert_array_equal(bro.cpu().numpy(), o[0])
+        np.testing.assert_array_equal(co.cpu().numpy(), o[1])
+        np.testing.assert_array_equal(bl.cpu().numpy(), o[2])
+
+
+def test_plan_multi_tile_status_codes():
+    """Status codes from the multi-tile path: a decreasing offset in a middle
+    tile, a total of 2^31 tokens or more, and too few chunk rows."""
+    B = 50000
+    new = np.full(B, 3)
+    cache = np.full(B, 5)
+    iro = np.concatenate([[0], np.cumsum(new)])
+    bad = iro.copy()
+    bad[30001] = bad[30000] - 1
+    assert gpu_plan(bad, cache, 1000, 500)[3] == mla.MLA_DEV_BAD_OFFSETS
+    big = np.full(B, 50000)     # 2.5e9 context tokens
+    assert gpu_plan(iro, big, 1 << 30, 4)[3] == mla.MLA_DEV_BAD_OFFSETS
+    assert gpu_plan(iro, cache, 1000, 399)[3] == mla.MLA_DEV_TOO_MANY_CHUNKS
+    _assert_plan_equal(iro, cache, 1000, 399)        # the rows that exist are still right
 
 
 def test_plan_unaligned_tables():

@@ -78,6 +78,14 @@ WORKLOADS = {
                             new_lens=(16384,), cache_lens=(16384,)),
 }
 
+# Reduced cases of the workloads above, small enough for a full profiler capture
+# (a few hundred MB on the device); timed by bench.py, not parity cases.
+PROFILE_CASES = {
+    "longctx_fp8_4k": Workload("longctx_fp8_4k", B=1, H=128, page_size=128,
+                               buffer_token_size=4096, max_chunks=2, dtype="e4m3",
+                               new_lens=(4096,), cache_lens=(4096,)),
+}
+
 
 def lengths(w: Workload):
     """Seeded (new_lens, cache_lens) as int64 numpy arrays."""
