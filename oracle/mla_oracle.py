@@ -11,8 +11,9 @@ API references from the Modular MAX kernel library:
   * "mla_prefill_plan" -- the chunk plan (Args: buffer_row_offsets,
     cache_offsets, buffer_lengths, input_row_offsets, buffer_token_size);
   * "mla_prefill_decode_graph_bf16" -- the whole BF16 MLA layer (Args: q,
-    w_k, w_uk, w_uv, scale, buffer_row_offsets, cache_offsets, buffer_length;
-    Parameters: kv_input_fn, mask_str);
+    freqs_cis, kv_norm_gamma, epsilon, w_k, w_uk, w_uv, scale,
+    buffer_row_offsets, cache_offsets, buffer_length; Parameters: kv_input_fn,
+    mask_str);
   * "flare_mla_prefill_dispatch" -- prefill attention (Parameters: q_depth,
     cache_depth, kv_num_heads, dtype, output_type; Args: k, v, k_rope,
     valid_length, scale, cache_offsets).
@@ -26,6 +27,11 @@ in the design notes of the repository):
   * the causal mask lets the new token ``i`` of sequence ``b`` (absolute
     position ``cache_len_b + i``) see context positions ``j <= cache_len_b + i``;
   * LSE is the natural log of the sum of exp of the scaled scores;
+  * the latent-cache write normalises the 512 latent values only (the
+    weights have kv_lora_rank entries) as x / sqrt(mean(x**2) + epsilon) *
+    gamma, and rotates rope values as 32 interleaved (real, imaginary) pairs
+    multiplied by the freqs_cis row of the token's absolute position, for the
+    latent's k_rope and for every query head's rope part;
   * K and V leave the up-projection in the storage dtype of the attention
     operands (bf16 for the BF16 graph, e4m3 for the fp8 path), rounded to
     nearest even, in the descale domain of the cache.
@@ -131,6 +137,87 @@ def decode(codes: np.ndarray, dtype: str) -> np.ndarray:
 
 def round_to(x: np.ndarray, dtype: str) -> np.ndarray:
     return round_to_bf16(x) if dtype == "bf16" else round_to_e4m3(x)
+
+
+# --------------------------------------------------------------------------
+# (0) Latent-cache write -- "mla_prefill_decode_graph_bf16", Args freqs_cis
+# ("precomputed RoPE frequency values", [max_seq_len, qk_rope_head_dim]),
+# kv_norm_gamma (RMSNorm weights, [kv_lora_rank]), epsilon, kv_collection.
+# Upstream of the plan: every new token's latent row is normalised, its rope
+# part rotated, and the row stored in the paged cache at the token's position;
+# the rope part of every query head is rotated with the same frequencies.
+# --------------------------------------------------------------------------
+
+def rms_norm(x, gamma, eps: float):
+    """RMSNorm over the last axis: x / sqrt(mean(x**2) + eps) * gamma."""
+    x = np.asarray(x, dtype=np.float64)
+    mean_sq = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(mean_sq + eps) * np.asarray(gamma, dtype=np.float64)
+
+
+def rope_rotate(x, freqs):
+    """Rotate rope values by a freqs_cis row.  Both hold 32 complex numbers as
+    interleaved (real, imaginary) pairs; the result is their complex product,
+    laid out the same way."""
+    x = np.asarray(x, dtype=np.float64)
+    f = np.asarray(freqs, dtype=np.float64)
+    z = (x[..., 0::2] + 1j * x[..., 1::2]) * (f[..., 0::2] + 1j * f[..., 1::2])
+    out = np.empty(z.shape[:-1] + (2 * z.shape[-1],), dtype=np.float64)
+    out[..., 0::2] = z.real
+    out[..., 1::2] = z.imag
+    return out
+
+
+def latent_cache_write(kv_latent, q, kv_norm_gamma, freqs_cis, input_row_offsets, cache_lengths,
+                       page_table, page_size: int, kv_cache_codes, epsilon: float,
+                       dtype: str = "bf16", inv_scale: float = 1.0):
+    """Write the new tokens' latent rows into the paged cache.
+
+    New token ``i`` of sequence ``b`` (row ``input_row_offsets[b] + i`` of
+    ``kv_latent`` and ``q``) sits at context position ``p = cache_lengths[b]
+    + i``.  Its 576 latent values are 512 c_kv values, normalised with
+    ``rms_norm(c_kv, kv_norm_gamma, epsilon)``, and 64 k_rope values, rotated
+    with ``rope_rotate(k_rope, freqs_cis[p])``.  The row, times ``inv_scale``
+    and rounded to the cache's storage type, goes to page
+    ``page_table[b, p // page_size]``, slot ``p % page_size``; every other cache
+    row is left as it was.  The rope part (last 64 values) of every head of
+    ``q[row]`` is rotated with the same ``freqs_cis[p]``.
+
+    ``kv_latent`` and ``q`` are values (float), the cache is storage codes.
+    Returns (cache codes after the write, rotated q as float64 or None,
+    status: 0, STATUS_BAD_OFFSETS for decreasing offsets or a position past
+    freqs_cis, STATUS_BAD_PAGE for a missing page).
+    """
+    lat = np.asarray(kv_latent, dtype=np.float64)
+    iro = np.asarray(input_row_offsets, dtype=np.int64)
+    cache = np.asarray(cache_lengths, dtype=np.int64)
+    pt = np.asarray(page_table, dtype=np.int64)
+    freqs = np.asarray(freqs_cis, dtype=np.float64)
+    kv = np.array(kv_cache_codes, copy=True)
+    q_out = None if q is None else np.array(q, dtype=np.float64, copy=True)
+    encode = bf16_encode if dtype == "bf16" else e4m3_encode
+    status = STATUS_OK
+    for b in range(cache.shape[0]):
+        n_new = int(iro[b + 1] - iro[b])
+        if n_new < 0:
+            status = STATUS_BAD_OFFSETS
+            continue
+        for i in range(n_new):
+            t = int(iro[b]) + i
+            p = int(cache[b]) + i
+            if p >= freqs.shape[0]:
+                status = STATUS_BAD_OFFSETS
+                continue
+            c_kv = rms_norm(lat[t, :R], kv_norm_gamma, epsilon)
+            k_rope = rope_rotate(lat[t, R:], freqs[p])
+            if q_out is not None:
+                q_out[t, :, DN:] = rope_rotate(q_out[t, :, DN:], freqs[p])
+            slot_page = p // page_size
+            if slot_page >= pt.shape[1] or pt[b, slot_page] < 0 or pt[b, slot_page] >= kv.shape[0]:
+                status = STATUS_BAD_PAGE
+                continue
+            kv[pt[b, slot_page], p % page_size] = encode(np.concatenate([c_kv, k_rope]) * inv_scale)
+    return kv, q_out, status
 
 
 # --------------------------------------------------------------------------

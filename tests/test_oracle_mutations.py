@@ -103,3 +103,49 @@ def test_unscaled_scores_are_caught(monkeypatch):
         return orig(q_nope, q_rope, k_nope, k_rope, v, q_pos, k_pos, 1.0)
     _plant(monkeypatch, "partial_attention", unscaled)
     _must_fail(P.test_attention_bruteforce_tiny, P.test_attention_closed_forms)
+
+
+def test_epsilon_outside_the_root_is_caught(monkeypatch):
+    def bad(x, gamma, eps):
+        x = np.asarray(x, dtype=np.float64)
+        return x / (np.sqrt(np.mean(x * x, axis=-1, keepdims=True)) + eps) * np.asarray(gamma)
+    _plant(monkeypatch, "rms_norm", bad)
+    _must_fail(P.test_rms_norm_closed_forms_and_library)
+
+
+def test_sum_instead_of_mean_is_caught(monkeypatch):
+    def bad(x, gamma, eps):
+        x = np.asarray(x, dtype=np.float64)
+        return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps) * np.asarray(gamma)
+    _plant(monkeypatch, "rms_norm", bad)
+    _must_fail(P.test_rms_norm_closed_forms_and_library, P.test_cache_write_round_trip_through_cache)
+
+
+def test_conjugate_rotation_is_caught(monkeypatch):
+    orig = M.rope_rotate
+
+    def conj(x, freqs):
+        f = np.array(freqs, dtype=np.float64, copy=True)
+        f[..., 1::2] *= -1
+        return orig(x, f)
+    _plant(monkeypatch, "rope_rotate", conj)
+    _must_fail(P.test_rope_rotation_special_cases)
+
+
+def test_half_split_rope_layout_is_caught(monkeypatch):
+    def half(x, freqs):
+        x = np.asarray(x, dtype=np.float64)
+        f = np.asarray(freqs, dtype=np.float64)
+        z = (x[..., :32] + 1j * x[..., 32:]) * (f[..., 0::2] + 1j * f[..., 1::2])
+        return np.concatenate([z.real, z.imag], axis=-1)
+    _plant(monkeypatch, "rope_rotate", half)
+    _must_fail(P.test_rope_rotation_special_cases)
+
+
+def test_position_off_by_one_is_caught(monkeypatch):
+    orig = M.latent_cache_write
+
+    def shifted(kv_latent, q, gamma, freqs, iro, cache_lengths, *a, **k):
+        return orig(kv_latent, q, gamma, np.asarray(freqs)[1:], iro, cache_lengths, *a, **k)
+    _plant(monkeypatch, "latent_cache_write", shifted)
+    _must_fail(P.test_cache_write_round_trip_through_cache, P.test_cache_write_page_permutation_and_e4m3)

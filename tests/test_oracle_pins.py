@@ -10,7 +10,146 @@ import torch
 
 import oracle as O
 from oracle import mla_oracle as M
-from workloads import WORKLOADS, make_inputs, scaled
+from workloads import WORKLOADS, make_cache_write_operands, make_inputs, scaled
+
+
+# ----------------------------------------------------------------------------
+# Latent-cache write: RMSNorm, RoPE rotation, the paged store
+# ----------------------------------------------------------------------------
+
+def test_rms_norm_closed_forms_and_library():
+    rng = np.random.default_rng(3)
+    g = 1.0 + 0.1 * rng.standard_normal(512)
+    # A constant row normalises to the weights times its sign (eps = 0).
+    np.testing.assert_allclose(O.rms_norm(np.full(512, -2.5), g, 0.0), -g, rtol=1e-15)
+    # A one-hot row a*e_j has mean square a**2/512.
+    x = np.zeros(512)
+    x[17] = 3.0
+    out = O.rms_norm(x, g, 1e-3)
+    assert out[17] == pytest.approx(g[17] * 3.0 / math.sqrt(9.0 / 512 + 1e-3), rel=1e-14)
+    assert np.count_nonzero(out) == 1
+    # Scale invariance and a unit mean square of out / g (eps = 0).
+    x = rng.standard_normal((4, 512))
+    np.testing.assert_allclose(O.rms_norm(7.0 * x, g, 0.0), O.rms_norm(x, g, 0.0), rtol=1e-13)
+    np.testing.assert_allclose(np.mean((O.rms_norm(x, g, 0.0) / g) ** 2, axis=-1), 1.0, rtol=1e-13)
+    # The library routine (torch, float64), with epsilon.
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(x), (512,), torch.from_numpy(g), eps=1e-5)
+    np.testing.assert_allclose(O.rms_norm(x, g, 1e-5), ref.numpy(), rtol=1e-13)
+
+
+def _freqs_from_angles(ang):
+    f = np.empty(ang.shape[:-1] + (2 * ang.shape[-1],))
+    f[..., 0::2] = np.cos(ang)
+    f[..., 1::2] = np.sin(ang)
+    return f
+
+
+def test_rope_rotation_special_cases():
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((3, 64))
+    # Angle 0 is the identity; a quarter turn maps each pair (a, b) to (-b, a).
+    np.testing.assert_array_equal(O.rope_rotate(x, np.tile([1.0, 0.0], 32)), x)
+    quarter = O.rope_rotate(x, np.tile([0.0, 1.0], 32))
+    np.testing.assert_array_equal(quarter[:, 0::2], -x[:, 1::2])
+    np.testing.assert_array_equal(quarter[:, 1::2], x[:, 0::2])
+    # Unit-modulus factors keep every pair's length; theta then -theta, and
+    # theta1 then theta2 against theta1 + theta2.
+    a1, a2 = rng.uniform(-7, 7, 32), rng.uniform(-7, 7, 32)
+    y = O.rope_rotate(x, _freqs_from_angles(a1))
+    np.testing.assert_allclose(np.hypot(y[:, 0::2], y[:, 1::2]), np.hypot(x[:, 0::2], x[:, 1::2]), rtol=1e-13)
+    np.testing.assert_allclose(O.rope_rotate(y, _freqs_from_angles(-a1)), x, atol=1e-13)
+    np.testing.assert_allclose(O.rope_rotate(y, _freqs_from_angles(a2)),
+                               O.rope_rotate(x, _freqs_from_angles(a1 + a2)), atol=1e-12)
+    # The library's complex product over the same interleaved layout.
+    f = rng.standard_normal(64)
+    z = torch.view_as_complex(torch.from_numpy(x).reshape(3, 32, 2).contiguous())
+    w = torch.view_as_complex(torch.from_numpy(f).reshape(32, 2).contiguous())
+    ref = torch.view_as_real(z * w).reshape(3, 64).numpy()
+    np.testing.assert_allclose(O.rope_rotate(x, f), ref, rtol=1e-14, atol=1e-15)
+
+
+def _cache_write_case(w, dtype="bf16", inv_scale=1.0, shuffle=False):
+    inp = make_inputs(scaled(w, dtype="bf16", shuffle_pages=shuffle))
+    T = inp["T_q"]
+    L = inp["new_lens"] + inp["cache_lens"]
+    lat, gamma, freqs = make_cache_write_operands(w, T, int(L.max()) + 1)
+    cache = O.codes(inp["kv_cache"])
+    if dtype == "e4m3":
+        cache = M.e4m3_encode(M.bf16_decode(cache))
+    return inp, O.decode(O.codes(lat), "bf16"), gamma.numpy().astype(np.float64), freqs.numpy(), cache
+
+
+def test_cache_write_round_trip_through_cache():
+    """Each sequence's context read back from the paged cache (an oracle
+    function of its own): cached tokens untouched, new tokens normalised and
+    rotated at their positions; q's nope parts untouched."""
+    w = scaled(WORKLOADS["tiny_ragged"], H=3, page_size=8)
+    inp, lat, gamma, freqs, cache = _cache_write_case(w, shuffle=True)
+    q = O.decode(O.codes(inp["q"]), "bf16")
+    iro, cl = inp["input_row_offsets"].numpy(), inp["cache_lengths"].numpy()
+    kv, q2, st = O.latent_cache_write(lat, q, gamma, freqs, iro, cl, inp["page_table"].numpy(),
+                                      inp["page_size"], cache, 1e-6)
+    assert st == 0
+    L = inp["new_lens"] + inp["cache_lens"]
+    before = O.context_latents(cache, inp["page_table"].numpy(), inp["page_size"], L)
+    after = O.context_latents(kv, inp["page_table"].numpy(), inp["page_size"], L)
+    for b in range(inp["B"]):
+        c = int(cl[b])
+        np.testing.assert_array_equal(after[b][:c], before[b][:c])
+        rows = lat[iro[b]:iro[b + 1]]
+        want = np.concatenate([O.rms_norm(rows[:, :512], gamma, 1e-6),
+                               O.rope_rotate(rows[:, 512:], freqs[c:c + len(rows)])], axis=1)
+        np.testing.assert_array_equal(after[b][c:], M.bf16_encode(want))
+        np.testing.assert_array_equal(q2[iro[b]:iro[b + 1], :, :128], q[iro[b]:iro[b + 1], :, :128])
+        for i in range(len(rows)):
+            np.testing.assert_allclose(q2[iro[b] + i, :, 128:], O.rope_rotate(q[iro[b] + i, :, 128:], freqs[c + i]),
+                                       rtol=0, atol=0)
+    # Pages no sequence uses hold exactly what they held.
+    used = set(inp["page_table"].numpy().ravel().tolist()) - {-1}
+    for pg in range(cache.shape[0]):
+        if pg not in used:
+            np.testing.assert_array_equal(kv[pg], cache[pg])
+
+
+def test_cache_write_page_permutation_and_e4m3():
+    """Relabelling the physical pages relabels the written cache; the e4m3
+    store is the e4m3 rounding of the row times the inverse scale."""
+    w = scaled(WORKLOADS["tiny_ragged"], H=2, page_size=8)
+    inp, lat, gamma, freqs, cache = _cache_write_case(w)
+    iro, cl, pt = inp["input_row_offsets"].numpy(), inp["cache_lengths"].numpy(), inp["page_table"].numpy()
+    kv, _, st = O.latent_cache_write(lat, None, gamma, freqs, iro, cl, pt, 8, cache, 1e-6)
+    perm = np.random.default_rng(9).permutation(cache.shape[0])
+    inv = np.argsort(perm)                 # new page id of old page j is inv[j]
+    pt2 = np.where(pt >= 0, inv[np.maximum(pt, 0)], -1)
+    kv2, _, st2 = O.latent_cache_write(lat, None, gamma, freqs, iro, cl, pt2, 8, cache[perm], 1e-6)
+    assert st == st2 == 0
+    np.testing.assert_array_equal(kv2, kv[perm])
+    _, _, _, _, cache8 = _cache_write_case(w, dtype="e4m3")
+    kv8, _, st8 = O.latent_cache_write(lat, None, gamma, freqs, iro, cl, pt, 8, cache8, 1e-6,
+                                       dtype="e4m3", inv_scale=0.5)
+    assert st8 == 0
+    L = inp["new_lens"] + inp["cache_lens"]
+    got = O.context_latents(kv8, pt, 8, L)
+    for b in range(inp["B"]):
+        c = int(cl[b])
+        rows = lat[iro[b]:iro[b + 1]]
+        want = np.concatenate([O.rms_norm(rows[:, :512], gamma, 1e-6),
+                               O.rope_rotate(rows[:, 512:], freqs[c:c + len(rows)])], axis=1)
+        np.testing.assert_array_equal(M.e4m3_decode(got[b][c:]), M.round_to_e4m3(0.5 * want))
+
+
+def test_cache_write_status():
+    w = scaled(WORKLOADS["tiny_ragged"], H=1, page_size=8)
+    inp, lat, gamma, freqs, cache = _cache_write_case(w)
+    iro, cl, pt = inp["input_row_offsets"].numpy(), inp["cache_lengths"].numpy(), inp["page_table"].numpy()
+    # A position past the frequency table.
+    _, _, st = O.latent_cache_write(lat, None, gamma, freqs[:10], iro, cl, pt, 8, cache, 1e-6)
+    assert st == M.STATUS_BAD_OFFSETS
+    # A missing page where new tokens go (sequence 1 writes positions 40..72).
+    pt2 = pt.copy()
+    pt2[1, 6] = -1
+    _, _, st = O.latent_cache_write(lat, None, gamma, freqs, iro, cl, pt2, 8, cache, 1e-6)
+    assert st == M.STATUS_BAD_PAGE
 
 
 # ----------------------------------------------------------------------------

@@ -189,6 +189,26 @@ def make_attention_operands(w: Workload, rows: int, seed_offset: int = 7):
     return k_nope, v, k_rope
 
 
+def make_cache_write_operands(w: Workload, T_q: int, max_seq_len: int, seed_offset: int = 11):
+    """Inputs of the latent-cache write ("mla_prefill_decode_graph_bf16", Args
+    freqs_cis, kv_norm_gamma, epsilon): the new tokens' latent rows before
+    normalisation ([T_q, 576] bf16, N(0, 2**2): a projection output of
+    arbitrary scale), the RMSNorm weights ([512] float32, 1 + N(0, 0.1**2)),
+    and a RoPE frequency table ([max_seq_len, 64] float32: for position p and
+    pair k the unit complex number at angle p * 10000**(-k/32), stored as
+    interleaved (cos, sin) values)."""
+    gen = torch.Generator().manual_seed(w.seed + seed_offset)
+    kv_latent = _normal(gen, (T_q, CACHE_DEPTH), 2.0).to(torch.bfloat16)
+    gamma = 1.0 + _normal(gen, (KV_LORA_RANK,), 0.1)
+    pos = np.arange(max_seq_len, dtype=np.float64)[:, None]
+    inv_freq = 10000.0 ** (-np.arange(QK_ROPE // 2, dtype=np.float64) / (QK_ROPE // 2))
+    ang = pos * inv_freq[None, :]
+    freqs = np.empty((max_seq_len, QK_ROPE), dtype=np.float32)
+    freqs[:, 0::2] = np.cos(ang)
+    freqs[:, 1::2] = np.sin(ang)
+    return kv_latent, gamma, torch.from_numpy(freqs)
+
+
 def scaled(w: Workload, **changes) -> Workload:
     """A copy of a workload with some fields replaced (smaller test variants)."""
     return dataclasses.replace(w, **changes)
