@@ -49,7 +49,7 @@ def _args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
-    ap.add_argument("--stage", default=None, choices=["plan", "gather"],
+    ap.add_argument("--stage", default=None, choices=["plan", "gather", "cache_write"],
                     help="time one HBM-bound stage alone on its stress shape")
     ap.add_argument("--batch", type=int, default=None, help="sequences for --stage")
     return ap.parse_args()
@@ -495,6 +495,26 @@ def run_stage(a):
         kernels = "plan_one_cta" if Bsz <= 4096 else "plan_tile_totals + plan_tile_tables"
         desc = {"workload": "plan_stress", "B": Bsz, "max_chunks": mc, "buffer_token_size": S,
                 "new_tokens": "U[0,63]", "cache_tokens": "U[0,63]"}
+    elif a.stage == "cache_write":
+        from workloads import WORKLOADS, make_cache_write_operands, make_inputs
+        w = WORKLOADS["v3_prefill"]
+        inp = make_inputs(w)
+        T, H, Bsz = inp["T_q"], w.H, inp["B"]
+        L = inp["new_lens"] + inp["cache_lens"]
+        lat, gamma, freqs = make_cache_write_operands(w, T, int(L.max()))
+        kv = inp["kv_cache"].to(dev)
+        q = inp["q"].to(dev)
+        lat, gamma, freqs = lat.to(dev), gamma.to(dev), freqs.to(dev)
+        iro, cl, pt = (inp[k].to(dev) for k in ("input_row_offsets", "cache_lengths", "page_table"))
+        # Per token: latent row read, cache row written, frequency row read,
+        # and every head's rope part of q read and written.
+        nbytes = T * (576 * 2 + 576 * 2 + 64 * 4 + 2 * H * 64 * 2) + 512 * 4
+        launch = lambda: mla.check(mla.mla_latent_cache_write(
+            kv, q, lat, gamma, freqs, iro, cl, pt, inp["num_pages"], inp["page_size"], inp["max_pages"],
+            Bsz, H, T, freqs.shape[0], 1e-6, 1.0, mla.MLA_BF16, st, stream))
+        kernels = "cache_write_kernel<2>"
+        desc = {"workload": "latent_cache_write_v3", "tokens": T, "H": H, "cache_dtype": "bf16",
+                "q": "bf16, rope part rotated in place"}
     else:
         Bsz = a.batch or 64
         L = 8192

@@ -3,7 +3,11 @@
  * Multi-head Latent Attention (MLA) prefill over a paged latent KV cache.
  *
  * The path has four stages, each an entry point below, plus a fused entry
- * point that runs them all:
+ * point that runs them all, and the step in front of it that writes the new
+ * tokens' latent rows into the paged cache:
+ *   0. mla_latent_cache_write -- RMSNorm + RoPE + paged store
+ *                                ("mla_prefill_decode_graph_bf16", Args:
+ *                                 freqs_cis, kv_norm_gamma, epsilon)
  *   1. mla_prefill_plan       -- chunk plan      ("mla_prefill_plan" page)
  *   2. mla_gather_latent      -- paged gather    ("mla_prefill_decode_graph_bf16",
  *                                                 Parameters: kv_input_fn)
@@ -81,6 +85,54 @@ int32_t mla_abi_version(void);
  * dtype.  The pages have no counterpart: this is an introspection call.
  */
 const char* mla_attention_kernel(int32_t dtype);
+
+/*
+ * 0. Latent-cache write.  Follows "mla_prefill_decode_graph_bf16" (Args:
+ * freqs_cis -- precomputed RoPE values [max_seq_len, qk_rope_head_dim];
+ * kv_norm_gamma -- RMSNorm weights [kv_lora_rank]; epsilon; kv_collection;
+ * Parameters: kv_input_fn, the [tot_seq_len, 576] latent rows).  The step in
+ * front of the prefill path: it puts the new tokens into the paged cache that
+ * mla_gather_latent reads.
+ *
+ * New token i of sequence b (row input_row_offsets[b] + i of kv_latent and q)
+ * sits at context position p = cache_lengths[b] + i.  Its latent row is 512
+ * c_kv values followed by 64 k_rope values:
+ *   c_kv'   = c_kv / sqrt(mean(c_kv^2) + epsilon) * kv_norm_gamma
+ *   k_rope' = k_rope rotated by freqs_cis[p]
+ * where a rotation treats the 64 values and the 64-value freqs_cis row as 32
+ * complex numbers stored as interleaved (real, imaginary) pairs and multiplies
+ * them.  The row [c_kv' | k_rope'] times kv_inv_scale, rounded to the cache's
+ * type (nearest even; e4m3 saturates at +-448), is stored at page
+ * page_table[b][p / page_size], slot p % page_size.  If q is not NULL, the
+ * rope part (values 128..191) of every head of q[row] is rotated in place by
+ * freqs_cis[p] and rounded to bf16; the nope part is left untouched.
+ *
+ * kv_cache:       [num_pages][page_size][576], bf16 or e4m3 (dtype), written
+ * q:              [total_q_tokens][H][192] bf16, rotated in place, or NULL
+ * kv_latent:      [total_q_tokens][576] bf16, the new tokens' latent rows
+ * kv_norm_gamma:  [512] float32
+ * freqs_cis:      [max_seq_len][64] float32
+ * input_row_offsets [B+1], cache_lengths [B], page_table [B][max_pages_per_seq]
+ *                 as in mla_prefill_plan and mla_gather_latent
+ * kv_inv_scale:   1 for bf16; for e4m3 the reciprocal of the cache's descale
+ * Pointers to kv_cache, q, kv_latent, kv_norm_gamma and freqs_cis must be
+ * 16-byte aligned.  Errors: host MLA_ERR_DTYPE for another cache dtype,
+ * MLA_ERR_ARG for null or misaligned pointers, B < 1, total_q_tokens < 0,
+ * H < 1 with q given, page_size, num_pages, max_pages_per_seq or max_seq_len
+ * < 1, epsilon < 0 or kv_inv_scale <= 0.  Device MLA_DEV_BAD_OFFSETS for a
+ * token outside every sequence or a position >= max_seq_len (that token is
+ * skipped), MLA_DEV_BAD_PAGE for a missing page (its cache row is not
+ * written; its q is still rotated).
+ */
+mla_status_t mla_latent_cache_write(void* kv_cache, void* q, const void* kv_latent,
+                                    const float* kv_norm_gamma, const float* freqs_cis,
+                                    const uint32_t* input_row_offsets,
+                                    const uint32_t* cache_lengths, const int32_t* page_table,
+                                    int32_t num_pages, int32_t page_size,
+                                    int32_t max_pages_per_seq, int32_t batch_size,
+                                    int32_t num_heads, int32_t total_q_tokens,
+                                    int32_t max_seq_len, float epsilon, float kv_inv_scale,
+                                    int32_t dtype, int32_t* d_status, mla_stream_t stream);
 
 /*
  * 1. Chunk plan.  Follows "mla_prefill_plan" (Args: buffer_row_offsets,

@@ -43,6 +43,8 @@ SIGNATURES = {
     "mla_abi_version": (_I, []),
     "mla_attention_kernel": (ctypes.c_char_p, [_I]),
     "mla_prefill_plan": (_I, [_P, _P, _P, _P, _P, _I, _I, _U, _P, _P]),
+    "mla_latent_cache_write": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
+                                    _F, _F, _I, _P, _P]),
     "mla_gather_latent": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _I, _I, _U, _I, _P, _P]),
     "mla_upproject": (_I, [_P, _P, _P, _P, _P, _P, _I, _U, _I, _I, _F, _F, _F, _P]),
     "mla_prefill_attention": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
@@ -121,6 +123,19 @@ def mla_prefill_plan(buffer_row_offsets, cache_offsets, buffer_lengths, input_ro
                                    _ptr(buffer_lengths), _ptr(input_row_offsets),
                                    _ptr(cache_lengths), batch_size, max_chunks,
                                    buffer_token_size, _ptr(d_status), _stream(stream))
+
+
+def mla_latent_cache_write(kv_cache, q, kv_latent, kv_norm_gamma, freqs_cis, input_row_offsets,
+                           cache_lengths, page_table, num_pages, page_size, max_pages_per_seq,
+                           batch_size, num_heads, total_q_tokens, max_seq_len, epsilon,
+                           kv_inv_scale, dtype, d_status=None, stream=None) -> int:
+    return load().mla_latent_cache_write(_ptr(kv_cache), _ptr(q), _ptr(kv_latent),
+                                         _ptr(kv_norm_gamma), _ptr(freqs_cis),
+                                         _ptr(input_row_offsets), _ptr(cache_lengths),
+                                         _ptr(page_table), num_pages, page_size,
+                                         max_pages_per_seq, batch_size, num_heads,
+                                         total_q_tokens, max_seq_len, epsilon, kv_inv_scale,
+                                         dtype, _ptr(d_status), _stream(stream))
 
 
 def mla_gather_latent(c_kv_buf, k_rope_buf, kv_cache, page_table, num_pages, page_size,

@@ -125,6 +125,46 @@ const char* mla_attention_kernel(int32_t dtype) {
   return mla::attention_uses_pair() ? "pair" : "single";
 }
 
+mla_status_t mla_latent_cache_write(void* kv_cache, void* q, const void* kv_latent,
+                                    const float* kv_norm_gamma, const float* freqs_cis,
+                                    const uint32_t* input_row_offsets,
+                                    const uint32_t* cache_lengths, const int32_t* page_table,
+                                    int32_t num_pages, int32_t page_size,
+                                    int32_t max_pages_per_seq, int32_t batch_size,
+                                    int32_t num_heads, int32_t total_q_tokens,
+                                    int32_t max_seq_len, float epsilon, float kv_inv_scale,
+                                    int32_t dtype, int32_t* d_status, mla_stream_t stream) {
+  if (!dtype_ok(dtype)) return MLA_ERR_DTYPE;
+  if (!kv_cache || !kv_latent || !kv_norm_gamma || !freqs_cis || !input_row_offsets ||
+      !cache_lengths || !page_table || !aligned16(kv_cache) || !aligned16(kv_latent) ||
+      !aligned16(kv_norm_gamma) || !aligned16(freqs_cis) || (q && !aligned16(q)) ||
+      batch_size < 1 || total_q_tokens < 0 || (q && num_heads < 1) || num_pages < 1 ||
+      page_size < 1 || max_pages_per_seq < 1 || max_seq_len < 1 || !(epsilon >= 0.0f) ||
+      !(kv_inv_scale > 0.0f))
+    return MLA_ERR_ARG;
+  mla::CacheWriteArgs a;
+  a.kv_cache = kv_cache;
+  a.q = q;
+  a.kv_latent = kv_latent;
+  a.gamma = kv_norm_gamma;
+  a.freqs = freqs_cis;
+  a.iro = input_row_offsets;
+  a.cache_len = cache_lengths;
+  a.page_table = page_table;
+  a.num_pages = num_pages;
+  a.page_size = page_size;
+  a.max_pages = max_pages_per_seq;
+  a.B = batch_size;
+  a.H = q ? num_heads : 0;
+  a.T = total_q_tokens;
+  a.max_seq_len = max_seq_len;
+  a.eps = epsilon;
+  a.inv_scale = kv_inv_scale;
+  a.elt_bytes = elt_bytes(dtype);
+  a.status = d_status;
+  return from_cuda(mla::launch_cache_write(a, static_cast<cudaStream_t>(stream)));
+}
+
 mla_status_t mla_prefill_plan(uint32_t* buffer_row_offsets, uint32_t* cache_offsets,
                               int32_t* buffer_lengths, const uint32_t* input_row_offsets,
                               const uint32_t* cache_lengths, int32_t batch_size,

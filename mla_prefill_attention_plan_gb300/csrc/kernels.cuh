@@ -14,6 +14,22 @@ cudaError_t launch_plan(uint32_t* bro, uint32_t* co, int32_t* bl, const uint32_t
                         const uint32_t* cache_len, int B, int max_chunks, uint32_t S,
                         int32_t* status, cudaStream_t stream);
 
+struct CacheWriteArgs {
+  void* kv_cache;
+  void* q;                  // bf16 [T][H][192] or null
+  const void* kv_latent;    // bf16 [T][576]
+  const float* gamma;       // [512]
+  const float* freqs;       // [max_seq_len][64]
+  const uint32_t* iro;
+  const uint32_t* cache_len;
+  const int32_t* page_table;
+  int num_pages, page_size, max_pages, B, H, T, max_seq_len;
+  float eps, inv_scale;
+  int elt_bytes;            // cache storage: 2 (bf16) or 1 (e4m3)
+  int32_t* status;
+};
+cudaError_t launch_cache_write(const CacheWriteArgs& a, cudaStream_t stream);
+
 cudaError_t launch_gather(void* c_kv_buf, void* k_rope_buf, const void* kv_cache,
                           const int32_t* page_table, int num_pages, int page_size, int max_pages,
                           const uint32_t* bro, const uint32_t* co, const int32_t* bl, int chunk,

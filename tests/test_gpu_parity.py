@@ -11,7 +11,8 @@ import torch
 import mla_prefill_attention_plan_gb300 as mla
 import oracle as O
 from oracle import mla_oracle as M
-from workloads import WORKLOADS, lengths, make_attention_operands, make_inputs, scaled
+from workloads import (WORKLOADS, lengths, make_attention_operands, make_cache_write_operands,
+                       make_inputs, scaled)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -185,6 +186,160 @@ def test_plan_status_codes():
     assert gpu_plan([0, 5, 3], [0, 0], 4, 4)[3] == mla.MLA_DEV_BAD_OFFSETS
     bro, co, bl, st = gpu_plan([0, 0, 0], [0, 0], 8, 3)
     assert st == 0 and list(bl) == [-1, -1, -1]
+
+
+# ----------------------------------------------------------------------------- latent-cache write
+
+def _assert_rounded(gpu_codes, exact, dtype, what, allow):
+    """Storage codes from the GPU against exact float64 values.  The oracle's
+    rounding (nearest even) must match, except where the exact value lies
+    within `allow` (the float32 error bound of the kernel's arithmetic for that
+    element) of a rounding midpoint: the kernel rounds its float32 result, so
+    there either neighbour is a correct rounding."""
+    want = M.bf16_encode(exact) if dtype == "bf16" else M.e4m3_encode(exact)
+    diff = np.asarray(gpu_codes) != want
+    if diff.any():
+        g = O.decode(np.asarray(gpu_codes)[diff], dtype)
+        w = O.decode(want[diff], dtype)
+        x = exact[diff]
+        near_tie = np.abs(x - 0.5 * (g + w)) <= allow[diff]
+        assert near_tie.all(), (f"{what}: {int((~near_tie).sum())} codes differ away from a tie, e.g. exact "
+                                f"{x[~near_tie][:3]} gpu {g[~near_tie][:3]} oracle {w[~near_tie][:3]}")
+    return int(diff.sum())
+
+
+def _rope_allow(x):
+    """Error bound of a float32 rotation of interleaved pairs (a, b): each
+    output is a*c -/+ b*s with |c|, |s| <= 1, so it is off by at most a few
+    units of 2**-24 times |a| + |b|."""
+    x = np.asarray(x, dtype=np.float64)
+    m = np.abs(x[..., 0::2]) + np.abs(x[..., 1::2])
+    return 1e-6 * np.repeat(m, 2, axis=-1)
+
+
+def _cache_write_case(w, cache_dtype="bf16", inv_scale=1.0, with_q=True, freqs_rows=None,
+                      drop_page=None):
+    inp = make_inputs(scaled(w, dtype="bf16"))
+    T, B = inp["T_q"], inp["B"]
+    L = inp["new_lens"] + inp["cache_lens"]
+    lat, gamma, freqs = make_cache_write_operands(w, T, int(L.max()) + 1)
+    if freqs_rows is not None:
+        freqs = freqs[:freqs_rows].contiguous()
+    cache = inp["kv_cache"] if cache_dtype == "bf16" else inp["kv_cache"].float().to(torch.float8_e4m3fn)
+    pt = inp["page_table"].clone()
+    if drop_page is not None:
+        pt[drop_page] = -1
+    eps = 1e-6
+    kv_d = cache.to(DEV)
+    q_d = inp["q"].to(DEV) if with_q else None
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    mla.check(mla.mla_latent_cache_write(
+        kv_d, q_d, lat.to(DEV), gamma.to(DEV), freqs.to(DEV), inp["input_row_offsets"].to(DEV),
+        inp["cache_lengths"].to(DEV), pt.to(DEV), inp["num_pages"], inp["page_size"],
+        inp["max_pages"], B, w.H, T, freqs.shape[0], eps, inv_scale,
+        mla.MLA_BF16 if cache_dtype == "bf16" else mla.MLA_E4M3, st))
+    torch.cuda.synchronize()
+    lat64 = O.decode(O.codes(lat), "bf16")
+    q64 = O.decode(O.codes(inp["q"]), "bf16") if with_q else None
+    kv_o, q_o, st_o = O.latent_cache_write(lat64, q64, gamma.numpy(), freqs.numpy(),
+                                           inp["input_row_offsets"].numpy(), inp["cache_lengths"].numpy(),
+                                           pt.numpy(), inp["page_size"], O.codes(cache), eps,
+                                           dtype=cache_dtype, inv_scale=inv_scale)
+    return dict(inp=inp, lat64=lat64, gamma=gamma.numpy(), freqs=freqs.numpy(), pt=pt.numpy(),
+                kv_gpu=O.codes(kv_d.cpu()), q_gpu=O.codes(q_d.cpu()) if with_q else None,
+                st_gpu=int(st.item()), kv_o=kv_o, q_o=q_o, st_o=st_o, eps=eps)
+
+
+def _check_cache_write(c, cache_dtype, inv_scale=1.0):
+    """Rows the oracle did not write are bit-identical; written rows and q's
+    rope parts agree with the oracle's exact values up to ties."""
+    inp = c["inp"]
+    assert c["st_gpu"] == c["st_o"]
+    iro, cl, ps = inp["input_row_offsets"].numpy(), inp["cache_lengths"].numpy(), inp["page_size"]
+    written = np.zeros(c["kv_o"].shape[:2], dtype=bool)
+    exact_rows = {}
+    for b in range(inp["B"]):
+        for i in range(int(iro[b + 1] - iro[b])):
+            p = int(cl[b]) + i
+            if p >= c["freqs"].shape[0]:
+                continue
+            pg = c["pt"][b, p // ps] if p // ps < c["pt"].shape[1] else -1
+            if pg < 0:
+                continue
+            t = int(iro[b]) + i
+            row = np.concatenate([O.rms_norm(c["lat64"][t, :512], c["gamma"], c["eps"]),
+                                  O.rope_rotate(c["lat64"][t, 512:], c["freqs"][p])])
+            # float32 RMSNorm: a relative error well under 5e-5 (512-term sum of squares,
+            # square root, two products); rotation: see _rope_allow.
+            allow = np.concatenate([5e-5 * np.abs(row[:512]), _rope_allow(c["lat64"][t, 512:])])
+            written[pg, p % ps] = True
+            exact_rows[(pg, p % ps)] = (row * inv_scale, allow * inv_scale)
+    np.testing.assert_array_equal(c["kv_gpu"][~written], c["kv_o"][~written])
+    keys = sorted(exact_rows)
+    ties = 0
+    if keys:
+        gpu = np.stack([c["kv_gpu"][k] for k in keys])
+        ex = np.stack([exact_rows[k][0] for k in keys])
+        allow = np.stack([exact_rows[k][1] for k in keys])
+        ties += _assert_rounded(gpu, ex, cache_dtype, "cache rows", allow)
+    if c["q_gpu"] is not None:
+        q_in = O.decode(O.codes(inp["q"]), "bf16")
+        np.testing.assert_array_equal(c["q_gpu"][:, :, :128], O.codes(inp["q"])[:, :, :128])
+        ties += _assert_rounded(c["q_gpu"][:, :, 128:], c["q_o"][:, :, 128:], "bf16", "q rope",
+                                _rope_allow(q_in[:, :, 128:]))
+    return ties
+
+
+def test_cache_write_tiny_ragged_bf16():
+    w = scaled(WORKLOADS["tiny_ragged"], H=4, page_size=8, shuffle_pages=True)
+    c = _cache_write_case(w)
+    _check_cache_write(c, "bf16")
+
+
+def test_cache_write_ragged_chunked_bf16():
+    w = scaled(WORKLOADS["ragged_chunked_cache"], H=3)
+    c = _cache_write_case(w)
+    ties = _check_cache_write(c, "bf16")
+    n = c["inp"]["T_q"] * (576 + 3 * 64)
+    assert ties < 1e-3 * n
+
+
+def test_cache_write_e4m3_cache_scaled():
+    w = scaled(WORKLOADS["tiny_ragged"], H=2, page_size=16)
+    c = _cache_write_case(w, cache_dtype="e4m3", inv_scale=2.0, with_q=False)
+    _check_cache_write(c, "e4m3", inv_scale=2.0)
+
+
+def test_cache_write_v3_full_size():
+    """The DeepSeek-V3 shape in full: 4096 new tokens, 128 heads, every cache
+    row and every q rope value compared."""
+    c = _cache_write_case(WORKLOADS["v3_prefill"])
+    ties = _check_cache_write(c, "bf16")
+    assert ties < 1e-3 * 4096 * (576 + 128 * 64)
+
+
+def test_cache_write_status_codes():
+    w = scaled(WORKLOADS["tiny_ragged"], H=2, page_size=8)
+    # Positions past the frequency table: those tokens are skipped entirely.
+    c = _cache_write_case(w, freqs_rows=50)
+    assert c["st_gpu"] == c["st_o"] == mla.MLA_DEV_BAD_OFFSETS
+    _check_cache_write(c, "bf16")
+    # A missing page where sequence 1's new tokens go: its rows stay unwritten.
+    c = _cache_write_case(w, drop_page=(1, 6))
+    assert c["st_gpu"] == c["st_o"] == mla.MLA_DEV_BAD_PAGE
+    _check_cache_write(c, "bf16")
+
+
+def test_cache_write_then_prefill_matches_oracle():
+    """The write feeds the prefill: the fused path over the written cache,
+    with the rotated q, matches the oracle's prefill over the oracle's cache."""
+    w = scaled(WORKLOADS["tiny_ragged"], H=3, page_size=8)
+    c = _cache_write_case(w)
+    bf16 = lambda codes: torch.from_numpy(np.ascontiguousarray(codes).view(np.int16)).view(torch.bfloat16)
+    gpu_in = dict(c["inp"], kv_cache=bf16(c["kv_gpu"]), q=bf16(c["q_gpu"]))
+    ora_in = dict(c["inp"], kv_cache=bf16(c["kv_o"]), q=bf16(M.bf16_encode(c["q_o"])))
+    out, lse = run_fused(gpu_in)
+    _compare(out, oracle_fused(ora_in), "bf16", lse)
 
 
 # ----------------------------------------------------------------------------- gather
