@@ -188,13 +188,12 @@ __global__ void __launch_bounds__(kSThreads, 5) plan_tile_tables(uint32_t* bro, 
                                                                  int32_t* status) {
   __shared__ uint32_t warp_tot[kSWarps];
   __shared__ uint64_t red[kSWarps];
-  __shared__ int s_last, s_bad;
+  __shared__ int s_last;
   const int t = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e0 = t * kSTile + warp * (32 * kSPerLane) + lane;   // this thread's first sequence
   const int nk = B > e0 ? min(kSPerLane, (B - e0 + 31) / 32) : 0;
   const uint32_t n_scratch = 1u + static_cast<uint32_t>(ntiles);
-  if (threadIdx.x == 0) s_bad = 0;
 
   // Context lengths and the warp-local exclusive scan of each 32-wide group.
   uint32_t L[kSPerLane], ex[kSPerLane];
@@ -221,7 +220,7 @@ __global__ void __launch_bounds__(kSThreads, 5) plan_tile_tables(uint32_t* bro, 
     run += __shfl_sync(0xffffffffu, incl, 31);
   }
   if (lane == 0) warp_tot[warp] = run;
-  if (bad) s_bad = 1;
+  const int any_bad = __syncthreads_or(bad);
 
   // Pass A has completed (and its writes are visible) past this point.
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -249,7 +248,7 @@ __global__ void __launch_bounds__(kSThreads, 5) plan_tile_tables(uint32_t* bro, 
         set_status(status, MLA_DEV_TOO_MANY_CHUNKS);
     }
   }
-  if (threadIdx.x == 0 && (s_bad || prefix >= (1ull << 31))) set_status(status, MLA_DEV_BAD_OFFSETS);
+  if (threadIdx.x == 0 && (any_bad || prefix >= (1ull << 31))) set_status(status, MLA_DEV_BAD_OFFSETS);
 
   // Every table row, chunk by chunk: with m = max(P_b, c*S),
   //   buffer_row_offsets = min(m - c*S, S),  cache_offsets = min(m - P_b, L_b).
