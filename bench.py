@@ -348,6 +348,8 @@ def run_ours(a):
     used_chunks = int((bl >= 0).sum().item())
     attn_ms_per_launch = attn_ms / (a.steps * max(used_chunks, 1))
     up_ms = sum(evs[k][ch][2].elapsed_time(evs[k][ch][3]) for k in range(a.steps) for ch in range(mc))
+    attn_ms_per_chunk = [sum(evs[k][ch][0].elapsed_time(evs[k][ch][1]) for k in range(a.steps)) / a.steps
+                         for ch in range(used_chunks)]
     assert status.item() == 0, mla.status_string(int(status.item()))
 
     # End to end through the fused entry point, as a serving loop runs it: every
@@ -448,6 +450,7 @@ def run_ours(a):
         "config": dict(_config(w, inp), parallelism=f"replicas{world}" if world > 1 else "single"),
         "attn_tflops": achieved,
         "attn_ms_per_launch": attn_ms_per_launch,
+        "attn_ms_per_chunk": attn_ms_per_chunk,
         "upproj_tflops": up_flops / (up_ms / a.steps * 1e-3) / 1e12,
         "upproj_ms_per_step": up_ms / a.steps,
         "step_flops": {"attention": attn_flops, "upproject": up_flops, "visible_pairs": pairs},

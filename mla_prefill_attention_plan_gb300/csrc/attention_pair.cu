@@ -49,7 +49,8 @@ constexpr int P_SMEM_Q = 0;
 constexpr int P_SMEM_K = P_SMEM_Q + PQ_BYTES;
 constexpr int P_SMEM_V = P_SMEM_K + PNK * PK_BYTES;
 constexpr int P_SMEM_BAR = P_SMEM_V + PNV * PV_BYTES;   // 212992
-constexpr int P_SMEM_TOTAL = P_SMEM_BAR + 256 + 1024;
+constexpr int P_SMEM_UNITS = P_SMEM_BAR + 256;                // compacted work units
+constexpr int P_SMEM_TOTAL = P_SMEM_UNITS + 4 * 4096 + 1024;
 constexpr int P_THREADS = 224;
 constexpr uint32_t P_TMEM_COLS = 512;
 constexpr uint32_t P_TM_S = 0, P_TM_O = 256, P_TM_Q = 384;
@@ -78,15 +79,33 @@ struct PairItem {
   int n_kv;    // key tiles both CTAs visit
 };
 
-__device__ __forceinline__ bool load_pair(const Params& p, int idx, uint32_t rank, PairItem& it) {
+// The chunk's work units (sequence b, query-tile pair tp) with work, in the
+// order the items visit them (heaviest pairs first), compacted in shared
+// memory by every CTA before the roles start.  Items are then (head group,
+// unit, head) over that list, so the static stride of the clusters walks
+// consecutive work and the clusters in flight stay within one head group and
+// share its K/V in L2.  (Striding over all units instead lets the clusters
+// drift into different head groups wherever most units of a chunk are empty,
+// and K/V then comes from DRAM about twice.)  More than kMaxUnits units: the
+// kernels walk all units and skip the empty ones.
+constexpr int kMaxUnits = 4096;
+
+struct WorkList {
+  const uint32_t* units;   // shared memory
+  int n;                   // units with work, or -1: walk all units
+};
+
+__device__ __forceinline__ bool load_pair(const Params& p, int idx, uint32_t rank, PairItem& it,
+                                          const WorkList& wl) {
   const int n_tp = (p.n_qtiles + 1) >> 1;   // tile pairs per sequence
-  const int n_units = n_tp * p.B;
+  const int n_units = wl.n >= 0 ? wl.n : n_tp * p.B;
   const int per_group = p.head_group * n_units;
   const int grp = idx / per_group;
   const int r = idx - grp * per_group;
   const int hg = min(p.head_group, p.H - grp * p.head_group);
-  const int unit = r / hg;
-  const int h = grp * p.head_group + (r - unit * hg);
+  const int ui = r / hg;
+  const int h = grp * p.head_group + (r - ui * hg);
+  const int unit = wl.n >= 0 ? static_cast<int>(wl.units[ui]) : ui;
   const int tp = n_tp - 1 - unit / p.B;   // heaviest pairs first
   const int b = unit % p.B;
   Item other;
@@ -97,10 +116,44 @@ __device__ __forceinline__ bool load_pair(const Params& p, int idx, uint32_t ran
 }
 
 __device__ __forceinline__ bool next_pair(const Params& p, int& idx, int stride, int total, uint32_t rank,
-                                          PairItem& it) {
+                                          PairItem& it, const WorkList& wl) {
   for (; idx < total; idx += stride)
-    if (load_pair(p, idx, rank, it)) return true;
+    if (load_pair(p, idx, rank, it, wl)) return true;
   return false;
+}
+
+// Every thread of the CTA: compact the units with work into `list`; returns
+// their count (the same in every thread), or -1 past kMaxUnits.
+__device__ int compact_units(const Params& p, uint32_t* list, int* warp_cnt) {
+  const int n_tp = (p.n_qtiles + 1) >> 1;
+  const int n_units = n_tp * p.B;
+  if (n_units > kMaxUnits) return -1;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nwarps = static_cast<int>(blockDim.x) >> 5;
+  int base = 0;
+  for (int u0 = 0; u0 < n_units; u0 += static_cast<int>(blockDim.x)) {
+    const int u = u0 + tid;
+    bool has = false;
+    if (u < n_units) {
+      const int tp = n_tp - 1 - u / p.B, b = u % p.B;
+      Item a, c;
+      tile_item(p, b, 0, 2 * tp, a);
+      tile_item(p, b, 0, 2 * tp + 1, c);
+      has = max(a.n_kv, c.n_kv) > 0;
+    }
+    const uint32_t m = __ballot_sync(0xffffffffu, has);
+    if (lane == 0) warp_cnt[warp] = __popc(m);
+    __syncthreads();
+    int off = base, tot = 0;
+    for (int w = 0; w < nwarps; ++w) {
+      if (w < warp) off += warp_cnt[w];
+      tot += warp_cnt[w];
+    }
+    if (has) list[off + __popc(m & ((1u << lane) - 1u))] = static_cast<uint32_t>(u);
+    base += tot;
+    __syncthreads();   // warp_cnt is rewritten by the next round
+  }
+  return base;
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
@@ -145,6 +198,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     tmem_alloc_pair(smem_u32(&sh->tmem), P_TMEM_COLS);
     tmem_relinquish_pair();
   }
+  __shared__ int warp_cnt[8];
+  const WorkList wl{reinterpret_cast<const uint32_t*>(smem + P_SMEM_UNITS),
+                    compact_units(p, reinterpret_cast<uint32_t*>(smem + P_SMEM_UNITS), warp_cnt)};
+  const int total = wl.n >= 0 ? wl.n * p.H : total_items;
   tc_fence_before();
   cluster_sync();   // barriers of both CTAs initialised, TMEM allocated
   tc_fence_after();
@@ -164,7 +221,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     int q_last = -1, k_last[PNK] = {-1, -1, -1, -1};
     bool ok = true;
     PairItem it;
-    for (int idx = pair_id; ok && next_pair(p, idx, n_pairs, total_items, rank, it); idx += n_pairs) {
+    for (int idx = pair_id; ok && next_pair(p, idx, n_pairs, total, rank, it, wl); idx += n_pairs) {
       if (it_n > 0 && !(ok = mbar_wait_warp(smem_u32(&sh->q_empty), (it_n - 1) & 1, status, abort_flag))) break;
       if (elect_one()) {
         const uint32_t qf = smem_u32(&sh->q_full);
@@ -215,7 +272,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     int v_last[PNV] = {-1, -1, -1, -1};
     bool ok = true;
     PairItem it;
-    for (int idx = pair_id; ok && next_pair(p, idx, n_pairs, total_items, rank, it); idx += n_pairs) {
+    for (int idx = pair_id; ok && next_pair(p, idx, n_pairs, total, rank, it, wl); idx += n_pairs) {
       for (int j = 0; j < it.n_kv; ++j) {
         const uint32_t gj = g + j;
         const int row = it.own.kv_row0 + j * BN;
@@ -249,7 +306,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
         const uint32_t q_t = tmem + P_TM_Q;
         const uint32_t o_t = tmem + P_TM_O;
         PairItem it;
-        for (int idx = pair_id; next_pair(p, idx, n_pairs, total_items, rank, it); idx += n_pairs) {
+        for (int idx = pair_id; next_pair(p, idx, n_pairs, total, rank, it, wl); idx += n_pairs) {
           if (!mbar_wait_cluster(smem_u32(&sh->q_ready), it_n & 1, status, abort_flag)) break;
           const int n = it.n_kv;
           auto issue_s = [&](int j) -> bool {
@@ -322,7 +379,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
           mbar_arrive_cluster(v_full0 + vs * 8);
           return true;
         };
-        for (int idx = pair_id; next_pair(p, idx, n_pairs, total_items, rank, it); idx += n_pairs) {
+        for (int idx = pair_id; next_pair(p, idx, n_pairs, total, rank, it, wl); idx += n_pairs) {
           const int n = it.n_kv;
           bool ok = relay_k(g);
           if (ok && n > 1) ok = relay_k(g + 1);
@@ -373,7 +430,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
 
     int idx = pair_id;
     PairItem it;
-    bool have = next_pair(p, idx, n_pairs, total_items, rank, it);
+    bool have = next_pair(p, idx, n_pairs, total, rank, it, wl);
     if (have) ok = stage_q(0);
     while (have && ok) {
       const Item& own = it.own;
@@ -467,7 +524,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
       g += it.n_kv;
       int nidx = idx + n_pairs;
       PairItem nx;
-      const bool have_next = next_pair(p, nidx, n_pairs, total_items, rank, nx);
+      const bool have_next = next_pair(p, nidx, n_pairs, total, rank, nx, wl);
       if (have_next && !(ok = stage_q(it_n + 1))) break;
       // ---------------------------------------------------------- epilogue
       if (!(ok = mbar_wait_cluster_warp(smem_u32(&sh->o_done[(g - 1) & 1]), ((g - 1) >> 1) & 1, status,
@@ -520,7 +577,8 @@ constexpr int E_SMEM_Q = 0;                                  // 2 slots
 constexpr int E_SMEM_K = E_SMEM_Q + 2 * EQ_BYTES;
 constexpr int E_SMEM_V = E_SMEM_K + PNK * EK_BYTES;          // f16 halves, as in the bf16 kernel
 constexpr int E_SMEM_BAR = E_SMEM_V + PNV * PV_BYTES;        // 163840
-constexpr int E_SMEM_TOTAL = E_SMEM_BAR + 256 + 1024;
+constexpr int E_SMEM_UNITS = E_SMEM_BAR + 256;                // compacted work units
+constexpr int E_SMEM_TOTAL = E_SMEM_UNITS + 4 * 4096 + 1024;
 constexpr uint32_t IDESC_QK8P = idesc_e4m3(256, 128, false, false);
 constexpr uint32_t IDESC_PV16P = idesc_f16(256, 128, false, true);
 static_assert(EQ_BYTES % 1024 == 0 && EK_BYTES % 1024 == 0 && E_SMEM_V % 1024 == 0, "swizzle alignment");
@@ -585,6 +643,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     tmem_alloc_pair(smem_u32(&sh->tmem), P_TMEM_COLS);
     tmem_relinquish_pair();
   }
+  __shared__ int warp_cnt[8];
+  const WorkList wl{reinterpret_cast<const uint32_t*>(smem + E_SMEM_UNITS),
+                    compact_units(p, reinterpret_cast<uint32_t*>(smem + E_SMEM_UNITS), warp_cnt)};
+  const int total = wl.n >= 0 ? wl.n * p.H : total_items;
   tc_fence_before();
   cluster_sync();   // barriers of both CTAs initialised, TMEM allocated
   tc_fence_after();
@@ -605,7 +667,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     int q_last[2] = {-1, -1}, k_last[PNK] = {-1, -1, -1, -1};
     bool ok = true;
     PairItem it;
-    for (int idx = pair_id; ok && next_pair(p, idx, n_pairs, total_items, rank, it); idx += n_pairs) {
+    for (int idx = pair_id; ok && next_pair(p, idx, n_pairs, total, rank, it, wl); idx += n_pairs) {
       // Q slot it_n & 1 is free once item it_n - 2's last S MMA completed
       // (the MMAs read Q from shared memory).
       const int qs = it_n & 1;
@@ -663,7 +725,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     int v_last[PNV] = {-1, -1, -1, -1};
     bool ok = true;
     PairItem it;
-    for (int idx = pair_id; ok && next_pair(p, idx, n_pairs, total_items, rank, it); idx += n_pairs) {
+    for (int idx = pair_id; ok && next_pair(p, idx, n_pairs, total, rank, it, wl); idx += n_pairs) {
       for (int j = 0; j < it.n_kv; ++j) {
         const uint32_t gj = g + j;
         const int row = it.own.kv_row0 + j * BN;
@@ -696,7 +758,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
         uint32_t g = 0, it_n = 0;
         const uint32_t o_t = tmem + P_TM_O;
         PairItem it;
-        for (int idx = pair_id; next_pair(p, idx, n_pairs, total_items, rank, it); idx += n_pairs) {
+        for (int idx = pair_id; next_pair(p, idx, n_pairs, total, rank, it, wl); idx += n_pairs) {
           if (!mbar_wait_cluster(smem_u32(&sh->q_ready), it_n & 1, status, abort_flag)) break;
           const int n = it.n_kv;
           auto issue_s = [&](int j) -> bool {
@@ -773,7 +835,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
           mbar_arrive_cluster(v_full0 + vs * 8);
           return true;
         };
-        for (int idx = pair_id; next_pair(p, idx, n_pairs, total_items, rank, it); idx += n_pairs) {
+        for (int idx = pair_id; next_pair(p, idx, n_pairs, total, rank, it, wl); idx += n_pairs) {
           const int n = it.n_kv;
           bool ok = relay_k(g);
           if (ok && n > 1) ok = relay_k(g + 1);
@@ -810,7 +872,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
 
     int idx = pair_id;
     PairItem it;
-    bool have = next_pair(p, idx, n_pairs, total_items, rank, it);
+    bool have = next_pair(p, idx, n_pairs, total, rank, it, wl);
     if (have) ok = stage_q(0);
     while (have && ok) {
       const Item& own = it.own;
@@ -904,7 +966,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
       g += it.n_kv;
       int nidx = idx + n_pairs;
       PairItem nx;
-      const bool have_next = next_pair(p, nidx, n_pairs, total_items, rank, nx);
+      const bool have_next = next_pair(p, nidx, n_pairs, total, rank, nx, wl);
       if (have_next && !(ok = stage_q(it_n + 1))) break;
       // ---------------------------------------------------------- epilogue
       if (!(ok = mbar_wait_cluster_warp(smem_u32(&sh->o_done[(g - 1) & 1]), ((g - 1) >> 1) & 1, status,
