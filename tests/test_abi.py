@@ -31,8 +31,8 @@ def lib():
 
 def test_header_declares_the_boundary():
     names = _declared()
-    for n in ("mla_prefill_plan", "mla_gather_latent", "mla_upproject", "mla_prefill_attention",
-              "mla_prefill", "mla_prefill_workspace_bytes", "mla_status_string"):
+    for n in ("mla_latent_cache_write", "mla_prefill_plan", "mla_gather_latent", "mla_upproject",
+              "mla_prefill_attention", "mla_prefill", "mla_prefill_workspace_bytes", "mla_status_string"):
         assert n in names
 
 
@@ -67,6 +67,31 @@ def test_host_argument_errors(lib):
     # chunk index outside the plan
     args = [16, None, 16, 16] + [16] * 9 + [3, 2, 1, 4, 16, 16, 8, 0.1]
     assert mla.mla_prefill_attention(*args, stream=s) == mla.MLA_ERR_ARG
+
+
+def test_cache_write_host_argument_errors(lib):
+    s = 1
+    # kv_cache, q, kv_latent, gamma, freqs, iro, cache_lengths, page_table, num_pages, page_size,
+    # max_pages, B, H, T, max_seq_len, epsilon, kv_inv_scale, dtype
+    ok = [16, 16, 16, 16, 16, 16, 16, 16, 4, 16, 2, 1, 2, 8, 64, 1e-6, 1.0, mla.MLA_BF16]
+
+    def call(**change):
+        a = list(ok)
+        names = ["kv", "q", "lat", "gamma", "freqs", "iro", "cl", "pt", "np", "ps", "mp", "B", "H", "T",
+                 "msl", "eps", "inv", "dt"]
+        for k, v in change.items():
+            a[names.index(k)] = v
+        return mla.mla_latent_cache_write(*a, None, s)
+    assert call(dt=7) == mla.MLA_ERR_DTYPE
+    assert call(kv=None) == mla.MLA_ERR_ARG
+    assert call(lat=24) == mla.MLA_ERR_ARG          # misaligned
+    assert call(freqs=20) == mla.MLA_ERR_ARG
+    assert call(B=0) == mla.MLA_ERR_ARG
+    assert call(T=-1) == mla.MLA_ERR_ARG
+    assert call(H=0) == mla.MLA_ERR_ARG             # q given without heads
+    assert call(msl=0) == mla.MLA_ERR_ARG
+    assert call(eps=-1.0) == mla.MLA_ERR_ARG
+    assert call(inv=0.0) == mla.MLA_ERR_ARG
 
 
 def test_workspace_size_and_errors(lib):
