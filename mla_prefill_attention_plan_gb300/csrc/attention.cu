@@ -47,7 +47,8 @@ constexpr int SMEM_Q = 0;
 constexpr int SMEM_K = SMEM_Q + Q_BYTES;
 constexpr int SMEM_V = SMEM_K + NK * K_BYTES;
 constexpr int SMEM_BAR = SMEM_V + NV * V_BYTES;   // 212992
-constexpr int SMEM_TOTAL = SMEM_BAR + 256 + 1024;
+constexpr int SMEM_UNITS = SMEM_BAR + 256;        // compaction counts, then the unit list
+constexpr int SMEM_TOTAL = SMEM_UNITS + 32 + 4 * 4096 + 1024;   // the largest launch
 constexpr int NUM_THREADS = 224;   // 7 warps: Q/K producer, MMA, 4 softmax, V producer
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_S = 0;      // S/P buffers: columns 0..127, 128..255
@@ -71,23 +72,65 @@ static_assert(sizeof(Smem) <= 256, "barrier block");
 // Item order: heads in groups of `head_group`; within a group, query tiles
 // heaviest first, and the group's heads side by side.  The CTAs in flight then
 // share the K/V of a few heads in L2 instead of streaming every head's K/V.
-__device__ __forceinline__ bool load_item(const Params& p, int idx, Item& it) {
-  const int n_pairs = p.n_qtiles * p.B;
-  const int per_group = p.head_group * n_pairs;
+// The units (sequence b, query tile qt) are those of the chunk with work,
+// compacted in shared memory by every CTA first (up to kMaxUnits; beyond that
+// all units are walked and the empty ones skipped), so that the static stride
+// walks consecutive work and the CTAs in flight stay within one head group.
+constexpr int kMaxUnits = 4096;
+
+struct WorkList {
+  const uint32_t* units;   // shared memory
+  int n;                   // units with work, or -1: walk all units
+};
+
+__device__ __forceinline__ bool load_item(const Params& p, int idx, Item& it, const WorkList& wl) {
+  const int n_units = wl.n >= 0 ? wl.n : p.n_qtiles * p.B;
+  const int per_group = p.head_group * n_units;
   const int grp = idx / per_group;
   const int r = idx - grp * per_group;
   const int hg = min(p.head_group, p.H - grp * p.head_group);   // heads in this group
-  const int pair = r / hg;
-  const int h = grp * p.head_group + (r - pair * hg);
-  const int qt = p.n_qtiles - 1 - pair / p.B;   // heaviest query tiles first
-  return tile_item(p, pair % p.B, h, qt, it);
+  const int ui = r / hg;
+  const int h = grp * p.head_group + (r - ui * hg);
+  const int unit = wl.n >= 0 ? static_cast<int>(wl.units[ui]) : ui;
+  const int qt = p.n_qtiles - 1 - unit / p.B;   // heaviest query tiles first
+  return tile_item(p, unit % p.B, h, qt, it);
 }
 
 // First item with work at or after `idx` (stepping by the grid size).
-__device__ __forceinline__ bool next_item(const Params& p, int& idx, int total, Item& it) {
+__device__ __forceinline__ bool next_item(const Params& p, int& idx, int total, Item& it, const WorkList& wl) {
   for (; idx < total; idx += gridDim.x)
-    if (load_item(p, idx, it)) return true;
+    if (load_item(p, idx, it, wl)) return true;
   return false;
+}
+
+// Every thread of the CTA: compact the units with work into `list`; returns
+// their count (the same in every thread), or -1 past kMaxUnits.
+__device__ int compact_units(const Params& p, uint32_t* list, int* warp_cnt) {
+  const int n_units = p.n_qtiles * p.B;
+  if (n_units > kMaxUnits) return -1;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nwarps = static_cast<int>(blockDim.x) >> 5;
+  int base = 0;
+  for (int u0 = 0; u0 < n_units; u0 += static_cast<int>(blockDim.x)) {
+    const int u = u0 + tid;
+    bool has = false;
+    if (u < n_units) {
+      Item a;
+      has = tile_item(p, u % p.B, 0, p.n_qtiles - 1 - u / p.B, a);
+    }
+    const uint32_t m = __ballot_sync(0xffffffffu, has);
+    if (lane == 0) warp_cnt[warp] = __popc(m);
+    __syncthreads();
+    int off = base, tot = 0;
+    for (int w = 0; w < nwarps; ++w) {
+      if (w < warp) off += warp_cnt[w];
+      tot += warp_cnt[w];
+    }
+    if (has) list[off + __popc(m & ((1u << lane) - 1u))] = static_cast<uint32_t>(u);
+    base += tot;
+    __syncthreads();   // warp_cnt is rewritten by the next round
+  }
+  return base;
 }
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -129,6 +172,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tmem_alloc(smem_u32(&sh->tmem), TMEM_COLS);
     tmem_relinquish();
   }
+  // Compaction counts (8 ints), then the list, sized by the launch.
+  const WorkList wl{reinterpret_cast<const uint32_t*>(smem + SMEM_UNITS + 32),
+                    compact_units(p, reinterpret_cast<uint32_t*>(smem + SMEM_UNITS + 32),
+                                  reinterpret_cast<int*>(smem + SMEM_UNITS))};
+  const int total = wl.n >= 0 ? wl.n * p.H : total_items;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -149,7 +197,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int q_last = -1, k_last[NK] = {-1, -1};
     bool ok = true;
     Item it;
-    for (int idx = blockIdx.x; ok && next_item(p, idx, total_items, it); idx += gridDim.x) {
+    for (int idx = blockIdx.x; ok && next_item(p, idx, total, it, wl); idx += gridDim.x) {
       // The shared-memory Q buffer is free once the previous item's Q is in TMEM.
       if (it_n > 0 && !(ok = mbar_wait_warp(smem_u32(&sh->q_empty), (it_n - 1) & 1, status, abort_flag))) break;
       if (elect_one()) {
@@ -195,7 +243,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int v_last[NV] = {-1, -1};
     bool ok = true;
     Item it;
-    for (int idx = blockIdx.x; ok && next_item(p, idx, total_items, it); idx += gridDim.x) {
+    for (int idx = blockIdx.x; ok && next_item(p, idx, total, it, wl); idx += gridDim.x) {
       for (int j = 0; j < it.n_kv; ++j) {
         const uint32_t gj = g + j;
         const int row = it.kv_row0 + j * BN;
@@ -231,7 +279,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t q_t = tmem + TM_Q;
       const uint32_t o_t = tmem + TM_O;
       Item it;
-      for (int idx = blockIdx.x; next_item(p, idx, total_items, it); idx += gridDim.x) {
+      for (int idx = blockIdx.x; next_item(p, idx, total, it, wl); idx += gridDim.x) {
         if (!mbar_wait(smem_u32(&sh->q_ready), it_n & 1, status, abort_flag)) break;
         const int n = it.n_kv;
         // S_j = Q K_j^T into S buffer j % 2 (it last held P_{j-2}, whose P*V
@@ -322,7 +370,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     int idx = blockIdx.x;
     Item it;
-    bool have = next_item(p, idx, total_items, it);
+    bool have = next_item(p, idx, total, it, wl);
     if (have) ok = stage_q(0);
     while (have && ok) {
       const long long qpos = static_cast<long long>(it.cb) + it.i0 + row;
@@ -427,7 +475,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // item's first MMAs run under this epilogue.
       int nidx = idx + gridDim.x;
       Item nx;
-      const bool have_next = next_item(p, nidx, total_items, nx);
+      const bool have_next = next_item(p, nidx, total, nx, wl);
       if (have_next && !(ok = stage_q(it_n + 1))) break;
       // ---------------------------------------------------------- epilogue
       if (!(ok = mbar_wait_warp(smem_u32(&sh->o_done[(g - 1) & 1]), ((g - 1) >> 1) & 1, status, abort_flag))) break;
@@ -508,7 +556,9 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   if (total <= 0) return cudaSuccess;
   const int grid = total < sm_count() ? static_cast<int>(total) : sm_count();
   cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
-  attn_kernel<<<grid, NUM_THREADS, SMEM_TOTAL, stream>>>(maps[0], maps[1], maps[2], maps[3], p,
+  const int n_units = p.n_qtiles * p.B;
+  const int smem_bytes = SMEM_UNITS + 32 + 4 * (n_units <= kMaxUnits ? n_units : 0) + 1024;
+  attn_kernel<<<grid, NUM_THREADS, smem_bytes, stream>>>(maps[0], maps[1], maps[2], maps[3], p,
                                                         static_cast<int>(total));
   return cudaGetLastError();
 }

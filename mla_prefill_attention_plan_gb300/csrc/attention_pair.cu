@@ -49,8 +49,8 @@ constexpr int P_SMEM_Q = 0;
 constexpr int P_SMEM_K = P_SMEM_Q + PQ_BYTES;
 constexpr int P_SMEM_V = P_SMEM_K + PNK * PK_BYTES;
 constexpr int P_SMEM_BAR = P_SMEM_V + PNV * PV_BYTES;   // 212992
-constexpr int P_SMEM_UNITS = P_SMEM_BAR + 256;                // compacted work units
-constexpr int P_SMEM_TOTAL = P_SMEM_UNITS + 4 * 4096 + 1024;
+constexpr int P_SMEM_UNITS = P_SMEM_BAR + 256;                // compaction counts, then the unit list
+constexpr int P_SMEM_TOTAL = P_SMEM_UNITS + 32 + 4 * 4096 + 1024;   // the largest launch
 constexpr int P_THREADS = 224;
 constexpr uint32_t P_TMEM_COLS = 512;
 constexpr uint32_t P_TM_S = 0, P_TM_O = 256, P_TM_Q = 384;
@@ -198,9 +198,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     tmem_alloc_pair(smem_u32(&sh->tmem), P_TMEM_COLS);
     tmem_relinquish_pair();
   }
-  __shared__ int warp_cnt[8];
-  const WorkList wl{reinterpret_cast<const uint32_t*>(smem + P_SMEM_UNITS),
-                    compact_units(p, reinterpret_cast<uint32_t*>(smem + P_SMEM_UNITS), warp_cnt)};
+  // Compaction counts (8 ints), then the list, sized by the launch.
+  const WorkList wl{reinterpret_cast<const uint32_t*>(smem + P_SMEM_UNITS + 32),
+                    compact_units(p, reinterpret_cast<uint32_t*>(smem + P_SMEM_UNITS + 32),
+                                  reinterpret_cast<int*>(smem + P_SMEM_UNITS))};
   const int total = wl.n >= 0 ? wl.n * p.H : total_items;
   tc_fence_before();
   cluster_sync();   // barriers of both CTAs initialised, TMEM allocated
@@ -577,8 +578,8 @@ constexpr int E_SMEM_Q = 0;                                  // 2 slots
 constexpr int E_SMEM_K = E_SMEM_Q + 2 * EQ_BYTES;
 constexpr int E_SMEM_V = E_SMEM_K + PNK * EK_BYTES;          // f16 halves, as in the bf16 kernel
 constexpr int E_SMEM_BAR = E_SMEM_V + PNV * PV_BYTES;        // 163840
-constexpr int E_SMEM_UNITS = E_SMEM_BAR + 256;                // compacted work units
-constexpr int E_SMEM_TOTAL = E_SMEM_UNITS + 4 * 4096 + 1024;
+constexpr int E_SMEM_UNITS = E_SMEM_BAR + 256;                // compaction counts, then the unit list
+constexpr int E_SMEM_TOTAL = E_SMEM_UNITS + 32 + 4 * 4096 + 1024;   // the largest launch
 constexpr uint32_t IDESC_QK8P = idesc_e4m3(256, 128, false, false);
 constexpr uint32_t IDESC_PV16P = idesc_f16(256, 128, false, true);
 static_assert(EQ_BYTES % 1024 == 0 && EK_BYTES % 1024 == 0 && E_SMEM_V % 1024 == 0, "swizzle alignment");
@@ -643,9 +644,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     tmem_alloc_pair(smem_u32(&sh->tmem), P_TMEM_COLS);
     tmem_relinquish_pair();
   }
-  __shared__ int warp_cnt[8];
-  const WorkList wl{reinterpret_cast<const uint32_t*>(smem + E_SMEM_UNITS),
-                    compact_units(p, reinterpret_cast<uint32_t*>(smem + E_SMEM_UNITS), warp_cnt)};
+  // Compaction counts (8 ints), then the list, sized by the launch.
+  const WorkList wl{reinterpret_cast<const uint32_t*>(smem + E_SMEM_UNITS + 32),
+                    compact_units(p, reinterpret_cast<uint32_t*>(smem + E_SMEM_UNITS + 32),
+                                  reinterpret_cast<int*>(smem + E_SMEM_UNITS))};
   const int total = wl.n >= 0 ? wl.n * p.H : total_items;
   tc_fence_before();
   cluster_sync();   // barriers of both CTAs initialised, TMEM allocated
@@ -1008,6 +1010,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
 
 // Two-CTA clusters of `kernel` (with `smem` bytes) that can be resident at
 // once, per device (0 if none).
+// Dynamic shared memory of a launch: the tiles and barriers, the compaction
+// counts and a unit list as long as the chunk can need (the kernels walk all
+// units without a list past kMaxUnits).
+static int pair_smem_bytes(int units_offset, const Params& p) {
+  const int n_units = ((p.n_qtiles + 1) >> 1) * p.B;
+  const int listed = n_units <= kMaxUnits ? n_units : 0;
+  return units_offset + 32 + 4 * listed + 1024;
+}
+
 template <typename Kernel>
 static int pair_clusters_of(Kernel kernel, int smem, int device, int slot) {
   static std::mutex mu;
@@ -1079,7 +1090,7 @@ cudaError_t launch_attention_pair(const AttnArgs& a, cudaStream_t stream) {
   const int clusters = pair_clusters(dev);
   if (clusters <= 0) return cudaErrorInvalidConfiguration;
   const int grid = 2 * static_cast<int>(total < clusters ? total : clusters);
-  attn_pair_kernel<<<grid, P_THREADS, P_SMEM_TOTAL, stream>>>(maps[0], maps[1], maps[2], maps[3], p,
+  attn_pair_kernel<<<grid, P_THREADS, pair_smem_bytes(P_SMEM_UNITS, p), stream>>>(maps[0], maps[1], maps[2], maps[3], p,
                                                              static_cast<int>(total));
   return cudaGetLastError();
 }
@@ -1125,7 +1136,7 @@ cudaError_t launch_attention_pair_e4m3(const AttnArgs& a, cudaStream_t stream) {
   const int clusters = pair_clusters_e4m3(dev);
   if (clusters <= 0) return cudaErrorInvalidConfiguration;
   const int grid = 2 * static_cast<int>(total < clusters ? total : clusters);
-  attn_pair_kernel_e4m3<<<grid, P_THREADS, E_SMEM_TOTAL, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4],
+  attn_pair_kernel_e4m3<<<grid, P_THREADS, pair_smem_bytes(E_SMEM_UNITS, p), stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4],
                                                                   p, static_cast<int>(total));
   return cudaGetLastError();
 }
