@@ -73,3 +73,25 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
                                       "--warmup", "0"])
     bench.main()
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_prints_the_contract_line(monkeypatch, capsys):
+    """The reference arm (the oracle on host cores) prints one JSON line with
+    the keys the benchmark contract names, on rank 0."""
+    import json
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.delenv("RANK", raising=False)
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--impl", "reference", "--steps", "1", "--warmup", "0"])
+    bench.main()
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["value"] > 0 and d["config"]["workload"] == "v3_prefill"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
