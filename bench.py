@@ -202,6 +202,31 @@ def _cores():
     return os.cpu_count() or 1
 
 
+def _cpu_model():
+    """The host CPU as /proc/cpuinfo names it (x86: model name; Arm: implementer and part)."""
+    import platform
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+    except OSError:
+        return platform.machine()
+    fields = {}
+    for line in info.splitlines():
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields.setdefault(k.strip(), v.strip())
+    if "model name" in fields:
+        return fields["model name"]
+    if "CPU part" in fields:
+        return f"{platform.machine()} implementer {fields.get('CPU implementer', '?')} part {fields['CPU part']}"
+    return platform.machine()
+
+
+def _cpu_desc():
+    return {"cores": _cores(), "cpu_model": _cpu_model(),
+            "omp_num_threads": os.environ.get("OMP_NUM_THREADS")}
+
+
 def run_reference(a):
     import numpy as np
     rank, world, _ = _dist()
@@ -235,7 +260,7 @@ def run_reference(a):
         "ms_per_step": secs / a.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": _config(w, inp),
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", **_cpu_desc(), "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -465,7 +490,7 @@ def run_ours(a):
     }
     if not a.no_cpu_baseline:
         v, secs, desc = _oracle_sample(w, inp, budget_s=15.0)
-        line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle",
+        line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", **_cpu_desc(), "kind": "oracle",
                                 "sample": desc, "seconds": secs}
     print(json.dumps(line), flush=True)
     if world > 1:

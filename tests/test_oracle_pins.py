@@ -219,8 +219,9 @@ def _token_walk(new, cache, S, max_chunks):
 
 
 def test_plan_matches_token_walk_random():
+    """10^4 random tiny cases (B <= 6, lengths <= 40, S in [1, 50])."""
     rng = np.random.default_rng(1234)
-    for _ in range(2000):
+    for _ in range(10000):
         B = int(rng.integers(0, 7))
         new = rng.integers(0, 41, size=B)
         cache = rng.integers(0, 41, size=B)
