@@ -179,6 +179,16 @@ def test_plan_unaligned_tables():
     np.testing.assert_array_equal(bl.cpu().numpy(), o[2])
 
 
+def test_plan_empty_batch():
+    """No sequences: every chunk is unused (length -1, row [0])."""
+    bro, co, bl, st = gpu_plan([0], [], 8, 3)
+    o = O.prefill_plan([0], [], 8, 3)
+    assert st == o[3] == 0
+    np.testing.assert_array_equal(bro, o[0])
+    np.testing.assert_array_equal(bl, o[2])
+    assert list(bl) == [-1, -1, -1]
+
+
 def test_plan_status_codes():
     assert gpu_plan([0, 10], [0], 4, 2)[3] == mla.MLA_DEV_TOO_MANY_CHUNKS
     _assert_plan_equal([0, 10], [0], 4, 2)          # truncated rows still written
