@@ -1,6 +1,7 @@
 """Planted mistakes in the oracle (CPU only): each plausible slip -- an
 off-by-one mask, a dropped rope term, a wrong weight slice, a shifted cache
 offset, swapped merge weights -- must make at least one pin fail."""
+import math
 import os
 
 import numpy as np
@@ -149,3 +150,51 @@ def test_position_off_by_one_is_caught(monkeypatch):
         return orig(kv_latent, q, gamma, np.asarray(freqs)[1:], iro, cache_lengths, *a, **k)
     _plant(monkeypatch, "latent_cache_write", shifted)
     _must_fail(P.test_cache_write_round_trip_through_cache, P.test_cache_write_page_permutation_and_e4m3)
+
+
+def test_gather_slot_off_by_one_is_caught(monkeypatch):
+    """A cache row read one slot later than its position: the rows encode
+    (sequence, position, column), so the construction pin sees it."""
+    orig = M.gather_latent
+
+    def shifted(kv_cache_codes, page_table, page_size, plan, chunk):
+        kv = np.asarray(kv_cache_codes)
+        rolled = np.roll(kv.reshape(-1, kv.shape[-1]), -1, axis=0).reshape(kv.shape)
+        return orig(rolled, page_table, page_size, plan, chunk)
+    _plant(monkeypatch, "gather_latent", shifted)
+    _must_fail(P.test_gather_by_construction)
+
+
+def test_bf16_truncation_is_caught(monkeypatch):
+    """Rounding toward zero instead of to nearest even."""
+    def trunc(x):
+        x = np.asarray(x, dtype=np.float64)
+        _, e = np.frexp(x)
+        q = np.ldexp(1.0, np.maximum(e - 1, -126) - 7)
+        return np.trunc(x / q) * q
+    monkeypatch.setattr(M, "round_to_bf16", trunc)
+    _must_fail(P.test_bf16_codec_against_torch)
+
+
+def test_e4m3_ties_away_from_zero_is_caught(monkeypatch):
+    """Ties rounded away from zero instead of to even."""
+    def away(x):
+        x = np.asarray(x, dtype=np.float64)
+        a = np.minimum(np.abs(x), M.E4M3_MAX)
+        _, e = np.frexp(a)
+        q = np.ldexp(1.0, np.maximum(e - 1, -6) - 3)
+        r = np.minimum(np.floor(a / q + 0.5) * q, M.E4M3_MAX)
+        return np.copysign(r, x)
+    monkeypatch.setattr(M, "round_to_e4m3", away)
+    _must_fail(P.test_e4m3_codec_against_torch, P.test_e4m3_spec_values)
+
+
+def test_log2_lse_is_caught(monkeypatch):
+    """The log-sum-exp in base 2 instead of the natural log."""
+    orig = M.softmax_weights
+
+    def log2(s):
+        w, lse = orig(s)
+        return w, lse / math.log(2.0)
+    _plant(monkeypatch, "softmax_weights", log2)
+    _must_fail(P.test_attention_closed_forms, P.test_merge_split_equals_one_shot)
