@@ -550,6 +550,70 @@ def mla_prefill(q_codes, kv_cache_codes, page_table, page_size, w_k_codes, w_uv_
     return acc, plan
 
 
+# --------------------------------------------------------------------------
+# (5) Decode branch -- "mla_prefill_decode_graph_bf16" (dispatches to decode by
+# the batch's max sequence length; Args w_uk, w_uv, num_partitions_in).  The
+# nope query is absorbed into latent space, attention runs over the 576-wide
+# latent rows read straight from the paged cache, the keys are split into
+# partitions whose partial results merge by LSE, and the latent result is
+# projected back per head.
+# --------------------------------------------------------------------------
+
+def mla_decode(q, kv_cache_codes, page_table, page_size: int, w_uk, w_uv, input_row_offsets,
+               cache_lengths, scale: float, num_partitions: int = 1, dtype: str = "bf16",
+               ckv_scale: float = 1.0):
+    """Decode attention in the absorbed form.
+
+    ``q`` [T, H, 192], ``w_uk`` [H, 512, 128] and ``w_uv`` [H, 128, 512] are
+    values; the cache is storage codes (real = stored * ``ckv_scale``).  New
+    token i of sequence b (row ``input_row_offsets[b] + i``) at position
+    p = cache_lengths[b] + i sees context positions 0..p.  Per head,
+    q_lat = w_uk[h] q_nope scores the latent rows (score = scale * (q_lat .
+    c_kv_j + q_rope . k_rope_j)); the p + 1 keys are cut into
+    ``num_partitions`` contiguous ranges of ceil((p + 1) / num_partitions)
+    keys (trailing ranges may be empty), each range gives a partial (latent O,
+    LSE), and the partials merge in order with ``merge_partials``.  The merged
+    latent O is projected by w_uv[h].
+
+    Returns a dict (b, h) -> (tokens, out [n, 128], LSE [n]).
+    """
+    iro = np.asarray(input_row_offsets, dtype=np.int64)
+    cache = np.asarray(cache_lengths, dtype=np.int64)
+    L = cache + (iro[1:] - iro[:-1])
+    ctx = context_latents(kv_cache_codes, page_table, page_size, L)
+    q = np.asarray(q, dtype=np.float64)
+    H = q.shape[1]
+    res = {}
+    for b in range(cache.shape[0]):
+        n = int(iro[b + 1] - iro[b])
+        if n <= 0:
+            continue
+        lat = decode(ctx[b], dtype) * ckv_scale
+        c_kv, k_rope = lat[:, :R], lat[:, R:]
+        for h in range(H):
+            out = np.zeros((n, DV))
+            lses = np.zeros(n)
+            for i in range(n):
+                t = int(iro[b]) + i
+                keys = int(cache[b]) + i + 1
+                q_lat = np.asarray(w_uk[h], dtype=np.float64) @ q[t, h, :DN]
+                s = scale * (c_kv[:keys] @ q_lat + k_rope[:keys] @ q[t, h, DN:])
+                size = -(-keys // num_partitions)
+                o, lse = np.zeros((1, R)), np.array([-np.inf])
+                for k in range(num_partitions):
+                    lo, hi = k * size, min((k + 1) * size, keys)
+                    if lo >= hi:
+                        o_k, lse_k = np.zeros((1, R)), np.array([-np.inf])
+                    else:
+                        w, lse_k = softmax_weights(s[None, lo:hi])
+                        o_k = w @ c_kv[lo:hi]
+                    o, lse = merge_partials(o, lse, o_k, lse_k)
+                out[i] = np.asarray(w_uv[h], dtype=np.float64) @ o[0]
+                lses[i] = lse[0]
+            res[(b, h)] = (np.arange(iro[b], iro[b + 1]), out, lses)
+    return res
+
+
 def causal_pairs(new_lens, cache_lens) -> int:
     """Number of visible (query, key) pairs: sum over b, i of cache_len_b + i + 1."""
     tot = 0

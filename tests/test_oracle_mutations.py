@@ -198,3 +198,13 @@ def test_log2_lse_is_caught(monkeypatch):
         return w, lse / math.log(2.0)
     _plant(monkeypatch, "softmax_weights", log2)
     _must_fail(P.test_attention_closed_forms, P.test_merge_split_equals_one_shot)
+
+
+def test_partials_averaged_instead_of_merged_is_caught(monkeypatch):
+    """Partition results averaged instead of weighted by their LSE."""
+    def average(o_a, lse_a, o_b, lse_b):
+        fa, fb = np.isfinite(lse_a), np.isfinite(lse_b)
+        o = np.where((fa & fb)[..., None], 0.5 * (o_a + o_b), np.where(fa[..., None], o_a, o_b))
+        return o, np.logaddexp(lse_a, lse_b)
+    monkeypatch.setattr(M, "merge_partials", average)
+    _must_fail(P.test_decode_partition_count_invariant)

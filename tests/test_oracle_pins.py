@@ -618,6 +618,47 @@ def test_absorbed_equals_upprojected():
         np.testing.assert_allclose(ab[key][2], up[key][2], rtol=1e-12, atol=1e-10)
 
 
+def _decode_case(seed=3, H=3):
+    """A decode-shaped batch: one or two new tokens per sequence over cached
+    context, w_uk built from w_k (w_uk[h] = W_k,h^T)."""
+    w = scaled(WORKLOADS["tiny_ragged"], H=H, B=3, page_size=8, new_lens=(1, 2, 1),
+               cache_lens=(20, 0, 37), seed=seed)
+    inp, c = _oracle_inputs(w)
+    wk = O.decode(c["w_k"], "bf16")
+    w_uk = np.stack([wk[h * M.DN:(h + 1) * M.DN].T for h in range(H)])
+    wuv = O.decode(c["w_uv"], "bf16")
+    q = O.decode(c["q"], "bf16")
+    return inp, c, q, w_uk, wuv
+
+
+def test_decode_equals_upprojected_attention():
+    """The absorbed decode over the paged cache equals up-projecting K and V and
+    attending over them (no rounding of K/V on either side)."""
+    inp, c, q, w_uk, wuv = _decode_case()
+    dec = O.mla_decode(q, c["kv_cache"], c["page_table"], inp["page_size"], w_uk, wuv,
+                       c["input_row_offsets"], c["cache_lengths"], inp["scale"], num_partitions=3)
+    up = _unchunked_pipeline(inp, c, store=False)
+    assert set(dec) == set(up)
+    for key in up:
+        np.testing.assert_array_equal(dec[key][0], up[key][0])
+        np.testing.assert_allclose(dec[key][1], up[key][1], rtol=1e-9, atol=1e-10)
+        np.testing.assert_allclose(dec[key][2], up[key][2], rtol=1e-12, atol=1e-10)
+
+
+def test_decode_partition_count_invariant():
+    """Any number of key partitions, including more partitions than keys (empty
+    ones), gives the same result."""
+    inp, c, q, w_uk, wuv = _decode_case(seed=5, H=2)
+    args = (q, c["kv_cache"], c["page_table"], inp["page_size"], w_uk, wuv, c["input_row_offsets"],
+            c["cache_lengths"], inp["scale"])
+    base = O.mla_decode(*args, num_partitions=1)
+    for parts in (2, 5, 16, 64):
+        got = O.mla_decode(*args, num_partitions=parts)
+        for key in base:
+            np.testing.assert_allclose(got[key][1], base[key][1], rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(got[key][2], base[key][2], rtol=1e-13, atol=1e-13)
+
+
 def test_fp8_pipeline_chunked_equals_unchunked():
     w = scaled(WORKLOADS["longctx_fp8"], H=2, new_lens=(40,), cache_lens=(50,),
                buffer_token_size=48, max_chunks=2, page_size=16)
