@@ -68,10 +68,12 @@ enum {
 
 enum { MLA_BF16 = 0, MLA_E4M3 = 1 };
 
-/* Human-readable text for a host or device status code (static storage). */
+/* Human-readable text for a host or device status code (static storage).
+ * Utility of this library; no counterpart on the pages. */
 const char* mla_status_string(int32_t code);
 
-/* ABI version of this header. */
+/* ABI version of this header.  Utility of this library; no counterpart on the
+ * pages. */
 int32_t mla_abi_version(void);
 #define MLA_ABI_VERSION 1
 
@@ -308,7 +310,12 @@ mla_status_t mla_prefill_attention_noalloc(void* out, float* lse, const void* q,
 /*
  * Workspace bytes needed by mla_prefill for these sizes (plan tables, the
  * chunk's latent, k_rope, K and V buffers, and the fp32 merge state when
- * max_chunks > 1).
+ * max_chunks > 1).  The buffers follow "mla_prefill_decode_graph_bf16" (Args:
+ * buffer_row_offsets, cache_offsets, buffer_length) and
+ * "flare_mla_prefill_dispatch" (Args: k, v, k_rope); the pages size none of
+ * them, so this call has no counterpart there.  Host only; returns 0 for
+ * invalid sizes (B < 0, H < 1, total_q_tokens < 0, max_chunks < 1,
+ * buffer_token_size == 0) or an unknown dtype.
  */
 size_t mla_prefill_workspace_bytes(int32_t batch_size, int32_t num_heads,
                                    int32_t total_q_tokens, int32_t max_chunks,

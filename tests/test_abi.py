@@ -36,6 +36,18 @@ def test_header_declares_the_boundary():
         assert n in names
 
 
+def test_every_entry_point_cites_its_passage():
+    """Each declaration in the header is preceded by a comment that names the
+    page it follows (a quoted page title) or says it has no counterpart there."""
+    import re
+    text = open(os.path.join(HEADER_DIR, "mla_prefill.h")).read()
+    for m in re.finditer(r"\n[a-z_0-9 \*]*\b(mla_[a-z_0-9]+)\(", text):
+        before = text[:m.start()]
+        comment = before[before.rfind("/*"):]
+        assert comment.startswith("/*") and "*/" in comment, m.group(1)
+        assert '"' in comment or "no counterpart" in comment, m.group(1)
+
+
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared():
         assert hasattr(lib, name), name
