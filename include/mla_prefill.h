@@ -32,6 +32,10 @@
  *     a pipeline wait that timed out) are written to the caller's
  *     `int32_t* d_status` (first error wins; kernels never clear it; the
  *     fused entry point clears it first).  `d_status` may be NULL.
+ *   - Every kernel that finds MLA_DEV_TIMEOUT already in *d_status when it
+ *     starts does no work and returns, so one timeout stops the rest of the
+ *     enqueued pipeline on that status word instead of letting it run on
+ *     partial results.  Outputs of such calls are left untouched.
  *   - fp8 scales are descales: real value = stored value * scale.
  */
 #ifndef MLA_PREFILL_H
@@ -75,18 +79,36 @@ const char* mla_status_string(int32_t code);
 /* ABI version of this header.  Utility of this library; no counterpart on the
  * pages. */
 int32_t mla_abi_version(void);
-#define MLA_ABI_VERSION 1
+#define MLA_ABI_VERSION 2
 
 /*
- * Which attention kernel mla_prefill_attention / mla_prefill will launch for
- * `dtype` on the current CUDA device: "pair" (bf16 on two-SM clusters, the
- * default where the device can keep such a cluster resident), "single" (bf16,
- * one SM per work item; also chosen by setting the environment variable
- * MLA_ATTENTION_KERNEL=single) or "e4m3" (two-SM clusters; the only e4m3
- * kernel, an error where the device cannot run it).  Static storage; NULL for an unknown
- * dtype.  The pages have no counterpart: this is an introspection call.
+ * Which attention kernel mla_prefill_attention / mla_prefill launch for
+ * `dtype`: "pair" (bf16 on two-SM clusters) or "e4m3" (the e4m3 form of the
+ * same kernel).  There is one kernel per dtype and no fallback: a device that
+ * cannot keep a two-CTA cluster of it resident gets MLA_ERR_LAUNCH from the
+ * call.  Static storage; NULL for an unknown dtype.  The pages have no
+ * counterpart: this is an introspection call.
  */
 const char* mla_attention_kernel(int32_t dtype);
+
+/*
+ * Self-test of the failure detection the kernels rely on (the pages have
+ * no counterpart to it).  Launches one cluster of `cluster_size` (1 or 2) CTAs that
+ * wait on barriers nothing ever arrives at.  With one CTA it waits
+ * `limit_ns`; with two, CTA 1 waits `limit_ns` and CTA 0 the library's full
+ * limit (2 s), and CTA 0 must return as soon as CTA 1 gives up, through the
+ * abort flag a timed-out wait raises in every CTA of its cluster.  Every wait
+ * of every kernel in this library is bounded the same way.
+ *
+ * d_status:      int32, receives MLA_DEV_TIMEOUT
+ * d_elapsed_ns:  int64 [cluster_size], 8-byte aligned: how long each CTA
+ *                waited (-1 if its barrier completed, which cannot happen)
+ * limit_ns:      1000 .. 2e9
+ * Errors: host MLA_ERR_ARG for null or misaligned pointers or sizes out of
+ * range; MLA_ERR_LAUNCH if the launch fails.
+ */
+mla_status_t mla_selftest_bounded_wait(int32_t* d_status, int64_t* d_elapsed_ns, int64_t limit_ns,
+                                       int32_t cluster_size, mla_stream_t stream);
 
 /*
  * 0. Latent-cache write.  Follows "mla_prefill_decode_graph_bf16" (Args:
@@ -216,13 +238,14 @@ mla_status_t mla_gather_latent(void* c_kv_buf, void* k_rope_buf, const void* kv_
  *             this storage choice)
  * c_kv_buf:   [buffer_token_size][512] dtype
  * w_k:        [num_heads*128][512] dtype;  w_uv: [num_heads][128][512] dtype
- * Errors: host MLA_ERR_ARG / MLA_ERR_DTYPE / MLA_ERR_GEOMETRY (num_heads < 1).
+ * Errors: host MLA_ERR_ARG / MLA_ERR_DTYPE / MLA_ERR_GEOMETRY (num_heads < 1),
+ * MLA_ERR_LAUNCH; device MLA_DEV_TIMEOUT (d_status may be NULL).
  */
 mla_status_t mla_upproject(void* k_nope, void* v, const void* c_kv_buf, const void* w_k,
                            const void* w_uv, const int32_t* buffer_lengths, int32_t chunk,
                            uint32_t buffer_token_size, int32_t num_heads, int32_t dtype,
                            float ckv_scale, float w_scale, float kv_out_inv_scale,
-                           mla_stream_t stream);
+                           int32_t* d_status, mla_stream_t stream);
 
 /*
  * 4. Prefill attention for one plan chunk.  Follows "flare_mla_prefill_dispatch"
@@ -255,7 +278,16 @@ mla_status_t mla_upproject(void* k_nope, void* v, const void* c_kv_buf, const vo
  * Rows of k_nope/k_rope beyond a sequence's keys are read but masked; rows of v
  * beyond them are never used.
  * max_prompt_len: largest new-token count of any sequence (sizes the grid).
- * Errors: host MLA_ERR_ARG / MLA_ERR_DTYPE / MLA_ERR_GEOMETRY; device MLA_DEV_TIMEOUT.
+ * Errors: host MLA_ERR_ARG / MLA_ERR_DTYPE / MLA_ERR_GEOMETRY, MLA_ERR_LAUNCH.
+ * Device:
+ *   MLA_DEV_TIMEOUT          a pipeline wait ran out; rows not yet stored keep
+ *                            whatever out held before.
+ *   MLA_DEV_TOO_MANY_CHUNKS  a row needs merge state but o_acc / lse_acc are
+ *                            NULL (more than one chunk holds its keys, or the
+ *                            plan was truncated at max_chunks); that row of
+ *                            out is not written.
+ *   MLA_DEV_BAD_OFFSETS      input_row_offsets[b+1] > total_q_tokens: sequence
+ *                            b is left out (its rows of out are not written).
  */
 mla_status_t mla_prefill_attention(void* out, float* lse, float* o_acc, float* lse_acc,
                                    const void* q, const void* k_nope, const void* v,
@@ -284,9 +316,11 @@ mla_status_t mla_prefill_attention(void* out, float* lse, float* o_acc, float* l
  *
  * - total_q_tokens * num_heads must be <= MLA_NOALLOC_MAX_ROWS; larger calls
  *   return MLA_ERR_WORKSPACE (use mla_prefill_attention with caller scratch).
- * - The first call on each device looks up the array's device address
- *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.  Failure of the lookup returns MLA_ERR_LAUNCH.
+ * - Every call looks up the array's device address on the current device
+ *   (cudaGetSymbolAddress), so the address stays right after a
+ *   cudaDeviceReset.  The first call on a device may load the library's
+ *   device code there; make that first call before any stream capture.
+ *   Failure of the lookup returns MLA_ERR_LAUNCH.
  * - All calls share the one array and it keeps the last call's contents.  A
  *   multi-chunk sequence of calls (chunk 0, 1, ...) relies on that; calls from
  *   different sequences that overlap on the GPU (other streams, other threads)

@@ -42,11 +42,12 @@ SIGNATURES = {
     "mla_status_string": (ctypes.c_char_p, [_I]),
     "mla_abi_version": (_I, []),
     "mla_attention_kernel": (ctypes.c_char_p, [_I]),
+    "mla_selftest_bounded_wait": (_I, [_P, _P, ctypes.c_int64, _I, _P]),
     "mla_prefill_plan": (_I, [_P, _P, _P, _P, _P, _I, _I, _U, _P, _P]),
     "mla_latent_cache_write": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                                     _F, _F, _I, _P, _P]),
     "mla_gather_latent": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _I, _I, _U, _I, _P, _P]),
-    "mla_upproject": (_I, [_P, _P, _P, _P, _P, _P, _I, _U, _I, _I, _F, _F, _F, _P]),
+    "mla_upproject": (_I, [_P, _P, _P, _P, _P, _P, _I, _U, _I, _I, _F, _F, _F, _P, _P]),
     "mla_prefill_attention": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                    _I, _I, _I, _I, _I, _I, _U, _F, _F, _F, _F, _I, _P, _P]),
     "mla_prefill_attention_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
@@ -116,6 +117,12 @@ def mla_attention_kernel(dtype) -> str:
     return r.decode() if r is not None else None
 
 
+def mla_selftest_bounded_wait(d_status, d_elapsed_ns, limit_ns, cluster_size, stream=None) -> int:
+    """Launch the bounded-wait self-test (see include/mla_prefill.h)."""
+    return load().mla_selftest_bounded_wait(_ptr(d_status), _ptr(d_elapsed_ns), int(limit_ns),
+                                            cluster_size, _stream(stream))
+
+
 def mla_prefill_plan(buffer_row_offsets, cache_offsets, buffer_lengths, input_row_offsets,
                      cache_lengths, batch_size, max_chunks, buffer_token_size, d_status=None,
                      stream=None) -> int:
@@ -150,10 +157,11 @@ def mla_gather_latent(c_kv_buf, k_rope_buf, kv_cache, page_table, num_pages, pag
 
 def mla_upproject(k_nope, v, c_kv_buf, w_k, w_uv, buffer_lengths, chunk, buffer_token_size,
                   num_heads, dtype, ckv_scale=1.0, w_scale=1.0, kv_out_inv_scale=1.0,
-                  stream=None) -> int:
+                  d_status=None, stream=None) -> int:
     return load().mla_upproject(_ptr(k_nope), _ptr(v), _ptr(c_kv_buf), _ptr(w_k), _ptr(w_uv),
                                 _ptr(buffer_lengths), chunk, buffer_token_size, num_heads, dtype,
-                                ckv_scale, w_scale, kv_out_inv_scale, _stream(stream))
+                                ckv_scale, w_scale, kv_out_inv_scale, _ptr(d_status),
+                                _stream(stream))
 
 
 def mla_prefill_attention(out, lse, o_acc, lse_acc, q, k_nope, v, k_rope, input_row_offsets,

@@ -122,7 +122,18 @@ int32_t mla_abi_version(void) { return MLA_ABI_VERSION; }
 const char* mla_attention_kernel(int32_t dtype) {
   if (dtype == MLA_E4M3) return "e4m3";
   if (dtype != MLA_BF16) return nullptr;
-  return mla::attention_uses_pair() ? "pair" : "single";
+  return "pair";
+}
+
+mla_status_t mla_selftest_bounded_wait(int32_t* d_status, int64_t* d_elapsed_ns, int64_t limit_ns,
+                                       int32_t cluster_size, mla_stream_t stream) {
+  if (!d_status || !d_elapsed_ns || (reinterpret_cast<uintptr_t>(d_elapsed_ns) & 7u) ||
+      (cluster_size != 1 && cluster_size != 2) || limit_ns < 1000 ||
+      limit_ns > static_cast<int64_t>(mla::kWaitLimitNs))
+    return MLA_ERR_ARG;
+  return from_cuda(mla::launch_bounded_wait_selftest(d_status, reinterpret_cast<long long*>(d_elapsed_ns),
+                                                     static_cast<uint64_t>(limit_ns), cluster_size,
+                                                     static_cast<cudaStream_t>(stream)));
 }
 
 mla_status_t mla_latent_cache_write(void* kv_cache, void* q, const void* kv_latent,
@@ -201,7 +212,7 @@ mla_status_t mla_upproject(void* k_nope, void* v, const void* c_kv_buf, const vo
                            const void* w_uv, const int32_t* buffer_lengths, int32_t chunk,
                            uint32_t buffer_token_size, int32_t num_heads, int32_t dtype,
                            float ckv_scale, float w_scale, float kv_out_inv_scale,
-                           mla_stream_t stream) {
+                           int32_t* d_status, mla_stream_t stream) {
   if (!dtype_ok(dtype)) return MLA_ERR_DTYPE;
   if (num_heads < 1) return MLA_ERR_GEOMETRY;
   if (!k_nope || !v || !c_kv_buf || !w_k || !w_uv || !aligned16(k_nope) || !aligned16(v) ||
@@ -220,7 +231,7 @@ mla_status_t mla_upproject(void* k_nope, void* v, const void* c_kv_buf, const vo
   a.H = num_heads;
   a.dtype = dtype;
   a.out_scale = ckv_scale * w_scale * kv_out_inv_scale;
-  a.status = nullptr;
+  a.status = d_status;
   return from_cuda(launch_upproject(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -336,7 +347,7 @@ mla_status_t mla_prefill(void* out, float* lse, const void* q, const uint32_t* i
                            dtype, d_status, stream_);
     if (st != MLA_OK) return st;
     st = mla_upproject(ws + L.knope, ws + L.v, ws + L.ckv, w_k, w_uv, bl, c, buffer_token_size,
-                       num_heads, dtype, ckv_scale, w_scale, kv_inv, stream_);
+                       num_heads, dtype, ckv_scale, w_scale, kv_inv, d_status, stream_);
     if (st != MLA_OK) return st;
     st = attention_impl(out, lse, oacc, lseacc, q, ws + L.knope, ws + L.v, ws + L.krope,
                         input_row_offsets, cache_lengths, bro, co, bl, c, max_chunks, batch_size,

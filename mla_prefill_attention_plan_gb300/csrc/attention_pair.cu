@@ -191,7 +191,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     }
     mbar_init(smem_u32(&sh->o_free), 8);
     mbar_init(smem_u32(&sh->drain), 1);
-    sh->abort = 0;
+    // A pipeline timeout recorded by an earlier kernel on this status word:
+    // do no work (the pair agrees through cluster_any below).
+    sh->abort = timed_out_before(p.status) ? 1 : 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -202,10 +204,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
   const WorkList wl{reinterpret_cast<const uint32_t*>(smem + P_SMEM_UNITS + 32),
                     compact_units(p, reinterpret_cast<uint32_t*>(smem + P_SMEM_UNITS + 32),
                                   reinterpret_cast<int*>(smem + P_SMEM_UNITS))};
-  const int total = wl.n >= 0 ? wl.n * p.H : total_items;
   tc_fence_before();
   cluster_sync();   // barriers of both CTAs initialised, TMEM allocated
   tc_fence_after();
+  const int total = cluster_any(&sh->abort) ? 0 : (wl.n >= 0 ? wl.n * p.H : total_items);
   const uint32_t tmem = sh->tmem;
   volatile int* abort_flag = &sh->abort;
   int32_t* status = p.status;
@@ -637,7 +639,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     }
     mbar_init(smem_u32(&sh->o_free), 8);
     mbar_init(smem_u32(&sh->drain), 1);
-    sh->abort = 0;
+    // A pipeline timeout recorded by an earlier kernel on this status word:
+    // do no work (the pair agrees through cluster_any below).
+    sh->abort = timed_out_before(p.status) ? 1 : 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -648,10 +652,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
   const WorkList wl{reinterpret_cast<const uint32_t*>(smem + E_SMEM_UNITS + 32),
                     compact_units(p, reinterpret_cast<uint32_t*>(smem + E_SMEM_UNITS + 32),
                                   reinterpret_cast<int*>(smem + E_SMEM_UNITS))};
-  const int total = wl.n >= 0 ? wl.n * p.H : total_items;
   tc_fence_before();
   cluster_sync();   // barriers of both CTAs initialised, TMEM allocated
   tc_fence_after();
+  const int total = cluster_any(&sh->abort) ? 0 : (wl.n >= 0 ? wl.n * p.H : total_items);
   const uint32_t tmem = sh->tmem;
   volatile int* abort_flag = &sh->abort;
   int32_t* status = p.status;
@@ -1019,6 +1023,8 @@ static int pair_smem_bytes(int units_offset, const Params& p) {
   return units_offset + 32 + 4 * listed + 1024;
 }
 
+// Two-CTA clusters of `kernel` (with `smem` bytes) that the current device can
+// keep resident at once, or 0 if the query fails or none fits.
 template <typename Kernel>
 static int pair_clusters_of(Kernel kernel, int smem, int device, int slot) {
   static std::mutex mu;
@@ -1045,12 +1051,6 @@ static int pair_clusters_of(Kernel kernel, int smem, int device, int slot) {
 static int pair_clusters(int device) { return pair_clusters_of(attn_pair_kernel, P_SMEM_TOTAL, device, 0); }
 static int pair_clusters_e4m3(int device) {
   return pair_clusters_of(attn_pair_kernel_e4m3, E_SMEM_TOTAL, device, 1);
-}
-
-bool attention_pair_available() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return false;
-  return pair_clusters(dev) > 0;
 }
 
 cudaError_t launch_attention_pair(const AttnArgs& a, cudaStream_t stream) {
@@ -1082,6 +1082,7 @@ cudaError_t launch_attention_pair(const AttnArgs& a, cudaStream_t stream) {
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.v_scale = a.v_scale;
   p.status = a.status;
+  p.T_q = a.T_q;
   const long long total = static_cast<long long>((p.n_qtiles + 1) / 2) * a.B * a.H;
   if (total <= 0) return cudaSuccess;
   int dev = 0;
@@ -1128,6 +1129,7 @@ cudaError_t launch_attention_pair_e4m3(const AttnArgs& a, cudaStream_t stream) {
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.v_scale = a.v_scale;
   p.status = a.status;
+  p.T_q = a.T_q;
   const long long total = static_cast<long long>((p.n_qtiles + 1) / 2) * a.B * a.H;
   if (total <= 0) return cudaSuccess;
   int dev = 0;
@@ -1139,6 +1141,13 @@ cudaError_t launch_attention_pair_e4m3(const AttnArgs& a, cudaStream_t stream) {
   attn_pair_kernel_e4m3<<<grid, P_THREADS, pair_smem_bytes(E_SMEM_UNITS, p), stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4],
                                                                   p, static_cast<int>(total));
   return cudaGetLastError();
+}
+
+// The one attention entry of the library: bf16 on the pair kernel, e4m3 on
+// its e4m3 form.  A device that cannot keep a two-CTA cluster of the kernel
+// resident gets an error (there is no other kernel to fall back to).
+cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
+  return a.dtype == MLA_E4M3 ? launch_attention_pair_e4m3(a, stream) : launch_attention_pair(a, stream);
 }
 
 }  // namespace mla

@@ -23,6 +23,7 @@ struct Params {
   const uint32_t* co;
   const int32_t* bl;
   int chunk, B, H, n_qtiles, head_group;
+  int T_q;            // rows of q / out / lse: no query row at or past it is read or written
   float scale_log2;   // softmax scale * descales * log2(e)
   float v_scale;
   int32_t* status;
@@ -49,10 +50,18 @@ __device__ __forceinline__ bool tile_item(const Params& p, int b, int h, int qt,
   const uint32_t* bro_c = p.bro + static_cast<size_t>(p.chunk) * (p.B + 1);
   const int r0 = static_cast<int>(bro_c[b]);
   it.n_cb = static_cast<int>(bro_c[b + 1]) - r0;
-  const int q0 = static_cast<int>(p.iro[b]);
-  const int new_b = static_cast<int>(p.iro[b + 1]) - q0;
+  const uint32_t qa = p.iro[b], qe = p.iro[b + 1];
   it.i0 = qt * BM;
   it.n_kv = 0;
+  if (qe > static_cast<uint32_t>(p.T_q)) {
+    // Offsets past the q / out rows: report them and leave the sequence out
+    // (a decreasing pair is simply empty).
+    set_status(p.status, MLA_DEV_BAD_OFFSETS);
+    it.nq = 0;
+    return false;
+  }
+  const int q0 = static_cast<int>(qa);
+  const int new_b = qe >= qa ? static_cast<int>(qe - qa) : 0;
   it.nq = max(0, min(BM, new_b - it.i0));
   it.q_row0 = q0 + it.i0;
   it.kv_row0 = r0;

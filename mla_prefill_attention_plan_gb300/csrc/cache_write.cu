@@ -47,6 +47,7 @@ __global__ void __launch_bounds__(kThreads)
   __shared__ float part[kThreads / 32];
   __shared__ int s_pos;
   __shared__ uint8_t* s_dst;
+  if (timed_out_before(status)) return;   // an earlier kernel timed out: no work
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const float4 g4 = reinterpret_cast<const float4*>(gamma)[tid];
 

@@ -30,7 +30,7 @@ __global__ void __launch_bounds__(kThreads)
                   const uint8_t* __restrict__ cache, const int32_t* __restrict__ page_table,
                   int num_pages, int page_size, int max_pages, const uint32_t* __restrict__ bro,
                   const uint32_t* __restrict__ co, const int32_t* __restrict__ bl, int chunk, int B,
-                  int32_t* status) {
+                  int S, int32_t* status) {
   constexpr int kRowBytes = 576 * ELT;
   constexpr int kVecPerRow = kRowBytes / 16;        // 72 (bf16) or 36 (e4m3)
   constexpr int kCkvVec = 512 * ELT / 16;           // 64 or 32
@@ -39,7 +39,8 @@ __global__ void __launch_bounds__(kThreads)
   constexpr int kPerThread = (kVecs + kThreads - 1) / kThreads;
 
   __shared__ const uint8_t* src_row[kRows];
-  const int n = bl[chunk];
+  if (timed_out_before(status)) return;   // an earlier kernel timed out: no work
+  const int n = min(bl[chunk], S);        // never past the buffers, whatever the table says
   const int r0 = blockIdx.x * kRows;
   if (r0 >= n) return;
   const uint32_t* bro_c = bro + static_cast<size_t>(chunk) * (B + 1);
@@ -101,12 +102,12 @@ cudaError_t launch_gather(void* c_kv_buf, void* k_rope_buf, const void* kv_cache
     gather_kernel<2><<<grid, kThreads, 0, stream>>>(
         static_cast<uint8_t*>(c_kv_buf), static_cast<uint8_t*>(k_rope_buf),
         static_cast<const uint8_t*>(kv_cache), page_table, num_pages, page_size, max_pages, bro,
-        co, bl, chunk, B, status);
+        co, bl, chunk, B, static_cast<int>(S), status);
   else
     gather_kernel<1><<<grid, kThreads, 0, stream>>>(
         static_cast<uint8_t*>(c_kv_buf), static_cast<uint8_t*>(k_rope_buf),
         static_cast<const uint8_t*>(kv_cache), page_table, num_pages, page_size, max_pages, bro,
-        co, bl, chunk, B, status);
+        co, bl, chunk, B, static_cast<int>(S), status);
   return cudaGetLastError();
 }
 

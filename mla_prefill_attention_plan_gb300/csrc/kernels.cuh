@@ -49,12 +49,9 @@ struct UpprojArgs {
   float out_scale;
   int32_t* status;
 };
+// The GEMM on two-SM pairs (cta_group::2 clusters, 256 x 256 tiles); an
+// error where the device cannot keep such a cluster resident.
 cudaError_t launch_upproject(const UpprojArgs& a, cudaStream_t stream);
-// The same GEMM on two-SM pairs (cta_group::2 clusters, 256 x 256 tiles);
-// launch_upproject uses it where the device can keep such a cluster resident
-// unless MLA_UPPROJ_KERNEL=single.
-bool upproject_pair_available(int dtype);
-cudaError_t launch_upproject_pair(const UpprojArgs& a, cudaStream_t stream);
 
 struct AttnArgs {
   void* out;
@@ -82,17 +79,17 @@ struct AttnArgs {
   int dtype;
   int32_t* status;
 };
+// bf16 attention on two-SM pairs (cta_group::2 clusters); e4m3 Q / K with V
+// as f16 holding e4m3-rounded values (as mla_upproject writes it), on the
+// same pairs.  An error where the device cannot keep such a cluster resident.
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream);
-// bf16 attention on two-SM pairs (cta_group::2 clusters); false / an error
-// when the device cannot keep a two-CTA cluster of the kernel resident.
-bool attention_pair_available();
-// The bf16 kernel launch_attention picks (MLA_ATTENTION_KERNEL=single forces
-// the one-SM kernel).
-bool attention_uses_pair();
 cudaError_t launch_attention_pair(const AttnArgs& a, cudaStream_t stream);
-// e4m3 Q / K with V as f16 holding e4m3-rounded values (as mla_upproject
-// writes it), on two-SM pairs; the only e4m3 attention kernel.
 cudaError_t launch_attention_pair_e4m3(const AttnArgs& a, cudaStream_t stream);
+
+// Self-test of the bounded waits (selftest.cu): one cluster of `cluster`
+// CTAs waiting on barriers nothing arrives at.
+cudaError_t launch_bounded_wait_selftest(int32_t* status, long long* elapsed_ns, uint64_t limit_ns,
+                                         int cluster, cudaStream_t stream);
 
 // Tensor-map encoder and device properties (abi.cu).
 bool encode_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, uint64_t inner,

@@ -11,36 +11,29 @@
 //
 // The array lives in this library's device image, so every GPU that loads the
 // library holds it (MLA_NOALLOC_MAX_ROWS * 129 floats, about 16.9 MB) until the
-// process exits.  Host code never uses the array's name as an address: the
-// device address is looked up once per device with cudaGetSymbolAddress and
-// then passed to the kernel.
-#include <mutex>
-
+// process exits.  Host code never uses the array's name as an address: every
+// call looks up the array's device address on the current device with
+// cudaGetSymbolAddress and passes that to the kernel.  (Looking it up on every
+// call, rather than once per device, keeps the address right after a
+// cudaDeviceReset or a reload of the module; the lookup is a host-side table
+// read once the module is loaded.)
 #include "kernels.cuh"
 
 namespace {
 
 constexpr size_t kMaxRows = MLA_NOALLOC_MAX_ROWS;  // total_q_tokens * num_heads
-constexpr int kMaxDevices = 64;
 
 // [kMaxRows][128] running O, then [kMaxRows] running LSE, all fp32.
 static __device__ __align__(256) float g_merge_scratch[kMaxRows * 128 + kMaxRows];
 
-std::mutex g_mutex;
-float* g_scratch[kMaxDevices] = {};
-
-// Device address of the scratch on the current device (looked up on the first
-// call for that device).  Null on failure.
+// Device address of the scratch on the current device; null on failure.
 float* scratch_on_current_device() {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(g_mutex);
-  if (g_scratch[dev] == nullptr) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_merge_scratch) != cudaSuccess) return nullptr;
-    g_scratch[dev] = static_cast<float*>(ptr);
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_merge_scratch) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
   }
-  return g_scratch[dev];
+  return static_cast<float*>(ptr);
 }
 
 }  // namespace

@@ -98,6 +98,7 @@ __global__ void __launch_bounds__(kThreads) plan_one_cta(uint32_t* bro, uint32_t
                                                          int32_t* status) {
   __shared__ uint64_t warp_tot[32];
   __shared__ int s_bad;
+  if (timed_out_before(status)) return;   // an earlier kernel timed out: no work
   if (threadIdx.x == 0) s_bad = (B >= 0 && iro[0] != 0) ? 1 : 0;
   __syncthreads();
   int bad = 0;
@@ -159,10 +160,12 @@ __device__ __forceinline__ uint64_t block_sum64(uint64_t v, uint64_t* red) {
 }
 
 __global__ void __launch_bounds__(kSThreads) plan_tile_totals(uint32_t* co, const uint32_t* iro,
-                                                              const uint32_t* cache_len, int B) {
+                                                              const uint32_t* cache_len, int B,
+                                                              const int32_t* status) {
   __shared__ uint64_t red[kSWarps];
   // Let pass B's CTAs start their own loads while this pass runs.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (timed_out_before(status)) return;   // pass B returns too
   const int t = blockIdx.x;
   const int base = t * kSTile;
   uint64_t v = 0;
@@ -189,6 +192,9 @@ __global__ void __launch_bounds__(kSThreads, 5) plan_tile_tables(uint32_t* bro, 
   __shared__ uint32_t warp_tot[kSWarps];
   __shared__ uint64_t red[kSWarps];
   __shared__ int s_last;
+  // After a pipeline timeout recorded on this status word, neither pass does
+  // any work (no pass writes that code, so both passes read the same value).
+  if (timed_out_before(status)) return;
   const int t = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e0 = t * kSTile + warp * (32 * kSPerLane) + lane;   // this thread's first sequence
@@ -304,7 +310,7 @@ cudaError_t launch_plan(uint32_t* bro, uint32_t* co, int32_t* bl, const uint32_t
     return cudaGetLastError();
   }
   const int ntiles = (B + kSTile - 1) / kSTile;
-  plan_tile_totals<<<ntiles, kSThreads, 0, stream>>>(co, iro, cache_len, B);
+  plan_tile_totals<<<ntiles, kSThreads, 0, stream>>>(co, iro, cache_len, B, status);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   // Pass B as a programmatic dependent launch of pass A.

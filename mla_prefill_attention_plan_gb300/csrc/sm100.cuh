@@ -57,10 +57,40 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return done != 0;
 }
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t n;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+  return n;
+}
+
+// Raise the abort flag of this CTA and, in a cluster, the flag at the same
+// shared-memory offset in every other CTA of the cluster, so that the CTAs
+// that wait on this one give up together instead of each running out its own
+// limit.  (The other CTAs are still resident: every cluster kernel here ends
+// with a cluster barrier that no CTA passes before the others reach it.)
+__device__ __forceinline__ void raise_abort(volatile int* abort_flag) {
+  *abort_flag = 1;
+  const uint32_t n = cluster_size();
+  // Only a flag in shared memory has a counterpart in the other CTAs (the
+  // drain waits pass a flag of their own in local memory).
+  if (n > 1 && __isShared(const_cast<int*>(abort_flag))) {
+    uint32_t me;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(me));
+    const uint32_t local = static_cast<uint32_t>(__cvta_generic_to_shared(const_cast<int*>(abort_flag)));
+    for (uint32_t r = 0; r < n; ++r) {
+      if (r == me) continue;
+      uint32_t remote;
+      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(r));
+      asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote), "r"(1) : "memory");
+    }
+  }
+}
+
 // Wait for the phase of parity `parity` to complete.  False on timeout (the
-// timeout is recorded in *status and in the CTA's abort flag).
+// timeout is recorded in *status and in the abort flags of the CTA and its
+// cluster) or once the abort flag is up.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* status,
-                                          volatile int* abort_flag) {
+                                          volatile int* abort_flag, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   uint32_t n = 0;
@@ -68,13 +98,38 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t
     if (mbar_try_wait(bar, parity)) return true;
     if ((++n & 63u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
+      if (globaltimer() - t0 > limit_ns) {
         set_status(status, MLA_DEV_TIMEOUT);
-        *abort_flag = 1;
+        raise_abort(abort_flag);
         return false;
       }
     }
   }
+}
+
+// Whether the flag at this shared-memory offset is set in any CTA of the
+// cluster.  Called after a cluster barrier that orders every CTA's write of
+// the flag, so that all CTAs get the same answer.
+__device__ __forceinline__ bool cluster_any(volatile int* flag) {
+  int any = *flag;
+  const uint32_t n = cluster_size();
+  uint32_t me;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(me));
+  const uint32_t local = static_cast<uint32_t>(__cvta_generic_to_shared(const_cast<int*>(flag)));
+  for (uint32_t r = 0; r < n; ++r) {
+    if (r == me) continue;
+    uint32_t remote, v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(r));
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
+    any |= static_cast<int>(v);
+  }
+  return any != 0;
+}
+
+// True when an earlier kernel on the caller's status word recorded a
+// pipeline timeout: the kernels then do no work and return.
+__device__ __forceinline__ bool timed_out_before(const int32_t* status) {
+  return status != nullptr && *reinterpret_cast<const volatile int32_t*>(status) == MLA_DEV_TIMEOUT;
 }
 
 // The same wait for a whole warp that runs warp-collective (.sync.aligned)

@@ -68,7 +68,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(U_THREADS, 1)
   if (rows <= 0) return;
   if (rows > S) rows = S;
   const int num_m = (rows + 2 * UBM - 1) / (2 * UBM);   // 256-row pair tiles
-  const int num_tiles = num_m * H;                      // N: 2*H*128 / 256
   constexpr int KB = 512 * ELT / UBKB;                  // k-blocks: 8 (bf16) or 4 (e4m3)
   constexpr int KSTEP = 32;                             // bytes of one MMA's K
   constexpr uint32_t IDESC = ELT == 2 ? idesc_bf16(2 * UBM, UBN, false, false) : idesc_e4m3(2 * UBM, UBN, false, false);
@@ -84,7 +83,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(U_THREADS, 1)
       mbar_init(smem_u32(&sh->tempty[i]), 8);
     }
     mbar_init(smem_u32(&sh->drain), 1);
-    sh->abort = 0;
+    // A pipeline timeout recorded by an earlier kernel on this status word:
+    // do no work (the pair agrees through cluster_any below).
+    sh->abort = timed_out_before(status) ? 1 : 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -94,6 +95,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(U_THREADS, 1)
   tc_fence_before();
   cluster_sync();
   tc_fence_after();
+  const int num_tiles = cluster_any(&sh->abort) ? 0 : num_m * H;   // N: 2*H*128 / 256
   const uint32_t tmem = sh->tmem;
   volatile int* abort_flag = &sh->abort;
 
@@ -307,13 +309,7 @@ int pair_gemm_clusters(int device) {
 
 }  // namespace
 
-bool upproject_pair_available(int dtype) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return false;
-  return (dtype == MLA_BF16 ? pair_gemm_clusters<2>(dev) : pair_gemm_clusters<1>(dev)) > 0;
-}
-
-cudaError_t launch_upproject_pair(const UpprojArgs& a, cudaStream_t stream) {
+cudaError_t launch_upproject(const UpprojArgs& a, cudaStream_t stream) {
   const int elt = a.dtype == MLA_BF16 ? 2 : 1;
   const CUtensorMapDataType dt =
       elt == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;

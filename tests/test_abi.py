@@ -56,7 +56,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_strings(lib):
-    assert mla.mla_abi_version() == 1
+    assert mla.mla_abi_version() == 2
     # dtype-only answers need no device
     assert mla.mla_attention_kernel(mla.MLA_E4M3) == "e4m3"
     assert mla.mla_attention_kernel(7) is None
@@ -79,6 +79,16 @@ def test_host_argument_errors(lib):
     # chunk index outside the plan
     args = [16, None, 16, 16] + [16] * 9 + [3, 2, 1, 4, 16, 16, 8, 0.1]
     assert mla.mla_prefill_attention(*args, stream=s) == mla.MLA_ERR_ARG
+
+
+def test_selftest_host_argument_errors(lib):
+    s = 1
+    assert mla.mla_selftest_bounded_wait(None, 16, 5_000_000, 2, s) == mla.MLA_ERR_ARG
+    assert mla.mla_selftest_bounded_wait(16, None, 5_000_000, 2, s) == mla.MLA_ERR_ARG
+    assert mla.mla_selftest_bounded_wait(16, 12, 5_000_000, 2, s) == mla.MLA_ERR_ARG   # misaligned
+    assert mla.mla_selftest_bounded_wait(16, 16, 5_000_000, 3, s) == mla.MLA_ERR_ARG
+    assert mla.mla_selftest_bounded_wait(16, 16, 10, 1, s) == mla.MLA_ERR_ARG
+    assert mla.mla_selftest_bounded_wait(16, 16, 3_000_000_000, 1, s) == mla.MLA_ERR_ARG
 
 
 def test_cache_write_host_argument_errors(lib):

@@ -28,21 +28,11 @@ def _built():
     assert torch.cuda.is_available()
 
 
-@pytest.fixture(params=["pair", "single"])
-def bf16_kernel(request, monkeypatch):
-    """Both bf16 attention kernels: the two-SM pair kernel (the default) and
-    the one-SM kernel, selected through MLA_ATTENTION_KERNEL."""
-    monkeypatch.setenv("MLA_ATTENTION_KERNEL", request.param)
-    # No silent fallback: on a GB300 the pair kernel must be the one that runs.
-    assert mla.mla_attention_kernel(mla.MLA_BF16) == request.param
-    return request.param
-
-
-@pytest.fixture(params=["pair", "single"])
-def upproj_kernel(request, monkeypatch):
-    """Both up-projection GEMMs: two-SM pairs (the default) and one SM per tile."""
-    monkeypatch.setenv("MLA_UPPROJ_KERNEL", request.param)
-    return request.param
+@pytest.fixture
+def bf16_kernel():
+    """The bf16 attention kernel: one kernel (two-SM pairs), no fallback."""
+    assert mla.mla_attention_kernel(mla.MLA_BF16) == "pair"
+    return "pair"
 
 
 def _dt(w):
@@ -424,7 +414,7 @@ def test_gather_bad_page_reports_status():
 
 @pytest.mark.parametrize("dtype,H,rows,S", [("bf16", 4, 89, 96), ("bf16", 3, 300, 320),
                                             ("bf16", 16, 1000, 1024), ("e4m3", 4, 200, 256)])
-def test_upproject(dtype, H, rows, S, upproj_kernel):
+def test_upproject(dtype, H, rows, S):
     w = scaled(WORKLOADS["tiny_ragged" if dtype == "bf16" else "longctx_fp8"], H=H)
     gen = torch.Generator().manual_seed(H * 1000 + rows)
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float8_e4m3fn
@@ -520,6 +510,32 @@ def _attention_stage(w, seed_base=11):
 
 def test_attention_stage_multi_chunk(bf16_kernel):
     _attention_stage(WORKLOADS["tiny_ragged"])
+
+
+def test_attention_offsets_past_total_q_tokens():
+    """input_row_offsets[B] beyond total_q_tokens: the device reports bad
+    offsets, leaves that sequence out and writes no row at or past
+    total_q_tokens (the guard row past the declared output stays as it was);
+    the sequence inside the bound is still computed."""
+    w = scaled(WORKLOADS["tiny_ragged"], buffer_token_size=128, max_chunks=1)
+    inp = make_inputs(w)
+    c = {k: O.codes(inp[k]) for k in ("input_row_offsets", "cache_lengths")}
+    S, B, H, T = 128, inp["B"], w.H, inp["T_q"]
+    g = gpu_plan(c["input_row_offsets"], c["cache_lengths"], S, 1)
+    tabs = [torch.as_tensor(x.astype(np.int32)).to(DEV) for x in g[:3]]
+    kn, vv, kr = (t.to(DEV) for t in make_attention_operands(w, S))
+    out = torch.full((T, H, 128), 3.0, dtype=torch.bfloat16, device=DEV)
+    lse = torch.full((T, H), 3.0, dtype=torch.float32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    mla.check(mla.mla_prefill_attention(out, lse, None, None, inp["q"].to(DEV), kn, vv, kr,
+                                        inp["input_row_offsets"].to(DEV),
+                                        inp["cache_lengths"].to(DEV), *tabs, 0, 1, B, H,
+                                        inp["max_prompt_len"], T - 1, S, inp["scale"], d_status=st))
+    torch.cuda.synchronize()
+    assert int(st.item()) == mla.MLA_DEV_BAD_OFFSETS
+    n0 = int(inp["new_lens"][0])
+    assert (out[n0:].float() == 3.0).all() and (lse[n0:] == 3.0).all()
+    assert not (out[:n0].float() == 3.0).any()
 
 
 def test_attention_stage_e4m3_multi_chunk():
@@ -688,8 +704,6 @@ def test_fused_full_size_sampled(name, bf16_kernel):
     """Full sizes, the launch configuration the benchmark times; the oracle
     checks a sample of heads and rows."""
     w = WORKLOADS[name]
-    if w.dtype != "bf16" and bf16_kernel != "pair":
-        pytest.skip("one e4m3 kernel")
     inp = make_inputs(w)
     out, lse = run_fused(inp)
     heads = [0, w.H // 2 + 1, w.H - 1]
