@@ -378,6 +378,81 @@ mla_status_t mla_prefill(void* out, float* lse, const void* q, const uint32_t* i
                          int32_t dtype, void* workspace, size_t workspace_bytes,
                          int32_t* d_status, mla_stream_t stream);
 
+/*
+ * Decode partitions the library picks for mla_decode when num_partitions is
+ * 0: enough (sequence, 128 query rows, key partition) work items for about two
+ * waves of SM pairs, at most 32.  Follows "mla_prefill_decode_graph_bf16"
+ * (Args: num_partitions_in, the override of this choice).  Host only; 1 for
+ * invalid sizes.
+ */
+int32_t mla_decode_partitions(int32_t batch_size, int32_t num_heads, int32_t max_new_tokens);
+
+/*
+ * Workspace bytes mla_decode needs: the 576-wide query rows (bf16), every
+ * partition's fp32 latent result and LSE, and the merged bf16 latent result.
+ * The decode branch of "mla_prefill_decode_graph_bf16" (Args: w_uk, w_uv,
+ * num_partitions_in) sizes no buffer, so this call has no counterpart on the
+ * pages.  Host only; 0 for invalid sizes.
+ */
+size_t mla_decode_workspace_bytes(int32_t num_heads, int32_t total_q_tokens, int32_t num_partitions);
+
+/*
+ * Decode attention in the absorbed form.  Follows the decode branch of
+ * "mla_prefill_decode_graph_bf16" (Args: q [tot_seq_len, num_heads, 192];
+ * w_uk [num_heads, kv_latent_dim, qk_nope_head_dim], projecting each head's
+ * nope query into latent space; w_uv [num_heads, v_head_dim, kv_latent_dim],
+ * projecting the result back; scale; num_partitions_in; and the sparse form:
+ * d_indices, indices_stride, topk_lengths, attn_sink_ptr).
+ *
+ * New token i of sequence b is row t = input_row_offsets[b] + i of q and out.
+ * For head h:
+ *   q_lat = w_uk[h] . q[t][h][0:128]                          (512 values)
+ *   s_j   = scale * (q_lat . c_kv_j + q[t][h][128:192] . k_rope_j)
+ *   out[t][h] = w_uv[h] . sum_j softmax(s)_j c_kv_j           (128 values)
+ * over keys j, each a 576-wide cache row (c_kv = values 0..511, k_rope =
+ * 512..575):
+ *   - dense (d_indices NULL): context positions 0 .. cache_lengths[b] + i of
+ *     sequence b, read from page page_table[b][j / page_size], slot
+ *     j % page_size (the cache holds the new tokens' rows too);
+ *   - sparse (d_indices given): the physical cache rows d_indices[b *
+ *     indices_stride + e] (row = page * page_size + slot) for e <
+ *     topk_lengths[b] (indices_stride when topk_lengths is NULL), the same
+ *     list for every token of sequence b, no causal limit.
+ * With attn_sink given, sink = attn_sink[b] is one more logit in every
+ * softmax of sequence b with no value row: out is scaled by
+ * e^LSE / (e^LSE + e^sink) and lse includes it.  The keys are split into
+ * num_partitions ranges (0: mla_decode_partitions) whose partial results
+ * merge by LSE; the result does not depend on that choice beyond rounding.
+ * q_lat and the merged latent result are rounded to bf16 for the tensor-core
+ * projections; scores, softmax and the merge run in fp32.
+ *
+ * out:      [total_q_tokens][num_heads][128] bf16, output
+ * lse:      [total_q_tokens][num_heads] fp32 output (natural log), or NULL
+ * q:        [total_q_tokens][num_heads][192] bf16
+ * kv_cache: [num_pages][page_size][576] bf16
+ * w_uk [num_heads][512][128], w_uv [num_heads][128][512] bf16
+ * input_row_offsets [B+1], cache_lengths [B], page_table [B][max_pages_per_seq]
+ * max_new_tokens: largest new-token count of any sequence (sizes the grid)
+ * workspace: device memory of at least mla_decode_workspace_bytes(num_heads,
+ *            total_q_tokens, the partition count used), 256-byte aligned.
+ * Errors: host MLA_ERR_DTYPE (bf16 only: the page's graph is bf16),
+ * MLA_ERR_GEOMETRY, MLA_ERR_ARG (null or misaligned pointers, bad sizes),
+ * MLA_ERR_WORKSPACE, MLA_ERR_LAUNCH.  Device MLA_DEV_BAD_OFFSETS
+ * (input_row_offsets[b+1] > total_q_tokens: sequence b left out),
+ * MLA_DEV_BAD_PAGE (a page id or sparse row out of range: those keys read
+ * zeros or row 0, and the result of their rows is not meaningful),
+ * MLA_DEV_TIMEOUT.
+ */
+mla_status_t mla_decode(void* out, float* lse, const void* q, const uint32_t* input_row_offsets,
+                        const uint32_t* cache_lengths, const void* kv_cache, const int32_t* page_table,
+                        int32_t num_pages, int32_t page_size, int32_t max_pages_per_seq,
+                        const void* w_uk, const void* w_uv, int32_t batch_size, int32_t num_heads,
+                        int32_t total_q_tokens, int32_t max_new_tokens, int32_t num_partitions,
+                        float scale, const int32_t* d_indices, int32_t indices_stride,
+                        const int32_t* topk_lengths, const float* attn_sink, int32_t dtype,
+                        void* workspace, size_t workspace_bytes, int32_t* d_status,
+                        mla_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

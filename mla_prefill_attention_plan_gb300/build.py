@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmla_prefill.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["cache_write.cu", "plan.cu", "gather.cu", "upproj_pair.cu", "attention_pair.cu", "abi.cu", "noalloc.cu", "selftest.cu"]
+SOURCES = ["cache_write.cu", "plan.cu", "gather.cu", "upproj_pair.cu", "attention_pair.cu", "decode.cu", "abi.cu", "noalloc.cu", "selftest.cu"]
 
 
 def _nvcc() -> str:

@@ -358,4 +358,72 @@ mla_status_t mla_prefill(void* out, float* lse, const void* q, const uint32_t* i
   return MLA_OK;
 }
 
+int32_t mla_decode_partitions(int32_t batch_size, int32_t num_heads, int32_t max_new_tokens) {
+  if (batch_size < 1 || num_heads < 1 || max_new_tokens < 1) return 1;
+  return mla::decode_default_partitions(batch_size, num_heads, max_new_tokens);
+}
+
+size_t mla_decode_workspace_bytes(int32_t num_heads, int32_t total_q_tokens, int32_t num_partitions) {
+  if (num_heads < 1 || total_q_tokens < 0 || num_partitions < 1) return 0;
+  return mla::decode_layout(total_q_tokens, num_heads, num_partitions).total;
+}
+
+mla_status_t mla_decode(void* out, float* lse, const void* q, const uint32_t* input_row_offsets,
+                        const uint32_t* cache_lengths, const void* kv_cache, const int32_t* page_table,
+                        int32_t num_pages, int32_t page_size, int32_t max_pages_per_seq,
+                        const void* w_uk, const void* w_uv, int32_t batch_size, int32_t num_heads,
+                        int32_t total_q_tokens, int32_t max_new_tokens, int32_t num_partitions,
+                        float scale, const int32_t* d_indices, int32_t indices_stride,
+                        const int32_t* topk_lengths, const float* attn_sink, int32_t dtype,
+                        void* workspace, size_t workspace_bytes, int32_t* d_status,
+                        mla_stream_t stream) {
+  if (dtype != MLA_BF16) return MLA_ERR_DTYPE;
+  if (num_heads < 1) return MLA_ERR_GEOMETRY;
+  if (!out || !q || !input_row_offsets || !cache_lengths || !kv_cache || !w_uk || !w_uv ||
+      !aligned16(out) || !aligned16(q) || !aligned16(kv_cache) || !aligned16(w_uk) ||
+      !aligned16(w_uv) || batch_size < 1 || total_q_tokens < 0 || max_new_tokens < 0 ||
+      num_partitions < 0 || num_pages < 1 || page_size < 1 || !(scale > 0.0f))
+    return MLA_ERR_ARG;
+  if (d_indices == nullptr && (!page_table || max_pages_per_seq < 1)) return MLA_ERR_ARG;
+  if (d_indices != nullptr && indices_stride < 1) return MLA_ERR_ARG;
+  const long long rows = static_cast<long long>(total_q_tokens) * num_heads;
+  if (rows >= (1ll << 31) / 4 || static_cast<long long>(num_pages) * page_size >= (1ll << 31))
+    return MLA_ERR_ARG;
+  if (total_q_tokens == 0 || max_new_tokens == 0) return MLA_OK;
+  const int parts = num_partitions > 0 ? num_partitions
+                                       : mla::decode_default_partitions(batch_size, num_heads, max_new_tokens);
+  const long long items = static_cast<long long>(batch_size) * parts *
+                          ((static_cast<long long>(max_new_tokens) * num_heads + 127) / 128);
+  if (items >= (1ll << 31)) return MLA_ERR_ARG;
+  const mla::DecodeLayout L = mla::decode_layout(total_q_tokens, num_heads, parts);
+  if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return MLA_ERR_WORKSPACE;
+  mla::DecodeArgs a;
+  a.out = out;
+  a.lse = lse;
+  a.q = q;
+  a.kv_cache = kv_cache;
+  a.page_table = page_table;
+  a.num_pages = num_pages;
+  a.page_size = page_size;
+  a.max_pages = max_pages_per_seq;
+  a.w_uk = w_uk;
+  a.w_uv = w_uv;
+  a.iro = input_row_offsets;
+  a.cache_len = cache_lengths;
+  a.B = batch_size;
+  a.H = num_heads;
+  a.T = total_q_tokens;
+  a.max_new = max_new_tokens;
+  a.parts = parts;
+  a.scale = scale;
+  a.indices = d_indices;
+  a.indices_stride = indices_stride;
+  a.topk = topk_lengths;
+  a.sink = attn_sink;
+  a.workspace = workspace;
+  a.status = d_status;
+  return from_cuda(mla::launch_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

@@ -1,0 +1,961 @@
+// MLA decode in the absorbed form ("mla_prefill_decode_graph_bf16": the graph
+// switches to decode by the batch's max sequence length; Args w_uk
+// [num_heads, kv_latent_dim, qk_nope_head_dim], w_uv [num_heads, v_head_dim,
+// kv_latent_dim], num_partitions_in; the sparse form: d_indices,
+// indices_stride, topk_lengths, attn_sink_ptr).
+//
+// Instead of up-projecting the cache to per-head K and V, the nope part of
+// every query head is projected into latent space and attends to the 576-wide
+// latent rows straight from the paged cache; the latent result is projected
+// back per head.  Four launches:
+//
+//   1. head_gemm_kernel  q_lat[t, h] = w_uk[h] q_nope[t, h]      (tcgen05 GEMM,
+//      M = tokens, N = 512, K = 128 per head), written with q's rope part as
+//      the 576-wide query rows q_full [T*H, 576] bf16.
+//   2. decode_attn_kernel  the latent attention over key partitions, on pairs
+//      of SMs.  A work item is (sequence, 128 query rows, key partition); the
+//      rows are (token, head) pairs of one sequence.  CTA r of the pair owns
+//      latent columns [256r, 256r + 256) and rope columns [32r, 32r + 32): it
+//      loads only those columns of each 64-key tile, contracts them against
+//      the same columns of Q (S_r, M = 128, N = 64, K = 288), sends S_r to
+//      the other CTA's shared memory with st.async and adds the S it
+//      receives, so both hold the full scores without computing any twice.
+//      Both run the same softmax and each accumulates O for its own 256 value
+//      columns (P V, N = 256).  The full fp32 O of 128 rows x 512 columns
+//      would fill a whole TMEM; split this way each SM holds S (2 x 64
+//      columns), O (256) and its half of Q (128), 512 columns in all.
+//   3. decode_merge_kernel  merges the partitions' (O, LSE) per row, adds the
+//      attention sink to the softmax denominator when given, rounds the latent
+//      result to bf16.
+//   4. head_gemm_kernel  out[t, h] = w_uv[h] o_lat[t, h]  (N = 128, K = 512).
+//
+// Key partitions: the context of sequence b (L_b = cached + new tokens, or the
+// top-k count in the sparse form) is cut into `parts` ranges of
+// ceil(L_b / parts) keys rounded up to the 64-key tile.  The result does not
+// depend on where the cuts fall (partials merge exactly by LSE).
+#include <algorithm>
+#include <mutex>
+
+#include "kernels.cuh"
+
+namespace mla {
+namespace {
+
+constexpr float kLn2d = 0.693147180559945309f;
+constexpr float kNegInfD = -__builtin_huge_valf();
+constexpr float kRescaleLog2 = 8.0f;
+
+// ============================================================ per-head GEMM
+// D[r, n] = sum_k A[r, k] B_h[n, k] for head h = blockIdx.y and rows
+// [128 blockIdx.x, +128).  A: a 2-D tensor map over bf16 rows, the head's K
+// columns starting at column a_col0 + h * a_hstride.  B_h: rows [h N, h N + N)
+// of a [H N, K] bf16 tensor map (K contiguous).  fp32 accumulation in TMEM,
+// bf16 result at out + row * out_ld + h * out_hstride.  With rope_src set,
+// the 64 values at rope_src + row * rope_ld + h * rope_hstride are copied
+// after the N results (the query's rope part next to its latent part).
+template <int N, int K, int STAGES>
+struct HeadGemm {
+  static constexpr int KB = K / 64;             // 64-column (128-byte) k-blocks
+  static constexpr int A_BYTES = 128 * 128;
+  static constexpr int B_BYTES = N * 128;
+  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int SMEM_BAR = STAGES * STAGE;
+  static constexpr int SMEM_TOTAL = SMEM_BAR + 256 + 1024;
+  static constexpr int NB = N > 256 ? 256 : N;   // N of one MMA (and rows of one B box)
+  static constexpr uint32_t TMEM_COLS = N <= 128 ? 128 : (N <= 256 ? 256 : 512);
+  static constexpr uint32_t IDESC = idesc_bf16(128, NB, false, false);
+  static_assert(K % 64 == 0 && N % NB == 0, "shape");
+};
+
+template <int N, int K, int STAGES>
+__global__ void __launch_bounds__(192, 1)
+    head_gemm_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap b_map,
+                     int a_col0, int a_hstride, __nv_bfloat16* __restrict__ out, long long out_ld,
+                     int out_hstride, const __nv_bfloat16* __restrict__ rope_src, long long rope_ld,
+                     int rope_hstride, int M, int32_t* status) {
+  using C = HeadGemm<N, K, STAGES>;
+  struct Bars {
+    uint64_t full[STAGES], empty[STAGES], done;
+    uint32_t tmem;
+    int abort;
+  };
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars* sh = reinterpret_cast<Bars*>(smem + C::SMEM_BAR);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y;
+  const int m0 = blockIdx.x * 128;
+  if (timed_out_before(status)) return;   // an earlier kernel timed out: no work
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&sh->full[s]), 1);
+      mbar_init(smem_u32(&sh->empty[s]), 1);
+    }
+    mbar_init(smem_u32(&sh->done), 1);
+    sh->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sh->tmem), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh->tmem;
+  volatile int* abort_flag = &sh->abort;
+
+  if (warp == 0) {
+    if (elect_one()) {
+      prefetch_tmap(&a_map);
+      prefetch_tmap(&b_map);
+      int last[STAGES];
+      for (int s = 0; s < STAGES; ++s) last[s] = -1;
+      for (int kb = 0; kb < C::KB; ++kb) {
+        const int s = kb % STAGES;
+        if (kb >= STAGES && !mbar_wait(smem_u32(&sh->empty[s]), ((kb / STAGES) & 1) ^ 1, status, abort_flag))
+          break;
+        const uint32_t full = smem_u32(&sh->full[s]);
+        const uint32_t a = smem_u32(smem + s * C::STAGE);
+        mbar_expect_tx(full, C::STAGE);
+        tma_load_2d(a, &a_map, full, a_col0 + h * a_hstride + kb * 64, m0);
+#pragma unroll
+        for (int nb = 0; nb < N; nb += C::NB)
+          tma_load_2d(a + C::A_BYTES + nb * 128, &b_map, full, kb * 64, h * N + nb);
+        last[s] = (kb / STAGES) & 1;
+      }
+      volatile int never = 0;
+      for (int s = 0; s < STAGES; ++s)
+        if (last[s] >= 0) mbar_wait(smem_u32(&sh->full[s]), uint32_t(last[s]), status, &never);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (elect_one()) {
+      bool ok = true;
+      for (int kb = 0; kb < C::KB && ok; ++kb) {
+        const int s = kb % STAGES;
+        if (!(ok = mbar_wait(smem_u32(&sh->full[s]), (kb / STAGES) & 1, status, abort_flag))) break;
+        tc_fence_after();
+        const uint32_t a = smem_u32(smem + s * C::STAGE);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint64_t ad = sdesc(a + k * 32, 16, 1024);
+#pragma unroll
+          for (int nb = 0; nb < N; nb += C::NB)
+            mma_f16_ss(tmem + nb, ad, sdesc(a + C::A_BYTES + nb * 128 + k * 32, 16, 1024), C::IDESC,
+                       (kb | k) != 0);
+        }
+        tc_commit(smem_u32(&sh->empty[s]));
+      }
+      tc_commit(smem_u32(&sh->done));
+      volatile int never = 0;
+      mbar_wait(smem_u32(&sh->done), 0, status, &never);
+    }
+    __syncwarp();
+  } else {
+    // Epilogue: TMEM lane quarter q = warp % 4 holds rows 32q..32q+31.
+    const int q4 = warp & 3;
+    const int row = q4 * 32 + lane;
+    const uint32_t lane_off = uint32_t(q4 * 32) << 16;
+    if (mbar_wait_warp(smem_u32(&sh->done), 0, status, abort_flag)) {
+      tc_fence_after();
+      const bool row_ok = m0 + row < M;
+      __nv_bfloat16* dst = out + static_cast<long long>(m0 + row) * out_ld + static_cast<long long>(h) * out_hstride;
+#pragma unroll 1
+      for (int c = 0; c < N / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + c * 32, r);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+        if (row_ok) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+      }
+      if (rope_src != nullptr && row_ok) {
+        const uint4* s4 = reinterpret_cast<const uint4*>(rope_src + static_cast<long long>(m0 + row) * rope_ld +
+                                                         static_cast<long long>(h) * rope_hstride);
+        uint4* d4 = reinterpret_cast<uint4*>(dst + N);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) d4[i] = s4[i];
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ============================================================ latent attention
+constexpr int DBN = 64;                           // keys per tile
+constexpr int D_KSTAGES = 3;
+constexpr int D_KBLK = 64 * 128;                  // 64 keys x 64 latent columns (128 B), 8 KB
+constexpr int D_KLAT = 4 * D_KBLK;                // this CTA's 256 latent columns
+constexpr int D_KBYTES = D_KLAT + 64 * 64;        // + its 32 rope columns (64 B a key)
+constexpr int D_QR_BYTES = 128 * 64;              // Q rope half: 128 rows x 64 B
+constexpr int D_X_BYTES = 32 * DBN * 4;           // one warp's partial scores: 32 rows x 64 fp32
+constexpr int D_SMEM_K = 0;
+constexpr int D_SMEM_QR = D_SMEM_K + D_KSTAGES * D_KBYTES;
+constexpr int D_SMEM_X = D_SMEM_QR + 2 * D_QR_BYTES;
+constexpr int D_SMEM_BAR = D_SMEM_X + 2 * 4 * D_X_BYTES;
+constexpr int D_SMEM_TOTAL = D_SMEM_BAR + 512 + 1024;
+constexpr int D_THREADS = 192;                    // producer, MMA, 4 softmax warps
+constexpr uint32_t D_TMEM_COLS = 512;
+constexpr uint32_t D_TM_S = 0, D_TM_O = 128, D_TM_Q = 384;   // S 2 x 64, O 256, Q 128 (bf16 pairs)
+constexpr uint32_t IDESC_DS = idesc_bf16(128, DBN, false, false);
+constexpr uint32_t IDESC_DPV = idesc_bf16(128, 256, false, true);
+static_assert(D_KBYTES % 1024 == 0 && D_SMEM_QR % 1024 == 0 && D_SMEM_X % 1024 == 0, "alignment");
+static_assert(D_SMEM_TOTAL <= 227 * 1024, "shared memory");
+
+struct DecodeSmem {
+  uint64_t q_full[2], q_free[2];   // Q rope half in shared memory (TMA), 2 slots
+  uint64_t q_ready;                // Q latent half staged in TMEM (4 warps)
+  uint64_t k_full[D_KSTAGES], k_empty[D_KSTAGES];
+  uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t o_free;                 // 4 warps read O
+  uint64_t x_full[2][4];           // the other CTA's partial scores landed (per warp, per slot)
+  uint64_t x_empty[2][4];          // the other CTA has read what this CTA sent
+  uint64_t drain;
+  uint32_t tmem;
+  int abort;
+};
+static_assert(sizeof(DecodeSmem) <= 512, "barrier block");
+
+struct DecodeParams {
+  const __nv_bfloat16* q_full;     // [R][576]
+  const uint32_t* iro;
+  const uint32_t* cache_len;
+  const int32_t* page_table;
+  const int32_t* indices;          // sparse form: [B][indices_stride] physical cache rows, or null
+  const int32_t* topk;             // sparse form: [B] valid entries
+  float* o_part;                   // [parts][R][512]
+  float* lse_part;                 // [parts][R]
+  int indices_stride;
+  int num_pages, page_size, max_pages;
+  int B, H, R, parts, m_tiles;
+  int dense_tiles;                 // 1: every 64-key tile is 64 consecutive rows of one page
+  float scale_log2;
+  int32_t* status;
+};
+
+// Keys of sequence b: its context (dense) or its top-k list (sparse).
+__device__ __forceinline__ long long decode_keys(const DecodeParams& p, int b, long long cb, long long nb) {
+  if (p.indices != nullptr) {
+    const long long k = p.topk != nullptr ? p.topk[b] : p.indices_stride;
+    return max(0ll, min(k, static_cast<long long>(p.indices_stride)));
+  }
+  return cb + nb;
+}
+__device__ __forceinline__ long long decode_part_size(long long L, int parts) {
+  const long long per = (L + parts - 1) / parts;
+  return (per + DBN - 1) / DBN * DBN;
+}
+
+struct DItem {
+  int b, k;
+  int row0;        // first global row of the tile (row = token * H + head)
+  int r0;          // first row of the tile within the sequence's rows
+  int nrows;       // valid rows
+  int qa;          // first token of the sequence
+  long long cb;    // cached tokens
+  long long L;     // keys of the sequence
+  long long key0, key1;   // the partition's keys (key1 before the tile's causal limit)
+  int n_kv;        // 64-key tiles to visit
+};
+
+__device__ __forceinline__ bool decode_item(const DecodeParams& p, int idx, DItem& it) {
+  const int m = idx % p.m_tiles;
+  const int bk = idx / p.m_tiles;
+  it.k = bk % p.parts;
+  it.b = bk / p.parts;
+  it.n_kv = 0;
+  const uint32_t qa = p.iro[it.b], qe = p.iro[it.b + 1];
+  if (static_cast<long long>(qe) * p.H > p.R) {
+    set_status(p.status, MLA_DEV_BAD_OFFSETS);
+    return false;
+  }
+  const long long nb = qe >= qa ? static_cast<long long>(qe - qa) : 0;
+  const long long rows_b = nb * p.H;
+  it.r0 = m * 128;
+  if (it.r0 >= rows_b) return false;
+  it.qa = static_cast<int>(qa);
+  it.row0 = static_cast<int>(static_cast<long long>(qa) * p.H + it.r0);
+  it.nrows = static_cast<int>(min(128ll, rows_b - it.r0));
+  it.cb = p.cache_len[it.b];
+  it.L = decode_keys(p, it.b, it.cb, nb);
+  const long long size = decode_part_size(it.L, p.parts);
+  it.key0 = it.k * size;
+  it.key1 = min(it.key0 + size, it.L);
+  long long hi = it.key1;
+  if (p.indices == nullptr) {   // causal: the tile's last token sees keys up to cb + i
+    const long long i_last = (it.r0 + it.nrows - 1) / p.H;
+    hi = min(hi, it.cb + i_last + 1);
+  }
+  if (hi <= it.key0) return false;
+  it.n_kv = static_cast<int>((hi - it.key0 + DBN - 1) / DBN);
+  return true;
+}
+
+__device__ __forceinline__ bool next_decode_item(const DecodeParams& p, int& idx, int stride, int total,
+                                                 DItem& it) {
+  for (; idx < total; idx += stride)
+    if (decode_item(p, idx, it)) return true;
+  return false;
+}
+
+// Physical cache row of key `pos` of sequence b, or -1 (page out of range:
+// reported, and the tile reads zeros there).
+__device__ __forceinline__ int decode_phys_row(const DecodeParams& p, int b, long long pos) {
+  long long row;
+  if (p.indices != nullptr) {
+    row = p.indices[static_cast<long long>(b) * p.indices_stride + pos];
+    if (row < 0 || row >= static_cast<long long>(p.num_pages) * p.page_size) {
+      set_status(p.status, MLA_DEV_BAD_PAGE);
+      return -1;
+    }
+    return static_cast<int>(row);
+  }
+  const long long pi = pos / p.page_size;
+  const int page = pi < p.max_pages ? p.page_table[static_cast<long long>(b) * p.max_pages + pi] : -1;
+  if (page < 0 || page >= p.num_pages) {
+    set_status(p.status, MLA_DEV_BAD_PAGE);
+    return -1;
+  }
+  return static_cast<int>(static_cast<long long>(page) * p.page_size + pos % p.page_size);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(D_THREADS, 1)
+    decode_attn_kernel(const __grid_constant__ CUtensorMap qr_map, const __grid_constant__ CUtensorMap kl_map,
+                       const __grid_constant__ CUtensorMap kr_map, const __grid_constant__ CUtensorMap kl1_map,
+                       const __grid_constant__ CUtensorMap kr1_map, const DecodeParams p, int total_items) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  DecodeSmem* sh = reinterpret_cast<DecodeSmem*>(smem + D_SMEM_BAR);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const uint32_t other = rank ^ 1u;
+  const int pair_id = blockIdx.x >> 1;
+  const int n_pairs = gridDim.x >> 1;
+  int32_t* status = p.status;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&sh->q_full[i]), 1);
+      mbar_init(smem_u32(&sh->q_free[i]), 1);
+      mbar_init(smem_u32(&sh->s_full[i]), 1);
+      mbar_init(smem_u32(&sh->p_full[i]), 4);
+      mbar_init(smem_u32(&sh->o_done[i]), 1);
+      for (int w = 0; w < 4; ++w) {
+        mbar_init(smem_u32(&sh->x_full[i][w]), 1);
+        mbar_init(smem_u32(&sh->x_empty[i][w]), 1);
+      }
+    }
+    mbar_init(smem_u32(&sh->q_ready), 4);
+    for (int s = 0; s < D_KSTAGES; ++s) {
+      mbar_init(smem_u32(&sh->k_full[s]), 1);
+      mbar_init(smem_u32(&sh->k_empty[s]), 1);
+    }
+    mbar_init(smem_u32(&sh->o_free), 4);
+    mbar_init(smem_u32(&sh->drain), 1);
+    sh->abort = timed_out_before(status) ? 1 : 0;
+    fence_mbar_init();
+    // The first phase of every receive slot expects one warp's scores.
+    for (int i = 0; i < 2; ++i)
+      for (int w = 0; w < 4; ++w) mbar_expect_tx(smem_u32(&sh->x_full[i][w]), D_X_BYTES);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sh->tmem), D_TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  cluster_sync();   // barriers of both CTAs initialised (the other CTA stores into them)
+  tc_fence_after();
+  const int total = cluster_any(&sh->abort) ? 0 : total_items;
+  const uint32_t tmem = sh->tmem;
+  volatile int* abort_flag = &sh->abort;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (elect_one()) {
+      prefetch_tmap(&qr_map);
+      prefetch_tmap(p.dense_tiles ? &kl_map : &kl1_map);
+      prefetch_tmap(p.dense_tiles ? &kr_map : &kr1_map);
+    }
+    __syncwarp();
+    uint32_t g = 0, it_n = 0;
+    int q_last[2] = {-1, -1}, k_last[D_KSTAGES] = {-1, -1, -1};
+    bool ok = true;
+    DItem it;
+    const int lat_x = 256 * static_cast<int>(rank);
+    const int rope_x = 512 + 32 * static_cast<int>(rank);
+    for (int idx = pair_id; ok && next_decode_item(p, idx, n_pairs, total, it); idx += n_pairs) {
+      const int qs = it_n & 1;
+      if (it_n >= 2 &&
+          !(ok = mbar_wait_warp(smem_u32(&sh->q_free[qs]), ((it_n >> 1) & 1) ^ 1, status, abort_flag)))
+        break;
+      if (elect_one()) {
+        const uint32_t qf = smem_u32(&sh->q_full[qs]);
+        mbar_expect_tx(qf, D_QR_BYTES);
+        tma_load_2d(smem_u32(smem + D_SMEM_QR + qs * D_QR_BYTES), &qr_map, qf, rope_x, it.row0);
+      }
+      __syncwarp();
+      q_last[qs] = int((it_n >> 1) & 1);
+      for (int j = 0; j < it.n_kv; ++j) {
+        const uint32_t gj = g + j;
+        const int st = gj % D_KSTAGES;
+        if (gj >= D_KSTAGES &&
+            !(ok = mbar_wait_warp(smem_u32(&sh->k_empty[st]), ((gj / D_KSTAGES) & 1) ^ 1, status, abort_flag)))
+          break;
+        const uint32_t kf = smem_u32(&sh->k_full[st]);
+        const uint32_t kd = smem_u32(smem + D_SMEM_K + st * D_KBYTES);
+        const long long pos0 = it.key0 + static_cast<long long>(j) * DBN;
+        if (p.dense_tiles) {
+          // 64 consecutive positions, all in one page.
+          if (elect_one()) {
+            int row = decode_phys_row(p, it.b, pos0);
+            if (row < 0) row = p.num_pages * p.page_size;   // past the end: reads zeros
+            mbar_expect_tx(kf, D_KBYTES);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tma_load_2d(kd + c * D_KBLK, &kl_map, kf, lat_x + 64 * c, row);
+            tma_load_2d(kd + D_KLAT, &kr_map, kf, rope_x, row);
+          }
+        } else {
+          // Any rows: four at a time (tile::gather4), 16 lanes each one group.
+          const long long pa = pos0 + lane, pb = pos0 + 32 + lane;
+          int ra = pa < it.L ? decode_phys_row(p, it.b, pa) : 0;
+          int rb = pb < it.L ? decode_phys_row(p, it.b, pb) : 0;
+          if (ra < 0) ra = 0;   // reported; the scores of such a key are wrong, the status says so
+          if (rb < 0) rb = 0;
+          int y[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int key = 4 * (lane & 15) + k;
+            const int va = __shfl_sync(0xffffffffu, ra, key & 31);
+            const int vb = __shfl_sync(0xffffffffu, rb, key & 31);
+            y[k] = key < 32 ? va : vb;
+          }
+          if (lane == 0) mbar_expect_tx(kf, D_KBYTES);
+          __syncwarp();
+          if (lane < 16) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              tma_gather4_2d(kd + c * D_KBLK + lane * 512, &kl1_map, kf, lat_x + 64 * c, y[0], y[1], y[2], y[3]);
+            tma_gather4_2d(kd + D_KLAT + lane * 256, &kr1_map, kf, rope_x, y[0], y[1], y[2], y[3]);
+          }
+        }
+        __syncwarp();
+        k_last[st] = int((gj / D_KSTAGES) & 1);
+      }
+      g += it.n_kv;
+      ++it_n;
+    }
+    // Every issued load lands before the CTA leaves.
+    volatile int never = 0;
+    for (int s = 0; s < 2; ++s)
+      if (q_last[s] >= 0) mbar_wait_warp(smem_u32(&sh->q_full[s]), uint32_t(q_last[s]), status, &never);
+    for (int s = 0; s < D_KSTAGES; ++s)
+      if (k_last[s] >= 0) mbar_wait_warp(smem_u32(&sh->k_full[s]), uint32_t(k_last[s]), status, &never);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (elect_one()) {
+      uint32_t g = 0, it_n = 0;
+      DItem it;
+      bool ok = true;
+      for (int idx = pair_id; ok && next_decode_item(p, idx, n_pairs, total, it); idx += n_pairs) {
+        const int qs = it_n & 1;
+        if (!(ok = mbar_wait(smem_u32(&sh->q_ready), it_n & 1, status, abort_flag))) break;
+        if (!(ok = mbar_wait(smem_u32(&sh->q_full[qs]), (it_n >> 1) & 1, status, abort_flag))) break;
+        const uint32_t qr = smem_u32(smem + D_SMEM_QR + qs * D_QR_BYTES);
+        const int n = it.n_kv;
+        auto issue_s = [&](int j) -> bool {
+          const uint32_t gj = g + j;
+          const int st = gj % D_KSTAGES;
+          if (!mbar_wait(smem_u32(&sh->k_full[st]), (gj / D_KSTAGES) & 1, status, abort_flag)) return false;
+          tc_fence_after();
+          const uint32_t kd = smem_u32(smem + D_SMEM_K + st * D_KBYTES);
+          const uint32_t d = tmem + D_TM_S + (gj & 1) * DBN;
+#pragma unroll
+          for (int kk = 0; kk < 16; ++kk)   // latent: A = Q half in TMEM, 16 bf16 = 8 columns a step
+            mma_f16_ts(d, tmem + D_TM_Q + kk * 8, sdesc(kd + (kk >> 2) * D_KBLK + (kk & 3) * 32, 16, 1024),
+                       IDESC_DS, kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk)    // rope: both operands in shared memory, 64-byte rows
+            mma_f16_ss(d, sdesc(qr + kk * 32, 16, 512, kSwizzle64),
+                       sdesc(kd + D_KLAT + kk * 32, 16, 512, kSwizzle64), IDESC_DS, 1);
+          tc_commit(smem_u32(&sh->s_full[gj & 1]));
+          if (j == n - 1) tc_commit(smem_u32(&sh->q_free[qs]));
+          return true;
+        };
+        auto issue_pv = [&](int j) -> bool {
+          const uint32_t gj = g + j;
+          const int st = gj % D_KSTAGES;
+          if (!mbar_wait(smem_u32(&sh->p_full[gj & 1]), (gj >> 1) & 1, status, abort_flag)) return false;
+          if (j == 0 && it_n >= 1 && !mbar_wait(smem_u32(&sh->o_free), (it_n - 1) & 1, status, abort_flag))
+            return false;
+          tc_fence_after();
+          const uint32_t kd = smem_u32(smem + D_SMEM_K + st * D_KBYTES);
+          const uint32_t pa = tmem + D_TM_S + (gj & 1) * DBN;
+#pragma unroll
+          for (int kk = 0; kk < DBN / 16; ++kk)   // V = the latent columns, MN-major (64-column blocks)
+            mma_f16_ts(tmem + D_TM_O, pa + kk * 8, sdesc(kd + kk * 2048, D_KBLK, 1024), IDESC_DPV,
+                       (j > 0 || kk > 0));
+          tc_commit(smem_u32(&sh->o_done[gj & 1]));
+          tc_commit(smem_u32(&sh->k_empty[st]));
+          return true;
+        };
+        ok = issue_s(0);
+        if (ok && n > 1) ok = issue_s(1);
+        for (int j = 0; j < n && ok; ++j) {
+          ok = issue_pv(j);
+          if (ok && j + 2 < n) ok = issue_s(j + 2);
+        }
+        if (!ok) break;
+        g += n;
+        ++it_n;
+      }
+      tc_commit(smem_u32(&sh->drain));
+      volatile int never = 0;
+      mbar_wait(smem_u32(&sh->drain), 0, status, &never);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int q4 = warp & 3;
+    const int row = q4 * 32 + lane;
+    const uint32_t lane_off = uint32_t(q4 * 32) << 16;
+    const float sl2 = p.scale_log2;
+    const float2 sl2v = make_float2(sl2, sl2);
+    // Where this warp's partial scores go in the other CTA, and its barrier there.
+    const uint32_t x_mine = smem_u32(smem + D_SMEM_X + q4 * D_X_BYTES);
+    const uint32_t x_other = cluster_addr(x_mine, other);
+    const uint32_t xf_other = cluster_addr(smem_u32(&sh->x_full[0][q4]), other);
+    const uint32_t xe_other = cluster_addr(smem_u32(&sh->x_empty[0][q4]), other);
+    constexpr uint32_t kSlotStep = 4 * D_X_BYTES;   // receive buffers: [slot][warp]
+    constexpr uint32_t kBarSlot = 4 * 8;            // barriers: [slot][warp]
+    uint32_t g = 0, it_n = 0;
+    uint32_t released[2] = {0, 0};                   // phases of each slot this warp handed back
+    uint32_t received[2] = {0, 0};
+    bool ok = true;
+
+    // The item's Q latent half (256 bf16 of the row) into TMEM columns
+    // D_TM_Q..+127; the MMAs read it from there.
+    auto stage_q = [&](const DItem& n_it) {
+      uint32_t v[128];
+      if (row < n_it.nrows) {
+        const uint4* src = reinterpret_cast<const uint4*>(p.q_full + static_cast<long long>(n_it.row0 + row) * 576 +
+                                                          256 * rank);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const uint4 x = src[i];
+          v[4 * i] = x.x; v[4 * i + 1] = x.y; v[4 * i + 2] = x.z; v[4 * i + 3] = x.w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) v[i] = 0u;
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_st32(tmem + lane_off + D_TM_Q + c * 32, v + c * 32);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh->q_ready));
+    };
+
+    int idx = pair_id;
+    DItem it;
+    bool have = next_decode_item(p, idx, n_pairs, total, it);
+    if (have) stage_q(it);
+    while (have && ok) {
+      // This row's keys: [key0, hi) of the partition, causal for dense decode.
+      const long long tok = (it.r0 + row) / p.H;
+      long long hi = it.key1;
+      if (p.indices == nullptr) hi = min(hi, it.cb + tok + 1);
+      if (row >= it.nrows) hi = it.key0;
+      float m_run = kNegInfD, l_run = 0.f;
+      for (int j = 0; j < it.n_kv; ++j) {
+        const uint32_t gj = g + j;
+        const uint32_t sb = gj & 1;
+        if (!(ok = mbar_wait_warp(smem_u32(&sh->s_full[sb]), (gj >> 1) & 1, status, abort_flag))) break;
+        tc_fence_after();
+        float x[DBN];
+        tmem_ld32(tmem + lane_off + D_TM_S + sb * DBN, *reinterpret_cast<uint32_t(*)[32]>(reinterpret_cast<uint32_t*>(x)));
+        tmem_ld32(tmem + lane_off + D_TM_S + sb * DBN + 32,
+                  *reinterpret_cast<uint32_t(*)[32]>(reinterpret_cast<uint32_t*>(x) + 32));
+        tmem_ld_wait();
+        // Send this CTA's partial scores to the other CTA's slot sb, once it has
+        // read what this warp sent there two tiles ago.
+        const uint32_t use = gj >> 1;
+        if (use > 0 &&
+            !(ok = mbar_wait_warp(smem_u32(&sh->x_empty[sb][q4]), (use - 1) & 1, status, abort_flag)))
+          break;
+#pragma unroll
+        for (int c = 0; c < DBN / 4; ++c)
+          st_async_v4(x_other + sb * kSlotStep + c * 512 + lane * 16,
+                      make_uint4(__float_as_uint(x[4 * c]), __float_as_uint(x[4 * c + 1]),
+                                 __float_as_uint(x[4 * c + 2]), __float_as_uint(x[4 * c + 3])),
+                      xf_other + sb * kBarSlot);
+        // ... and add the other CTA's partial scores for the same rows.
+        if (!(ok = mbar_wait_warp(smem_u32(&sh->x_full[sb][q4]), received[sb] & 1, status, abort_flag))) break;
+        ++received[sb];
+#pragma unroll
+        for (int c = 0; c < DBN / 4; ++c) {
+          const uint4 y = *reinterpret_cast<const uint4*>(smem + D_SMEM_X + sb * kSlotStep + q4 * D_X_BYTES +
+                                                                    c * 512 + lane * 16);
+          x[4 * c] += __uint_as_float(y.x);
+          x[4 * c + 1] += __uint_as_float(y.y);
+          x[4 * c + 2] += __uint_as_float(y.z);
+          x[4 * c + 3] += __uint_as_float(y.w);
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_expect_tx(smem_u32(&sh->x_full[sb][q4]), D_X_BYTES);   // the slot's next phase
+          mbar_arrive_cluster(xe_other + sb * kBarSlot);              // the other CTA may send again
+        }
+        ++released[sb];
+        // Mask keys outside [key0, hi) of this row.
+        const long long lim = hi - (it.key0 + static_cast<long long>(j) * DBN);
+        if (lim < DBN) {
+#pragma unroll
+          for (int k = 0; k < DBN; ++k) x[k] = k < lim ? x[k] : kNegInfD;
+        }
+        float mx = fmax3(x[0], x[1], x[2]);
+#pragma unroll
+        for (int k = 3; k < DBN - 1; k += 2) mx = fmax3(mx, x[k], x[k + 1]);
+        mx = fmaxf(mx, x[DBN - 1]);
+        const float m_new = fmaxf(m_run, mx * sl2);
+        const bool need = m_new > m_run + kRescaleLog2;
+        const float f = need ? ex2(m_run - m_new) : 1.0f;
+        if (need) m_run = m_new;
+        const float msub = m_run == kNegInfD ? 0.f : m_run;
+        const float2 negm = make_float2(-msub, -msub);
+        uint32_t pk[DBN / 2];
+        float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int k = 0; k < DBN / 2; ++k) {
+          const float2 t = __ffma2_rn(make_float2(x[2 * k], x[2 * k + 1]), sl2v, negm);
+          const float2 e = make_float2(ex2(t.x), ex2(t.y));
+          acc[k & 1] = __fadd2_rn(acc[k & 1], e);
+          pk[k] = pack_bf16(e.x, e.y);
+        }
+        const float2 a = __fadd2_rn(acc[0], acc[1]);
+        l_run = l_run * f + (a.x + a.y);
+        if (j == it.n_kv - 1 && it.key0 + static_cast<long long>(j + 1) * DBN > it.key1) {
+          // Keys past the partition in the last tile: zero this CTA's latent
+          // columns of those rows (stale or non-finite cache slots) before P V.
+          const long long vlim = it.key1 - (it.key0 + static_cast<long long>(j) * DBN);
+          const int st = gj % D_KSTAGES;
+          const int vr = row >> 1, half = row & 1;
+          if (vr >= vlim) {
+            uint8_t* base = smem + D_SMEM_K + st * D_KBYTES + vr * 128;
+#pragma unroll
+            for (int c = 2 * half; c < 2 * half + 2; ++c)
+#pragma unroll
+              for (int i = 0; i < 8; ++i) reinterpret_cast<uint4*>(base + c * D_KBLK)[i] = make_uint4(0, 0, 0, 0);
+          }
+          fence_async_smem();
+        }
+        tmem_st32(tmem + lane_off + D_TM_S + sb * DBN, pk);
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+          // Rescale O only when the row maximum grew by more than 2^8, once
+          // P V of the previous tile has completed.
+          if (!(ok = mbar_wait_warp(smem_u32(&sh->o_done[(gj - 1) & 1]), ((gj - 1) >> 1) & 1, status, abort_flag)))
+            break;
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < 8; ++c) {
+            uint32_t r[32];
+            const uint32_t ta = tmem + lane_off + D_TM_O + c * 32;
+            tmem_ld32(ta, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
+            tmem_st32(ta, r);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sh->p_full[sb]));
+      }
+      if (!ok) break;
+      g += it.n_kv;
+      int nidx = idx + n_pairs;
+      DItem nx;
+      const bool have_next = next_decode_item(p, nidx, n_pairs, total, nx);
+      // Every S MMA of this item has completed (its last s_full): the next
+      // item's Q may replace this one's in TMEM.
+      if (have_next) stage_q(nx);
+      // ---------------------------------------------------------- epilogue
+      if (!(ok = mbar_wait_warp(smem_u32(&sh->o_done[(g - 1) & 1]), ((g - 1) >> 1) & 1, status, abort_flag)))
+        break;
+      tc_fence_after();
+      const bool store = row < it.nrows;
+      const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
+      const long long grow = it.row0 + row;
+      float* dst = p.o_part + (static_cast<long long>(it.k) * p.R + grow) * 512 + 256 * rank;
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + D_TM_O + c * 32, r);
+        tmem_ld_wait();
+        if (store) {
+          float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            d4[i] = make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
+                                __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh->o_free));
+      if (store && rank == 0)
+        p.lse_part[static_cast<long long>(it.k) * p.R + grow] =
+            l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2d : kNegInfD;
+      it = nx;
+      idx = nidx;
+      have = have_next;
+      ++it_n;
+    }
+    if (!ok) {
+      // Aborted: the other CTA may still be storing into a slot this warp
+      // handed back; let those stores land (briefly) before the CTA leaves.
+      volatile int never = 0;
+      for (int s = 0; s < 2; ++s)
+        if (released[s] + 1 > received[s])
+          mbar_wait_warp(smem_u32(&sh->x_full[s][q4]), received[s] & 1, status, &never, 10000000ull);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // neither CTA leaves while the other may still store into it
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, D_TMEM_COLS);
+  }
+}
+
+// ============================================================ partition merge
+// One row (token, head) per 128 threads, 4 latent columns a thread: merge the
+// partitions' (O, LSE) by LSE, add the attention sink (a logit with no value)
+// to the denominator when given, and round the latent result to bf16.
+__global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p, __nv_bfloat16* __restrict__ o_lat,
+                                                           float* __restrict__ lse_out,
+                                                           const float* __restrict__ sink) {
+  if (timed_out_before(p.status)) return;
+  const int sub = threadIdx.x >> 7;            // row within the CTA's pair of rows
+  const int c = (threadIdx.x & 127) * 4;       // first latent column
+  for (long long grow = static_cast<long long>(blockIdx.x) * 2 + sub; grow < p.R;
+       grow += static_cast<long long>(gridDim.x) * 2) {
+    const int t = static_cast<int>(grow / p.H);
+    int lo = 0, hi_b = p.B;                    // largest b with iro[b] <= t
+    while (hi_b - lo > 1) {
+      const int mid = (lo + hi_b) >> 1;
+      if (p.iro[mid] <= static_cast<uint32_t>(t)) lo = mid; else hi_b = mid;
+    }
+    const int b = lo;
+    const uint32_t qa = p.iro[b], qe = p.iro[b + 1];
+    if (!(qa <= static_cast<uint32_t>(t) && static_cast<uint32_t>(t) < qe)) {
+      // A token outside every sequence: zeros, so the projection reads no garbage.
+      *reinterpret_cast<uint2*>(o_lat + grow * 512 + c) = make_uint2(0u, 0u);
+      if (lse_out != nullptr && c == 0) lse_out[grow] = kNegInfD;
+      continue;
+    }
+    const long long cb = p.cache_len[b];
+    const long long L = decode_keys(p, b, cb, static_cast<long long>(qe - qa));
+    long long lim = L;
+    if (p.indices == nullptr) lim = min(lim, cb + (t - static_cast<long long>(qa)) + 1);
+    const long long size = decode_part_size(L, p.parts);
+    float mx = kNegInfD;
+    for (int k = 0; k < p.parts; ++k)
+      if (static_cast<long long>(k) * size < lim) mx = fmaxf(mx, p.lse_part[static_cast<long long>(k) * p.R + grow]);
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    float tot = 0.f;
+    if (mx != kNegInfD) {
+      for (int k = 0; k < p.parts; ++k) {
+        if (static_cast<long long>(k) * size >= lim) continue;
+        const float lk = p.lse_part[static_cast<long long>(k) * p.R + grow];
+        const float wk = __expf(lk - mx);
+        tot += wk;
+        const float4 v = *reinterpret_cast<const float4*>(p.o_part + (static_cast<long long>(k) * p.R + grow) * 512 + c);
+        o.x += wk * v.x; o.y += wk * v.y; o.z += wk * v.z; o.w += wk * v.w;
+      }
+    }
+    float lse = tot > 0.f ? mx + __logf(tot) : kNegInfD;
+    float w = tot > 0.f ? 1.0f / tot : 0.f;
+    if (sink != nullptr) {
+      // The sink joins the softmax denominator: LSE' = log(e^LSE + e^sink).
+      const float s = sink[b];
+      const float m2 = fmaxf(lse, s);
+      const float e1 = lse == kNegInfD ? 0.f : __expf(lse - m2), e2 = __expf(s - m2);
+      const float lse2 = m2 + __logf(e1 + e2);
+      w *= lse == kNegInfD ? 0.f : __expf(lse - lse2);
+      lse = lse2;
+    }
+    uint2 pk;
+    pk.x = pack_bf16(o.x * w, o.y * w);
+    pk.y = pack_bf16(o.z * w, o.w * w);
+    *reinterpret_cast<uint2*>(o_lat + grow * 512 + c) = pk;
+    if (lse_out != nullptr && c == 0) lse_out[grow] = lse;
+  }
+}
+
+// Two-CTA clusters of the attention kernel the current device can keep
+// resident, or 0.
+int decode_clusters(int device) {
+  static std::mutex mu;
+  static int cached[64];
+  static bool done[64];
+  std::lock_guard<std::mutex> lock(mu);
+  if (device < 0 || device >= 64) return 0;
+  if (!done[device]) {
+    cudaFuncSetAttribute(decode_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, D_SMEM_TOTAL);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(D_THREADS);
+    cfg.dynamicSmemBytes = D_SMEM_TOTAL;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, decode_attn_kernel, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+    cached[device] = n;
+    done[device] = true;
+  }
+  return cached[device];
+}
+
+template <int N, int K, int STAGES>
+cudaError_t launch_head_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, int a_col0, int a_hstride,
+                             __nv_bfloat16* out, long long out_ld, int out_hstride, const __nv_bfloat16* rope_src,
+                             long long rope_ld, int rope_hstride, int M, int H, int32_t* status,
+                             cudaStream_t stream) {
+  using C = HeadGemm<N, K, STAGES>;
+  cudaError_t e = cudaFuncSetAttribute(head_gemm_kernel<N, K, STAGES>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_TOTAL);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((M + 127) / 128, H);
+  head_gemm_kernel<N, K, STAGES><<<grid, 192, C::SMEM_TOTAL, stream>>>(
+      a_map, b_map, a_col0, a_hstride, out, out_ld, out_hstride, rope_src, rope_ld, rope_hstride, M, status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+DecodeLayout decode_layout(int T, int H, int parts) {
+  const size_t R = static_cast<size_t>(T) * H;
+  DecodeLayout L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = (off + bytes + 255) / 256 * 256;
+    return at;
+  };
+  L.q_full = take(R * 576 * 2);
+  L.o_part = take(static_cast<size_t>(parts) * R * 512 * 4);
+  L.lse_part = take(static_cast<size_t>(parts) * R * 4);
+  L.o_lat = take(R * 512 * 2);
+  L.total = off;
+  return L;
+}
+
+int decode_default_partitions(int B, int H, int max_new) {
+  const int pairs = std::max(1, sm_count() / 2);
+  const long long tiles = static_cast<long long>(B) * ((static_cast<long long>(max_new) * H + 127) / 128);
+  // Enough items for about two waves of SM pairs, at most 32 partitions.
+  long long parts = (2ll * pairs + tiles - 1) / std::max(1ll, tiles);
+  return static_cast<int>(std::min(32ll, std::max(1ll, parts)));
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
+  const int H = a.H, T = a.T;
+  const long long R = static_cast<long long>(T) * H;
+  if (T == 0) return cudaSuccess;
+  const DecodeLayout L = decode_layout(T, H, a.parts);
+  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  __nv_bfloat16* q_full = reinterpret_cast<__nv_bfloat16*>(ws + L.q_full);
+  float* o_part = reinterpret_cast<float*>(ws + L.o_part);
+  float* lse_part = reinterpret_cast<float*>(ws + L.lse_part);
+  __nv_bfloat16* o_lat = reinterpret_cast<__nv_bfloat16*>(ws + L.o_lat);
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+
+  // 1. q_lat = w_uk[h] q_nope, with the rope part alongside: q_full [T*H, 576].
+  CUtensorMap qa_map, wuk_map;
+  if (!encode_2d(&qa_map, a.q, bf, static_cast<uint64_t>(H) * 192, T, static_cast<uint64_t>(H) * 384, 64, 128,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&wuk_map, a.w_uk, bf, 128, static_cast<uint64_t>(H) * 512, 256, 64, 256,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  cudaError_t e = launch_head_gemm<512, 128, 2>(qa_map, wuk_map, 0, 192, q_full, static_cast<long long>(H) * 576,
+                                                576, static_cast<const __nv_bfloat16*>(a.q) + 128,
+                                                static_cast<long long>(H) * 192, 192, T, H, a.status, stream);
+  if (e != cudaSuccess) return e;
+
+  // 2. Latent attention over the key partitions.
+  const uint64_t cache_rows = static_cast<uint64_t>(a.num_pages) * a.page_size;
+  CUtensorMap qr_map, kl_map, kr_map, kl1_map, kr1_map;
+  if (!encode_2d(&qr_map, q_full, bf, 576, R, 1152, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !encode_2d(&kl_map, a.kv_cache, bf, 576, cache_rows, 1152, 64, DBN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&kr_map, a.kv_cache, bf, 576, cache_rows, 1152, 32, DBN, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !encode_2d(&kl1_map, a.kv_cache, bf, 576, cache_rows, 1152, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&kr1_map, a.kv_cache, bf, 576, cache_rows, 1152, 32, 1, CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
+  DecodeParams p;
+  p.q_full = q_full;
+  p.iro = a.iro;
+  p.cache_len = a.cache_len;
+  p.page_table = a.page_table;
+  p.indices = a.indices;
+  p.topk = a.topk;
+  p.o_part = o_part;
+  p.lse_part = lse_part;
+  p.indices_stride = a.indices_stride;
+  p.num_pages = a.num_pages;
+  p.page_size = a.page_size;
+  p.max_pages = a.max_pages;
+  p.B = a.B;
+  p.H = H;
+  p.R = static_cast<int>(R);
+  p.parts = a.parts;
+  p.m_tiles = static_cast<int>((static_cast<long long>(a.max_new) * H + 127) / 128);
+  p.dense_tiles = (a.indices == nullptr && a.page_size % DBN == 0) ? 1 : 0;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.status = a.status;
+  const long long total = static_cast<long long>(a.B) * a.parts * p.m_tiles;
+  if (total > 0) {
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    const int clusters = decode_clusters(dev);
+    if (clusters <= 0) return cudaErrorInvalidConfiguration;
+    const int grid = 2 * static_cast<int>(std::min<long long>(total, clusters));
+    decode_attn_kernel<<<grid, D_THREADS, D_SMEM_TOTAL, stream>>>(qr_map, kl_map, kr_map, kl1_map, kr1_map, p,
+                                                                  static_cast<int>(total));
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+
+  // 3. Merge the partitions (and the sink) into the bf16 latent result.
+  const long long blocks = std::min<long long>((R + 1) / 2, 8ll * sm_count());
+  decode_merge_kernel<<<static_cast<unsigned>(std::max(1ll, blocks)), 256, 0, stream>>>(p, o_lat, a.lse, a.sink);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  // 4. out = w_uv[h] o_lat.
+  CUtensorMap ol_map, wuv_map;
+  if (!encode_2d(&ol_map, o_lat, bf, static_cast<uint64_t>(H) * 512, T, static_cast<uint64_t>(H) * 1024, 64, 128,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&wuv_map, a.w_uv, bf, 512, static_cast<uint64_t>(H) * 128, 1024, 64, 128,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  return launch_head_gemm<128, 512, 4>(ol_map, wuv_map, 0, 512, static_cast<__nv_bfloat16*>(a.out),
+                                       static_cast<long long>(H) * 128, 128, nullptr, 0, 0, T, H, a.status, stream);
+}
+
+}  // namespace mla

@@ -86,6 +86,34 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_attention_pair(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_attention_pair_e4m3(const AttnArgs& a, cudaStream_t stream);
 
+// Absorbed MLA decode (decode.cu).
+struct DecodeArgs {
+  void* out;                  // [T][H][128] bf16
+  float* lse;                 // [T][H] or null
+  const void* q;              // [T][H][192] bf16
+  const void* kv_cache;       // [num_pages][page_size][576] bf16
+  const int32_t* page_table;  // [B][max_pages]
+  int num_pages, page_size, max_pages;
+  const void* w_uk;           // [H][512][128] bf16
+  const void* w_uv;           // [H][128][512] bf16
+  const uint32_t* iro;
+  const uint32_t* cache_len;
+  int B, H, T, max_new, parts;
+  float scale;
+  const int32_t* indices;     // sparse: [B][indices_stride] physical cache rows, or null
+  int indices_stride;
+  const int32_t* topk;        // sparse: [B] or null
+  const float* sink;          // [B] or null
+  void* workspace;
+  int32_t* status;
+};
+struct DecodeLayout {
+  size_t q_full, o_part, lse_part, o_lat, total;
+};
+DecodeLayout decode_layout(int T, int H, int parts);
+int decode_default_partitions(int B, int H, int max_new);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
 // Self-test of the bounded waits (selftest.cu): one cluster of `cluster`
 // CTAs waiting on barriers nothing arrives at.
 cudaError_t launch_bounded_wait_selftest(int32_t* status, long long* elapsed_ns, uint64_t limit_ns,

@@ -136,8 +136,8 @@ __device__ __forceinline__ bool timed_out_before(const int32_t* status) {
 // instructions afterwards: every lane waits, and the outcome is made uniform so
 // that a timeout can never leave part of the warp behind.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, int32_t* status,
-                                               volatile int* abort_flag) {
-  const bool ok = mbar_wait(bar, parity, status, abort_flag);
+                                               volatile int* abort_flag, uint64_t limit_ns = kWaitLimitNs) {
+  const bool ok = mbar_wait(bar, parity, status, abort_flag, limit_ns);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -162,6 +162,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+// Four rows (y0..y3) of a 2-D tensor map whose box is one row high, landing
+// as four consecutive box rows at dst (swizzled like rows of one tile).
+__device__ __forceinline__ void tma_gather4_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                               int32_t x, int32_t y0, int32_t y1, int32_t y2,
+                                               int32_t y3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
       : "memory");
 }
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x,
@@ -206,6 +217,16 @@ __device__ __forceinline__ uint32_t cluster_addr(uint32_t local_smem, uint32_t r
 // cluster-scope release costs ~2000 clk per arrive (measured).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+// Asynchronous 16-byte store into shared memory of another CTA of the cluster
+// (addresses from cluster_addr); its bytes count toward the transaction count
+// of the barrier `cluster_bar` in that CTA.
+__device__ __forceinline__ void st_async_v4(uint32_t cluster_dst, uint4 v, uint32_t cluster_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+          cluster_dst),
+      "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(cluster_bar)
+      : "memory");
 }
 // Every thread of every CTA of the cluster.
 __device__ __forceinline__ void cluster_sync() {

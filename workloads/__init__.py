@@ -78,6 +78,15 @@ WORKLOADS = {
                             new_lens=(16384,), cache_lens=(16384,)),
 }
 
+# Decode (the absorbed branch of the same graph): a few new tokens per sequence
+# over long cached contexts, DeepSeek-V3 dims.  Inputs come from make_inputs
+# with with_w_uk=True; the cache holds every context token, new ones included.
+DECODE_WORKLOADS = {
+    "v3_decode": Workload("v3_decode", B=64, H=128, page_size=128, buffer_token_size=1,
+                          max_chunks=1, new_range=(1, 2), cache_range=(4096, 16384),
+                          shuffle_pages=True),
+}
+
 # Reduced cases of the workloads above, small enough for a full profiler capture
 # (a few hundred MB on the device); timed by bench.py, not parity cases.
 PROFILE_CASES = {
