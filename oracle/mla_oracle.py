@@ -12,8 +12,9 @@ API references from the Modular MAX kernel library:
     cache_offsets, buffer_lengths, input_row_offsets, buffer_token_size);
   * "mla_prefill_decode_graph_bf16" -- the whole BF16 MLA layer (Args: q,
     freqs_cis, kv_norm_gamma, epsilon, w_k, w_uk, w_uv, scale,
-    buffer_row_offsets, cache_offsets, buffer_length; Parameters: kv_input_fn,
-    mask_str);
+    buffer_row_offsets, cache_offsets, buffer_length, num_partitions_in,
+    d_indices, indices_stride, topk_lengths, attn_sink_ptr; Parameters:
+    kv_input_fn, mask_str, sparse_mla, sparse_indices_stride);
   * "flare_mla_prefill_dispatch" -- prefill attention (Parameters: q_depth,
     cache_depth, kv_num_heads, dtype, output_type; Args: k, v, k_rope,
     valid_length, scale, cache_offsets).
@@ -34,7 +35,11 @@ in the design notes of the repository):
     latent's k_rope and for every query head's rope part;
   * K and V leave the up-projection in the storage dtype of the attention
     operands (bf16 for the BF16 graph, e4m3 for the fp8 path), rounded to
-    nearest even, in the descale domain of the cache.
+    nearest even, in the descale domain of the cache;
+  * sparse decode: a d_indices entry is a physical cache row (page *
+    page_size + slot), the list of batch entry b serves every new token of
+    sequence b with no causal limit, and an attention sink is one extra logit
+    per batch entry with no value row.
 """
 from __future__ import annotations
 
@@ -609,6 +614,66 @@ def mla_decode(q, kv_cache_codes, page_table, page_size: int, w_uk, w_uv, input_
                         o_k = w @ c_kv[lo:hi]
                     o, lse = merge_partials(o, lse, o_k, lse_k)
                 out[i] = np.asarray(w_uv[h], dtype=np.float64) @ o[0]
+                lses[i] = lse[0]
+            res[(b, h)] = (np.arange(iro[b], iro[b + 1]), out, lses)
+    return res
+
+
+# --------------------------------------------------------------------------
+# (6) Sparse decode and attention sinks -- "mla_prefill_decode_graph_bf16"
+# (Parameters sparse_mla, sparse_indices_stride; Args d_indices, packed int32
+# physical KV row indices; indices_stride, the stride between batch rows;
+# topk_lengths, the valid top-k count of each batch entry; attn_sink_ptr,
+# per-batch attention sink weights).
+# --------------------------------------------------------------------------
+
+def mla_sparse_decode(q, kv_cache_codes, page_size: int, w_uk, w_uv, input_row_offsets, indices,
+                      topk_lengths, scale: float, attn_sink=None, dtype: str = "bf16",
+                      ckv_scale: float = 1.0):
+    """Sparse decode in the absorbed form.
+
+    ``indices`` [B, stride] int: physical cache rows, row = page * page_size +
+    slot of the cache [num_pages, page_size, 576] viewed as rows; entry e of
+    batch row b is used when e < topk_lengths[b] (all ``stride`` when
+    ``topk_lengths`` is None).  Every new token of sequence b attends to
+    exactly those rows (the list is per batch entry; no causal limit).  For
+    head h, q_lat = w_uk[h] q_nope, score_e = scale * (q_lat . c_kv_e +
+    q_rope . k_rope_e), out = w_uv[h] (sum_e softmax_e c_kv_e).
+
+    ``attn_sink`` [B] (reading: one logit per batch entry, in the scaled-score
+    domain): an extra entry of every softmax of sequence b that has no value
+    row, so it only adds e^sink to the denominator; the LSE includes it.
+
+    Returns a dict (b, h) -> (tokens, out [n, 128], LSE [n]).
+    """
+    iro = np.asarray(input_row_offsets, dtype=np.int64)
+    idx = np.asarray(indices, dtype=np.int64)
+    B = iro.shape[0] - 1
+    stride = idx.shape[1]
+    kv = np.asarray(kv_cache_codes)
+    rows_all = kv.reshape(-1, kv.shape[-1])
+    q = np.asarray(q, dtype=np.float64)
+    H = q.shape[1]
+    res = {}
+    for b in range(B):
+        n = int(iro[b + 1] - iro[b])
+        if n <= 0:
+            continue
+        k = stride if topk_lengths is None else max(0, min(int(topk_lengths[b]), stride))
+        lat = decode(rows_all[idx[b, :k]], dtype) * ckv_scale
+        c_kv, k_rope = lat[:, :R], lat[:, R:]
+        for h in range(H):
+            out = np.zeros((n, DV))
+            lses = np.zeros(n)
+            for i in range(n):
+                t = int(iro[b]) + i
+                q_lat = np.asarray(w_uk[h], dtype=np.float64) @ q[t, h, :DN]
+                s = scale * (c_kv @ q_lat + k_rope @ q[t, h, DN:])
+                if attn_sink is not None:
+                    s = np.concatenate([s, [float(attn_sink[b])]])
+                w, lse = softmax_weights(s[None, :])
+                o = w[0, :k] @ c_kv if k > 0 else np.zeros(R)
+                out[i] = np.asarray(w_uv[h], dtype=np.float64) @ o
                 lses[i] = lse[0]
             res[(b, h)] = (np.arange(iro[b], iro[b + 1]), out, lses)
     return res

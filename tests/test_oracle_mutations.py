@@ -208,3 +208,45 @@ def test_partials_averaged_instead_of_merged_is_caught(monkeypatch):
         return o, np.logaddexp(lse_a, lse_b)
     monkeypatch.setattr(M, "merge_partials", average)
     _must_fail(P.test_decode_partition_count_invariant)
+
+
+def test_sink_left_out_of_the_output_is_caught(monkeypatch):
+    """The sink enters the LSE but the output is normalised over the listed
+    rows only (as if the sink had no place in the denominator)."""
+    orig = M.mla_sparse_decode
+
+    def bad(q, kv, ps, w_uk, w_uv, iro, idx, topk, scale, attn_sink=None, dtype="bf16", ckv_scale=1.0):
+        res = orig(q, kv, ps, w_uk, w_uv, iro, idx, topk, scale, None, dtype, ckv_scale)
+        if attn_sink is None:
+            return res
+        with_sink = orig(q, kv, ps, w_uk, w_uv, iro, idx, topk, scale, attn_sink, dtype, ckv_scale)
+        return {k: (v[0], v[1], with_sink[k][2]) for k, v in res.items()}
+    _plant(monkeypatch, "mla_sparse_decode", bad)
+    _must_fail(P.test_attention_sink_closed_forms)
+
+
+def test_causal_limit_on_sparse_lists_is_caught(monkeypatch):
+    """A causal limit applied to the positions of a sparse list (new token i
+    keeping only the first i + 1 entries) instead of using the whole list."""
+    orig = M.mla_sparse_decode
+
+    def bad(q, kv, ps, w_uk, w_uv, iro, idx, topk, scale, attn_sink=None, dtype="bf16", ckv_scale=1.0):
+        iro = np.asarray(iro)
+        res = {}
+        for b in range(len(iro) - 1):
+            for i in range(int(iro[b + 1] - iro[b])):
+                t = int(iro[b]) + i
+                sub = np.asarray([0, 1])
+                keep = np.asarray(idx)[b:b + 1, :i + 1]
+                one = orig(q[t:t + 1], kv, ps, w_uk, w_uv, sub, keep, None, scale,
+                           None if attn_sink is None else np.asarray(attn_sink)[b:b + 1], dtype, ckv_scale)
+                for (_, h), (_, o, l) in one.items():
+                    tok, out, lse = res.get((b, h), (np.arange(iro[b], iro[b + 1]),
+                                                     np.zeros((iro[b + 1] - iro[b], M.DV)),
+                                                     np.zeros(iro[b + 1] - iro[b])))
+                    out[i], lse[i] = o[0], l[0]
+                    res[(b, h)] = (tok, out, lse)
+        return res
+    _plant(monkeypatch, "mla_sparse_decode", bad)
+    _must_fail(P.test_sparse_decode_over_the_whole_context_equals_dense_decode,
+               P.test_sparse_decode_is_a_set_and_ignores_entries_past_topk)

@@ -659,6 +659,109 @@ def test_decode_partition_count_invariant():
             np.testing.assert_allclose(got[key][2], base[key][2], rtol=1e-13, atol=1e-13)
 
 
+def _sparse_args(inp, c, q, w_uk, wuv):
+    """Each sequence's whole context as physical cache rows, padded with -1."""
+    ps = inp["page_size"]
+    L = inp["new_lens"] + inp["cache_lens"]
+    stride = int(L.max()) + 3
+    idx = np.full((inp["B"], stride), -1, dtype=np.int64)
+    for b in range(inp["B"]):
+        pos = np.arange(int(L[b]))
+        idx[b, :L[b]] = c["page_table"][b, pos // ps] * ps + pos % ps
+    return idx, L
+
+
+def test_sparse_decode_over_the_whole_context_equals_dense_decode():
+    """One new token per sequence: listing every context row of the sequence
+    gives exactly the dense decode (whose pins tie it to up-projected attention)."""
+    w = scaled(WORKLOADS["tiny_ragged"], H=2, B=3, page_size=8, new_lens=(1, 1, 1),
+               cache_lens=(20, 0, 37), seed=9)
+    inp, c = _oracle_inputs(w)
+    wk = O.decode(c["w_k"], "bf16")
+    w_uk = np.stack([wk[h * M.DN:(h + 1) * M.DN].T for h in range(2)])
+    wuv = O.decode(c["w_uv"], "bf16")
+    q = O.decode(c["q"], "bf16")
+    idx, L = _sparse_args(inp, c, q, w_uk, wuv)
+    dense = O.mla_decode(q, c["kv_cache"], c["page_table"], inp["page_size"], w_uk, wuv,
+                         c["input_row_offsets"], c["cache_lengths"], inp["scale"])
+    sparse = O.mla_sparse_decode(q, c["kv_cache"], inp["page_size"], w_uk, wuv, c["input_row_offsets"],
+                                 idx, L, inp["scale"])
+    assert set(dense) == set(sparse)
+    for key in dense:
+        np.testing.assert_array_equal(sparse[key][0], dense[key][0])
+        np.testing.assert_allclose(sparse[key][1], dense[key][1], rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(sparse[key][2], dense[key][2], rtol=1e-13, atol=1e-13)
+
+
+def _sparse_case(seed=4):
+    inp, c, q, w_uk, wuv = _decode_case(seed=seed, H=2)
+    idx, L = _sparse_args(inp, c, q, w_uk, wuv)
+    return inp, c, q, w_uk, wuv, idx, L
+
+
+def test_sparse_decode_is_a_set_and_ignores_entries_past_topk():
+    """Permuting the listed rows changes nothing; entries past topk_lengths are
+    never read (garbage there changes nothing)."""
+    inp, c, q, w_uk, wuv, idx, L = _sparse_case()
+    args = (q, c["kv_cache"], inp["page_size"], w_uk, wuv, c["input_row_offsets"])
+    base = O.mla_sparse_decode(*args, idx, L, inp["scale"])
+    rng = np.random.default_rng(1)
+    perm = idx.copy()
+    for b in range(idx.shape[0]):
+        perm[b, :L[b]] = rng.permutation(idx[b, :L[b]])
+        perm[b, L[b]:] = 10 ** 6   # out of range: must not be read
+    got = O.mla_sparse_decode(*args, perm, L, inp["scale"])
+    for key in base:
+        np.testing.assert_allclose(got[key][1], base[key][1], rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(got[key][2], base[key][2], rtol=1e-13)
+
+
+def test_sparse_decode_closed_forms():
+    """top-1: the output is w_uv[h] times that row's latent values and the LSE
+    is its score; a row listed twice weighs twice (LSE grows by log 2)."""
+    inp, c, q, w_uk, wuv, idx, L = _sparse_case(seed=6)
+    rows = c["kv_cache"].reshape(-1, 576)
+    one = np.ones(inp["B"], dtype=np.int64)
+    res = O.mla_sparse_decode(q, c["kv_cache"], inp["page_size"], w_uk, wuv, c["input_row_offsets"],
+                              idx, one, inp["scale"])
+    for (b, h), (tok, out, lse) in res.items():
+        lat = O.decode(rows[idx[b, 0]], "bf16")
+        for n, t in enumerate(tok):
+            s = inp["scale"] * ((w_uk[h] @ q[t, h, :M.DN]) @ lat[:M.R] + q[t, h, M.DN:] @ lat[M.R:])
+            np.testing.assert_allclose(out[n], wuv[h] @ lat[:M.R], rtol=1e-12, atol=1e-13)
+            np.testing.assert_allclose(lse[n], s, rtol=1e-12, atol=1e-13)
+    twice = np.concatenate([idx[:, :1], idx[:, :1]], axis=1)
+    res2 = O.mla_sparse_decode(q, c["kv_cache"], inp["page_size"], w_uk, wuv, c["input_row_offsets"],
+                               twice, None, inp["scale"])
+    for key in res:
+        np.testing.assert_allclose(res2[key][1], res[key][1], rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(res2[key][2], res[key][2] + math.log(2.0), rtol=1e-12)
+
+
+def test_attention_sink_closed_forms():
+    """A sink of -inf changes nothing.  With q = 0 every score is 0, so over n
+    rows and a sink s: LSE = log(n + e^s) and out = n / (n + e^s) times w_uv[h]
+    applied to the mean latent row."""
+    inp, c, q, w_uk, wuv, idx, L = _sparse_case(seed=8)
+    args = (c["kv_cache"], inp["page_size"], w_uk, wuv, c["input_row_offsets"], idx, L, inp["scale"])
+    base = O.mla_sparse_decode(q, *args)
+    none = O.mla_sparse_decode(q, *args, attn_sink=np.full(inp["B"], -np.inf))
+    for key in base:
+        np.testing.assert_allclose(none[key][1], base[key][1], rtol=1e-13, atol=1e-14)
+        np.testing.assert_allclose(none[key][2], base[key][2], rtol=1e-13)
+    sink = np.array([0.5, -1.25, 2.0])
+    zq = np.zeros_like(q)
+    got = O.mla_sparse_decode(zq, *args, attn_sink=sink)
+    rows = c["kv_cache"].reshape(-1, 576)
+    for (b, h), (tok, out, lse) in got.items():
+        n = int(L[b])
+        mean = O.decode(rows[idx[b, :n]], "bf16")[:, :M.R].mean(axis=0)
+        frac = n / (n + math.exp(sink[b]))
+        for k in range(len(tok)):
+            np.testing.assert_allclose(lse[k], math.log(n + math.exp(sink[b])), rtol=1e-12)
+            np.testing.assert_allclose(out[k], frac * (wuv[h] @ mean), rtol=1e-10, atol=1e-12)
+
+
 def test_fp8_pipeline_chunked_equals_unchunked():
     w = scaled(WORKLOADS["longctx_fp8"], H=2, new_lens=(40,), cache_lens=(50,),
                buffer_token_size=48, max_chunks=2, page_size=16)
