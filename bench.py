@@ -50,7 +50,8 @@ def _args():
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
     ap.add_argument("--no-stages", action="store_true", help="skip the plan / gather stage figures")
-    ap.add_argument("--stage", default=None, choices=["plan", "gather", "cache_write"],
+    ap.add_argument("--stage", default=None, choices=["plan", "gather", "cache_write", "decode",
+                                                      "sparse_decode"],
                     help="time one HBM-bound stage alone on its stress shape")
     ap.add_argument("--batch", type=int, default=None, help="sequences for --stage")
     return ap.parse_args()
@@ -645,7 +646,96 @@ def measure_stage(stage, batch=None, steps=20, warmup=5):
 
 
 def run_stage(a):
+    if a.stage in ("decode", "sparse_decode"):
+        import torch
+        from mla_prefill_attention_plan_gb300 import build as B
+        B.build()
+        torch.cuda.set_device(0)
+        name = "v3_decode" if a.stage == "decode" else "v3_sparse_decode"
+        print(json.dumps(measure_decode(name, a.steps, a.warmup)), flush=True)
+        return
     print(json.dumps(measure_stage(a.stage, a.batch, a.steps, a.warmup)), flush=True)
+
+
+def measure_decode(name, steps=20, warmup=5):
+    """The absorbed decode (mla_decode, four launches) on a decode workload,
+    CUDA events around each call, the L2 flushed before every timed call.
+    Algorithmic bytes: every key row a sequence attends to (1152 B) once, q,
+    out, w_uk and w_uv; flops: the q_lat and output projections plus 2 * H *
+    (576 + 512) per visible (query, key) pair."""
+    import numpy as np
+    import torch
+    import mla_prefill_attention_plan_gb300 as mla
+    from workloads import DECODE_WORKLOADS, make_attention_sinks, make_inputs, make_sparse_indices
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream(dev)
+    w = DECODE_WORKLOADS[name]
+    inp = make_inputs(w, with_w_uk=True)
+    B, H, T = inp["B"], w.H, inp["T_q"]
+    new, cache = inp["new_lens"], inp["cache_lens"]
+    sparse = "sparse" in name
+    topk_n = 2048
+    d = {k: inp[k].to(dev) for k in ("q", "input_row_offsets", "cache_lengths", "kv_cache", "page_table",
+                                     "w_uk", "w_uv")}
+    if sparse:
+        idx, topk = make_sparse_indices(inp, topk_n)
+        idx, topk = idx.to(dev), topk.to(dev)
+        sink = make_attention_sinks(B).to(dev)
+        keys = [int(k) for k in topk.cpu()]
+        pairs = sum(int(n) * k for n, k in zip(new, keys))
+        rows_read = sum(keys)
+    else:
+        idx = topk = sink = None
+        pairs = sum(int(n) * int(c) + int(n) * (int(n) + 1) // 2 for n, c in zip(new, cache))
+        rows_read = int(sum(int(n) + int(c) for n, c in zip(new, cache)))
+    max_new = int(new.max())
+    max_seq = int((new + cache).max())
+    parts = mla.mla_decode_partitions(B, H, max_new, min(topk_n, max_seq) if sparse else max_seq)
+    nbytes = mla.mla_decode_workspace_bytes(H, T, parts)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    out = torch.empty(T, H, 128, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(T, H, dtype=torch.float32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def launch():
+        mla.check(mla.mla_decode(out, lse, d["q"], d["input_row_offsets"], d["cache_lengths"], d["kv_cache"],
+                                 d["page_table"], inp["num_pages"], inp["page_size"], inp["max_pages"], d["w_uk"],
+                                 d["w_uv"], B, H, T, max_new, max_seq, 0, inp["scale"], d_indices=idx,
+                                 indices_stride=topk_n if sparse else 0, topk_lengths=topk, attn_sink=sink,
+                                 workspace=ws, workspace_bytes=nbytes, d_status=st, stream=stream))
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush_rd = torch.ones(512 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(max(3, warmup)):
+        launch()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        flush.fill_(1)
+        flush_rd.amax()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        launch()
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    assert st.item() == 0, mla.status_string(int(st.item()))
+    ms = statistics.median(times)
+    algo_bytes = rows_read * 1152 + T * H * (192 + 128) * 2 + 2 * H * 512 * 128 * 2
+    flops = T * H * 2 * (2 * 128 * 512) + 2 * H * (576 + 512) * pairs
+    peaks, src = _peaks()
+    gbs = algo_bytes / (ms * 1e-3) / 1e9
+    tflops = flops / (ms * 1e-3) / 1e12
+    del flush, flush_rd, d, ws
+    torch.cuda.empty_cache()
+    return {"workload": name, "B": B, "new_tokens": T, "H": H,
+            "keys": "top-%d lists, per-batch sinks" % topk_n if sparse else "cached + new context, causal",
+            "context_tokens": int(sum(int(n) + int(c) for n, c in zip(new, cache))),
+            "partitions": "library choice (at most %d a sequence)" % parts, "kernels": "head_gemm (w_uk), decode_attn_kernel, decode_merge_kernel, head_gemm (w_uv)",
+            "ms_median": ms, "ms_min": min(times), "gbs": gbs, "hbm_frac": gbs / peaks["hbm_gbs"],
+            "tflops": tflops, "bf16_burst_frac": tflops / peaks["bf16_tflops"],
+            "algorithmic_bytes": algo_bytes, "flops": flops, "bound": "hbm",
+            "peak_source": f"{src} copy bandwidth {peaks['hbm_gbs']:.0f} GB/s",
+            "l2": "flushed before every timed call"}
 
 
 def _stages_summary():
@@ -662,6 +752,8 @@ def _stages_summary():
                     "frac": rf["frac"], "algorithmic_bytes": rf["algorithmic_bytes"],
                     "ms_median": r["ms_per_step"], "ms_min": r["ms_min"],
                     "l2": "flushed before every timed launch"}
+    for name in ("v3_decode", "v3_sparse_decode"):
+        out["decode_" + name] = measure_decode(name)
     return out
 
 

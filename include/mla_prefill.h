@@ -379,13 +379,18 @@ mla_status_t mla_prefill(void* out, float* lse, const void* q, const uint32_t* i
                          int32_t* d_status, mla_stream_t stream);
 
 /*
- * Decode partitions the library picks for mla_decode when num_partitions is
- * 0: enough (sequence, 128 query rows, key partition) work items for about two
- * waves of SM pairs, at most 32.  Follows "mla_prefill_decode_graph_bf16"
- * (Args: num_partitions_in, the override of this choice).  Host only; 1 for
- * invalid sizes.
+ * Partitions per sequence the library uses for mla_decode when num_partitions
+ * is 0 (size the workspace with it).  It cuts every sequence's keys into
+ * pieces of about the same size -- between 256 and 2048 keys, chosen from the
+ * batch's sizes for about four waves of work on the GPU's SM pairs -- so that
+ * short and long sequences make items of equal cost; this returns the most
+ * pieces a sequence can get.  max_keys: max_seq_len for dense decode (the
+ * longest context, new tokens included), the list stride for sparse decode.
+ * Follows "mla_prefill_decode_graph_bf16" (Args: num_partitions_in, the
+ * caller's override; max_seq_len).  Host only; 1 for invalid sizes.
  */
-int32_t mla_decode_partitions(int32_t batch_size, int32_t num_heads, int32_t max_new_tokens);
+int32_t mla_decode_partitions(int32_t batch_size, int32_t num_heads, int32_t max_new_tokens,
+                              int32_t max_keys);
 
 /*
  * Workspace bytes mla_decode needs: the 576-wide query rows (bf16), every
@@ -421,8 +426,10 @@ size_t mla_decode_workspace_bytes(int32_t num_heads, int32_t total_q_tokens, int
  * With attn_sink given, sink = attn_sink[b] is one more logit in every
  * softmax of sequence b with no value row: out is scaled by
  * e^LSE / (e^LSE + e^sink) and lse includes it.  The keys are split into
- * num_partitions ranges (0: mla_decode_partitions) whose partial results
- * merge by LSE; the result does not depend on that choice beyond rounding.
+ * ranges whose partial results merge by LSE; the result does not depend on
+ * the split beyond rounding.
+ * num_partitions > 0 splits every sequence into that many ranges; 0 lets the
+ * library pick ranges of equal size (mla_decode_partitions).
  * q_lat and the merged latent result are rounded to bf16 for the tensor-core
  * projections; scores, softmax and the merge run in fp32.
  *
@@ -433,8 +440,11 @@ size_t mla_decode_workspace_bytes(int32_t num_heads, int32_t total_q_tokens, int
  * w_uk [num_heads][512][128], w_uv [num_heads][128][512] bf16
  * input_row_offsets [B+1], cache_lengths [B], page_table [B][max_pages_per_seq]
  * max_new_tokens: largest new-token count of any sequence (sizes the grid)
+ * max_seq_len: largest context (cached + new tokens) of any sequence; bounds
+ *            the partitions when num_partitions is 0
  * workspace: device memory of at least mla_decode_workspace_bytes(num_heads,
- *            total_q_tokens, the partition count used), 256-byte aligned.
+ *            total_q_tokens, num_partitions or mla_decode_partitions(...)),
+ *            256-byte aligned.
  * Errors: host MLA_ERR_DTYPE (bf16 only: the page's graph is bf16),
  * MLA_ERR_GEOMETRY, MLA_ERR_ARG (null or misaligned pointers, bad sizes),
  * MLA_ERR_WORKSPACE, MLA_ERR_LAUNCH.  Device MLA_DEV_BAD_OFFSETS
@@ -447,8 +457,9 @@ mla_status_t mla_decode(void* out, float* lse, const void* q, const uint32_t* in
                         const uint32_t* cache_lengths, const void* kv_cache, const int32_t* page_table,
                         int32_t num_pages, int32_t page_size, int32_t max_pages_per_seq,
                         const void* w_uk, const void* w_uv, int32_t batch_size, int32_t num_heads,
-                        int32_t total_q_tokens, int32_t max_new_tokens, int32_t num_partitions,
-                        float scale, const int32_t* d_indices, int32_t indices_stride,
+                        int32_t total_q_tokens, int32_t max_new_tokens, int32_t max_seq_len,
+                        int32_t num_partitions, float scale, const int32_t* d_indices,
+                        int32_t indices_stride,
                         const int32_t* topk_lengths, const float* attn_sink, int32_t dtype,
                         void* workspace, size_t workspace_bytes, int32_t* d_status,
                         mla_stream_t stream);

@@ -56,10 +56,10 @@ SIGNATURES = {
     "mla_prefill_workspace_bytes": (_Z, [_I, _I, _I, _I, _U, _I]),
     "mla_prefill": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _I, _I, _I, _U, _I,
                          _F, _F, _F, _F, _I, _P, _Z, _P, _P]),
-    "mla_decode_partitions": (_I, [_I, _I, _I]),
+    "mla_decode_partitions": (_I, [_I, _I, _I, _I]),
     "mla_decode_workspace_bytes": (_Z, [_I, _I, _I]),
-    "mla_decode": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _I, _I, _I, _I, _F,
-                        _P, _I, _P, _P, _I, _P, _Z, _P, _P]),
+    "mla_decode": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _I, _I, _I, _I, _I,
+                        _F, _P, _I, _P, _P, _I, _P, _Z, _P, _P]),
 }
 
 _lib = None
@@ -220,8 +220,8 @@ def mla_prefill(out, lse, q, input_row_offsets, cache_lengths, kv_cache, page_ta
         workspace_bytes, _ptr(d_status), _stream(stream))
 
 
-def mla_decode_partitions(batch_size, num_heads, max_new_tokens) -> int:
-    return load().mla_decode_partitions(batch_size, num_heads, max_new_tokens)
+def mla_decode_partitions(batch_size, num_heads, max_new_tokens, max_keys) -> int:
+    return load().mla_decode_partitions(batch_size, num_heads, max_new_tokens, max_keys)
 
 
 def mla_decode_workspace_bytes(num_heads, total_q_tokens, num_partitions) -> int:
@@ -230,13 +230,14 @@ def mla_decode_workspace_bytes(num_heads, total_q_tokens, num_partitions) -> int
 
 def mla_decode(out, lse, q, input_row_offsets, cache_lengths, kv_cache, page_table, num_pages,
                page_size, max_pages_per_seq, w_uk, w_uv, batch_size, num_heads, total_q_tokens,
-               max_new_tokens, num_partitions, scale, d_indices=None, indices_stride=0,
+               max_new_tokens, max_seq_len, num_partitions, scale, d_indices=None, indices_stride=0,
                topk_lengths=None, attn_sink=None, dtype=MLA_BF16, workspace=None,
                workspace_bytes=0, d_status=None, stream=None) -> int:
     return load().mla_decode(
         _ptr(out), _ptr(lse), _ptr(q), _ptr(input_row_offsets), _ptr(cache_lengths),
         _ptr(kv_cache), _ptr(page_table), num_pages, page_size, max_pages_per_seq, _ptr(w_uk),
-        _ptr(w_uv), batch_size, num_heads, total_q_tokens, max_new_tokens, num_partitions, scale,
+        _ptr(w_uv), batch_size, num_heads, total_q_tokens, max_new_tokens, max_seq_len,
+        num_partitions, scale,
         _ptr(d_indices), indices_stride, _ptr(topk_lengths), _ptr(attn_sink), dtype,
         _ptr(workspace), workspace_bytes, _ptr(d_status), _stream(stream))
 

@@ -1,6 +1,7 @@
 // C ABI of the library (declared in include/mla_prefill.h): argument checks,
 // tensor-map encoding, workspace layout and the fused chunk loop.  No entry
 // point allocates memory or synchronises the stream.
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -358,9 +359,10 @@ mla_status_t mla_prefill(void* out, float* lse, const void* q, const uint32_t* i
   return MLA_OK;
 }
 
-int32_t mla_decode_partitions(int32_t batch_size, int32_t num_heads, int32_t max_new_tokens) {
-  if (batch_size < 1 || num_heads < 1 || max_new_tokens < 1) return 1;
-  return mla::decode_default_partitions(batch_size, num_heads, max_new_tokens);
+int32_t mla_decode_partitions(int32_t batch_size, int32_t num_heads, int32_t max_new_tokens,
+                              int32_t max_keys) {
+  if (batch_size < 1 || num_heads < 1) return 1;
+  return mla::decode_partitioning(batch_size, num_heads, max_new_tokens, max_keys).parts;
 }
 
 size_t mla_decode_workspace_bytes(int32_t num_heads, int32_t total_q_tokens, int32_t num_partitions) {
@@ -372,8 +374,8 @@ mla_status_t mla_decode(void* out, float* lse, const void* q, const uint32_t* in
                         const uint32_t* cache_lengths, const void* kv_cache, const int32_t* page_table,
                         int32_t num_pages, int32_t page_size, int32_t max_pages_per_seq,
                         const void* w_uk, const void* w_uv, int32_t batch_size, int32_t num_heads,
-                        int32_t total_q_tokens, int32_t max_new_tokens, int32_t num_partitions,
-                        float scale, const int32_t* d_indices, int32_t indices_stride,
+                        int32_t total_q_tokens, int32_t max_new_tokens, int32_t max_seq_len,
+                        int32_t num_partitions, float scale, const int32_t* d_indices, int32_t indices_stride,
                         const int32_t* topk_lengths, const float* attn_sink, int32_t dtype,
                         void* workspace, size_t workspace_bytes, int32_t* d_status,
                         mla_stream_t stream) {
@@ -382,7 +384,7 @@ mla_status_t mla_decode(void* out, float* lse, const void* q, const uint32_t* in
   if (!out || !q || !input_row_offsets || !cache_lengths || !kv_cache || !w_uk || !w_uv ||
       !aligned16(out) || !aligned16(q) || !aligned16(kv_cache) || !aligned16(w_uk) ||
       !aligned16(w_uv) || batch_size < 1 || total_q_tokens < 0 || max_new_tokens < 0 ||
-      num_partitions < 0 || num_pages < 1 || page_size < 1 || !(scale > 0.0f))
+      max_seq_len < 1 || num_partitions < 0 || num_pages < 1 || page_size < 1 || !(scale > 0.0f))
     return MLA_ERR_ARG;
   if (d_indices == nullptr && (!page_table || max_pages_per_seq < 1)) return MLA_ERR_ARG;
   if (d_indices != nullptr && indices_stride < 1) return MLA_ERR_ARG;
@@ -390,8 +392,10 @@ mla_status_t mla_decode(void* out, float* lse, const void* q, const uint32_t* in
   if (rows >= (1ll << 31) / 4 || static_cast<long long>(num_pages) * page_size >= (1ll << 31))
     return MLA_ERR_ARG;
   if (total_q_tokens == 0 || max_new_tokens == 0) return MLA_OK;
-  const int parts = num_partitions > 0 ? num_partitions
-                                       : mla::decode_default_partitions(batch_size, num_heads, max_new_tokens);
+  const int max_keys = d_indices != nullptr ? std::min(indices_stride, max_seq_len) : max_seq_len;
+  const mla::DecodePartitioning auto_parts =
+      mla::decode_partitioning(batch_size, num_heads, max_new_tokens, max_keys);
+  const int parts = num_partitions > 0 ? num_partitions : auto_parts.parts;
   const long long items = static_cast<long long>(batch_size) * parts *
                           ((static_cast<long long>(max_new_tokens) * num_heads + 127) / 128);
   if (items >= (1ll << 31)) return MLA_ERR_ARG;
@@ -416,6 +420,7 @@ mla_status_t mla_decode(void* out, float* lse, const void* q, const uint32_t* in
   a.T = total_q_tokens;
   a.max_new = max_new_tokens;
   a.parts = parts;
+  a.part_keys = num_partitions > 0 ? 0 : auto_parts.part_keys;
   a.scale = scale;
   a.indices = d_indices;
   a.indices_stride = indices_stride;

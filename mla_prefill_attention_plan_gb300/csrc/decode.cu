@@ -196,23 +196,24 @@ __global__ void __launch_bounds__(192, 1)
 
 // ============================================================ latent attention
 constexpr int DBN = 64;                           // keys per tile
-constexpr int D_KSTAGES = 3;
+constexpr int D_KSTAGES = 4;
 constexpr int D_KBLK = 64 * 128;                  // 64 keys x 64 latent columns (128 B), 8 KB
 constexpr int D_KLAT = 4 * D_KBLK;                // this CTA's 256 latent columns
 constexpr int D_KBYTES = D_KLAT + 64 * 64;        // + its 32 rope columns (64 B a key)
 constexpr int D_QR_BYTES = 128 * 64;              // Q rope half: 128 rows x 64 B
-constexpr int D_X_BYTES = 32 * DBN * 4;           // one warp's partial scores: 32 rows x 64 fp32
+constexpr int D_X_BYTES = 32 * DBN * 2;           // one warp's partial scores: 32 rows x 64 fp16
 constexpr int D_SMEM_K = 0;
 constexpr int D_SMEM_QR = D_SMEM_K + D_KSTAGES * D_KBYTES;
-constexpr int D_SMEM_X = D_SMEM_QR + 2 * D_QR_BYTES;
-constexpr int D_SMEM_BAR = D_SMEM_X + 2 * 4 * D_X_BYTES;
+constexpr int D_SMEM_XS = D_SMEM_QR + 2 * D_QR_BYTES;        // send buffers [slot][warp]
+constexpr int D_SMEM_XR = D_SMEM_XS + 2 * 4 * D_X_BYTES;     // receive buffers [slot][warp]
+constexpr int D_SMEM_BAR = D_SMEM_XR + 2 * 4 * D_X_BYTES;
 constexpr int D_SMEM_TOTAL = D_SMEM_BAR + 512 + 1024;
-constexpr int D_THREADS = 192;                    // producer, MMA, 4 softmax warps
+constexpr int D_THREADS = 320;                    // producer, MMA, 4 softmax warps, 4 exchange warps
 constexpr uint32_t D_TMEM_COLS = 512;
 constexpr uint32_t D_TM_S = 0, D_TM_O = 128, D_TM_Q = 384;   // S 2 x 64, O 256, Q 128 (bf16 pairs)
 constexpr uint32_t IDESC_DS = idesc_bf16(128, DBN, false, false);
 constexpr uint32_t IDESC_DPV = idesc_bf16(128, 256, false, true);
-static_assert(D_KBYTES % 1024 == 0 && D_SMEM_QR % 1024 == 0 && D_SMEM_X % 1024 == 0, "alignment");
+static_assert(D_KBYTES % 1024 == 0 && D_SMEM_QR % 1024 == 0 && D_SMEM_XS % 1024 == 0, "alignment");
 static_assert(D_SMEM_TOTAL <= 227 * 1024, "shared memory");
 
 struct DecodeSmem {
@@ -221,6 +222,7 @@ struct DecodeSmem {
   uint64_t k_full[D_KSTAGES], k_empty[D_KSTAGES];
   uint64_t s_full[2], p_full[2], o_done[2];
   uint64_t o_free;                 // 4 warps read O
+  uint64_t x_sent[2];              // this CTA's exchange warps have read S of the slot (4 warps)
   uint64_t x_full[2][4];           // the other CTA's partial scores landed (per warp, per slot)
   uint64_t x_empty[2][4];          // the other CTA has read what this CTA sent
   uint64_t drain;
@@ -241,6 +243,7 @@ struct DecodeParams {
   int indices_stride;
   int num_pages, page_size, max_pages;
   int B, H, R, parts, m_tiles;
+  int part_keys;                   // > 0: partitions of about this many keys (at most `parts`)
   int dense_tiles;                 // 1: every 64-key tile is 64 consecutive rows of one page
   float scale_log2;
   int32_t* status;
@@ -254,8 +257,16 @@ __device__ __forceinline__ long long decode_keys(const DecodeParams& p, int b, l
   }
   return cb + nb;
 }
-__device__ __forceinline__ long long decode_part_size(long long L, int parts) {
-  const long long per = (L + parts - 1) / parts;
+// Partitions of a sequence with L keys: `parts` of them (a count from the
+// caller), or, with part_keys set, ceil(L / part_keys) of them capped at
+// `parts` (the library's choice: items of about the same size whatever the
+// sequence's length).  Each holds ceil(L / count) keys rounded up to the tile.
+__device__ __forceinline__ int decode_part_count(const DecodeParams& p, long long L) {
+  if (p.part_keys <= 0) return p.parts;
+  return static_cast<int>(max(1ll, min(static_cast<long long>(p.parts), (L + p.part_keys - 1) / p.part_keys)));
+}
+__device__ __forceinline__ long long decode_part_size(long long L, int count) {
+  const long long per = (L + count - 1) / count;
   return (per + DBN - 1) / DBN * DBN;
 }
 
@@ -272,10 +283,14 @@ struct DItem {
 };
 
 __device__ __forceinline__ bool decode_item(const DecodeParams& p, int idx, DItem& it) {
+  // Partition-major order: the (sequence, row tile) items of partition 0
+  // first, then partition 1, ..., so the items that exist are spread evenly
+  // over the SM pairs' static stride; row tiles of one sequence and partition
+  // stay adjacent (they read the same keys).
   const int m = idx % p.m_tiles;
-  const int bk = idx / p.m_tiles;
-  it.k = bk % p.parts;
-  it.b = bk / p.parts;
+  const int kb = idx / p.m_tiles;
+  it.b = kb % p.B;
+  it.k = kb / p.B;
   it.n_kv = 0;
   const uint32_t qa = p.iro[it.b], qe = p.iro[it.b + 1];
   if (static_cast<long long>(qe) * p.H > p.R) {
@@ -291,7 +306,9 @@ __device__ __forceinline__ bool decode_item(const DecodeParams& p, int idx, DIte
   it.nrows = static_cast<int>(min(128ll, rows_b - it.r0));
   it.cb = p.cache_len[it.b];
   it.L = decode_keys(p, it.b, it.cb, nb);
-  const long long size = decode_part_size(it.L, p.parts);
+  const int count = decode_part_count(p, it.L);
+  if (it.k >= count) return false;
+  const long long size = decode_part_size(it.L, count);
   it.key0 = it.k * size;
   it.key1 = min(it.key0 + size, it.L);
   long long hi = it.key1;
@@ -353,6 +370,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(D_THREADS, 1)
       mbar_init(smem_u32(&sh->s_full[i]), 1);
       mbar_init(smem_u32(&sh->p_full[i]), 4);
       mbar_init(smem_u32(&sh->o_done[i]), 1);
+      mbar_init(smem_u32(&sh->x_sent[i]), 4);
       for (int w = 0; w < 4; ++w) {
         mbar_init(smem_u32(&sh->x_full[i][w]), 1);
         mbar_init(smem_u32(&sh->x_empty[i][w]), 1);
@@ -391,7 +409,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(D_THREADS, 1)
     }
     __syncwarp();
     uint32_t g = 0, it_n = 0;
-    int q_last[2] = {-1, -1}, k_last[D_KSTAGES] = {-1, -1, -1};
+    uint32_t q_issued = 0, k_issued = 0;   // Q-rope and K-tile loads issued
     bool ok = true;
     DItem it;
     const int lat_x = 256 * static_cast<int>(rank);
@@ -407,33 +425,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(D_THREADS, 1)
         tma_load_2d(smem_u32(smem + D_SMEM_QR + qs * D_QR_BYTES), &qr_map, qf, rope_x, it.row0);
       }
       __syncwarp();
-      q_last[qs] = int((it_n >> 1) & 1);
+      ++q_issued;
       for (int j = 0; j < it.n_kv; ++j) {
         const uint32_t gj = g + j;
         const int st = gj % D_KSTAGES;
+        const long long pos0 = it.key0 + static_cast<long long>(j) * DBN;
+        // The tile's cache rows (a page-table or index read) before waiting for
+        // its stage, so that the read's latency overlaps the wait.
+        int ra, rb;
+        if (p.dense_tiles) {
+          // 64 consecutive positions, all in one page.
+          ra = decode_phys_row(p, it.b, pos0);
+          if (ra < 0) ra = p.num_pages * p.page_size;   // past the end: reads zeros
+          rb = 0;
+        } else {
+          const long long pa = pos0 + lane, pb = pos0 + 32 + lane;
+          ra = pa < it.L ? decode_phys_row(p, it.b, pa) : 0;
+          rb = pb < it.L ? decode_phys_row(p, it.b, pb) : 0;
+          if (ra < 0) ra = 0;   // reported; the scores of such a key are wrong, the status says so
+          if (rb < 0) rb = 0;
+        }
         if (gj >= D_KSTAGES &&
             !(ok = mbar_wait_warp(smem_u32(&sh->k_empty[st]), ((gj / D_KSTAGES) & 1) ^ 1, status, abort_flag)))
           break;
         const uint32_t kf = smem_u32(&sh->k_full[st]);
         const uint32_t kd = smem_u32(smem + D_SMEM_K + st * D_KBYTES);
-        const long long pos0 = it.key0 + static_cast<long long>(j) * DBN;
         if (p.dense_tiles) {
-          // 64 consecutive positions, all in one page.
           if (elect_one()) {
-            int row = decode_phys_row(p, it.b, pos0);
-            if (row < 0) row = p.num_pages * p.page_size;   // past the end: reads zeros
             mbar_expect_tx(kf, D_KBYTES);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tma_load_2d(kd + c * D_KBLK, &kl_map, kf, lat_x + 64 * c, row);
-            tma_load_2d(kd + D_KLAT, &kr_map, kf, rope_x, row);
+            for (int c = 0; c < 4; ++c) tma_load_2d(kd + c * D_KBLK, &kl_map, kf, lat_x + 64 * c, ra);
+            tma_load_2d(kd + D_KLAT, &kr_map, kf, rope_x, ra);
           }
         } else {
           // Any rows: four at a time (tile::gather4), 16 lanes each one group.
-          const long long pa = pos0 + lane, pb = pos0 + 32 + lane;
-          int ra = pa < it.L ? decode_phys_row(p, it.b, pa) : 0;
-          int rb = pb < it.L ? decode_phys_row(p, it.b, pb) : 0;
-          if (ra < 0) ra = 0;   // reported; the scores of such a key are wrong, the status says so
-          if (rb < 0) rb = 0;
           int y[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
@@ -452,17 +477,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(D_THREADS, 1)
           }
         }
         __syncwarp();
-        k_last[st] = int((gj / D_KSTAGES) & 1);
+        ++k_issued;
       }
       g += it.n_kv;
       ++it_n;
     }
-    // Every issued load lands before the CTA leaves.
+    // Every issued load lands before the CTA leaves: the last phase of each
+    // slot and stage that a load used.
     volatile int never = 0;
-    for (int s = 0; s < 2; ++s)
-      if (q_last[s] >= 0) mbar_wait_warp(smem_u32(&sh->q_full[s]), uint32_t(q_last[s]), status, &never);
-    for (int s = 0; s < D_KSTAGES; ++s)
-      if (k_last[s] >= 0) mbar_wait_warp(smem_u32(&sh->k_full[s]), uint32_t(k_last[s]), status, &never);
+    for (uint32_t s = 0; s < 2; ++s)
+      if (q_issued > s) {
+        const uint32_t last = s + 2 * ((q_issued - 1 - s) / 2);
+        mbar_wait_warp(smem_u32(&sh->q_full[s]), (last >> 1) & 1, status, &never);
+      }
+    for (uint32_t s = 0; s < D_KSTAGES; ++s)
+      if (k_issued > s) {
+        const uint32_t last = s + D_KSTAGES * ((k_issued - 1 - s) / D_KSTAGES);
+        mbar_wait_warp(smem_u32(&sh->k_full[s]), (last / D_KSTAGES) & 1, status, &never);
+      }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (elect_one()) {
@@ -479,6 +511,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(D_THREADS, 1)
           const uint32_t gj = g + j;
           const int st = gj % D_KSTAGES;
           if (!mbar_wait(smem_u32(&sh->k_full[st]), (gj / D_KSTAGES) & 1, status, abort_flag)) return false;
+          // The exchange warps have read S of the tile two back from this buffer.
+          if (gj >= 2 && !mbar_wait(smem_u32(&sh->x_sent[gj & 1]), ((gj >> 1) - 1) & 1, status, abort_flag))
+            return false;
           tc_fence_after();
           const uint32_t kd = smem_u32(smem + D_SMEM_K + st * D_KBYTES);
           const uint32_t d = tmem + D_TM_S + (gj & 1) * DBN;
@@ -526,6 +561,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(D_THREADS, 1)
       mbar_wait(smem_u32(&sh->drain), 0, status, &never);
     }
     __syncwarp();
+  } else if (warp >= 6) {
+    // ------------------------------------------------------------ exchange
+    // Every tile's partial scores of this warp's 32 rows, read from TMEM as
+    // soon as the S MMA completes, rounded to fp16 and shipped to the other
+    // CTA's receive slot gj & 1 with one bulk copy, once it has read what this
+    // warp sent there two tiles ago.  (Both CTAs add the same two rounded
+    // halves, so both get the same scores.)
+    const int q4 = warp & 3;
+    const uint32_t lane_off = uint32_t(q4 * 32) << 16;
+    constexpr uint32_t kSlotStep = 4 * D_X_BYTES;
+    constexpr uint32_t kBarSlot = 4 * 8;
+    const uint32_t xs_mine = smem_u32(smem + D_SMEM_XS + q4 * D_X_BYTES);
+    const uint32_t xr_other = cluster_addr(smem_u32(smem + D_SMEM_XR + q4 * D_X_BYTES), other);
+    const uint32_t xf_other = cluster_addr(smem_u32(&sh->x_full[0][q4]), other);
+    uint32_t g = 0;
+    bool ok = true;
+    DItem it;
+    for (int idx = pair_id; ok && next_decode_item(p, idx, n_pairs, total, it); idx += n_pairs) {
+      for (int j = 0; j < it.n_kv; ++j) {
+        const uint32_t gj = g + j;
+        const uint32_t sb = gj & 1, use = gj >> 1;
+        if (!(ok = mbar_wait_warp(smem_u32(&sh->s_full[sb]), use & 1, status, abort_flag))) break;
+        tc_fence_after();
+        uint32_t x[DBN];
+        tmem_ld32(tmem + lane_off + D_TM_S + sb * DBN, *reinterpret_cast<uint32_t(*)[32]>(x));
+        tmem_ld32(tmem + lane_off + D_TM_S + sb * DBN + 32, *reinterpret_cast<uint32_t(*)[32]>(x + 32));
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sh->x_sent[sb]));
+        uint32_t h[DBN / 2];
+#pragma unroll
+        for (int k = 0; k < DBN / 2; ++k) h[k] = pack_f16(__uint_as_float(x[2 * k]), __uint_as_float(x[2 * k + 1]));
+        if (use > 0 && !(ok = mbar_wait_warp(smem_u32(&sh->x_empty[sb][q4]), (use - 1) & 1, status, abort_flag)))
+          break;
+        uint8_t* sbuf = smem + D_SMEM_XS + sb * kSlotStep + q4 * D_X_BYTES;
+#pragma unroll
+        for (int c = 0; c < DBN / 8; ++c)
+          *reinterpret_cast<uint4*>(sbuf + c * 512 + lane * 16) = make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0)
+          bulk_copy_to_cluster(xr_other + sb * kSlotStep, xs_mine + sb * kSlotStep, D_X_BYTES,
+                               xf_other + sb * kBarSlot);
+      }
+      g += it.n_kv;
+    }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
     const int q4 = warp & 3;
@@ -533,16 +615,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(D_THREADS, 1)
     const uint32_t lane_off = uint32_t(q4 * 32) << 16;
     const float sl2 = p.scale_log2;
     const float2 sl2v = make_float2(sl2, sl2);
-    // Where this warp's partial scores go in the other CTA, and its barrier there.
-    const uint32_t x_mine = smem_u32(smem + D_SMEM_X + q4 * D_X_BYTES);
-    const uint32_t x_other = cluster_addr(x_mine, other);
-    const uint32_t xf_other = cluster_addr(smem_u32(&sh->x_full[0][q4]), other);
+    constexpr uint32_t kSlotStep = 4 * D_X_BYTES;
+    constexpr uint32_t kBarSlot = 4 * 8;
     const uint32_t xe_other = cluster_addr(smem_u32(&sh->x_empty[0][q4]), other);
-    constexpr uint32_t kSlotStep = 4 * D_X_BYTES;   // receive buffers: [slot][warp]
-    constexpr uint32_t kBarSlot = 4 * 8;            // barriers: [slot][warp]
     uint32_t g = 0, it_n = 0;
-    uint32_t released[2] = {0, 0};                   // phases of each slot this warp handed back
-    uint32_t received[2] = {0, 0};
+    uint32_t taken0 = 0, taken1 = 0;   // phases of each receive slot this warp has consumed
     bool ok = true;
 
     // The item's Q latent half (256 bf16 of the row) into TMEM columns
@@ -580,46 +657,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(D_THREADS, 1)
       if (p.indices == nullptr) hi = min(hi, it.cb + tok + 1);
       if (row >= it.nrows) hi = it.key0;
       float m_run = kNegInfD, l_run = 0.f;
-      for (int j = 0; j < it.n_kv; ++j) {
+      for (int j = 0; j < it.n_kv && ok; ++j) {
         const uint32_t gj = g + j;
         const uint32_t sb = gj & 1;
+        // This CTA's partial scores of the tile (rounded to fp16 as the
+        // exchange warp sends them), then the other CTA's.
         if (!(ok = mbar_wait_warp(smem_u32(&sh->s_full[sb]), (gj >> 1) & 1, status, abort_flag))) break;
         tc_fence_after();
-        float x[DBN];
-        tmem_ld32(tmem + lane_off + D_TM_S + sb * DBN, *reinterpret_cast<uint32_t(*)[32]>(reinterpret_cast<uint32_t*>(x)));
-        tmem_ld32(tmem + lane_off + D_TM_S + sb * DBN + 32,
-                  *reinterpret_cast<uint32_t(*)[32]>(reinterpret_cast<uint32_t*>(x) + 32));
-        tmem_ld_wait();
-        // Send this CTA's partial scores to the other CTA's slot sb, once it has
-        // read what this warp sent there two tiles ago.
-        const uint32_t use = gj >> 1;
-        if (use > 0 &&
-            !(ok = mbar_wait_warp(smem_u32(&sh->x_empty[sb][q4]), (use - 1) & 1, status, abort_flag)))
-          break;
+        uint32_t own[DBN];
+        tmem_ld32(tmem + lane_off + D_TM_S + sb * DBN, *reinterpret_cast<uint32_t(*)[32]>(own));
+        tmem_ld32(tmem + lane_off + D_TM_S + sb * DBN + 32, *reinterpret_cast<uint32_t(*)[32]>(own + 32));
+        const uint32_t taken = sb ? taken1 : taken0;
+        if (!(ok = mbar_wait_warp(smem_u32(&sh->x_full[sb][q4]), taken & 1, status, abort_flag))) break;
+        if (sb) ++taken1; else ++taken0;
+        uint32_t theirs[DBN / 2];
+        const uint8_t* rbuf = smem + D_SMEM_XR + sb * kSlotStep + q4 * D_X_BYTES;
 #pragma unroll
-        for (int c = 0; c < DBN / 4; ++c)
-          st_async_v4(x_other + sb * kSlotStep + c * 512 + lane * 16,
-                      make_uint4(__float_as_uint(x[4 * c]), __float_as_uint(x[4 * c + 1]),
-                                 __float_as_uint(x[4 * c + 2]), __float_as_uint(x[4 * c + 3])),
-                      xf_other + sb * kBarSlot);
-        // ... and add the other CTA's partial scores for the same rows.
-        if (!(ok = mbar_wait_warp(smem_u32(&sh->x_full[sb][q4]), received[sb] & 1, status, abort_flag))) break;
-        ++received[sb];
-#pragma unroll
-        for (int c = 0; c < DBN / 4; ++c) {
-          const uint4 y = *reinterpret_cast<const uint4*>(smem + D_SMEM_X + sb * kSlotStep + q4 * D_X_BYTES +
-                                                                    c * 512 + lane * 16);
-          x[4 * c] += __uint_as_float(y.x);
-          x[4 * c + 1] += __uint_as_float(y.y);
-          x[4 * c + 2] += __uint_as_float(y.z);
-          x[4 * c + 3] += __uint_as_float(y.w);
+        for (int c = 0; c < DBN / 8; ++c) {
+          const uint4 y = *reinterpret_cast<const uint4*>(rbuf + c * 512 + lane * 16);
+          theirs[4 * c] = y.x; theirs[4 * c + 1] = y.y; theirs[4 * c + 2] = y.z; theirs[4 * c + 3] = y.w;
         }
         __syncwarp();
         if (lane == 0) {
           mbar_expect_tx(smem_u32(&sh->x_full[sb][q4]), D_X_BYTES);   // the slot's next phase
           mbar_arrive_cluster(xe_other + sb * kBarSlot);              // the other CTA may send again
         }
-        ++released[sb];
+        tmem_ld_wait();
+        float x[DBN];
+#pragma unroll
+        for (int k = 0; k < DBN / 2; ++k) {
+          const float2 a = f16x2_to_float2(pack_f16(__uint_as_float(own[2 * k]), __uint_as_float(own[2 * k + 1])));
+          const float2 b = f16x2_to_float2(theirs[k]);
+          x[2 * k] = a.x + b.x;
+          x[2 * k + 1] = a.y + b.y;
+        }
         // Mask keys outside [key0, hi) of this row.
         const long long lim = hi - (it.key0 + static_cast<long long>(j) * DBN);
         if (lim < DBN) {
@@ -726,12 +797,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(D_THREADS, 1)
       ++it_n;
     }
     if (!ok) {
-      // Aborted: the other CTA may still be storing into a slot this warp
-      // handed back; let those stores land (briefly) before the CTA leaves.
+      // Aborted: the other CTA may still be copying into a slot this warp
+      // handed back; let those copies land (briefly) before the CTA leaves.
       volatile int never = 0;
-      for (int s = 0; s < 2; ++s)
-        if (released[s] + 1 > received[s])
-          mbar_wait_warp(smem_u32(&sh->x_full[s][q4]), received[s] & 1, status, &never, 10000000ull);
+      mbar_wait_warp(smem_u32(&sh->x_full[0][q4]), taken0 & 1, status, &never, 10000000ull);
+      mbar_wait_warp(smem_u32(&sh->x_full[1][q4]), taken1 & 1, status, &never, 10000000ull);
     }
   }
 
@@ -774,14 +844,15 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p,
     const long long L = decode_keys(p, b, cb, static_cast<long long>(qe - qa));
     long long lim = L;
     if (p.indices == nullptr) lim = min(lim, cb + (t - static_cast<long long>(qa)) + 1);
-    const long long size = decode_part_size(L, p.parts);
+    const int count = decode_part_count(p, L);
+    const long long size = decode_part_size(L, count);
     float mx = kNegInfD;
-    for (int k = 0; k < p.parts; ++k)
+    for (int k = 0; k < count; ++k)
       if (static_cast<long long>(k) * size < lim) mx = fmaxf(mx, p.lse_part[static_cast<long long>(k) * p.R + grow]);
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
     float tot = 0.f;
     if (mx != kNegInfD) {
-      for (int k = 0; k < p.parts; ++k) {
+      for (int k = 0; k < count; ++k) {
         if (static_cast<long long>(k) * size >= lim) continue;
         const float lk = p.lse_part[static_cast<long long>(k) * p.R + grow];
         const float wk = __expf(lk - mx);
@@ -868,12 +939,18 @@ DecodeLayout decode_layout(int T, int H, int parts) {
   return L;
 }
 
-int decode_default_partitions(int B, int H, int max_new) {
-  const int pairs = std::max(1, sm_count() / 2);
-  const long long tiles = static_cast<long long>(B) * ((static_cast<long long>(max_new) * H + 127) / 128);
-  // Enough items for about two waves of SM pairs, at most 32 partitions.
-  long long parts = (2ll * pairs + tiles - 1) / std::max(1ll, tiles);
-  return static_cast<int>(std::min(32ll, std::max(1ll, parts)));
+DecodePartitioning decode_partitioning(int B, int H, int max_new, int max_keys) {
+  // Items of about the same size, enough of them for about four waves of SM
+  // pairs, each between 256 and 2048 keys; at most kDecodeMaxParts a sequence.
+  const long long pairs = std::max(1, sm_count() / 2);
+  const long long m_tiles = (static_cast<long long>(std::max(1, max_new)) * H + 127) / 128;
+  const long long keys = std::max(1, max_keys);
+  long long pk = static_cast<long long>(B) * m_tiles * keys / (4 * pairs);
+  pk = std::min<long long>(2048, std::max<long long>(256, (pk + 63) / 64 * 64));
+  DecodePartitioning d;
+  d.part_keys = static_cast<int>(pk);
+  d.parts = static_cast<int>(std::min<long long>(kDecodeMaxParts, std::max(1ll, (keys + pk - 1) / pk)));
+  return d;
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
@@ -926,6 +1003,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.H = H;
   p.R = static_cast<int>(R);
   p.parts = a.parts;
+  p.part_keys = a.part_keys;
   p.m_tiles = static_cast<int>((static_cast<long long>(a.max_new) * H + 127) / 128);
   p.dense_tiles = (a.indices == nullptr && a.page_size % DBN == 0) ? 1 : 0;
   p.scale_log2 = a.scale * 1.4426950408889634f;

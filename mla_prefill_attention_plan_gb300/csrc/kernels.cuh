@@ -99,6 +99,7 @@ struct DecodeArgs {
   const uint32_t* iro;
   const uint32_t* cache_len;
   int B, H, T, max_new, parts;
+  int part_keys;              // > 0: about this many keys a partition, at most `parts` of them
   float scale;
   const int32_t* indices;     // sparse: [B][indices_stride] physical cache rows, or null
   int indices_stride;
@@ -111,7 +112,13 @@ struct DecodeLayout {
   size_t q_full, o_part, lse_part, o_lat, total;
 };
 DecodeLayout decode_layout(int T, int H, int parts);
-int decode_default_partitions(int B, int H, int max_new);
+// The library's partitioning: about part_keys keys a partition (at most
+// `parts` of them), from the batch's sizes and its longest key list.
+constexpr int kDecodeMaxParts = 64;
+struct DecodePartitioning {
+  int parts, part_keys;
+};
+DecodePartitioning decode_partitioning(int B, int H, int max_new, int max_keys);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
 // Self-test of the bounded waits (selftest.cu): one cluster of `cluster`

@@ -7,6 +7,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -228,6 +229,17 @@ __device__ __forceinline__ void st_async_v4(uint32_t cluster_dst, uint4 v, uint3
       "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(cluster_bar)
       : "memory");
 }
+// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to
+// shared memory of another CTA of the cluster (cluster address); completion
+// counts toward the transaction count of `cluster_bar` in that CTA.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t cluster_dst, uint32_t src, uint32_t bytes,
+                                                     uint32_t cluster_bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          cluster_dst),
+      "r"(src), "r"(bytes), "r"(cluster_bar)
+      : "memory");
+}
 // Every thread of every CTA of the cluster.
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
@@ -438,6 +450,10 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn, bool b
          (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 // max(a, b, c) in one instruction (sm_100+).
+// Packed f16x2 (lo in bits 0..15) -> two floats; exact.
+__device__ __forceinline__ float2 f16x2_to_float2(uint32_t v) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&v));
+}
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));

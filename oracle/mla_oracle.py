@@ -671,7 +671,10 @@ def mla_sparse_decode(q, kv_cache_codes, page_size: int, w_uk, w_uv, input_row_o
                 s = scale * (c_kv @ q_lat + k_rope @ q[t, h, DN:])
                 if attn_sink is not None:
                     s = np.concatenate([s, [float(attn_sink[b])]])
-                w, lse = softmax_weights(s[None, :])
+                if s.size == 0:   # nothing listed and no sink: no weights, LSE -inf
+                    w, lse = np.zeros((1, 0)), np.array([-np.inf])
+                else:
+                    w, lse = softmax_weights(s[None, :])
                 o = w[0, :k] @ c_kv if k > 0 else np.zeros(R)
                 out[i] = np.asarray(w_uv[h], dtype=np.float64) @ o
                 lses[i] = lse[0]

@@ -8,7 +8,8 @@ import torch
 
 import mla_prefill_attention_plan_gb300 as mla
 import oracle as O
-from workloads import DECODE_WORKLOADS, WORKLOADS, make_inputs, scaled
+from workloads import (DECODE_WORKLOADS, WORKLOADS, make_attention_sinks, make_inputs,
+                       make_sparse_indices, scaled)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -31,7 +32,9 @@ def run_decode(inp, parts=0, lse=True, sink=None, indices=None, stride=0, topk=N
     w = inp["workload"]
     B, H, T = inp["B"], w.H, inp["T_q"]
     max_new = int(inp["new_lens"].max())
-    nparts = parts or mla.mla_decode_partitions(B, H, max_new)
+    max_seq = int((inp["new_lens"] + inp["cache_lens"]).max())
+    max_keys = min(stride, max_seq) if indices is not None else max_seq
+    nparts = parts or mla.mla_decode_partitions(B, H, max_new, max_keys)
     nbytes = mla.mla_decode_workspace_bytes(H, T, nparts)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
     out = torch.full((T, H, 128), float("nan"), dtype=torch.bfloat16, device=DEV)
@@ -41,7 +44,7 @@ def run_decode(inp, parts=0, lse=True, sink=None, indices=None, stride=0, topk=N
                                      "w_uk", "w_uv")}
     mla.check(mla.mla_decode(out, l, d["q"], d["input_row_offsets"], d["cache_lengths"], d["kv_cache"],
                              d["page_table"], inp["num_pages"], inp["page_size"], inp["max_pages"],
-                             d["w_uk"], d["w_uv"], B, H, T, max_new, nparts, inp["scale"],
+                             d["w_uk"], d["w_uv"], B, H, T, max_new, max_seq, parts, inp["scale"],
                              d_indices=indices, indices_stride=stride, topk_lengths=topk, attn_sink=sink,
                              workspace=ws, workspace_bytes=nbytes, d_status=st))
     torch.cuda.synchronize()
@@ -147,4 +150,87 @@ def test_decode_bad_page_reports_status():
     inp["page_table"][1, 0] = inp["num_pages"] + 5
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
     run_decode(inp, 1, status=st)
+    assert int(st.item()) == mla.MLA_DEV_BAD_PAGE
+
+
+def oracle_sparse(inp, idx, topk, sink=None, heads=None, seqs=None):
+    """The oracle's sparse decode on a sample of heads and sequences."""
+    w = inp["workload"]
+    hs = list(range(w.H)) if heads is None else list(heads)
+    bs = list(range(inp["B"])) if seqs is None else list(seqs)
+    iro = inp["input_row_offsets"].numpy().astype(np.int64)
+    rows = np.concatenate([np.arange(iro[b], iro[b + 1]) for b in bs])
+    new = np.array([iro[b + 1] - iro[b] for b in bs])
+    iro_s = np.concatenate([[0], np.cumsum(new)])
+    q = O.decode(O.codes(inp["q"]), "bf16")[rows][:, hs]
+    w_uk = O.decode(O.codes(inp["w_uk"]), "bf16")[hs]
+    w_uv = O.decode(O.codes(inp["w_uv"]), "bf16")[hs]
+    res = O.mla_sparse_decode(q, O.codes(inp["kv_cache"]), inp["page_size"], w_uk, w_uv, iro_s,
+                              idx.numpy()[bs], None if topk is None else topk.numpy()[bs], inp["scale"],
+                              attn_sink=None if sink is None else sink.numpy()[bs])
+    return {(bs[bi], hs[hi]): (rows[tok], o, l) for (bi, hi), (tok, o, l) in res.items()}
+
+
+@pytest.mark.parametrize("with_sink", [False, True])
+def test_sparse_decode_listed_rows(with_sink):
+    """Sparse decode over top-k lists of physical rows (4 rows a gather), with
+    counts below the list stride (garbage past them is never read), several
+    tokens per sequence sharing one list, and optional sinks."""
+    w = _decode_workload(3, 8, (1, 3, 2), (300, 90, 1000), page_size=32)
+    inp = make_inputs(w, with_w_uk=True)
+    idx, topk = make_sparse_indices(inp, 150, stride=160, pad=2 ** 30)
+    sink = make_attention_sinks(3) if with_sink else None
+    out, lse = run_decode(inp, 2, indices=idx.to(DEV), stride=160, topk=topk.to(DEV),
+                          sink=None if sink is None else sink.to(DEV))
+    _compare(out, lse, oracle_sparse(inp, idx, topk, sink))
+
+
+def test_sparse_decode_empty_and_single_lists():
+    """A sequence with no listed row (LSE -inf, output 0; with a sink, LSE =
+    sink) and one with a single row (output = w_uv[h] times that row)."""
+    w = _decode_workload(3, 4, (1, 1, 2), (64, 200, 10), page_size=16)
+    inp = make_inputs(w, with_w_uk=True)
+    idx, cnt = make_sparse_indices(inp, 40, stride=40)
+    topk = torch.tensor([0, 1, int(cnt[2])], dtype=torch.int32)
+    for sink in (None, make_attention_sinks(3, seed=3)):
+        out, lse = run_decode(inp, 3, indices=idx.to(DEV), stride=40, topk=topk.to(DEV),
+                              sink=None if sink is None else sink.to(DEV))
+        ref = oracle_sparse(inp, idx, topk, sink, seqs=[1, 2])
+        _compare(out, lse, ref)
+        assert (out[0].float() == 0).all()
+        expect = float("-inf") if sink is None else float(sink[0])
+        assert torch.all(lse[0].cpu() == expect)
+
+
+def test_dense_decode_with_sink_equals_sparse_over_the_context():
+    """Dense decode with sinks equals the oracle's sparse decode listing each
+    sequence's whole context (one new token each, so the causal limit is the
+    whole context)."""
+    w = _decode_workload(3, 16, (1, 1, 1), (700, 64, 1500))
+    inp = make_inputs(w, with_w_uk=True)
+    L = inp["new_lens"] + inp["cache_lens"]
+    idx, topk = make_sparse_indices(inp, int(L.max()))
+    sink = make_attention_sinks(3, seed=5)
+    out, lse = run_decode(inp, 3, sink=sink.to(DEV))
+    _compare(out, lse, oracle_sparse(inp, idx, topk, sink))
+
+
+def test_sparse_decode_full_size_sampled():
+    """64 sequences over 4k-16k cached tokens, top-2048 lists, per-batch sinks:
+    the launch configuration the benchmark times; 3 heads of 6 sequences."""
+    w = DECODE_WORKLOADS["v3_sparse_decode"]
+    inp = make_inputs(w, with_w_uk=True)
+    idx, topk = make_sparse_indices(inp, 2048)
+    sink = make_attention_sinks(w.B)
+    out, lse = run_decode(inp, indices=idx.to(DEV), stride=2048, topk=topk.to(DEV), sink=sink.to(DEV))
+    _compare(out, lse, oracle_sparse(inp, idx, topk, sink, heads=[0, 50, 127], seqs=[0, 7, 19, 33, 48, 63]))
+
+
+def test_sparse_decode_bad_row_reports_status():
+    w = _decode_workload(2, 4, (1, 1), (100, 150), page_size=16)
+    inp = make_inputs(w, with_w_uk=True)
+    idx, topk = make_sparse_indices(inp, 30)
+    idx[1, 3] = inp["num_pages"] * inp["page_size"]
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    run_decode(inp, 1, indices=idx.to(DEV), stride=30, topk=topk.to(DEV), status=st)
     assert int(st.item()) == mla.MLA_DEV_BAD_PAGE

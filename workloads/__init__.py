@@ -85,6 +85,11 @@ DECODE_WORKLOADS = {
     "v3_decode": Workload("v3_decode", B=64, H=128, page_size=128, buffer_token_size=1,
                           max_chunks=1, new_range=(1, 2), cache_range=(4096, 16384),
                           shuffle_pages=True),
+    # Sparse decode: each sequence attends to 2048 listed rows of its context
+    # (make_sparse_indices), with per-batch sinks (make_attention_sinks).
+    "v3_sparse_decode": Workload("v3_sparse_decode", B=64, H=128, page_size=128,
+                                 buffer_token_size=1, max_chunks=1, new_range=(1, 1),
+                                 cache_range=(4096, 16384), shuffle_pages=True),
 }
 
 # Reduced cases of the workloads above, small enough for a full profiler capture
@@ -216,6 +221,33 @@ def make_cache_write_operands(w: Workload, T_q: int, max_seq_len: int, seed_offs
     freqs[:, 0::2] = np.cos(ang)
     freqs[:, 1::2] = np.sin(ang)
     return kv_latent, gamma, torch.from_numpy(freqs)
+
+
+def make_sparse_indices(inp, topk: int, stride: int | None = None, seed: int = 13, pad: int = -1):
+    """Top-k lists for sparse decode ("mla_prefill_decode_graph_bf16", Args
+    d_indices, indices_stride, topk_lengths): for each sequence, min(topk, L_b)
+    distinct context positions drawn uniformly (seeded), stored as physical
+    cache rows page * page_size + slot; entries past the count hold `pad`.
+    Returns (indices int32 [B, stride], topk_lengths int32 [B])."""
+    rng = np.random.default_rng(seed)
+    L = inp["new_lens"] + inp["cache_lens"]
+    stride = stride or max(1, topk)
+    ps = inp["page_size"]
+    pt = inp["page_table"].numpy().astype(np.int64)
+    idx = np.full((inp["B"], stride), pad, dtype=np.int64)
+    cnt = np.zeros(inp["B"], dtype=np.int64)
+    for b in range(inp["B"]):
+        k = min(topk, int(L[b]), stride)
+        pos = np.sort(rng.choice(int(L[b]), size=k, replace=False))
+        idx[b, :k] = pt[b, pos // ps] * ps + pos % ps
+        cnt[b] = k
+    return torch.from_numpy(idx.astype(np.int32)), torch.from_numpy(cnt.astype(np.int32))
+
+
+def make_attention_sinks(B: int, seed: int = 17):
+    """Per-batch attention sink logits ("attn_sink_ptr"), N(0, 1) float32."""
+    gen = torch.Generator().manual_seed(seed)
+    return _normal(gen, (B,))
 
 
 def scaled(w: Workload, **changes) -> Workload:
