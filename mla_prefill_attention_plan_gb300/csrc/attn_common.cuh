@@ -47,10 +47,15 @@ struct Item {
 __device__ __forceinline__ bool tile_item(const Params& p, int b, int h, int qt, Item& it) {
   it.b = b;
   it.h = h;
+  // Every table read first: they are independent, so they share one round
+  // trip to L2 (the tables are read-only while the kernel runs).
   const uint32_t* bro_c = p.bro + static_cast<size_t>(p.chunk) * (p.B + 1);
-  const int r0 = static_cast<int>(bro_c[b]);
-  it.n_cb = static_cast<int>(bro_c[b + 1]) - r0;
-  const uint32_t qa = p.iro[b], qe = p.iro[b + 1];
+  const uint32_t r0u = __ldg(bro_c + b), r1u = __ldg(bro_c + b + 1);
+  const uint32_t qa = __ldg(p.iro + b), qe = __ldg(p.iro + b + 1);
+  const uint32_t cou = __ldg(p.co + static_cast<size_t>(p.chunk) * p.B + b);
+  const uint32_t cbu = __ldg(p.cache_len + b);
+  const int r0 = static_cast<int>(r0u);
+  it.n_cb = static_cast<int>(r1u) - r0;
   it.i0 = qt * BM;
   it.n_kv = 0;
   if (qe > static_cast<uint32_t>(p.T_q)) {
@@ -65,8 +70,8 @@ __device__ __forceinline__ bool tile_item(const Params& p, int b, int h, int qt,
   it.nq = max(0, min(BM, new_b - it.i0));
   it.q_row0 = q0 + it.i0;
   it.kv_row0 = r0;
-  it.co = static_cast<int>(p.co[static_cast<size_t>(p.chunk) * p.B + b]);
-  it.cb = static_cast<int>(p.cache_len[b]);
+  it.co = static_cast<int>(cou);
+  it.cb = static_cast<int>(cbu);
   if (it.n_cb <= 0 || it.nq <= 0) return false;
   // Keys visible to the tile's last row: relative key index <= last.
   const long long last = static_cast<long long>(it.cb) + it.i0 + it.nq - 1 - it.co;
