@@ -34,9 +34,9 @@ sys.path.insert(0, ROOT)
 # DRAM bytes (read + write) per attention launch from one ncu capture of the
 # current kernel (dram__bytes_read.sum + dram__bytes_write.sum), keyed by
 # (workload, kernel); absent where the kernel has changed since its capture.
-ATTN_DRAM_BYTES_PER_LAUNCH = {("v3_prefill", "attn_pair_kernel"): 484_961_024 + 118_374_400}
+ATTN_DRAM_BYTES_PER_LAUNCH = {("v3_prefill", "attn_pair_kernel"): 480_141_056 + 117_703_680}
 # CUDA kernel name of each attention variant the library reports.
-ATTN_KERNEL_NAMES = {"pair": "attn_pair_kernel", "single": "attn_kernel", "e4m3": "attn_pair_kernel_e4m3"}
+ATTN_KERNEL_NAMES = {"pair": "attn_pair_kernel", "e4m3": "attn_pair_kernel_e4m3"}
 
 
 def _args():

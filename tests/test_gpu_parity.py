@@ -392,6 +392,14 @@ def test_gather_e4m3():
     _gather_case(w)
 
 
+@pytest.mark.parametrize("name", ["ragged_chunked_cache", "longctx_fp8"])
+def test_gather_full_size_every_chunk_bit_exact(name):
+    """The full-size gathers the benchmark runs (seeded shuffled pages and 8192-row
+    chunks; 16k + 16k e4m3 tokens), every chunk compared bit for bit with the
+    oracle, the rows past the chunk untouched."""
+    _gather_case(WORKLOADS[name])
+
+
 def test_gather_bad_page_reports_status():
     w = WORKLOADS["tiny_ragged"]
     inp = make_inputs(w)
@@ -536,6 +544,46 @@ def test_attention_offsets_past_total_q_tokens():
     n0 = int(inp["new_lens"][0])
     assert (out[n0:].float() == 3.0).all() and (lse[n0:] == 3.0).all()
     assert not (out[:n0].float() == 3.0).any()
+
+
+def test_head_split_equals_full_call_bit_for_bit():
+    """The multi-GPU split of the path is by heads (w_k, w_uv, q, K/V and out
+    sliced on H, no collective): two attention calls on heads [0, H/2) and
+    [H/2, H), each given its own contiguous slices, reproduce the full-H
+    call bit for bit, on a multi-chunk plan."""
+    w = scaled(WORKLOADS["ragged_chunked_cache"], H=8, B=3, buffer_token_size=700, max_chunks=5,
+               new_range=(100, 600), cache_range=(0, 900))
+    inp = make_inputs(w)
+    c = {k: O.codes(inp[k]) for k in ("input_row_offsets", "cache_lengths")}
+    S, B, H, T = w.buffer_token_size, inp["B"], w.H, inp["T_q"]
+    mc = -(-int((inp["new_lens"] + inp["cache_lens"]).sum()) // S)
+    g = gpu_plan(c["input_row_offsets"], c["cache_lengths"], S, mc)
+    tabs = [torch.as_tensor(x.astype(np.int32)).to(DEV) for x in g[:3]]
+    ops = [tuple(t.to(DEV) for t in make_attention_operands(w, S, seed_offset=31 + ch)) for ch in range(mc)]
+    q = inp["q"].to(DEV)
+    iro, cl = inp["input_row_offsets"].to(DEV), inp["cache_lengths"].to(DEV)
+
+    def run(h0, h1):
+        hs = h1 - h0
+        out = torch.empty(T, hs, 128, dtype=torch.bfloat16, device=DEV)
+        lse = torch.empty(T, hs, dtype=torch.float32, device=DEV)
+        oacc = torch.empty(T, hs, 128, dtype=torch.float32, device=DEV)
+        lacc = torch.empty(T, hs, dtype=torch.float32, device=DEV)
+        st = torch.zeros(1, dtype=torch.int32, device=DEV)
+        qs = q[:, h0:h1].contiguous()
+        for ch in range(mc):
+            kn, vv, kr = ops[ch]
+            mla.check(mla.mla_prefill_attention(out, lse, oacc, lacc, qs, kn[:, h0:h1].contiguous(),
+                                                vv[:, h0:h1].contiguous(), kr, iro, cl, *tabs, ch, mc, B,
+                                                hs, inp["max_prompt_len"], T, S, inp["scale"], d_status=st))
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        return out, lse
+    full_o, full_l = run(0, H)
+    lo_o, lo_l = run(0, H // 2)
+    hi_o, hi_l = run(H // 2, H)
+    assert torch.equal(torch.cat([lo_o, hi_o], 1).view(torch.int16), full_o.view(torch.int16))
+    assert torch.equal(torch.cat([lo_l, hi_l], 1), full_l)
 
 
 def test_attention_stage_e4m3_multi_chunk():
