@@ -302,6 +302,41 @@ mla_status_t mla_prefill_attention(void* out, float* lse, float* o_acc, float* l
                                    int32_t dtype, int32_t* d_status, mla_stream_t stream);
 
 /*
+ * 4'. Prefill attention for one plan chunk with k_rope read straight from the
+ * paged cache, as "flare_mla_prefill_dispatch" does (Parameters: k_rope_t is a
+ * KVCacheMHAOperand; Args: k_rope with shape [cache_len, 1, 64] and
+ * cache_offsets, the per-sequence start of the chunk in the cache).  No
+ * k_rope buffer is needed, so mla_gather_latent need not write one.
+ *
+ * Same arguments, results and errors as mla_prefill_attention, except that
+ * k_rope is replaced by the cache (as mla_gather_latent takes it):
+ * kv_cache:   [num_pages][page_size][576] dtype; columns 512..575 are k_rope
+ * page_table: [batch_size][max_pages_per_seq] int32 page ids
+ * The chunk's key r of sequence b (r - buffer_row_offsets[chunk][b] = i) is
+ * the cache row of context position j = cache_offsets[chunk][b] + i, on page
+ * page_table[b][j / page_size], row j % page_size.  k_nope and v stay
+ * buffer rows.  num_pages * page_size must be < 2^31.
+ * Device errors add MLA_DEV_BAD_PAGE: a key's page index is >= max_pages_per_seq
+ * or its page id is outside [0, num_pages); that key's score is meaningless.
+ */
+mla_status_t mla_prefill_attention_paged(void* out, float* lse, float* o_acc, float* lse_acc,
+                                         const void* q, const void* k_nope, const void* v,
+                                         const void* kv_cache, const int32_t* page_table,
+                                         int32_t num_pages, int32_t page_size,
+                                         int32_t max_pages_per_seq,
+                                         const uint32_t* input_row_offsets,
+                                         const uint32_t* cache_lengths,
+                                         const uint32_t* buffer_row_offsets,
+                                         const uint32_t* cache_offsets,
+                                         const int32_t* buffer_lengths, int32_t chunk,
+                                         int32_t max_chunks, int32_t batch_size,
+                                         int32_t num_heads, int32_t max_prompt_len,
+                                         int32_t total_q_tokens, uint32_t buffer_token_size,
+                                         float scale, float q_scale, float k_scale,
+                                         float v_scale, int32_t dtype, int32_t* d_status,
+                                         mla_stream_t stream);
+
+/*
  * Prefill attention for one plan chunk without caller scratch.  The pages have
  * no counterpart to this entry point.
  *

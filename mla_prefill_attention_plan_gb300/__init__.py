@@ -50,6 +50,9 @@ SIGNATURES = {
     "mla_upproject": (_I, [_P, _P, _P, _P, _P, _P, _I, _U, _I, _I, _F, _F, _F, _P, _P]),
     "mla_prefill_attention": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                    _I, _I, _I, _I, _I, _I, _U, _F, _F, _F, _F, _I, _P, _P]),
+    "mla_prefill_attention_paged": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P,
+                                         _P, _P, _I, _I, _I, _I, _I, _I, _U, _F, _F, _F, _F, _I,
+                                         _P, _P]),
     "mla_prefill_attention_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                            _I, _I, _I, _I, _I, _I, _U, _F, _F, _F, _F, _I, _P,
                                            _P]),
@@ -176,6 +179,22 @@ def mla_prefill_attention(out, lse, o_acc, lse_acc, q, k_nope, v, k_rope, input_
     return load().mla_prefill_attention(
         _ptr(out), _ptr(lse), _ptr(o_acc), _ptr(lse_acc), _ptr(q), _ptr(k_nope), _ptr(v),
         _ptr(k_rope), _ptr(input_row_offsets), _ptr(cache_lengths), _ptr(buffer_row_offsets),
+        _ptr(cache_offsets), _ptr(buffer_lengths), chunk, max_chunks, batch_size, num_heads,
+        max_prompt_len, total_q_tokens, buffer_token_size, scale, q_scale, k_scale, v_scale,
+        dtype, _ptr(d_status), _stream(stream))
+
+
+def mla_prefill_attention_paged(out, lse, o_acc, lse_acc, q, k_nope, v, kv_cache, page_table,
+                                num_pages, page_size, max_pages_per_seq, input_row_offsets,
+                                cache_lengths, buffer_row_offsets, cache_offsets, buffer_lengths,
+                                chunk, max_chunks, batch_size, num_heads, max_prompt_len,
+                                total_q_tokens, buffer_token_size, scale, q_scale=1.0,
+                                k_scale=1.0, v_scale=1.0, dtype=MLA_BF16, d_status=None,
+                                stream=None) -> int:
+    return load().mla_prefill_attention_paged(
+        _ptr(out), _ptr(lse), _ptr(o_acc), _ptr(lse_acc), _ptr(q), _ptr(k_nope), _ptr(v),
+        _ptr(kv_cache), _ptr(page_table), num_pages, page_size, max_pages_per_seq,
+        _ptr(input_row_offsets), _ptr(cache_lengths), _ptr(buffer_row_offsets),
         _ptr(cache_offsets), _ptr(buffer_lengths), chunk, max_chunks, batch_size, num_heads,
         max_prompt_len, total_q_tokens, buffer_token_size, scale, q_scale, k_scale, v_scale,
         dtype, _ptr(d_status), _stream(stream))

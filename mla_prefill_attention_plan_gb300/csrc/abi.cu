@@ -236,9 +236,12 @@ mla_status_t mla_upproject(void* k_nope, void* v, const void* c_kv_buf, const vo
   return from_cuda(launch_upproject(a, static_cast<cudaStream_t>(stream)));
 }
 
+// k_rope from the [S][64] buffer, or (kv_cache given) from the paged cache.
 static mla_status_t attention_impl(void* out, float* lse, float* o_acc, float* lse_acc,
                                    const void* q, const void* k_nope, const void* v,
-                                   const void* k_rope, const uint32_t* iro,
+                                   const void* k_rope, const void* kv_cache,
+                                   const int32_t* page_table, int32_t num_pages, int32_t page_size,
+                                   int32_t max_pages, const uint32_t* iro,
                                    const uint32_t* cache_lengths, const uint32_t* bro,
                                    const uint32_t* co, const int32_t* bl, int32_t chunk,
                                    int32_t max_chunks, int32_t B, int32_t H,
@@ -247,11 +250,19 @@ static mla_status_t attention_impl(void* out, float* lse, float* o_acc, float* l
                                    int32_t* d_status, cudaStream_t stream) {
   if (!dtype_ok(dtype)) return MLA_ERR_DTYPE;
   if (H < 1) return MLA_ERR_GEOMETRY;
-  if (!out || !q || !k_nope || !v || !k_rope || !iro || !cache_lengths || !bro || !co || !bl ||
-      !aligned16(out) || !aligned16(q) || !aligned16(k_nope) || !aligned16(v) ||
-      !aligned16(k_rope) || B < 1 || T_q < 0 || max_prompt_len < 0 || chunk < 0 ||
-      chunk >= max_chunks || S == 0 || S > 0x7FFFFFFFu)
+  if (!out || !q || !k_nope || !v || !iro || !cache_lengths || !bro || !co || !bl ||
+      !aligned16(out) || !aligned16(q) || !aligned16(k_nope) || !aligned16(v) || B < 1 ||
+      T_q < 0 || max_prompt_len < 0 || chunk < 0 || chunk >= max_chunks || S == 0 ||
+      S > 0x7FFFFFFFu)
     return MLA_ERR_ARG;
+  if (kv_cache) {
+    // cache rows are addressed as int32 tensor-map coordinates
+    if (!aligned16(kv_cache) || !page_table || num_pages < 1 || page_size < 1 || max_pages < 1 ||
+        static_cast<int64_t>(num_pages) * page_size > 0x7FFFFFFFll)
+      return MLA_ERR_ARG;
+  } else if (!k_rope || !aligned16(k_rope)) {
+    return MLA_ERR_ARG;
+  }
   if (max_chunks > 1 && (!o_acc || !lse_acc || !aligned16(o_acc))) return MLA_ERR_ARG;
   if (T_q == 0 || max_prompt_len == 0) return MLA_OK;
   AttnArgs a;
@@ -262,7 +273,12 @@ static mla_status_t attention_impl(void* out, float* lse, float* o_acc, float* l
   a.q = q;
   a.k_nope = k_nope;
   a.v = v;
-  a.k_rope = k_rope;
+  a.k_rope = kv_cache ? nullptr : k_rope;
+  a.kv_cache = kv_cache;
+  a.page_table = page_table;
+  a.num_pages = num_pages;
+  a.page_size = page_size;
+  a.max_pages = max_pages;
   a.iro = iro;
   a.cache_len = cache_lengths;
   a.bro = bro;
@@ -293,10 +309,36 @@ mla_status_t mla_prefill_attention(void* out, float* lse, float* o_acc, float* l
                                    int32_t total_q_tokens, uint32_t buffer_token_size,
                                    float scale, float q_scale, float k_scale, float v_scale,
                                    int32_t dtype, int32_t* d_status, mla_stream_t stream) {
-  return attention_impl(out, lse, o_acc, lse_acc, q, k_nope, v, k_rope, input_row_offsets,
-                        cache_lengths, buffer_row_offsets, cache_offsets, buffer_lengths, chunk,
-                        max_chunks, batch_size, num_heads, max_prompt_len, total_q_tokens,
-                        buffer_token_size, scale, q_scale, k_scale, v_scale, dtype, d_status,
+  if (!k_rope) return MLA_ERR_ARG;
+  return attention_impl(out, lse, o_acc, lse_acc, q, k_nope, v, k_rope, nullptr, nullptr, 0, 0, 0,
+                        input_row_offsets, cache_lengths, buffer_row_offsets, cache_offsets,
+                        buffer_lengths, chunk, max_chunks, batch_size, num_heads, max_prompt_len,
+                        total_q_tokens, buffer_token_size, scale, q_scale, k_scale, v_scale, dtype,
+                        d_status, static_cast<cudaStream_t>(stream));
+}
+
+mla_status_t mla_prefill_attention_paged(void* out, float* lse, float* o_acc, float* lse_acc,
+                                         const void* q, const void* k_nope, const void* v,
+                                         const void* kv_cache, const int32_t* page_table,
+                                         int32_t num_pages, int32_t page_size,
+                                         int32_t max_pages_per_seq,
+                                         const uint32_t* input_row_offsets,
+                                         const uint32_t* cache_lengths,
+                                         const uint32_t* buffer_row_offsets,
+                                         const uint32_t* cache_offsets,
+                                         const int32_t* buffer_lengths, int32_t chunk,
+                                         int32_t max_chunks, int32_t batch_size,
+                                         int32_t num_heads, int32_t max_prompt_len,
+                                         int32_t total_q_tokens, uint32_t buffer_token_size,
+                                         float scale, float q_scale, float k_scale,
+                                         float v_scale, int32_t dtype, int32_t* d_status,
+                                         mla_stream_t stream) {
+  if (!kv_cache) return MLA_ERR_ARG;
+  return attention_impl(out, lse, o_acc, lse_acc, q, k_nope, v, nullptr, kv_cache, page_table,
+                        num_pages, page_size, max_pages_per_seq, input_row_offsets, cache_lengths,
+                        buffer_row_offsets, cache_offsets, buffer_lengths, chunk, max_chunks,
+                        batch_size, num_heads, max_prompt_len, total_q_tokens, buffer_token_size,
+                        scale, q_scale, k_scale, v_scale, dtype, d_status,
                         static_cast<cudaStream_t>(stream));
 }
 
@@ -350,8 +392,8 @@ mla_status_t mla_prefill(void* out, float* lse, const void* q, const uint32_t* i
     st = mla_upproject(ws + L.knope, ws + L.v, ws + L.ckv, w_k, w_uv, bl, c, buffer_token_size,
                        num_heads, dtype, ckv_scale, w_scale, kv_inv, d_status, stream_);
     if (st != MLA_OK) return st;
-    st = attention_impl(out, lse, oacc, lseacc, q, ws + L.knope, ws + L.v, ws + L.krope,
-                        input_row_offsets, cache_lengths, bro, co, bl, c, max_chunks, batch_size,
+    st = attention_impl(out, lse, oacc, lseacc, q, ws + L.knope, ws + L.v, ws + L.krope, nullptr,
+                        nullptr, 0, 0, 0, input_row_offsets, cache_lengths, bro, co, bl, c, max_chunks, batch_size,
                         num_heads, max_prompt_len, total_q_tokens, buffer_token_size, scale,
                         q_scale, kv_descale, kv_descale, dtype, d_status, stream);
     if (st != MLA_OK) return st;

@@ -90,6 +90,25 @@ struct PairItem {
 // kernels walk all units and skip the empty ones.
 constexpr int kMaxUnits = 4096;
 
+// 64 rows of a one-row-box tensor map into consecutive box rows at `dst`
+// (row_bytes apart, swizzled as one tile): lane l holds rows l (ra) and
+// l + 32 (rb); lanes 0..15 each issue one tile::gather4 of rows 4l..4l+3.
+// The caller has registered the bytes on `bar` already.
+__device__ __forceinline__ void gather_rows64(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int ra,
+                                              int rb, int row_bytes) {
+  const int lane = threadIdx.x & 31;
+  int y[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int key = 4 * (lane & 15) + k;
+    const int va = __shfl_sync(0xffffffffu, ra, key & 31);
+    const int vb = __shfl_sync(0xffffffffu, rb, key & 31);
+    y[k] = key < 32 ? va : vb;
+  }
+  if (lane < 16) tma_gather4_2d(dst + lane * 4 * row_bytes, map, bar, x, y[0], y[1], y[2], y[3]);
+  __syncwarp();
+}
+
 struct WorkList {
   const uint32_t* units;   // shared memory
   int n;                   // units with work, or -1: walk all units
@@ -239,18 +258,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
         const uint32_t gj = g + j;
         const int row = it.own.kv_row0 + j * BN + static_cast<int>(rank) * 64;
         const int ks = gj % PNK;
+        // Paged k_rope: the cache rows of this half tile's 64 keys (two a
+        // lane), read before the stage wait so their latency overlaps it.
+        int ra = 0, rb = 0;
+        if (p.paged) {
+          const int k0 = j * BN + static_cast<int>(rank) * 64;
+          ra = paged_key_row(p, it.own, k0 + lane);
+          rb = paged_key_row(p, it.own, k0 + 32 + lane);
+        }
         if (gj >= PNK &&
             !(ok = mbar_wait_cluster_warp(smem_u32(&sh->k_empty[ks]), ((gj / PNK) & 1) ^ 1, status, abort_flag)))
           break;
+        const uint32_t kf = smem_u32(&sh->k_full[ks]);
+        const uint32_t kdst = smem_u32(smem + P_SMEM_K + ks * PK_BYTES);
         if (elect_one()) {
-          const uint32_t kf = smem_u32(&sh->k_full[ks]);
           mbar_expect_tx(kf, PK_BYTES);
-          const uint32_t kdst = smem_u32(smem + P_SMEM_K + ks * PK_BYTES);
           tma_load_2d(kdst, &kn_map, kf, it.own.h * 128, row);
           tma_load_2d(kdst + HBLK, &kn_map, kf, it.own.h * 128 + 64, row);
-          tma_load_2d(kdst + 2 * HBLK, &kr_map, kf, 0, row);
+          if (!p.paged) tma_load_2d(kdst + 2 * HBLK, &kr_map, kf, 0, row);
         }
         __syncwarp();
+        if (p.paged) gather_rows64(kdst + 2 * HBLK, &kr_map, kf, 512, ra, rb, 128);
         k_last[ks] = int((gj / PNK) & 1);
       }
       g += it.n_kv;
@@ -693,17 +721,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
         const uint32_t gj = g + j;
         const int row = it.own.kv_row0 + j * BN + static_cast<int>(rank) * 64;
         const int ks = gj % PNK;
+        int ra = 0, rb = 0;   // paged k_rope: the half tile's cache rows (see the bf16 kernel)
+        if (p.paged) {
+          const int k0 = j * BN + static_cast<int>(rank) * 64;
+          ra = paged_key_row(p, it.own, k0 + lane);
+          rb = paged_key_row(p, it.own, k0 + 32 + lane);
+        }
         if (gj >= PNK &&
             !(ok = mbar_wait_cluster_warp(smem_u32(&sh->k_empty[ks]), ((gj / PNK) & 1) ^ 1, status, abort_flag)))
           break;
+        const uint32_t kf = smem_u32(&sh->k_full[ks]);
+        const uint32_t kdst = smem_u32(smem + E_SMEM_K + ks * EK_BYTES);
         if (elect_one()) {
-          const uint32_t kf = smem_u32(&sh->k_full[ks]);
           mbar_expect_tx(kf, EK_BYTES);
-          const uint32_t kdst = smem_u32(smem + E_SMEM_K + ks * EK_BYTES);
           tma_load_2d(kdst, &kn_map, kf, it.own.h * 128, row);      // nope: 64 keys x 128 B
-          tma_load_2d(kdst + EKN_BYTES, &kr_map, kf, 0, row);      // rope: 64 keys x 64 B
+          if (!p.paged) tma_load_2d(kdst + EKN_BYTES, &kr_map, kf, 0, row);   // rope: 64 keys x 64 B
         }
         __syncwarp();
+        if (p.paged) gather_rows64(kdst + EKN_BYTES, &kr_map, kf, 512, ra, rb, 64);
         k_last[ks] = int((gj / PNK) & 1);
       }
       g += it.n_kv;
@@ -1058,9 +1093,12 @@ cudaError_t launch_attention_pair(const AttnArgs& a, cudaStream_t stream) {
   const uint64_t QW = static_cast<uint64_t>(a.H) * 192;
   const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUtensorMap maps[4];
+  const bool paged = a.kv_cache != nullptr;
+  const uint64_t cache_rows = static_cast<uint64_t>(a.num_pages) * a.page_size;
   const bool ok = encode_2d(&maps[0], a.q, dt, QW, a.T_q, QW * 2, 64, BM, CU_TENSOR_MAP_SWIZZLE_128B) &&
                   encode_2d(&maps[1], a.k_nope, dt, HN, a.S, HN * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
-                  encode_2d(&maps[2], a.k_rope, dt, 64, a.S, 128, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+                  (paged ? encode_2d(&maps[2], a.kv_cache, dt, 576, cache_rows, 1152, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B)
+                         : encode_2d(&maps[2], a.k_rope, dt, 64, a.S, 128, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)) &&
                   encode_2d(&maps[3], a.v, dt, HN, a.S, HN * 2, 64, BN, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return cudaErrorInvalidValue;
   Params p;
@@ -1083,6 +1121,11 @@ cudaError_t launch_attention_pair(const AttnArgs& a, cudaStream_t stream) {
   p.v_scale = a.v_scale;
   p.status = a.status;
   p.T_q = a.T_q;
+  p.paged = a.kv_cache != nullptr ? 1 : 0;
+  p.page_table = a.page_table;
+  p.page_size = a.page_size;
+  p.max_pages = a.max_pages;
+  p.num_pages = a.num_pages;
   const long long total = static_cast<long long>((p.n_qtiles + 1) / 2) * a.B * a.H;
   if (total <= 0) return cudaSuccess;
   int dev = 0;
@@ -1105,7 +1148,10 @@ cudaError_t launch_attention_pair_e4m3(const AttnArgs& a, cudaStream_t stream) {
       encode_2d(&maps[0], a.q, u8, QW, a.T_q, QW, 128, BM, CU_TENSOR_MAP_SWIZZLE_128B) &&    // Q nope
       encode_2d(&maps[1], a.q, u8, QW, a.T_q, QW, 64, BM, CU_TENSOR_MAP_SWIZZLE_64B) &&      // Q rope
       encode_2d(&maps[2], a.k_nope, u8, HN, a.S, HN, 128, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
-      encode_2d(&maps[3], a.k_rope, u8, 64, a.S, 64, 64, 64, CU_TENSOR_MAP_SWIZZLE_64B) &&
+      (a.kv_cache != nullptr
+           ? encode_2d(&maps[3], a.kv_cache, u8, 576, static_cast<uint64_t>(a.num_pages) * a.page_size, 576, 64, 1,
+                       CU_TENSOR_MAP_SWIZZLE_64B)
+           : encode_2d(&maps[3], a.k_rope, u8, 64, a.S, 64, 64, 64, CU_TENSOR_MAP_SWIZZLE_64B)) &&
       encode_2d(&maps[4], a.v, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, HN, a.S, HN * 2, 64, BN,
                 CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return cudaErrorInvalidValue;
@@ -1130,6 +1176,11 @@ cudaError_t launch_attention_pair_e4m3(const AttnArgs& a, cudaStream_t stream) {
   p.v_scale = a.v_scale;
   p.status = a.status;
   p.T_q = a.T_q;
+  p.paged = a.kv_cache != nullptr ? 1 : 0;
+  p.page_table = a.page_table;
+  p.page_size = a.page_size;
+  p.max_pages = a.max_pages;
+  p.num_pages = a.num_pages;
   const long long total = static_cast<long long>((p.n_qtiles + 1) / 2) * a.B * a.H;
   if (total <= 0) return cudaSuccess;
   int dev = 0;

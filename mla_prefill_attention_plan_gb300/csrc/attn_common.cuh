@@ -24,6 +24,10 @@ struct Params {
   const int32_t* bl;
   int chunk, B, H, n_qtiles, head_group;
   int T_q;            // rows of q / out / lse: no query row at or past it is read or written
+  // k_rope straight from the paged cache (paged != 0): key i of an item is the
+  // cache row of context position co + i of its sequence.
+  const int32_t* page_table;
+  int page_size, max_pages, num_pages, paged;
   float scale_log2;   // softmax scale * descales * log2(e)
   float v_scale;
   int32_t* status;
@@ -79,6 +83,21 @@ __device__ __forceinline__ bool tile_item(const Params& p, int b, int h, int qt,
   const long long nkeys = min(static_cast<long long>(it.n_cb), last + 1);
   it.n_kv = static_cast<int>((nkeys + BN - 1) / BN);
   return true;
+}
+
+// Physical cache row of the chunk's key `k` (0-based within the sequence's
+// keys in this chunk) of the item's sequence, or 0 for a key past them or a
+// page out of range (reported; those keys' scores are then not meaningful).
+__device__ __forceinline__ int paged_key_row(const Params& p, const Item& it, int k) {
+  if (k >= it.n_cb) return 0;
+  const long long pos = static_cast<long long>(it.co) + k;
+  const long long pi = pos / p.page_size;
+  const int page = pi < p.max_pages ? __ldg(p.page_table + static_cast<long long>(it.b) * p.max_pages + pi) : -1;
+  if (page < 0 || page >= p.num_pages) {
+    set_status(p.status, MLA_DEV_BAD_PAGE);
+    return 0;
+  }
+  return static_cast<int>(static_cast<long long>(page) * p.page_size + pos % p.page_size);
 }
 
 // Epilogue of one query row: O / l, this chunk's natural-log LSE, merge with

@@ -61,7 +61,10 @@ struct AttnArgs {
   const void* q;
   const void* k_nope;
   const void* v;
-  const void* k_rope;
+  const void* k_rope;           // [S][64] buffer, or null when k_rope comes from the paged cache
+  const void* kv_cache = nullptr;  // paged cache [num_pages][page_size][576] (k_rope = columns 512..575)
+  const int32_t* page_table = nullptr;  // [B][max_pages]
+  int num_pages = 0, page_size = 0, max_pages = 0;
   const uint32_t* iro;
   const uint32_t* cache_len;
   const uint32_t* bro;
@@ -93,7 +96,7 @@ struct DecodeArgs {
   const void* q;              // [T][H][192] bf16
   const void* kv_cache;       // [num_pages][page_size][576] bf16
   const int32_t* page_table;  // [B][max_pages]
-  int num_pages, page_size, max_pages;
+  int num_pages = 0, page_size = 0, max_pages = 0;
   const void* w_uk;           // [H][512][128] bf16
   const void* w_uv;           // [H][128][512] bf16
   const uint32_t* iro;

@@ -81,6 +81,34 @@ def test_host_argument_errors(lib):
     assert mla.mla_prefill_attention(*args, stream=s) == mla.MLA_ERR_ARG
 
 
+def test_paged_attention_host_argument_errors(lib):
+    s = 1
+    # out, lse, o_acc, lse_acc, q, k_nope, v, kv_cache, page_table, num_pages, page_size,
+    # max_pages, iro, cache_lengths, bro, co, bl, chunk, max_chunks, B, H, max_prompt_len, T, S, scale
+    ok = [16, None, None, None, 16, 16, 16, 16, 16, 4, 16, 2, 16, 16, 16, 16, 16, 0, 1, 1, 4, 16,
+          16, 8, 0.1]
+    names = ["out", "lse", "oacc", "lacc", "q", "kn", "v", "kv", "pt", "np", "ps", "mp", "iro", "cl",
+             "bro", "co", "bl", "ch", "mc", "B", "H", "mpl", "T", "S", "scale"]
+
+    def call(**change):
+        a = list(ok)
+        for k, v in change.items():
+            a[names.index(k)] = v
+        return mla.mla_prefill_attention_paged(*a, stream=s)
+    assert call(kv=None) == mla.MLA_ERR_ARG
+    assert call(kv=24) == mla.MLA_ERR_ARG              # misaligned cache
+    assert call(pt=None) == mla.MLA_ERR_ARG
+    assert call(np=0) == mla.MLA_ERR_ARG
+    assert call(ps=0) == mla.MLA_ERR_ARG
+    assert call(mp=0) == mla.MLA_ERR_ARG
+    assert call(np=1 << 20, ps=1 << 11) == mla.MLA_ERR_ARG   # 2^31 cache rows
+    assert call(H=0) == mla.MLA_ERR_GEOMETRY
+    assert call(mc=2) == mla.MLA_ERR_ARG               # merge scratch missing
+    # the buffered entry point still wants its k_rope buffer
+    args = [16, None, None, None, 16, 16, 16, None] + [16] * 5 + [0, 1, 1, 4, 16, 16, 8, 0.1]
+    assert mla.mla_prefill_attention(*args, stream=s) == mla.MLA_ERR_ARG
+
+
 def test_selftest_host_argument_errors(lib):
     s = 1
     assert mla.mla_selftest_bounded_wait(None, 16, 5_000_000, 2, s) == mla.MLA_ERR_ARG

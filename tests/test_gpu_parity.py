@@ -586,6 +586,102 @@ def test_head_split_equals_full_call_bit_for_bit():
     assert torch.equal(torch.cat([lo_l, hi_l], 1), full_l)
 
 
+def _paged_attention_case(w, seed_base=41, oracle=True, bad_page=False):
+    """mla_prefill_attention_paged, k_rope read from the paged cache, chunk by
+    chunk: (1) bit for bit equal to mla_prefill_attention given the gathered
+    k_rope rows (the masked keys past a sequence read other rows in the two
+    calls and must change nothing), and (2) against the oracle, whose k_rope
+    for a key is the cache row of its context position."""
+    inp = make_inputs(w)
+    dt = w.dtype
+    c = {k: O.codes(inp[k]) for k in ("q", "input_row_offsets", "cache_lengths", "kv_cache",
+                                      "page_table")}
+    S, mc, B, H, T = w.buffer_token_size, w.max_chunks, inp["B"], w.H, inp["T_q"]
+    plan = O.prefill_plan(c["input_row_offsets"], c["cache_lengths"], S, mc)
+    g = gpu_plan(c["input_row_offsets"], c["cache_lengths"], S, mc)
+    tabs = [torch.as_tensor(x.astype(np.int32)).to(DEV) for x in g[:3]]
+    kv, pt = inp["kv_cache"].to(DEV), inp["page_table"].to(DEV)
+    if bad_page:
+        pt[B - 1, 0] = inp["num_pages"]
+    q = inp["q"].to(DEV)
+    iro, cl = inp["input_row_offsets"].to(DEV), inp["cache_lengths"].to(DEV)
+    paging = (inp["num_pages"], inp["page_size"], inp["max_pages"])
+    res = {}
+    for mode in ("paged",) if bad_page else ("buffer", "paged"):
+        out = torch.full((T, H, 128), float("nan"), dtype=torch.bfloat16, device=DEV)
+        lse = torch.full((T, H), float("nan"), dtype=torch.float32, device=DEV)
+        oacc = torch.empty(T, H, 128, dtype=torch.float32, device=DEV)
+        lacc = torch.empty(T, H, dtype=torch.float32, device=DEV)
+        st = torch.zeros(1, dtype=torch.int32, device=DEV)
+        for ch in range(mc):
+            kn, vv, _ = (t.to(DEV) for t in make_attention_operands(w, S, seed_offset=seed_base + ch))
+            if mode == "buffer":
+                ckv = torch.zeros(S, 512, dtype=kv.dtype, device=DEV)
+                kr = torch.zeros(S, 64, dtype=kv.dtype, device=DEV)
+                mla.check(mla.mla_gather_latent(ckv, kr, kv, pt, *paging, *tabs, ch, B, S, _dt(w), st))
+                mla.check(mla.mla_prefill_attention(out, lse, oacc, lacc, q, kn, vv, kr, iro, cl, *tabs,
+                                                    ch, mc, B, H, inp["max_prompt_len"], T, S,
+                                                    inp["scale"], dtype=_dt(w), d_status=st))
+            else:
+                mla.check(mla.mla_prefill_attention_paged(out, lse, oacc, lacc, q, kn, vv, kv, pt,
+                                                          *paging, iro, cl, *tabs, ch, mc, B, H,
+                                                          inp["max_prompt_len"], T, S, inp["scale"],
+                                                          dtype=_dt(w), d_status=st))
+        torch.cuda.synchronize()
+        res[mode] = (out, lse, int(st.item()))
+    if bad_page:
+        assert res["paged"][2] == mla.MLA_DEV_BAD_PAGE
+        return None
+    assert res["buffer"][2] == 0 and res["paged"][2] == 0
+    assert torch.equal(res["buffer"][0].view(torch.int16), res["paged"][0].view(torch.int16))
+    assert torch.equal(res["buffer"][1], res["paged"][1])
+    if not oracle:
+        return None
+
+    def operands(ch):
+        kn, vv, _ = make_attention_operands(w, S, seed_offset=seed_base + ch)
+        _, kr, ost = O.gather_latent(c["kv_cache"], c["page_table"], inp["page_size"], plan, ch)
+        assert ost == 0
+        v64 = vv.double().numpy() if dt == "e4m3" else O.decode(O.codes(vv), dt)
+        return (O.decode(O.codes(kn), dt), O.decode(kr, dt), v64)
+    ref = O.attention_over_chunks(O.decode(c["q"], dt), operands, plan, c["input_row_offsets"],
+                                  c["cache_lengths"], inp["scale"])
+    return _compare(res["paged"][0], ref, dt, res["paged"][1])
+
+
+def test_paged_attention_shuffled_pages_multi_chunk(bf16_kernel):
+    """Shuffled 16-row pages (a 64-key half tile spans four pages), ragged
+    sequences, several chunks."""
+    w = scaled(WORKLOADS["ragged_chunked_cache"], H=2, B=3, buffer_token_size=700, max_chunks=4,
+               new_range=(100, 600), cache_range=(0, 900), page_size=16)
+    _paged_attention_case(w)
+
+
+def test_paged_attention_one_row_pages(bf16_kernel):
+    """page_size 1: every key on a page of its own."""
+    w = scaled(WORKLOADS["tiny_ragged"], page_size=1, shuffle_pages=True)
+    _paged_attention_case(w)
+
+
+def test_paged_attention_e4m3():
+    w = scaled(WORKLOADS["longctx_fp8"], H=2, B=2, new_lens=(300, 41), cache_lens=(200, 0),
+               buffer_token_size=192, max_chunks=3, page_size=64, shuffle_pages=True)
+    _paged_attention_case(w)
+
+
+@pytest.mark.parametrize("name", ["ragged_chunked_cache", "longctx_fp8"])
+def test_paged_attention_full_size_equals_buffered(name):
+    """The full-size workloads (seeded shuffled pages, every chunk): the paged
+    call equals the buffered call bit for bit; the buffered call's own
+    parity with the oracle at these sizes is covered by the fused tests."""
+    _paged_attention_case(WORKLOADS[name], oracle=False)
+
+
+def test_paged_attention_bad_page_reports_status():
+    w = scaled(WORKLOADS["tiny_ragged"], page_size=16)
+    _paged_attention_case(w, bad_page=True)
+
+
 def test_attention_stage_e4m3_multi_chunk():
     w = scaled(WORKLOADS["longctx_fp8"], H=2, B=2, new_lens=(300, 41), cache_lens=(200, 0),
                buffer_token_size=192, max_chunks=3, page_size=64)
