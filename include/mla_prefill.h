@@ -3,8 +3,8 @@
  * Multi-head Latent Attention (MLA) prefill over a paged latent KV cache.
  *
  * The path has four stages, each an entry point below, plus a fused entry
- * point that runs them all, and the step in front of it that writes the new
- * tokens' latent rows into the paged cache:
+ * point that runs plan, 3' and 4', and the step in front of it that writes
+ * the new tokens' latent rows into the paged cache:
  *   0. mla_latent_cache_write -- RMSNorm + RoPE + paged store
  *                                ("mla_prefill_decode_graph_bf16", Args:
  *                                 freqs_cis, kv_norm_gamma, epsilon)
@@ -15,6 +15,9 @@
  *                                                 Args: w_k, w_uv)
  *   4. mla_prefill_attention  -- causal attention with LSE merge across chunks
  *                                                ("flare_mla_prefill_dispatch")
+ *   3'. mla_upproject_paged, 4'. mla_prefill_attention_paged -- stages 3 and 4
+ *       reading the latent and k_rope rows straight from the paged cache, so
+ *       that stage 2 (a copy) is not needed on the fused path.
  *
  * Conventions shared by every entry point
  *   - Every pointer argument is a DEVICE pointer owned by the caller, unless
@@ -248,6 +251,32 @@ mla_status_t mla_upproject(void* k_nope, void* v, const void* c_kv_buf, const vo
                            int32_t* d_status, mla_stream_t stream);
 
 /*
+ * 3'. Up-projection of one plan chunk with the c_kv rows read straight from
+ * the paged cache ("mla_prefill_decode_graph_bf16", Args: w_k, w_uv, and the
+ * kv_collection the prefill branch reads the chunk's latent rows from).  The
+ * result equals mla_gather_latent followed by mla_upproject, without the c_kv
+ * buffer in between.
+ *
+ * Arguments as in mla_upproject, with c_kv_buf replaced by the cache and the
+ * plan tables that locate the chunk's rows in it (as mla_gather_latent takes
+ * them): buffer row r of sequence b (buffer_row_offsets[chunk][b] <= r <
+ * buffer_row_offsets[chunk][b+1]) is the cache row of context position
+ * cache_offsets[chunk][b] + r - buffer_row_offsets[chunk][b].  buffer_lengths
+ * is required here; batch_size >= 1; num_pages * page_size must be < 2^31.
+ * Errors: as mla_upproject, plus device MLA_DEV_BAD_PAGE for a position
+ * outside the page table or a page id outside [0, num_pages) (that row's
+ * outputs are then meaningless).
+ */
+mla_status_t mla_upproject_paged(void* k_nope, void* v, const void* kv_cache,
+                                 const int32_t* page_table, int32_t num_pages, int32_t page_size,
+                                 int32_t max_pages_per_seq, const uint32_t* buffer_row_offsets,
+                                 const uint32_t* cache_offsets, const int32_t* buffer_lengths,
+                                 int32_t chunk, int32_t batch_size, uint32_t buffer_token_size,
+                                 const void* w_k, const void* w_uv, int32_t num_heads,
+                                 int32_t dtype, float ckv_scale, float w_scale,
+                                 float kv_out_inv_scale, int32_t* d_status, mla_stream_t stream);
+
+/*
  * 4. Prefill attention for one plan chunk.  Follows "flare_mla_prefill_dispatch"
  * (Args: output [total_q_tokens, num_heads, v_depth]; q [total_q_tokens,
  * num_heads, q_depth]; k, v (ragged K nope and V); k_rope [cache_len, 1,
@@ -378,8 +407,8 @@ mla_status_t mla_prefill_attention_noalloc(void* out, float* lse, const void* q,
 
 /*
  * Workspace bytes needed by mla_prefill for these sizes (plan tables, the
- * chunk's latent, k_rope, K and V buffers, and the fp32 merge state when
- * max_chunks > 1).  The buffers follow "mla_prefill_decode_graph_bf16" (Args:
+ * chunk's K and V buffers, and the fp32 merge state when max_chunks > 1; the
+ * latent and k_rope rows are read from the cache in place).  The buffers follow "mla_prefill_decode_graph_bf16" (Args:
  * buffer_row_offsets, cache_offsets, buffer_length) and
  * "flare_mla_prefill_dispatch" (Args: k, v, k_rope); the pages size none of
  * them, so this call has no counterpart there.  Host only; returns 0 for
@@ -391,10 +420,14 @@ size_t mla_prefill_workspace_bytes(int32_t batch_size, int32_t num_heads,
                                    uint32_t buffer_token_size, int32_t dtype);
 
 /*
- * Fused path: plan, then for every chunk c < max_chunks gather, up-project and
- * attend, all enqueued on `stream` with no host synchronisation (chunks the
- * plan leaves unused exit on the device).  Follows the prefill branch of
- * "mla_prefill_decode_graph_bf16" with the tables of "mla_prefill_plan".
+ * Fused path: plan, then for every chunk c < max_chunks up-project
+ * (mla_upproject_paged) and attend (mla_prefill_attention_paged), all enqueued
+ * on `stream` with no host synchronisation (chunks the plan leaves unused exit
+ * on the device).  Follows the prefill branch of "mla_prefill_decode_graph_bf16"
+ * with the tables of "mla_prefill_plan"; the chunk's latent rows are read from
+ * the cache by the projection itself instead of being gathered into a buffer
+ * first (the result is the same: the gather is a copy).  Errors add
+ * MLA_ERR_ARG for num_pages * page_size >= 2^31.
  *
  * out [total_q_tokens][num_heads][128] bf16 output; lse [total_q_tokens]
  * [num_heads] fp32 output or NULL.  Inputs as in the stage entry points.  For

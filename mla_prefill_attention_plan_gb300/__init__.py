@@ -48,6 +48,8 @@ SIGNATURES = {
                                     _F, _F, _I, _P, _P]),
     "mla_gather_latent": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _I, _I, _U, _I, _P, _P]),
     "mla_upproject": (_I, [_P, _P, _P, _P, _P, _P, _I, _U, _I, _I, _F, _F, _F, _P, _P]),
+    "mla_upproject_paged": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _I, _I, _U, _P, _P, _I, _I,
+                                 _F, _F, _F, _P, _P]),
     "mla_prefill_attention": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                    _I, _I, _I, _I, _I, _I, _U, _F, _F, _F, _F, _I, _P, _P]),
     "mla_prefill_attention_paged": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P,
@@ -169,6 +171,18 @@ def mla_upproject(k_nope, v, c_kv_buf, w_k, w_uv, buffer_lengths, chunk, buffer_
                                 _ptr(buffer_lengths), chunk, buffer_token_size, num_heads, dtype,
                                 ckv_scale, w_scale, kv_out_inv_scale, _ptr(d_status),
                                 _stream(stream))
+
+
+def mla_upproject_paged(k_nope, v, kv_cache, page_table, num_pages, page_size, max_pages_per_seq,
+                        buffer_row_offsets, cache_offsets, buffer_lengths, chunk, batch_size,
+                        buffer_token_size, w_k, w_uv, num_heads, dtype=MLA_BF16, ckv_scale=1.0,
+                        w_scale=1.0, kv_out_inv_scale=1.0, d_status=None, stream=None) -> int:
+    return load().mla_upproject_paged(_ptr(k_nope), _ptr(v), _ptr(kv_cache), _ptr(page_table),
+                                      num_pages, page_size, max_pages_per_seq,
+                                      _ptr(buffer_row_offsets), _ptr(cache_offsets),
+                                      _ptr(buffer_lengths), chunk, batch_size, buffer_token_size,
+                                      _ptr(w_k), _ptr(w_uv), num_heads, dtype, ckv_scale, w_scale,
+                                      kv_out_inv_scale, _ptr(d_status), _stream(stream))
 
 
 def mla_prefill_attention(out, lse, o_acc, lse_acc, q, k_nope, v, k_rope, input_row_offsets,

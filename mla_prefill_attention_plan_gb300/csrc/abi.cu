@@ -42,7 +42,7 @@ mla_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_E
 
 // Workspace layout of the fused entry point.
 struct Layout {
-  size_t bro, co, bl, ckv, krope, knope, v, oacc, lseacc, total;
+  size_t bro, co, bl, knope, v, oacc, lseacc, total;
 };
 
 Layout layout(int B, int H, int T_q, int max_chunks, uint32_t S, int dtype) {
@@ -57,8 +57,6 @@ Layout layout(int B, int H, int T_q, int max_chunks, uint32_t S, int dtype) {
   L.bro = take(sizeof(uint32_t) * size_t(max_chunks) * (B + 1));
   L.co = take(sizeof(uint32_t) * size_t(max_chunks) * (B > 0 ? B : 1));
   L.bl = take(sizeof(int32_t) * size_t(max_chunks));
-  L.ckv = take(size_t(S) * 512 * e);
-  L.krope = take(size_t(S) * 64 * e);
   L.knope = take(size_t(S) * H * 128 * e);
   L.v = take(size_t(S) * H * 128 * 2);   // bf16, or f16 holding e4m3-rounded values
   const bool merge = max_chunks > 1;
@@ -209,18 +207,38 @@ mla_status_t mla_gather_latent(void* c_kv_buf, void* k_rope_buf, const void* kv_
                                  elt_bytes(dtype), d_status, static_cast<cudaStream_t>(stream)));
 }
 
-mla_status_t mla_upproject(void* k_nope, void* v, const void* c_kv_buf, const void* w_k,
-                           const void* w_uv, const int32_t* buffer_lengths, int32_t chunk,
-                           uint32_t buffer_token_size, int32_t num_heads, int32_t dtype,
-                           float ckv_scale, float w_scale, float kv_out_inv_scale,
-                           int32_t* d_status, mla_stream_t stream) {
+// A rows from the c_kv buffer, or (kv_cache given) from the paged cache.
+static mla_status_t upproject_impl(void* k_nope, void* v, const void* c_kv_buf,
+                                   const void* kv_cache, const int32_t* page_table,
+                                   int32_t num_pages, int32_t page_size, int32_t max_pages,
+                                   const uint32_t* bro, const uint32_t* co, int32_t B,
+                                   const void* w_k, const void* w_uv,
+                                   const int32_t* buffer_lengths, int32_t chunk,
+                                   uint32_t buffer_token_size, int32_t num_heads, int32_t dtype,
+                                   float ckv_scale, float w_scale, float kv_out_inv_scale,
+                                   int32_t* d_status, mla_stream_t stream) {
   if (!dtype_ok(dtype)) return MLA_ERR_DTYPE;
   if (num_heads < 1) return MLA_ERR_GEOMETRY;
-  if (!k_nope || !v || !c_kv_buf || !w_k || !w_uv || !aligned16(k_nope) || !aligned16(v) ||
-      !aligned16(c_kv_buf) || !aligned16(w_k) || !aligned16(w_uv) || chunk < 0 ||
-      buffer_token_size == 0 || buffer_token_size > 0x7FFFFFFFu)
+  if (!k_nope || !v || !w_k || !w_uv || !aligned16(k_nope) || !aligned16(v) || !aligned16(w_k) ||
+      !aligned16(w_uv) || chunk < 0 || buffer_token_size == 0 || buffer_token_size > 0x7FFFFFFFu)
     return MLA_ERR_ARG;
+  if (kv_cache) {
+    if (!aligned16(kv_cache) || !page_table || !bro || !co || !buffer_lengths || B < 1 ||
+        num_pages < 1 || page_size < 1 || max_pages < 1 ||
+        static_cast<int64_t>(num_pages) * page_size > 0x7FFFFFFFll)
+      return MLA_ERR_ARG;
+  } else if (!c_kv_buf || !aligned16(c_kv_buf)) {
+    return MLA_ERR_ARG;
+  }
   UpprojArgs a;
+  a.kv_cache = kv_cache;
+  a.page_table = page_table;
+  a.bro = bro;
+  a.co = co;
+  a.B = B;
+  a.num_pages = num_pages;
+  a.page_size = page_size;
+  a.max_pages = max_pages;
   a.k_nope = k_nope;
   a.v = v;
   a.c_kv = c_kv_buf;
@@ -234,6 +252,32 @@ mla_status_t mla_upproject(void* k_nope, void* v, const void* c_kv_buf, const vo
   a.out_scale = ckv_scale * w_scale * kv_out_inv_scale;
   a.status = d_status;
   return from_cuda(launch_upproject(a, static_cast<cudaStream_t>(stream)));
+}
+
+mla_status_t mla_upproject(void* k_nope, void* v, const void* c_kv_buf, const void* w_k,
+                           const void* w_uv, const int32_t* buffer_lengths, int32_t chunk,
+                           uint32_t buffer_token_size, int32_t num_heads, int32_t dtype,
+                           float ckv_scale, float w_scale, float kv_out_inv_scale,
+                           int32_t* d_status, mla_stream_t stream) {
+  if (dtype_ok(dtype) && num_heads >= 1 && !c_kv_buf) return MLA_ERR_ARG;
+  return upproject_impl(k_nope, v, c_kv_buf, nullptr, nullptr, 0, 0, 0, nullptr, nullptr, 0, w_k,
+                        w_uv, buffer_lengths, chunk, buffer_token_size, num_heads, dtype,
+                        ckv_scale, w_scale, kv_out_inv_scale, d_status, stream);
+}
+
+mla_status_t mla_upproject_paged(void* k_nope, void* v, const void* kv_cache,
+                                 const int32_t* page_table, int32_t num_pages, int32_t page_size,
+                                 int32_t max_pages_per_seq, const uint32_t* buffer_row_offsets,
+                                 const uint32_t* cache_offsets, const int32_t* buffer_lengths,
+                                 int32_t chunk, int32_t batch_size, uint32_t buffer_token_size,
+                                 const void* w_k, const void* w_uv, int32_t num_heads,
+                                 int32_t dtype, float ckv_scale, float w_scale,
+                                 float kv_out_inv_scale, int32_t* d_status, mla_stream_t stream) {
+  if (dtype_ok(dtype) && num_heads >= 1 && !kv_cache) return MLA_ERR_ARG;
+  return upproject_impl(k_nope, v, nullptr, kv_cache, page_table, num_pages, page_size,
+                        max_pages_per_seq, buffer_row_offsets, cache_offsets, batch_size, w_k,
+                        w_uv, buffer_lengths, chunk, buffer_token_size, num_heads, dtype,
+                        ckv_scale, w_scale, kv_out_inv_scale, d_status, stream);
 }
 
 // k_rope from the [S][64] buffer, or (kv_cache given) from the paged cache.
@@ -364,7 +408,8 @@ mla_status_t mla_prefill(void* out, float* lse, const void* q, const uint32_t* i
   if (!out || !q || !input_row_offsets || !cache_lengths || !kv_cache || !page_table || !w_k ||
       !w_uv || batch_size < 1 || total_q_tokens < 0 || max_prompt_len < 0 || max_chunks < 1 ||
       buffer_token_size == 0 || buffer_token_size > 0x7FFFFFFFu || num_pages < 1 ||
-      page_size < 1 || max_pages_per_seq < 1 || ckv_scale == 0.f)
+      page_size < 1 || max_pages_per_seq < 1 || ckv_scale == 0.f || !aligned16(kv_cache) ||
+      static_cast<int64_t>(num_pages) * page_size > 0x7FFFFFFFll)
     return MLA_ERR_ARG;
   const Layout L = layout(batch_size, num_heads, total_q_tokens, max_chunks, buffer_token_size, dtype);
   if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
@@ -384,16 +429,16 @@ mla_status_t mla_prefill(void* out, float* lse, const void* q, const uint32_t* i
   // fp8: K and V are stored in the cache's descale domain.
   const float kv_inv = dtype == MLA_E4M3 ? 1.0f / ckv_scale : 1.0f;
   const float kv_descale = dtype == MLA_E4M3 ? ckv_scale : 1.0f;
+  // Per chunk: K_nope / V projected from c_kv rows read straight from the
+  // paged cache, then attention with k_rope read from the cache too.
   for (int c = 0; c < max_chunks; ++c) {
-    st = mla_gather_latent(ws + L.ckv, ws + L.krope, kv_cache, page_table, num_pages, page_size,
-                           max_pages_per_seq, bro, co, bl, c, batch_size, buffer_token_size,
-                           dtype, d_status, stream_);
+    st = mla_upproject_paged(ws + L.knope, ws + L.v, kv_cache, page_table, num_pages, page_size,
+                             max_pages_per_seq, bro, co, bl, c, batch_size, buffer_token_size,
+                             w_k, w_uv, num_heads, dtype, ckv_scale, w_scale, kv_inv, d_status,
+                             stream_);
     if (st != MLA_OK) return st;
-    st = mla_upproject(ws + L.knope, ws + L.v, ws + L.ckv, w_k, w_uv, bl, c, buffer_token_size,
-                       num_heads, dtype, ckv_scale, w_scale, kv_inv, d_status, stream_);
-    if (st != MLA_OK) return st;
-    st = attention_impl(out, lse, oacc, lseacc, q, ws + L.knope, ws + L.v, ws + L.krope, nullptr,
-                        nullptr, 0, 0, 0, input_row_offsets, cache_lengths, bro, co, bl, c, max_chunks, batch_size,
+    st = attention_impl(out, lse, oacc, lseacc, q, ws + L.knope, ws + L.v, nullptr, kv_cache,
+                        page_table, num_pages, page_size, max_pages_per_seq, input_row_offsets, cache_lengths, bro, co, bl, c, max_chunks, batch_size,
                         num_heads, max_prompt_len, total_q_tokens, buffer_token_size, scale,
                         q_scale, kv_descale, kv_descale, dtype, d_status, stream);
     if (st != MLA_OK) return st;

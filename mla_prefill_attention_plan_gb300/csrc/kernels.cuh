@@ -48,6 +48,14 @@ struct UpprojArgs {
   int dtype;
   float out_scale;
   int32_t* status;
+  // A rows straight from the paged cache (kv_cache given): buffer row r of
+  // the chunk is the cache row of sequence b's context position
+  // cache_offsets[chunk][b] + r - buffer_row_offsets[chunk][b].
+  const void* kv_cache = nullptr;
+  const int32_t* page_table = nullptr;
+  const uint32_t* bro = nullptr;
+  const uint32_t* co = nullptr;
+  int B = 0, num_pages = 0, page_size = 0, max_pages = 0;
 };
 // The GEMM on two-SM pairs (cta_group::2 clusters, 256 x 256 tiles); an
 // error where the device cannot keep such a cluster resident.

@@ -9,6 +9,10 @@
 // delivers to every SM at once (~72 B/clk).
 //
 //   warp 0      TMA producer: own A rows and own B half per k-block, 6-stage ring.
+//               A comes from the chunk's c_kv buffer (one tile load), or
+//               straight from the paged cache: each lane locates four of the
+//               tile's 128 rows once per tile and loads them with one
+//               tile::gather4 per k-block.
 //   warp 1      both CTAs: TMEM allocation (512 columns, pair form).
 //               CTA 0: one elected lane issues the pair MMAs (M=256, N=256)
 //               into one of two 256-column accumulators and commits to the
@@ -48,13 +52,56 @@ struct PairGemmSmem {
 };
 static_assert(sizeof(PairGemmSmem) <= 256, "barrier block");
 
+// Where the A rows live when they are read from the paged cache.
+struct PagedA {
+  const uint32_t* bro;        // [max_chunks][B + 1]
+  const uint32_t* co;         // [max_chunks][B]
+  const int32_t* page_table;  // [B][max_pages], or null: A is the c_kv buffer
+  int B, page_size, max_pages, num_pages;
+};
+
+// Cache rows of the chunk's buffer rows r0 .. r0 + 3 (rows at or past `rows`
+// read row 0, and the epilogue zeroes their outputs).  The sequence of a row
+// is the last b with bro[chunk][b] <= row, found by bisection once and then
+// stepped forward.  A position outside the page table or a page id out of
+// range is reported and reads row 0.
+__device__ __forceinline__ void paged_a_rows(const PagedA& pa, int chunk, int r0, int rows, int32_t* status,
+                                             int (&y)[4]) {
+  const uint32_t* bro_c = pa.bro + static_cast<size_t>(chunk) * (pa.B + 1);
+  const uint32_t* co_c = pa.co + static_cast<size_t>(chunk) * pa.B;
+  int lo = 0, hi = pa.B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(bro_c + mid) <= static_cast<uint32_t>(r0)) lo = mid;
+    else hi = mid - 1;
+  }
+  int b = lo;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int r = r0 + k;
+    y[k] = 0;
+    if (r >= rows) continue;
+    while (b + 1 < pa.B && __ldg(bro_c + b + 1) <= static_cast<uint32_t>(r)) ++b;
+    const long long pos = static_cast<long long>(__ldg(co_c + b)) + r - static_cast<long long>(__ldg(bro_c + b));
+    const long long pi = pos >= 0 ? pos / pa.page_size : -1;
+    const int page = pi >= 0 && pi < pa.max_pages
+                         ? __ldg(pa.page_table + static_cast<long long>(b) * pa.max_pages + pi)
+                         : -1;
+    if (page < 0 || page >= pa.num_pages) {
+      set_status(status, MLA_DEV_BAD_PAGE);
+      continue;
+    }
+    y[k] = static_cast<int>(static_cast<long long>(page) * pa.page_size + pos % pa.page_size);
+  }
+}
+
 template <int ELT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(U_THREADS, 1)
     upproj_pair_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap wk_map,
                        const __grid_constant__ CUtensorMap wuv_map,
                        const __grid_constant__ CUtensorMap k_out_map,
                        const __grid_constant__ CUtensorMap v_out_map, const int32_t* buffer_lengths,
-                       int chunk, int S, int H, float out_scale, int32_t* status) {
+                       int chunk, int S, int H, float out_scale, int32_t* status, const PagedA pa) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   PairGemmSmem* sh = reinterpret_cast<PairGemmSmem*>(smem + U_SMEM_BAR);
@@ -100,32 +147,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(U_THREADS, 1)
   volatile int* abort_flag = &sh->abort;
 
   if (warp == 0) {
+    // The whole warp runs the loop (paged A: every lane issues a gather).
+    const bool paged = pa.page_table != nullptr;
     if (lane == 0) {
       prefetch_tmap(&a_map);
       prefetch_tmap(&wk_map);
       prefetch_tmap(&wuv_map);
-      int stage = 0;
-      uint32_t phase = 0;
-      int last_ph[USTAGES];
-      for (int s = 0; s < USTAGES; ++s) last_ph[s] = -1;
-      for (int t = pair_id; t < num_tiles && !*abort_flag; t += n_pairs) {
-        const int m0 = (t % num_m) * 2 * UBM + static_cast<int>(rank) * UBM;
-        const int nt = t / num_m;
-        const int hf = 2 * nt + static_cast<int>(rank);   // this CTA's 128-wide block of N
-        const CUtensorMap* wmap = hf < H ? &wk_map : &wuv_map;
-        bool ok = true;
-        for (int kb = 0; kb < KB; ++kb) {
-          if (!(ok = mbar_wait(smem_u32(&sh->empty[stage]), phase ^ 1, status, abort_flag))) break;
-          const uint32_t full = smem_u32(&sh->full[stage]);
+    }
+    int stage = 0;
+    uint32_t phase = 0;
+    int last_ph[USTAGES];
+    for (int s = 0; s < USTAGES; ++s) last_ph[s] = -1;
+    for (int t = pair_id; t < num_tiles && !__any_sync(0xffffffffu, *abort_flag != 0); t += n_pairs) {
+      const int m0 = (t % num_m) * 2 * UBM + static_cast<int>(rank) * UBM;
+      const int nt = t / num_m;
+      const int hf = 2 * nt + static_cast<int>(rank);   // this CTA's 128-wide block of N
+      const CUtensorMap* wmap = hf < H ? &wk_map : &wuv_map;
+      int y[4];
+      if (paged) paged_a_rows(pa, chunk, m0 + 4 * lane, rows, status, y);
+      bool ok = true;
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!(ok = mbar_wait_warp(smem_u32(&sh->empty[stage]), phase ^ 1, status, abort_flag))) break;
+        const uint32_t full = smem_u32(&sh->full[stage]);
+        const uint32_t adst = smem_u32(smem + U_SMEM_A + stage * UA_BYTES);
+        const int x = kb * (UBKB / ELT);
+        if (elect_one()) {
           mbar_expect_tx(full, UA_BYTES + UB_BYTES);
-          const int x = kb * (UBKB / ELT);
-          tma_load_2d(smem_u32(smem + U_SMEM_A + stage * UA_BYTES), &a_map, full, x, m0);
+          if (!paged) tma_load_2d(adst, &a_map, full, x, m0);
           tma_load_2d(smem_u32(smem + U_SMEM_B + stage * UB_BYTES), wmap, full, x, (hf % H) * 128);
-          last_ph[stage] = int(phase);
-          if (++stage == USTAGES) { stage = 0; phase ^= 1; }
         }
-        if (!ok) break;
+        __syncwarp();
+        // Four 128-byte rows a lane, in tile row order (the swizzle follows
+        // the shared-memory address, as for the tile load).
+        if (paged) tma_gather4_2d(adst + lane * 4 * UBKB, &a_map, full, x, y[0], y[1], y[2], y[3]);
+        last_ph[stage] = int(phase);
+        if (++stage == USTAGES) { stage = 0; phase ^= 1; }
       }
+      if (!ok) break;
+    }
+    if (lane == 0) {
       volatile int never = 0;
       for (int s = 0; s < USTAGES; ++s)
         if (last_ph[s] >= 0) mbar_wait(smem_u32(&sh->full[s]), uint32_t(last_ph[s]), status, &never);
@@ -134,6 +194,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(U_THREADS, 1)
       for (int s = 0; s < USTAGES; ++s)
         if (last_ph[s] >= 0) mbar_wait(smem_u32(&sh->empty[s]), uint32_t(last_ph[s]), status, abort_flag);
     }
+    __syncwarp();
   } else if (warp == 1) {
     if (rank == 0) {
       // One elected lane runs the whole issue loop (no reconvergence while
@@ -316,8 +377,12 @@ cudaError_t launch_upproject(const UpprojArgs& a, cudaStream_t stream) {
   const uint32_t box_k = UBKB / elt;
   const uint64_t HN = static_cast<uint64_t>(a.H) * 128;
   CUtensorMap a_map, wk_map, wuv_map, k_map, v_map;
+  const bool paged = a.kv_cache != nullptr;
+  PagedA pa = {a.bro, a.co, paged ? a.page_table : nullptr, a.B, a.page_size, a.max_pages, a.num_pages};
   const bool ok =
-      encode_2d(&a_map, a.c_kv, dt, 512, a.S, 512ull * elt, box_k, UBM, CU_TENSOR_MAP_SWIZZLE_128B) &&
+      (paged ? encode_2d(&a_map, a.kv_cache, dt, 576, static_cast<uint64_t>(a.num_pages) * a.page_size,
+                         576ull * elt, box_k, 1, CU_TENSOR_MAP_SWIZZLE_128B)
+             : encode_2d(&a_map, a.c_kv, dt, 512, a.S, 512ull * elt, box_k, UBM, CU_TENSOR_MAP_SWIZZLE_128B)) &&
       encode_2d(&wk_map, a.w_k, dt, 512, HN, 512ull * elt, box_k, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
       encode_2d(&wuv_map, a.w_uv, dt, 512, HN, 512ull * elt, box_k, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
       encode_2d(&k_map, a.k_nope, dt, HN, a.S, HN * elt, box_k, 32, CU_TENSOR_MAP_SWIZZLE_128B) &&
@@ -335,11 +400,11 @@ cudaError_t launch_upproject(const UpprojArgs& a, cudaStream_t stream) {
   if (elt == 2)
     upproj_pair_kernel<2><<<grid, U_THREADS, U_SMEM_TOTAL, stream>>>(a_map, wk_map, wuv_map, k_map, v_map,
                                                                     a.buffer_lengths, a.chunk, int(a.S), a.H,
-                                                                    a.out_scale, a.status);
+                                                                    a.out_scale, a.status, pa);
   else
     upproj_pair_kernel<1><<<grid, U_THREADS, U_SMEM_TOTAL, stream>>>(a_map, wk_map, wuv_map, k_map, v_map,
                                                                     a.buffer_lengths, a.chunk, int(a.S), a.H,
-                                                                    a.out_scale, a.status);
+                                                                    a.out_scale, a.status, pa);
   return cudaGetLastError();
 }
 

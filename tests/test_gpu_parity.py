@@ -454,6 +454,100 @@ def test_upproject(dtype, H, rows, S):
     assert np.all(gk[pad:] == 3.0) and np.all(gv[pad:] == 3.0)       # untouched beyond it
 
 
+def _paged_upproject_case(w, oracle=True, bad_page=False):
+    """mla_upproject_paged, c_kv rows read from the paged cache, every chunk:
+    (1) bit for bit equal to mla_gather_latent + mla_upproject over the whole
+    K and V buffers (the zeroed tile tail and the untouched rows past it
+    included), and (2) within rounding of the oracle's projection of the
+    oracle's gathered rows."""
+    inp = make_inputs(w)
+    dt = w.dtype
+    c = {k: O.codes(inp[k]) for k in ("kv_cache", "page_table", "input_row_offsets", "cache_lengths",
+                                      "w_k", "w_uv")}
+    S, mc, B, H = w.buffer_token_size, w.max_chunks, inp["B"], w.H
+    plan = O.prefill_plan(c["input_row_offsets"], c["cache_lengths"], S, mc)
+    g = gpu_plan(c["input_row_offsets"], c["cache_lengths"], S, mc)
+    bro, co, bl = [torch.as_tensor(x.astype(np.int32)).to(DEV) for x in g[:3]]
+    kv, pt = inp["kv_cache"].to(DEV), inp["page_table"].to(DEV)
+    if bad_page:
+        pt[B - 1] = inp["num_pages"]
+    wk, wuv = inp["w_k"].to(DEV), inp["w_uv"].to(DEV)
+    wsc = inp["w_scale"]
+    paging = (inp["num_pages"], inp["page_size"], inp["max_pages"])
+    vdt = torch.bfloat16 if dt == "bf16" else torch.float16
+    st_bad = torch.zeros(1, dtype=torch.int32, device=DEV)
+    for ch in range(mc):
+        res = {}
+        for mode in ("paged",) if bad_page else ("buffer", "paged"):
+            kn = torch.full((S, H, 128), 3.0).to(kv.dtype).to(DEV)
+            vv = torch.full((S, H, 128), 3.0, dtype=vdt, device=DEV)
+            st = st_bad if bad_page else torch.zeros(1, dtype=torch.int32, device=DEV)
+            if mode == "buffer":
+                ckv = torch.zeros(S, 512, dtype=kv.dtype, device=DEV)
+                kr = torch.zeros(S, 64, dtype=kv.dtype, device=DEV)
+                mla.check(mla.mla_gather_latent(ckv, kr, kv, pt, *paging, bro, co, bl, ch, B, S, _dt(w), st))
+                mla.check(mla.mla_upproject(kn, vv, ckv, wk, wuv, bl, ch, S, H, _dt(w), 1.0, wsc, 1.0, st))
+            else:
+                mla.check(mla.mla_upproject_paged(kn, vv, kv, pt, *paging, bro, co, bl, ch, B, S, wk, wuv,
+                                                  H, _dt(w), 1.0, wsc, 1.0, st))
+            torch.cuda.synchronize()
+            res[mode] = (kn, vv, int(st.item()))
+        if bad_page:
+            continue
+        assert res["buffer"][2] == 0 and res["paged"][2] == 0
+        for i in (0, 1):
+            assert torch.equal(res["buffer"][i].view(torch.uint8), res["paged"][i].view(torch.uint8)), (ch, i)
+        n = max(int(plan[2][ch]), 0)
+        if not oracle or n == 0:
+            continue
+        o_ckv, _, ost = O.gather_latent(c["kv_cache"], c["page_table"], inp["page_size"], plan, ch)
+        assert ost == 0
+        rk, rv = O.upproject(O.decode(o_ckv, dt), O.decode(c["w_k"], dt) * wsc,
+                             O.decode(c["w_uv"], dt) * wsc)
+        gk = res["paged"][0].float().cpu().double().numpy()[:n]
+        gv = res["paged"][1].float().cpu().double().numpy()[:n]
+        if dt == "bf16":
+            bound = lambda ref: 2.0 ** -8 * np.abs(ref) + 1e-3
+        else:
+            bound = lambda ref: 2.0 ** -3 * np.abs(ref) + 2.0 ** -8
+        assert np.all(np.abs(gk - rk) <= bound(rk))
+        assert np.all(np.abs(gv - rv) <= bound(rv))
+    if bad_page:
+        assert int(st_bad.item()) == mla.MLA_DEV_BAD_PAGE
+
+
+def test_paged_upproject_shuffled_pages_multi_chunk():
+    w = scaled(WORKLOADS["ragged_chunked_cache"], H=2, B=3, buffer_token_size=700, max_chunks=4,
+               new_range=(100, 600), cache_range=(0, 900), page_size=16)
+    _paged_upproject_case(w)
+
+
+def test_paged_upproject_many_short_sequences():
+    """300 sequences of 1..8 tokens: every 128-row tile spans dozens of them
+    (the row -> sequence search), one-row pages."""
+    w = scaled(WORKLOADS["ragged_chunked_cache"], H=2, B=300, buffer_token_size=512, max_chunks=8,
+               new_range=(1, 5), cache_range=(0, 4), page_size=1)
+    _paged_upproject_case(w)
+
+
+def test_paged_upproject_e4m3():
+    w = scaled(WORKLOADS["longctx_fp8"], H=2, B=2, new_lens=(300, 41), cache_lens=(200, 0),
+               buffer_token_size=192, max_chunks=3, page_size=64, shuffle_pages=True)
+    _paged_upproject_case(w)
+
+
+@pytest.mark.parametrize("name", ["ragged_chunked_cache", "longctx_fp8"])
+def test_paged_upproject_full_size_equals_buffered(name):
+    """Full size, every chunk: bit for bit equal to gather + buffered
+    projection (whose own parity is covered above and by the fused tests)."""
+    _paged_upproject_case(WORKLOADS[name], oracle=False)
+
+
+def test_paged_upproject_bad_page_reports_status():
+    w = scaled(WORKLOADS["tiny_ragged"], page_size=16)
+    _paged_upproject_case(w, bad_page=True)
+
+
 # ----------------------------------------------------------------------------- attention
 
 def _compare(out, ref, dtype, lse=None):
