@@ -34,7 +34,7 @@ sys.path.insert(0, ROOT)
 # DRAM bytes (read + write) per attention launch from one ncu capture of the
 # current kernel (dram__bytes_read.sum + dram__bytes_write.sum), keyed by
 # (workload, kernel); absent where the kernel has changed since its capture.
-ATTN_DRAM_BYTES_PER_LAUNCH = {("v3_prefill", "attn_pair_kernel"): 480_141_056 + 117_703_680}
+ATTN_DRAM_BYTES_PER_LAUNCH = {}
 # CUDA kernel name of each attention variant the library reports.
 ATTN_KERNEL_NAMES = {"pair": "attn_pair_kernel", "e4m3": "attn_pair_kernel_e4m3"}
 
@@ -50,6 +50,7 @@ def _args():
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
     ap.add_argument("--no-stages", action="store_true", help="skip the plan / gather stage figures")
+    ap.add_argument("--no-paged", action="store_true", help="skip timing the in-place paged stages")
     ap.add_argument("--stage", default=None, choices=["plan", "gather", "cache_write", "decode",
                                                       "sparse_decode"],
                     help="time one HBM-bound stage alone on its stress shape")
@@ -419,6 +420,8 @@ def run_ours(a):
     ms_per_step = total_ms / a.steps
     attn_ms = sum(evs[k][ch][0].elapsed_time(evs[k][ch][1]) for k in range(a.steps) for ch in range(mc))
     used_chunks = int((bl >= 0).sum().item())
+    paged = None if a.no_paged else _paged_alternates(mla, d, inp, w, bro, co, bl, ckv, krope, knope, vbuf,
+                                                      out, oacc, lacc, status, stream)
     attn_ms_per_launch = attn_ms / (a.steps * max(used_chunks, 1))
     up_ms = sum(evs[k][ch][2].elapsed_time(evs[k][ch][3]) for k in range(a.steps) for ch in range(mc))
     attn_ms_per_chunk = [sum(evs[k][ch][0].elapsed_time(evs[k][ch][1]) for k in range(a.steps)) / a.steps
@@ -519,6 +522,7 @@ def run_ours(a):
         "upproj_ms_per_step": up_ms / a.steps,
         "step_flops": {"attention": attn_flops, "upproject": up_flops, "visible_pairs": pairs},
         "roofline": roofline,
+        "paged_alternates": paged,
         "e2e": e2e,
         "gpu_launches": launches_per_step * a.steps,
         "clocks": clk,
@@ -534,6 +538,62 @@ def run_ours(a):
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def _paged_alternates(mla, d, inp, w, bro, co, bl, ckv, krope, knope, vbuf, out, oacc, lacc, status,
+                      stream, reps=10):
+    """Chunk 0 of the workload through the stages the fused path uses
+    (gather, mla_upproject, mla_prefill_attention) and through the ones that
+    read the paged cache in place (mla_chunk_cache_rows, mla_upproject_paged,
+    mla_prefill_attention_paged): median per-launch milliseconds of each, CUDA
+    events on the launching stream, after the timed region."""
+    import statistics
+    import torch
+    S, mc, Bsz, H, T = w.buffer_token_size, w.max_chunks, inp["B"], w.H, inp["T_q"]
+    dt = mla.MLA_BF16 if w.dtype == "bf16" else mla.MLA_E4M3
+    paging = (inp["num_pages"], inp["page_size"], inp["max_pages"])
+    ncr = inp["num_pages"] * inp["page_size"]
+    rows = torch.empty(mc, S, dtype=torch.int32, device=d["q"].device)
+    kv_descale = inp["ckv_scale"] if w.dtype == "e4m3" else 1.0
+    kv_inv = 1.0 / inp["ckv_scale"] if w.dtype == "e4m3" else 1.0
+    attn = dict(lse=None, o_acc=oacc, lse_acc=lacc, q=d["q"], k_nope=knope, v=vbuf,
+                input_row_offsets=d["input_row_offsets"], cache_lengths=d["cache_lengths"],
+                buffer_row_offsets=bro, cache_offsets=co, buffer_lengths=bl, chunk=0, max_chunks=mc,
+                batch_size=Bsz, num_heads=H, max_prompt_len=inp["max_prompt_len"], total_q_tokens=T,
+                buffer_token_size=S, scale=inp["scale"], q_scale=inp["q_scale"], k_scale=kv_descale,
+                v_scale=kv_descale, dtype=dt, d_status=status, stream=stream)
+    calls = {
+        "gather": lambda: mla.mla_gather_latent(ckv, krope, d["kv_cache"], d["page_table"], *paging, bro, co,
+                                                bl, 0, Bsz, S, dt, status, stream),
+        "cache_rows_all_chunks": lambda: mla.mla_chunk_cache_rows(rows, d["page_table"], *paging, bro, co, bl,
+                                                                  mc, Bsz, S, status, stream),
+        "upproject": lambda: mla.mla_upproject(knope, vbuf, ckv, d["w_k"], d["w_uv"], bl, 0, S, H, dt,
+                                               inp["ckv_scale"], inp["w_scale"], kv_inv, status, stream),
+        "upproject_paged": lambda: mla.mla_upproject_paged(knope, vbuf, d["kv_cache"], rows[0], ncr, bl, 0, S,
+                                                           d["w_k"], d["w_uv"], H, dt, inp["ckv_scale"],
+                                                           inp["w_scale"], kv_inv, status, stream),
+        "attention": lambda: mla.mla_prefill_attention(out, k_rope=krope, **attn),
+        "attention_paged": lambda: mla.mla_prefill_attention_paged(out, kv_cache=d["kv_cache"],
+                                                                   cache_rows=rows[0], num_cache_rows=ncr,
+                                                                   **attn),
+    }
+    res = {}
+    for k, f in calls.items():
+        mla.check(f())
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            mla.check(f())
+            e1.record(stream)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        res[k + "_ms"] = statistics.median(ts)
+    assert status.item() == 0, mla.status_string(int(status.item()))
+    res["chunk"] = 0
+    res["note"] = ("per-launch medians on chunk 0; the fused path runs gather + upproject + attention, "
+                   "the paged stages read the cache in place and are slower here")
+    return res
 
 
 def measure_stage(stage, batch=None, steps=20, warmup=5):

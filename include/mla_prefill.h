@@ -3,7 +3,7 @@
  * Multi-head Latent Attention (MLA) prefill over a paged latent KV cache.
  *
  * The path has four stages, each an entry point below, plus a fused entry
- * point that runs plan, 3' and 4', and the step in front of it that writes
+ * point that runs 1 to 4, and the step in front of it that writes
  * the new tokens' latent rows into the paged cache:
  *   0. mla_latent_cache_write -- RMSNorm + RoPE + paged store
  *                                ("mla_prefill_decode_graph_bf16", Args:
@@ -15,9 +15,13 @@
  *                                                 Args: w_k, w_uv)
  *   4. mla_prefill_attention  -- causal attention with LSE merge across chunks
  *                                                ("flare_mla_prefill_dispatch")
- *   3'. mla_upproject_paged, 4'. mla_prefill_attention_paged -- stages 3 and 4
- *       reading the latent and k_rope rows straight from the paged cache, so
- *       that stage 2 (a copy) is not needed on the fused path.
+ *   2'. mla_chunk_cache_rows, 3'. mla_upproject_paged,
+ *   4'. mla_prefill_attention_paged -- a table of where each buffer row lives
+ *       in the paged cache, and stages 3 and 4 reading the latent and k_rope
+ *       rows there in place instead of from stage 2's buffers.  Same results;
+ *       on GB300 they run slower than stage 2 plus 3 and 4 (the projection
+ *       re-reads each latent row once per head tile), so the fused entry
+ *       point does not use them.
  *
  * Conventions shared by every entry point
  *   - Every pointer argument is a DEVICE pointer owned by the caller, unless
@@ -251,29 +255,54 @@ mla_status_t mla_upproject(void* k_nope, void* v, const void* c_kv_buf, const vo
                            int32_t* d_status, mla_stream_t stream);
 
 /*
+ * 2'. Cache-row table of every plan chunk: where in the paged cache each
+ * buffer row lives ("mla_prefill_decode_graph_bf16", Args: buffer_row_offsets,
+ * cache_offsets, and the kv_collection's pages; "flare_mla_prefill_dispatch",
+ * Args: cache_offsets, the start of a chunk's keys in the paged k_rope).  It is
+ * the lookup mla_gather_latent does, kept as 4 bytes per row instead of the
+ * row itself, so that stages 3' and 4' read the rows in place.
+ *
+ * cache_rows: [max_chunks][buffer_token_size] int32 output.  For chunk c and
+ *             buffer row r < buffer_lengths[c] of sequence b
+ *             (buffer_row_offsets[c][b] <= r < buffer_row_offsets[c][b+1]),
+ *             position j = cache_offsets[c][b] + r - buffer_row_offsets[c][b]:
+ *             cache_rows[c][r] = page_table[b][j / page_size] * page_size +
+ *             j % page_size, the row's index in the cache seen as
+ *             [num_pages * page_size][576].  Rows at or past buffer_lengths[c]
+ *             (and every row of an unused chunk) are 0.
+ * Other arguments as in mla_gather_latent, for all chunks at once.
+ * Errors: host MLA_ERR_ARG (null pointers, sizes < 1, num_pages * page_size
+ * >= 2^31, max_chunks > 65535), MLA_ERR_LAUNCH; device MLA_DEV_BAD_PAGE (a
+ * position outside the page table or a page id outside [0, num_pages): that
+ * row's entry is 0), MLA_DEV_TIMEOUT seen on entry (no work).
+ */
+mla_status_t mla_chunk_cache_rows(int32_t* cache_rows, const int32_t* page_table,
+                                  int32_t num_pages, int32_t page_size, int32_t max_pages_per_seq,
+                                  const uint32_t* buffer_row_offsets, const uint32_t* cache_offsets,
+                                  const int32_t* buffer_lengths, int32_t max_chunks,
+                                  int32_t batch_size, uint32_t buffer_token_size, int32_t* d_status,
+                                  mla_stream_t stream);
+
+/*
  * 3'. Up-projection of one plan chunk with the c_kv rows read straight from
  * the paged cache ("mla_prefill_decode_graph_bf16", Args: w_k, w_uv, and the
  * kv_collection the prefill branch reads the chunk's latent rows from).  The
  * result equals mla_gather_latent followed by mla_upproject, without the c_kv
  * buffer in between.
  *
- * Arguments as in mla_upproject, with c_kv_buf replaced by the cache and the
- * plan tables that locate the chunk's rows in it (as mla_gather_latent takes
- * them): buffer row r of sequence b (buffer_row_offsets[chunk][b] <= r <
- * buffer_row_offsets[chunk][b+1]) is the cache row of context position
- * cache_offsets[chunk][b] + r - buffer_row_offsets[chunk][b].  buffer_lengths
- * is required here; batch_size >= 1; num_pages * page_size must be < 2^31.
- * Errors: as mla_upproject, plus device MLA_DEV_BAD_PAGE for a position
- * outside the page table or a page id outside [0, num_pages) (that row's
- * outputs are then meaningless).
+ * Arguments as in mla_upproject, with c_kv_buf replaced by
+ * kv_cache:       the cache as [num_cache_rows][576] dtype
+ * cache_rows:     the chunk's [buffer_token_size] row of mla_chunk_cache_rows
+ *                 (buffer row r is cache row cache_rows[r])
+ * num_cache_rows: num_pages * page_size; an entry outside [0, num_cache_rows)
+ *                 is reported (MLA_DEV_BAD_PAGE) and read as row 0.
+ * buffer_lengths is required here.
  */
 mla_status_t mla_upproject_paged(void* k_nope, void* v, const void* kv_cache,
-                                 const int32_t* page_table, int32_t num_pages, int32_t page_size,
-                                 int32_t max_pages_per_seq, const uint32_t* buffer_row_offsets,
-                                 const uint32_t* cache_offsets, const int32_t* buffer_lengths,
-                                 int32_t chunk, int32_t batch_size, uint32_t buffer_token_size,
-                                 const void* w_k, const void* w_uv, int32_t num_heads,
-                                 int32_t dtype, float ckv_scale, float w_scale,
+                                 const int32_t* cache_rows, int32_t num_cache_rows,
+                                 const int32_t* buffer_lengths, int32_t chunk,
+                                 uint32_t buffer_token_size, const void* w_k, const void* w_uv,
+                                 int32_t num_heads, int32_t dtype, float ckv_scale, float w_scale,
                                  float kv_out_inv_scale, int32_t* d_status, mla_stream_t stream);
 
 /*
@@ -338,21 +367,19 @@ mla_status_t mla_prefill_attention(void* out, float* lse, float* o_acc, float* l
  * k_rope buffer is needed, so mla_gather_latent need not write one.
  *
  * Same arguments, results and errors as mla_prefill_attention, except that
- * k_rope is replaced by the cache (as mla_gather_latent takes it):
- * kv_cache:   [num_pages][page_size][576] dtype; columns 512..575 are k_rope
- * page_table: [batch_size][max_pages_per_seq] int32 page ids
- * The chunk's key r of sequence b (r - buffer_row_offsets[chunk][b] = i) is
- * the cache row of context position j = cache_offsets[chunk][b] + i, on page
- * page_table[b][j / page_size], row j % page_size.  k_nope and v stay
- * buffer rows.  num_pages * page_size must be < 2^31.
- * Device errors add MLA_DEV_BAD_PAGE: a key's page index is >= max_pages_per_seq
- * or its page id is outside [0, num_pages); that key's score is meaningless.
+ * k_rope is replaced by
+ * kv_cache:       the cache as [num_cache_rows][576] dtype; columns 512..575
+ *                 are k_rope
+ * cache_rows:     the chunk's [buffer_token_size] row of mla_chunk_cache_rows:
+ *                 key r (a buffer row) is cache row cache_rows[r]
+ * num_cache_rows: num_pages * page_size.
+ * k_nope and v stay buffer rows.  Device errors add MLA_DEV_BAD_PAGE: a key's
+ * entry is outside [0, num_cache_rows) (its score is then meaningless).
  */
 mla_status_t mla_prefill_attention_paged(void* out, float* lse, float* o_acc, float* lse_acc,
                                          const void* q, const void* k_nope, const void* v,
-                                         const void* kv_cache, const int32_t* page_table,
-                                         int32_t num_pages, int32_t page_size,
-                                         int32_t max_pages_per_seq,
+                                         const void* kv_cache, const int32_t* cache_rows,
+                                         int32_t num_cache_rows,
                                          const uint32_t* input_row_offsets,
                                          const uint32_t* cache_lengths,
                                          const uint32_t* buffer_row_offsets,
@@ -407,8 +434,8 @@ mla_status_t mla_prefill_attention_noalloc(void* out, float* lse, const void* q,
 
 /*
  * Workspace bytes needed by mla_prefill for these sizes (plan tables, the
- * chunk's K and V buffers, and the fp32 merge state when max_chunks > 1; the
- * latent and k_rope rows are read from the cache in place).  The buffers follow "mla_prefill_decode_graph_bf16" (Args:
+ * chunk's latent, k_rope, K and V buffers, and the fp32 merge state when
+ * max_chunks > 1).  The buffers follow "mla_prefill_decode_graph_bf16" (Args:
  * buffer_row_offsets, cache_offsets, buffer_length) and
  * "flare_mla_prefill_dispatch" (Args: k, v, k_rope); the pages size none of
  * them, so this call has no counterpart there.  Host only; returns 0 for
@@ -420,14 +447,11 @@ size_t mla_prefill_workspace_bytes(int32_t batch_size, int32_t num_heads,
                                    uint32_t buffer_token_size, int32_t dtype);
 
 /*
- * Fused path: plan, then for every chunk c < max_chunks up-project
- * (mla_upproject_paged) and attend (mla_prefill_attention_paged), all enqueued
- * on `stream` with no host synchronisation (chunks the plan leaves unused exit
- * on the device).  Follows the prefill branch of "mla_prefill_decode_graph_bf16"
- * with the tables of "mla_prefill_plan"; the chunk's latent rows are read from
- * the cache by the projection itself instead of being gathered into a buffer
- * first (the result is the same: the gather is a copy).  Errors add
- * MLA_ERR_ARG for num_pages * page_size >= 2^31.
+ * Fused path: plan, then for every chunk c < max_chunks gather, up-project and
+ * attend, all enqueued on `stream` with no host synchronisation (chunks the
+ * plan leaves unused exit on the device).  Follows the prefill branch of
+ * "mla_prefill_decode_graph_bf16" with the tables of "mla_prefill_plan".
+ * Errors add MLA_ERR_ARG for num_pages * page_size >= 2^31.
  *
  * out [total_q_tokens][num_heads][128] bf16 output; lse [total_q_tokens]
  * [num_heads] fp32 output or NULL.  Inputs as in the stage entry points.  For

@@ -48,13 +48,13 @@ SIGNATURES = {
                                     _F, _F, _I, _P, _P]),
     "mla_gather_latent": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _I, _I, _U, _I, _P, _P]),
     "mla_upproject": (_I, [_P, _P, _P, _P, _P, _P, _I, _U, _I, _I, _F, _F, _F, _P, _P]),
-    "mla_upproject_paged": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _I, _I, _U, _P, _P, _I, _I,
-                                 _F, _F, _F, _P, _P]),
+    "mla_chunk_cache_rows": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _I, _I, _U, _P, _P]),
+    "mla_upproject_paged": (_I, [_P, _P, _P, _P, _I, _P, _I, _U, _P, _P, _I, _I, _F, _F, _F, _P,
+                                 _P]),
     "mla_prefill_attention": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                    _I, _I, _I, _I, _I, _I, _U, _F, _F, _F, _F, _I, _P, _P]),
-    "mla_prefill_attention_paged": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P,
-                                         _P, _P, _I, _I, _I, _I, _I, _I, _U, _F, _F, _F, _F, _I,
-                                         _P, _P]),
+    "mla_prefill_attention_paged": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P, _P,
+                                         _I, _I, _I, _I, _I, _I, _U, _F, _F, _F, _F, _I, _P, _P]),
     "mla_prefill_attention_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                            _I, _I, _I, _I, _I, _I, _U, _F, _F, _F, _F, _I, _P,
                                            _P]),
@@ -173,16 +173,24 @@ def mla_upproject(k_nope, v, c_kv_buf, w_k, w_uv, buffer_lengths, chunk, buffer_
                                 _stream(stream))
 
 
-def mla_upproject_paged(k_nope, v, kv_cache, page_table, num_pages, page_size, max_pages_per_seq,
-                        buffer_row_offsets, cache_offsets, buffer_lengths, chunk, batch_size,
+def mla_chunk_cache_rows(cache_rows, page_table, num_pages, page_size, max_pages_per_seq,
+                         buffer_row_offsets, cache_offsets, buffer_lengths, max_chunks, batch_size,
+                         buffer_token_size, d_status=None, stream=None) -> int:
+    return load().mla_chunk_cache_rows(_ptr(cache_rows), _ptr(page_table), num_pages, page_size,
+                                       max_pages_per_seq, _ptr(buffer_row_offsets),
+                                       _ptr(cache_offsets), _ptr(buffer_lengths), max_chunks,
+                                       batch_size, buffer_token_size, _ptr(d_status),
+                                       _stream(stream))
+
+
+def mla_upproject_paged(k_nope, v, kv_cache, cache_rows, num_cache_rows, buffer_lengths, chunk,
                         buffer_token_size, w_k, w_uv, num_heads, dtype=MLA_BF16, ckv_scale=1.0,
                         w_scale=1.0, kv_out_inv_scale=1.0, d_status=None, stream=None) -> int:
-    return load().mla_upproject_paged(_ptr(k_nope), _ptr(v), _ptr(kv_cache), _ptr(page_table),
-                                      num_pages, page_size, max_pages_per_seq,
-                                      _ptr(buffer_row_offsets), _ptr(cache_offsets),
-                                      _ptr(buffer_lengths), chunk, batch_size, buffer_token_size,
-                                      _ptr(w_k), _ptr(w_uv), num_heads, dtype, ckv_scale, w_scale,
-                                      kv_out_inv_scale, _ptr(d_status), _stream(stream))
+    return load().mla_upproject_paged(_ptr(k_nope), _ptr(v), _ptr(kv_cache), _ptr(cache_rows),
+                                      num_cache_rows, _ptr(buffer_lengths), chunk,
+                                      buffer_token_size, _ptr(w_k), _ptr(w_uv), num_heads, dtype,
+                                      ckv_scale, w_scale, kv_out_inv_scale, _ptr(d_status),
+                                      _stream(stream))
 
 
 def mla_prefill_attention(out, lse, o_acc, lse_acc, q, k_nope, v, k_rope, input_row_offsets,
@@ -198,20 +206,19 @@ def mla_prefill_attention(out, lse, o_acc, lse_acc, q, k_nope, v, k_rope, input_
         dtype, _ptr(d_status), _stream(stream))
 
 
-def mla_prefill_attention_paged(out, lse, o_acc, lse_acc, q, k_nope, v, kv_cache, page_table,
-                                num_pages, page_size, max_pages_per_seq, input_row_offsets,
-                                cache_lengths, buffer_row_offsets, cache_offsets, buffer_lengths,
-                                chunk, max_chunks, batch_size, num_heads, max_prompt_len,
-                                total_q_tokens, buffer_token_size, scale, q_scale=1.0,
-                                k_scale=1.0, v_scale=1.0, dtype=MLA_BF16, d_status=None,
-                                stream=None) -> int:
+def mla_prefill_attention_paged(out, lse, o_acc, lse_acc, q, k_nope, v, kv_cache, cache_rows,
+                                num_cache_rows, input_row_offsets, cache_lengths,
+                                buffer_row_offsets, cache_offsets, buffer_lengths, chunk,
+                                max_chunks, batch_size, num_heads, max_prompt_len, total_q_tokens,
+                                buffer_token_size, scale, q_scale=1.0, k_scale=1.0, v_scale=1.0,
+                                dtype=MLA_BF16, d_status=None, stream=None) -> int:
     return load().mla_prefill_attention_paged(
         _ptr(out), _ptr(lse), _ptr(o_acc), _ptr(lse_acc), _ptr(q), _ptr(k_nope), _ptr(v),
-        _ptr(kv_cache), _ptr(page_table), num_pages, page_size, max_pages_per_seq,
-        _ptr(input_row_offsets), _ptr(cache_lengths), _ptr(buffer_row_offsets),
-        _ptr(cache_offsets), _ptr(buffer_lengths), chunk, max_chunks, batch_size, num_heads,
-        max_prompt_len, total_q_tokens, buffer_token_size, scale, q_scale, k_scale, v_scale,
-        dtype, _ptr(d_status), _stream(stream))
+        _ptr(kv_cache), _ptr(cache_rows), num_cache_rows, _ptr(input_row_offsets),
+        _ptr(cache_lengths), _ptr(buffer_row_offsets), _ptr(cache_offsets), _ptr(buffer_lengths),
+        chunk, max_chunks, batch_size, num_heads, max_prompt_len, total_q_tokens,
+        buffer_token_size, scale, q_scale, k_scale, v_scale, dtype, _ptr(d_status),
+        _stream(stream))
 
 
 MLA_NOALLOC_MAX_ROWS = 32768

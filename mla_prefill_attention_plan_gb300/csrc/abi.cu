@@ -42,7 +42,7 @@ mla_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_E
 
 // Workspace layout of the fused entry point.
 struct Layout {
-  size_t bro, co, bl, knope, v, oacc, lseacc, total;
+  size_t bro, co, bl, ckv, krope, knope, v, oacc, lseacc, total;
 };
 
 Layout layout(int B, int H, int T_q, int max_chunks, uint32_t S, int dtype) {
@@ -57,6 +57,8 @@ Layout layout(int B, int H, int T_q, int max_chunks, uint32_t S, int dtype) {
   L.bro = take(sizeof(uint32_t) * size_t(max_chunks) * (B + 1));
   L.co = take(sizeof(uint32_t) * size_t(max_chunks) * (B > 0 ? B : 1));
   L.bl = take(sizeof(int32_t) * size_t(max_chunks));
+  L.ckv = take(size_t(S) * 512 * e);
+  L.krope = take(size_t(S) * 64 * e);
   L.knope = take(size_t(S) * H * 128 * e);
   L.v = take(size_t(S) * H * 128 * 2);   // bf16, or f16 holding e4m3-rounded values
   const bool merge = max_chunks > 1;
@@ -207,12 +209,28 @@ mla_status_t mla_gather_latent(void* c_kv_buf, void* k_rope_buf, const void* kv_
                                  elt_bytes(dtype), d_status, static_cast<cudaStream_t>(stream)));
 }
 
-// A rows from the c_kv buffer, or (kv_cache given) from the paged cache.
+mla_status_t mla_chunk_cache_rows(int32_t* cache_rows, const int32_t* page_table,
+                                  int32_t num_pages, int32_t page_size, int32_t max_pages_per_seq,
+                                  const uint32_t* buffer_row_offsets, const uint32_t* cache_offsets,
+                                  const int32_t* buffer_lengths, int32_t max_chunks,
+                                  int32_t batch_size, uint32_t buffer_token_size, int32_t* d_status,
+                                  mla_stream_t stream) {
+  if (!cache_rows || !page_table || !buffer_row_offsets || !cache_offsets || !buffer_lengths ||
+      num_pages < 1 || page_size < 1 || max_pages_per_seq < 1 || max_chunks < 1 ||
+      max_chunks > 65535 || batch_size < 1 || buffer_token_size == 0 ||
+      buffer_token_size > 0x7FFFFFFFu || static_cast<int64_t>(num_pages) * page_size > 0x7FFFFFFFll)
+    return MLA_ERR_ARG;
+  return from_cuda(launch_cache_rows(cache_rows, page_table, num_pages, page_size, max_pages_per_seq,
+                                     buffer_row_offsets, cache_offsets, buffer_lengths, max_chunks,
+                                     batch_size, buffer_token_size, d_status,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+// A rows from the c_kv buffer, or (kv_cache given) from the cache rows the
+// chunk's table names.
 static mla_status_t upproject_impl(void* k_nope, void* v, const void* c_kv_buf,
-                                   const void* kv_cache, const int32_t* page_table,
-                                   int32_t num_pages, int32_t page_size, int32_t max_pages,
-                                   const uint32_t* bro, const uint32_t* co, int32_t B,
-                                   const void* w_k, const void* w_uv,
+                                   const void* kv_cache, const int32_t* cache_rows,
+                                   int32_t num_cache_rows, const void* w_k, const void* w_uv,
                                    const int32_t* buffer_lengths, int32_t chunk,
                                    uint32_t buffer_token_size, int32_t num_heads, int32_t dtype,
                                    float ckv_scale, float w_scale, float kv_out_inv_scale,
@@ -223,22 +241,14 @@ static mla_status_t upproject_impl(void* k_nope, void* v, const void* c_kv_buf,
       !aligned16(w_uv) || chunk < 0 || buffer_token_size == 0 || buffer_token_size > 0x7FFFFFFFu)
     return MLA_ERR_ARG;
   if (kv_cache) {
-    if (!aligned16(kv_cache) || !page_table || !bro || !co || !buffer_lengths || B < 1 ||
-        num_pages < 1 || page_size < 1 || max_pages < 1 ||
-        static_cast<int64_t>(num_pages) * page_size > 0x7FFFFFFFll)
-      return MLA_ERR_ARG;
+    if (!aligned16(kv_cache) || !cache_rows || !buffer_lengths || num_cache_rows < 1) return MLA_ERR_ARG;
   } else if (!c_kv_buf || !aligned16(c_kv_buf)) {
     return MLA_ERR_ARG;
   }
   UpprojArgs a;
   a.kv_cache = kv_cache;
-  a.page_table = page_table;
-  a.bro = bro;
-  a.co = co;
-  a.B = B;
-  a.num_pages = num_pages;
-  a.page_size = page_size;
-  a.max_pages = max_pages;
+  a.cache_rows = cache_rows;
+  a.num_cache_rows = num_cache_rows;
   a.k_nope = k_nope;
   a.v = v;
   a.c_kv = c_kv_buf;
@@ -260,32 +270,29 @@ mla_status_t mla_upproject(void* k_nope, void* v, const void* c_kv_buf, const vo
                            float ckv_scale, float w_scale, float kv_out_inv_scale,
                            int32_t* d_status, mla_stream_t stream) {
   if (dtype_ok(dtype) && num_heads >= 1 && !c_kv_buf) return MLA_ERR_ARG;
-  return upproject_impl(k_nope, v, c_kv_buf, nullptr, nullptr, 0, 0, 0, nullptr, nullptr, 0, w_k,
-                        w_uv, buffer_lengths, chunk, buffer_token_size, num_heads, dtype,
-                        ckv_scale, w_scale, kv_out_inv_scale, d_status, stream);
+  return upproject_impl(k_nope, v, c_kv_buf, nullptr, nullptr, 0, w_k, w_uv, buffer_lengths, chunk,
+                        buffer_token_size, num_heads, dtype, ckv_scale, w_scale, kv_out_inv_scale,
+                        d_status, stream);
 }
 
 mla_status_t mla_upproject_paged(void* k_nope, void* v, const void* kv_cache,
-                                 const int32_t* page_table, int32_t num_pages, int32_t page_size,
-                                 int32_t max_pages_per_seq, const uint32_t* buffer_row_offsets,
-                                 const uint32_t* cache_offsets, const int32_t* buffer_lengths,
-                                 int32_t chunk, int32_t batch_size, uint32_t buffer_token_size,
-                                 const void* w_k, const void* w_uv, int32_t num_heads,
-                                 int32_t dtype, float ckv_scale, float w_scale,
+                                 const int32_t* cache_rows, int32_t num_cache_rows,
+                                 const int32_t* buffer_lengths, int32_t chunk,
+                                 uint32_t buffer_token_size, const void* w_k, const void* w_uv,
+                                 int32_t num_heads, int32_t dtype, float ckv_scale, float w_scale,
                                  float kv_out_inv_scale, int32_t* d_status, mla_stream_t stream) {
   if (dtype_ok(dtype) && num_heads >= 1 && !kv_cache) return MLA_ERR_ARG;
-  return upproject_impl(k_nope, v, nullptr, kv_cache, page_table, num_pages, page_size,
-                        max_pages_per_seq, buffer_row_offsets, cache_offsets, batch_size, w_k,
-                        w_uv, buffer_lengths, chunk, buffer_token_size, num_heads, dtype,
-                        ckv_scale, w_scale, kv_out_inv_scale, d_status, stream);
+  return upproject_impl(k_nope, v, nullptr, kv_cache, cache_rows, num_cache_rows, w_k, w_uv,
+                        buffer_lengths, chunk, buffer_token_size, num_heads, dtype, ckv_scale,
+                        w_scale, kv_out_inv_scale, d_status, stream);
 }
 
 // k_rope from the [S][64] buffer, or (kv_cache given) from the paged cache.
 static mla_status_t attention_impl(void* out, float* lse, float* o_acc, float* lse_acc,
                                    const void* q, const void* k_nope, const void* v,
                                    const void* k_rope, const void* kv_cache,
-                                   const int32_t* page_table, int32_t num_pages, int32_t page_size,
-                                   int32_t max_pages, const uint32_t* iro,
+                                   const int32_t* cache_rows, int32_t num_cache_rows,
+                                   const uint32_t* iro,
                                    const uint32_t* cache_lengths, const uint32_t* bro,
                                    const uint32_t* co, const int32_t* bl, int32_t chunk,
                                    int32_t max_chunks, int32_t B, int32_t H,
@@ -300,10 +307,7 @@ static mla_status_t attention_impl(void* out, float* lse, float* o_acc, float* l
       S > 0x7FFFFFFFu)
     return MLA_ERR_ARG;
   if (kv_cache) {
-    // cache rows are addressed as int32 tensor-map coordinates
-    if (!aligned16(kv_cache) || !page_table || num_pages < 1 || page_size < 1 || max_pages < 1 ||
-        static_cast<int64_t>(num_pages) * page_size > 0x7FFFFFFFll)
-      return MLA_ERR_ARG;
+    if (!aligned16(kv_cache) || !cache_rows || num_cache_rows < 1) return MLA_ERR_ARG;
   } else if (!k_rope || !aligned16(k_rope)) {
     return MLA_ERR_ARG;
   }
@@ -319,10 +323,8 @@ static mla_status_t attention_impl(void* out, float* lse, float* o_acc, float* l
   a.v = v;
   a.k_rope = kv_cache ? nullptr : k_rope;
   a.kv_cache = kv_cache;
-  a.page_table = page_table;
-  a.num_pages = num_pages;
-  a.page_size = page_size;
-  a.max_pages = max_pages;
+  a.cache_rows = cache_rows;
+  a.num_cache_rows = num_cache_rows;
   a.iro = iro;
   a.cache_len = cache_lengths;
   a.bro = bro;
@@ -354,7 +356,7 @@ mla_status_t mla_prefill_attention(void* out, float* lse, float* o_acc, float* l
                                    float scale, float q_scale, float k_scale, float v_scale,
                                    int32_t dtype, int32_t* d_status, mla_stream_t stream) {
   if (!k_rope) return MLA_ERR_ARG;
-  return attention_impl(out, lse, o_acc, lse_acc, q, k_nope, v, k_rope, nullptr, nullptr, 0, 0, 0,
+  return attention_impl(out, lse, o_acc, lse_acc, q, k_nope, v, k_rope, nullptr, nullptr, 0,
                         input_row_offsets, cache_lengths, buffer_row_offsets, cache_offsets,
                         buffer_lengths, chunk, max_chunks, batch_size, num_heads, max_prompt_len,
                         total_q_tokens, buffer_token_size, scale, q_scale, k_scale, v_scale, dtype,
@@ -363,9 +365,8 @@ mla_status_t mla_prefill_attention(void* out, float* lse, float* o_acc, float* l
 
 mla_status_t mla_prefill_attention_paged(void* out, float* lse, float* o_acc, float* lse_acc,
                                          const void* q, const void* k_nope, const void* v,
-                                         const void* kv_cache, const int32_t* page_table,
-                                         int32_t num_pages, int32_t page_size,
-                                         int32_t max_pages_per_seq,
+                                         const void* kv_cache, const int32_t* cache_rows,
+                                         int32_t num_cache_rows,
                                          const uint32_t* input_row_offsets,
                                          const uint32_t* cache_lengths,
                                          const uint32_t* buffer_row_offsets,
@@ -378,12 +379,11 @@ mla_status_t mla_prefill_attention_paged(void* out, float* lse, float* o_acc, fl
                                          float v_scale, int32_t dtype, int32_t* d_status,
                                          mla_stream_t stream) {
   if (!kv_cache) return MLA_ERR_ARG;
-  return attention_impl(out, lse, o_acc, lse_acc, q, k_nope, v, nullptr, kv_cache, page_table,
-                        num_pages, page_size, max_pages_per_seq, input_row_offsets, cache_lengths,
-                        buffer_row_offsets, cache_offsets, buffer_lengths, chunk, max_chunks,
-                        batch_size, num_heads, max_prompt_len, total_q_tokens, buffer_token_size,
-                        scale, q_scale, k_scale, v_scale, dtype, d_status,
-                        static_cast<cudaStream_t>(stream));
+  return attention_impl(out, lse, o_acc, lse_acc, q, k_nope, v, nullptr, kv_cache, cache_rows,
+                        num_cache_rows, input_row_offsets, cache_lengths, buffer_row_offsets,
+                        cache_offsets, buffer_lengths, chunk, max_chunks, batch_size, num_heads,
+                        max_prompt_len, total_q_tokens, buffer_token_size, scale, q_scale, k_scale,
+                        v_scale, dtype, d_status, static_cast<cudaStream_t>(stream));
 }
 
 size_t mla_prefill_workspace_bytes(int32_t batch_size, int32_t num_heads, int32_t total_q_tokens,
@@ -429,18 +429,23 @@ mla_status_t mla_prefill(void* out, float* lse, const void* q, const uint32_t* i
   // fp8: K and V are stored in the cache's descale domain.
   const float kv_inv = dtype == MLA_E4M3 ? 1.0f / ckv_scale : 1.0f;
   const float kv_descale = dtype == MLA_E4M3 ? ckv_scale : 1.0f;
-  // Per chunk: K_nope / V projected from c_kv rows read straight from the
-  // paged cache, then attention with k_rope read from the cache too.
+  // Per chunk: gather the chunk's latent and k_rope rows out of the paged
+  // cache, project K_nope / V, attend.  (Reading the rows in place instead,
+  // mla_upproject_paged and mla_prefill_attention_paged, measures slower: the
+  // projection re-reads every A tile once per head tile, and the copy costs
+  // about 1 % of a chunk.)
   for (int c = 0; c < max_chunks; ++c) {
-    st = mla_upproject_paged(ws + L.knope, ws + L.v, kv_cache, page_table, num_pages, page_size,
-                             max_pages_per_seq, bro, co, bl, c, batch_size, buffer_token_size,
-                             w_k, w_uv, num_heads, dtype, ckv_scale, w_scale, kv_inv, d_status,
-                             stream_);
+    st = mla_gather_latent(ws + L.ckv, ws + L.krope, kv_cache, page_table, num_pages, page_size,
+                           max_pages_per_seq, bro, co, bl, c, batch_size, buffer_token_size,
+                           dtype, d_status, stream_);
     if (st != MLA_OK) return st;
-    st = attention_impl(out, lse, oacc, lseacc, q, ws + L.knope, ws + L.v, nullptr, kv_cache,
-                        page_table, num_pages, page_size, max_pages_per_seq, input_row_offsets, cache_lengths, bro, co, bl, c, max_chunks, batch_size,
-                        num_heads, max_prompt_len, total_q_tokens, buffer_token_size, scale,
-                        q_scale, kv_descale, kv_descale, dtype, d_status, stream);
+    st = mla_upproject(ws + L.knope, ws + L.v, ws + L.ckv, w_k, w_uv, bl, c, buffer_token_size,
+                       num_heads, dtype, ckv_scale, w_scale, kv_inv, d_status, stream_);
+    if (st != MLA_OK) return st;
+    st = attention_impl(out, lse, oacc, lseacc, q, ws + L.knope, ws + L.v, ws + L.krope, nullptr,
+                        nullptr, 0, input_row_offsets, cache_lengths, bro, co, bl, c, max_chunks,
+                        batch_size, num_heads, max_prompt_len, total_q_tokens, buffer_token_size,
+                        scale, q_scale, kv_descale, kv_descale, dtype, d_status, stream);
     if (st != MLA_OK) return st;
   }
   return MLA_OK;

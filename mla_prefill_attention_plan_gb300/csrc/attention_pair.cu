@@ -90,23 +90,40 @@ struct PairItem {
 // kernels walk all units and skip the empty ones.
 constexpr int kMaxUnits = 4096;
 
-// 64 rows of a one-row-box tensor map into consecutive box rows at `dst`
-// (row_bytes apart, swizzled as one tile): lane l holds rows l (ra) and
-// l + 32 (rb); lanes 0..15 each issue one tile::gather4 of rows 4l..4l+3.
-// The caller has registered the bytes on `bar` already.
-__device__ __forceinline__ void gather_rows64(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int ra,
-                                              int rb, int row_bytes) {
+// The 64 k_rope rows of a half tile from the paged cache, 16 bytes per
+// cp.async: lane l holds cache rows ra (key l) and rb (key l + 32); each warp
+// instruction copies 32 / CH whole rows (CH = 16-byte chunks per row), chunk
+// l % CH of row RPI * i + l / CH, into the swizzled layout a tensor-map load
+// would give (SW128 for 128-byte rows, SW64 for 64-byte rows; the tile base
+// is aligned to the swizzle period).  Commits one cp.async group.
+template <int ROW_BYTES>
+__device__ __forceinline__ void rope_rows_cp_async(uint32_t dst, const uint8_t* rope_col0, int cache_row_bytes,
+                                                   int ra, int rb) {
+  constexpr int CH = ROW_BYTES / 16;
+  constexpr int RPI = 32 / CH;
+  constexpr int ITERS = 64 / RPI;
   const int lane = threadIdx.x & 31;
-  int y[4];
+  const int c = lane % CH;
+  const uint8_t* src = rope_col0 + c * 16;
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int key = 4 * (lane & 15) + k;
-    const int va = __shfl_sync(0xffffffffu, ra, key & 31);
-    const int vb = __shfl_sync(0xffffffffu, rb, key & 31);
-    y[k] = key < 32 ? va : vb;
+  for (int i = 0; i < ITERS; ++i) {
+    const int r = RPI * i + lane / CH;
+    const int row = __shfl_sync(0xffffffffu, i < ITERS / 2 ? ra : rb, r & 31);
+    const int sw = ROW_BYTES == 128 ? (r & 7) : ((r >> 1) & 3);
+    cp_async16(dst + r * ROW_BYTES + ((c ^ sw) << 4), src + static_cast<size_t>(row) * cache_row_bytes);
   }
-  if (lane < 16) tma_gather4_2d(dst + lane * 4 * row_bytes, map, bar, x, y[0], y[1], y[2], y[3]);
+  cp_async_commit();
+}
+
+// The k_rope copies of a stage have landed (all but the newest PENDING
+// cp.async groups of the warp): fence them into the async proxy the MMAs
+// read through, then count them on the stage's barrier `bar`.
+template <int PENDING>
+__device__ __forceinline__ void rope_rows_landed(uint32_t bar) {
+  cp_async_wait<PENDING>();
+  fence_async_smem();
   __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
 struct WorkList {
@@ -175,10 +192,13 @@ __device__ int compact_units(const Params& p, uint32_t* list, int* warp_cnt) {
   return base;
 }
 
+// PAGED: k_rope from the paged cache through the chunk's cache-row table
+// (an instantiation of its own, so that the buffered one carries no trace of it).
+template <bool PAGED>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     attn_pair_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap kn_map,
                      const __grid_constant__ CUtensorMap kr_map, const __grid_constant__ CUtensorMap v_map,
-                     const Params p, int total_items) {
+                     const Params p, int total_items, const PagedRope pr) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   PairSmem* sh = reinterpret_cast<PairSmem*>(smem + P_SMEM_BAR);
@@ -196,7 +216,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     mbar_init(smem_u32(&sh->q_empty), 4);
     mbar_init(smem_u32(&sh->q_ready), 8);
     for (int i = 0; i < PNK; ++i) {
-      mbar_init(smem_u32(&sh->k_full[i]), 1 + lead);   // CTA 0: own bytes + the relay
+      // own bytes (+ the paged k_rope rows) + in CTA 0 the relay
+      mbar_init(smem_u32(&sh->k_full[i]), 1 + lead + (PAGED ? 1u : 0u));
       mbar_init(smem_u32(&sh->k_empty[i]), 1);
     }
     for (int i = 0; i < PNV; ++i) {
@@ -241,6 +262,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     __syncwarp();
     uint32_t g = 0, it_n = 0;
     int q_last = -1, k_last[PNK] = {-1, -1, -1, -1};
+    int k_pend = -1;   // stage whose paged k_rope rows are in flight
     bool ok = true;
     PairItem it;
     for (int idx = pair_id; ok && next_pair(p, idx, n_pairs, total, rank, it, wl); idx += n_pairs) {
@@ -254,36 +276,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
       }
       __syncwarp();
       q_last = int(it_n & 1);
+      // Paged k_rope: table entries of the half tile's 64 keys (two a lane),
+      // loaded a stage ahead of their use.
+      int ra = 0, rb = 0;
+      if constexpr (PAGED) {
+        ra = cache_row_entry(pr, it.own, static_cast<int>(rank) * 64 + lane);
+        rb = cache_row_entry(pr, it.own, static_cast<int>(rank) * 64 + 32 + lane);
+      }
       for (int j = 0; j < it.n_kv; ++j) {
         const uint32_t gj = g + j;
         const int row = it.own.kv_row0 + j * BN + static_cast<int>(rank) * 64;
         const int ks = gj % PNK;
-        // Paged k_rope: the cache rows of this half tile's 64 keys (two a
-        // lane), read before the stage wait so their latency overlaps it.
-        int ra = 0, rb = 0;
-        if (p.paged) {
-          const int k0 = j * BN + static_cast<int>(rank) * 64;
-          ra = paged_key_row(p, it.own, k0 + lane);
-          rb = paged_key_row(p, it.own, k0 + 32 + lane);
-        }
         if (gj >= PNK &&
             !(ok = mbar_wait_cluster_warp(smem_u32(&sh->k_empty[ks]), ((gj / PNK) & 1) ^ 1, status, abort_flag)))
           break;
         const uint32_t kf = smem_u32(&sh->k_full[ks]);
         const uint32_t kdst = smem_u32(smem + P_SMEM_K + ks * PK_BYTES);
         if (elect_one()) {
-          mbar_expect_tx(kf, PK_BYTES);
+          mbar_expect_tx(kf, PAGED ? 2 * HBLK : PK_BYTES);
           tma_load_2d(kdst, &kn_map, kf, it.own.h * 128, row);
           tma_load_2d(kdst + HBLK, &kn_map, kf, it.own.h * 128 + 64, row);
-          if (!p.paged) tma_load_2d(kdst + 2 * HBLK, &kr_map, kf, 0, row);
+          if constexpr (!PAGED) tma_load_2d(kdst + 2 * HBLK, &kr_map, kf, 0, row);
         }
         __syncwarp();
-        if (p.paged) gather_rows64(kdst + 2 * HBLK, &kr_map, kf, 512, ra, rb, 128);
+        if constexpr (PAGED) {
+          // k_rope rows by cp.async (one-row TMA gathers cost far more per
+          // byte); the previous stage's rows are counted once they land.
+          rope_rows_cp_async<128>(kdst + 2 * HBLK, pr.kv_cache + 1024, pr.cache_row_bytes, checked_cache_row(p, pr, ra),
+                                     checked_cache_row(p, pr, rb));
+          if (j + 1 < it.n_kv) {
+            const int k1 = (j + 1) * BN + static_cast<int>(rank) * 64;
+            ra = cache_row_entry(pr, it.own, k1 + lane);
+            rb = cache_row_entry(pr, it.own, k1 + 32 + lane);
+          }
+          if (k_pend >= 0) rope_rows_landed<1>(smem_u32(&sh->k_full[k_pend]));
+          k_pend = ks;
+        }
         k_last[ks] = int((gj / PNK) & 1);
       }
+      // The item's last k_rope rows, before any other wait.
+      if (k_pend >= 0) rope_rows_landed<0>(smem_u32(&sh->k_full[k_pend]));
+      k_pend = -1;
       g += it.n_kv;
       ++it_n;
     }
+    if (k_pend >= 0) rope_rows_landed<0>(smem_u32(&sh->k_full[k_pend]));
     // Drain: every issued load lands before the CTA leaves.  (In CTA 0 the
     // K barriers also count the relay's arrival, so wait on the bytes only
     // through the phases this warp started: a bounded wait either way.)
@@ -630,10 +667,12 @@ struct PairSmem8 {
 };
 static_assert(sizeof(PairSmem8) <= 256, "barrier block");
 
+template <bool PAGED>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     attn_pair_kernel_e4m3(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap qr_map,
                           const __grid_constant__ CUtensorMap kn_map, const __grid_constant__ CUtensorMap kr_map,
-                          const __grid_constant__ CUtensorMap v_map, const Params p, int total_items) {
+                          const __grid_constant__ CUtensorMap v_map, const Params p, int total_items,
+                          const PagedRope pr) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   PairSmem8* sh = reinterpret_cast<PairSmem8*>(smem + E_SMEM_BAR);
@@ -653,7 +692,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     }
     mbar_init(smem_u32(&sh->q_ready), 8);
     for (int i = 0; i < PNK; ++i) {
-      mbar_init(smem_u32(&sh->k_full[i]), 1 + lead);   // CTA 0: own bytes + the relay
+      // own bytes (+ the paged k_rope rows) + in CTA 0 the relay
+      mbar_init(smem_u32(&sh->k_full[i]), 1 + lead + (PAGED ? 1u : 0u));
       mbar_init(smem_u32(&sh->k_empty[i]), 1);
     }
     for (int i = 0; i < PNV; ++i) {
@@ -699,6 +739,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     __syncwarp();
     uint32_t g = 0, it_n = 0;
     int q_last[2] = {-1, -1}, k_last[PNK] = {-1, -1, -1, -1};
+    int k_pend = -1;   // stage whose paged k_rope rows are in flight
     bool ok = true;
     PairItem it;
     for (int idx = pair_id; ok && next_pair(p, idx, n_pairs, total, rank, it, wl); idx += n_pairs) {
@@ -717,33 +758,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
       }
       __syncwarp();
       q_last[qs] = int((it_n >> 1) & 1);
+      // Paged k_rope: table entries of the half tile's 64 keys (two a lane),
+      // loaded a stage ahead of their use.
+      int ra = 0, rb = 0;
+      if constexpr (PAGED) {
+        ra = cache_row_entry(pr, it.own, static_cast<int>(rank) * 64 + lane);
+        rb = cache_row_entry(pr, it.own, static_cast<int>(rank) * 64 + 32 + lane);
+      }
       for (int j = 0; j < it.n_kv; ++j) {
         const uint32_t gj = g + j;
         const int row = it.own.kv_row0 + j * BN + static_cast<int>(rank) * 64;
         const int ks = gj % PNK;
-        int ra = 0, rb = 0;   // paged k_rope: the half tile's cache rows (see the bf16 kernel)
-        if (p.paged) {
-          const int k0 = j * BN + static_cast<int>(rank) * 64;
-          ra = paged_key_row(p, it.own, k0 + lane);
-          rb = paged_key_row(p, it.own, k0 + 32 + lane);
-        }
         if (gj >= PNK &&
             !(ok = mbar_wait_cluster_warp(smem_u32(&sh->k_empty[ks]), ((gj / PNK) & 1) ^ 1, status, abort_flag)))
           break;
         const uint32_t kf = smem_u32(&sh->k_full[ks]);
         const uint32_t kdst = smem_u32(smem + E_SMEM_K + ks * EK_BYTES);
         if (elect_one()) {
-          mbar_expect_tx(kf, EK_BYTES);
+          mbar_expect_tx(kf, PAGED ? EKN_BYTES : EK_BYTES);
           tma_load_2d(kdst, &kn_map, kf, it.own.h * 128, row);      // nope: 64 keys x 128 B
-          if (!p.paged) tma_load_2d(kdst + EKN_BYTES, &kr_map, kf, 0, row);   // rope: 64 keys x 64 B
+          if constexpr (!PAGED) tma_load_2d(kdst + EKN_BYTES, &kr_map, kf, 0, row);   // rope: 64 keys x 64 B
         }
         __syncwarp();
-        if (p.paged) gather_rows64(kdst + EKN_BYTES, &kr_map, kf, 512, ra, rb, 64);
+        if constexpr (PAGED) {   // as in the bf16 kernel
+          rope_rows_cp_async<64>(kdst + EKN_BYTES, pr.kv_cache + 512, pr.cache_row_bytes, checked_cache_row(p, pr, ra),
+                                     checked_cache_row(p, pr, rb));
+          if (j + 1 < it.n_kv) {
+            const int k1 = (j + 1) * BN + static_cast<int>(rank) * 64;
+            ra = cache_row_entry(pr, it.own, k1 + lane);
+            rb = cache_row_entry(pr, it.own, k1 + 32 + lane);
+          }
+          if (k_pend >= 0) rope_rows_landed<1>(smem_u32(&sh->k_full[k_pend]));
+          k_pend = ks;
+        }
         k_last[ks] = int((gj / PNK) & 1);
       }
+      if (k_pend >= 0) rope_rows_landed<0>(smem_u32(&sh->k_full[k_pend]));
+      k_pend = -1;
       g += it.n_kv;
       ++it_n;
     }
+    if (k_pend >= 0) rope_rows_landed<0>(smem_u32(&sh->k_full[k_pend]));
     // Drain: every issued load lands before the CTA leaves.  (In CTA 0 the
     // K barriers also count the relay's arrival, so wait on the bytes only
     // through the phases this warp started: a bounded wait either way.)
@@ -1063,8 +1118,8 @@ static int pair_smem_bytes(int units_offset, const Params& p) {
 template <typename Kernel>
 static int pair_clusters_of(Kernel kernel, int smem, int device, int slot) {
   static std::mutex mu;
-  static int cached[2][64];
-  static bool done[2][64];
+  static int cached[4][64];
+  static bool done[4][64];
   std::lock_guard<std::mutex> lock(mu);
   if (device < 0 || device >= 64) return 0;
   if (!done[slot][device]) {
@@ -1083,9 +1138,13 @@ static int pair_clusters_of(Kernel kernel, int smem, int device, int slot) {
   }
   return cached[slot][device];
 }
-static int pair_clusters(int device) { return pair_clusters_of(attn_pair_kernel, P_SMEM_TOTAL, device, 0); }
-static int pair_clusters_e4m3(int device) {
-  return pair_clusters_of(attn_pair_kernel_e4m3, E_SMEM_TOTAL, device, 1);
+static int pair_clusters(int device, bool paged) {
+  return paged ? pair_clusters_of(attn_pair_kernel<true>, P_SMEM_TOTAL, device, 2)
+               : pair_clusters_of(attn_pair_kernel<false>, P_SMEM_TOTAL, device, 0);
+}
+static int pair_clusters_e4m3(int device, bool paged) {
+  return paged ? pair_clusters_of(attn_pair_kernel_e4m3<true>, E_SMEM_TOTAL, device, 3)
+               : pair_clusters_of(attn_pair_kernel_e4m3<false>, E_SMEM_TOTAL, device, 1);
 }
 
 cudaError_t launch_attention_pair(const AttnArgs& a, cudaStream_t stream) {
@@ -1094,7 +1153,7 @@ cudaError_t launch_attention_pair(const AttnArgs& a, cudaStream_t stream) {
   const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUtensorMap maps[4];
   const bool paged = a.kv_cache != nullptr;
-  const uint64_t cache_rows = static_cast<uint64_t>(a.num_pages) * a.page_size;
+  const uint64_t cache_rows = static_cast<uint64_t>(a.num_cache_rows);
   const bool ok = encode_2d(&maps[0], a.q, dt, QW, a.T_q, QW * 2, 64, BM, CU_TENSOR_MAP_SWIZZLE_128B) &&
                   encode_2d(&maps[1], a.k_nope, dt, HN, a.S, HN * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
                   (paged ? encode_2d(&maps[2], a.kv_cache, dt, 576, cache_rows, 1152, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B)
@@ -1121,21 +1180,23 @@ cudaError_t launch_attention_pair(const AttnArgs& a, cudaStream_t stream) {
   p.v_scale = a.v_scale;
   p.status = a.status;
   p.T_q = a.T_q;
-  p.paged = a.kv_cache != nullptr ? 1 : 0;
-  p.page_table = a.page_table;
-  p.page_size = a.page_size;
-  p.max_pages = a.max_pages;
-  p.num_pages = a.num_pages;
+  const PagedRope pr{static_cast<const uint8_t*>(a.kv_cache), a.cache_rows, a.num_cache_rows,
+                     a.dtype == MLA_E4M3 ? 576 : 1152};
   const long long total = static_cast<long long>((p.n_qtiles + 1) / 2) * a.B * a.H;
   if (total <= 0) return cudaSuccess;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const int clusters = pair_clusters(dev);
+  const int clusters = pair_clusters(dev, paged);
   if (clusters <= 0) return cudaErrorInvalidConfiguration;
   const int grid = 2 * static_cast<int>(total < clusters ? total : clusters);
-  attn_pair_kernel<<<grid, P_THREADS, pair_smem_bytes(P_SMEM_UNITS, p), stream>>>(maps[0], maps[1], maps[2], maps[3], p,
-                                                             static_cast<int>(total));
+  const int smem = pair_smem_bytes(P_SMEM_UNITS, p);
+  if (paged)
+    attn_pair_kernel<true><<<grid, P_THREADS, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], p,
+                                                              static_cast<int>(total), pr);
+  else
+    attn_pair_kernel<false><<<grid, P_THREADS, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], p,
+                                                               static_cast<int>(total), pr);
   return cudaGetLastError();
 }
 
@@ -1149,7 +1210,7 @@ cudaError_t launch_attention_pair_e4m3(const AttnArgs& a, cudaStream_t stream) {
       encode_2d(&maps[1], a.q, u8, QW, a.T_q, QW, 64, BM, CU_TENSOR_MAP_SWIZZLE_64B) &&      // Q rope
       encode_2d(&maps[2], a.k_nope, u8, HN, a.S, HN, 128, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
       (a.kv_cache != nullptr
-           ? encode_2d(&maps[3], a.kv_cache, u8, 576, static_cast<uint64_t>(a.num_pages) * a.page_size, 576, 64, 1,
+           ? encode_2d(&maps[3], a.kv_cache, u8, 576, static_cast<uint64_t>(a.num_cache_rows), 576, 64, 1,
                        CU_TENSOR_MAP_SWIZZLE_64B)
            : encode_2d(&maps[3], a.k_rope, u8, 64, a.S, 64, 64, 64, CU_TENSOR_MAP_SWIZZLE_64B)) &&
       encode_2d(&maps[4], a.v, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, HN, a.S, HN * 2, 64, BN,
@@ -1176,21 +1237,24 @@ cudaError_t launch_attention_pair_e4m3(const AttnArgs& a, cudaStream_t stream) {
   p.v_scale = a.v_scale;
   p.status = a.status;
   p.T_q = a.T_q;
-  p.paged = a.kv_cache != nullptr ? 1 : 0;
-  p.page_table = a.page_table;
-  p.page_size = a.page_size;
-  p.max_pages = a.max_pages;
-  p.num_pages = a.num_pages;
+  const PagedRope pr{static_cast<const uint8_t*>(a.kv_cache), a.cache_rows, a.num_cache_rows,
+                     a.dtype == MLA_E4M3 ? 576 : 1152};
   const long long total = static_cast<long long>((p.n_qtiles + 1) / 2) * a.B * a.H;
   if (total <= 0) return cudaSuccess;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const int clusters = pair_clusters_e4m3(dev);
+  const bool paged = a.kv_cache != nullptr;
+  const int clusters = pair_clusters_e4m3(dev, paged);
   if (clusters <= 0) return cudaErrorInvalidConfiguration;
   const int grid = 2 * static_cast<int>(total < clusters ? total : clusters);
-  attn_pair_kernel_e4m3<<<grid, P_THREADS, pair_smem_bytes(E_SMEM_UNITS, p), stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4],
-                                                                  p, static_cast<int>(total));
+  const int smem = pair_smem_bytes(E_SMEM_UNITS, p);
+  if (paged)
+    attn_pair_kernel_e4m3<true><<<grid, P_THREADS, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4],
+                                                                   p, static_cast<int>(total), pr);
+  else
+    attn_pair_kernel_e4m3<false><<<grid, P_THREADS, smem, stream>>>(maps[0], maps[1], maps[2], maps[3],
+                                                                    maps[4], p, static_cast<int>(total), pr);
   return cudaGetLastError();
 }
 

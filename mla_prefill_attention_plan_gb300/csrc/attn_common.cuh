@@ -24,13 +24,18 @@ struct Params {
   const int32_t* bl;
   int chunk, B, H, n_qtiles, head_group;
   int T_q;            // rows of q / out / lse: no query row at or past it is read or written
-  // k_rope straight from the paged cache (paged != 0): key i of an item is the
-  // cache row of context position co + i of its sequence.
-  const int32_t* page_table;
-  int page_size, max_pages, num_pages, paged;
   float scale_log2;   // softmax scale * descales * log2(e)
   float v_scale;
   int32_t* status;
+};
+
+// k_rope straight from the paged cache (the PAGED kernels, a launch
+// parameter of its own): buffer row r is cache row cache_rows[r]
+// (< num_cache_rows, each cache_row_bytes long).
+struct PagedRope {
+  const uint8_t* kv_cache;
+  const int32_t* cache_rows;
+  int num_cache_rows, cache_row_bytes;
 };
 
 // One work item, as every role sees it.
@@ -85,19 +90,18 @@ __device__ __forceinline__ bool tile_item(const Params& p, int b, int h, int qt,
   return true;
 }
 
-// Physical cache row of the chunk's key `k` (0-based within the sequence's
-// keys in this chunk) of the item's sequence, or 0 for a key past them or a
-// page out of range (reported; those keys' scores are then not meaningful).
-__device__ __forceinline__ int paged_key_row(const Params& p, const Item& it, int k) {
-  if (k >= it.n_cb) return 0;
-  const long long pos = static_cast<long long>(it.co) + k;
-  const long long pi = pos / p.page_size;
-  const int page = pi < p.max_pages ? __ldg(p.page_table + static_cast<long long>(it.b) * p.max_pages + pi) : -1;
-  if (page < 0 || page >= p.num_pages) {
-    set_status(p.status, MLA_DEV_BAD_PAGE);
-    return 0;
-  }
-  return static_cast<int>(static_cast<long long>(page) * p.page_size + pos % p.page_size);
+// The table entry of the item's key `k` (0-based within the sequence's keys
+// in this chunk), or 0 past them: a plain load, checked where it is used
+// (checked_cache_row), so that it can be issued a stage ahead.
+__device__ __forceinline__ int cache_row_entry(const PagedRope& pr, const Item& it, int k) {
+  return k < it.n_cb ? __ldg(pr.cache_rows + it.kv_row0 + k) : 0;
+}
+// A table entry outside the cache is reported and read as row 0 (that key's
+// score is then meaningless).
+__device__ __forceinline__ int checked_cache_row(const Params& p, const PagedRope& pr, int row) {
+  if (static_cast<unsigned>(row) < static_cast<unsigned>(pr.num_cache_rows)) return row;
+  set_status(p.status, MLA_DEV_BAD_PAGE);
+  return 0;
 }
 
 // Epilogue of one query row: O / l, this chunk's natural-log LSE, merge with

@@ -91,7 +91,52 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// Cache-row table of the plan's chunks: cache_rows[c][r] = the cache row
+// holding buffer row r of chunk c (the same lookup as above, 4 bytes per row
+// instead of the row itself), 0 for r >= buffer_lengths[c] and for a row
+// whose page is out of range (reported).  One thread per (chunk, row).
+__global__ void __launch_bounds__(256)
+    cache_rows_kernel(int32_t* __restrict__ cache_rows, const int32_t* __restrict__ page_table,
+                      int num_pages, int page_size, int max_pages, const uint32_t* __restrict__ bro,
+                      const uint32_t* __restrict__ co, const int32_t* __restrict__ bl, int B, int S,
+                      int32_t* status) {
+  if (timed_out_before(status)) return;
+  const int chunk = blockIdx.y;
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= S) return;
+  const int n = min(__ldg(bl + chunk), S);
+  int row = 0;
+  if (r < n) {
+    const uint32_t* bro_c = bro + static_cast<size_t>(chunk) * (B + 1);
+    const uint32_t* co_c = co + static_cast<size_t>(chunk) * B;
+    int lo = 0, hi = B;  // invariant: bro_c[lo] <= r < bro_c[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(bro_c + mid) <= static_cast<uint32_t>(r)) lo = mid; else hi = mid;
+    }
+    const uint32_t pos = __ldg(co_c + lo) + (static_cast<uint32_t>(r) - __ldg(bro_c + lo));
+    const uint32_t pidx = pos / static_cast<uint32_t>(page_size);
+    const int page = pidx < static_cast<uint32_t>(max_pages)
+                         ? __ldg(page_table + static_cast<size_t>(lo) * max_pages + pidx) : -1;
+    if (page >= 0 && page < num_pages)
+      row = static_cast<int>(static_cast<long long>(page) * page_size + pos % page_size);
+    else
+      set_status(status, MLA_DEV_BAD_PAGE);
+  }
+  cache_rows[static_cast<size_t>(chunk) * S + r] = row;
+}
+
 }  // namespace
+
+cudaError_t launch_cache_rows(int32_t* cache_rows, const int32_t* page_table, int num_pages,
+                              int page_size, int max_pages, const uint32_t* bro, const uint32_t* co,
+                              const int32_t* bl, int max_chunks, int B, uint32_t S, int32_t* status,
+                              cudaStream_t stream) {
+  const dim3 grid(static_cast<unsigned>((static_cast<uint64_t>(S) + 255) / 256), static_cast<unsigned>(max_chunks));
+  cache_rows_kernel<<<grid, 256, 0, stream>>>(cache_rows, page_table, num_pages, page_size, max_pages, bro, co,
+                                               bl, B, static_cast<int>(S), status);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_gather(void* c_kv_buf, void* k_rope_buf, const void* kv_cache,
                           const int32_t* page_table, int num_pages, int page_size, int max_pages,

@@ -35,6 +35,12 @@ cudaError_t launch_gather(void* c_kv_buf, void* k_rope_buf, const void* kv_cache
                           const uint32_t* bro, const uint32_t* co, const int32_t* bl, int chunk,
                           int B, uint32_t S, int elt_bytes, int32_t* status, cudaStream_t stream);
 
+// Per chunk, the cache row of every buffer row (gather.cu).
+cudaError_t launch_cache_rows(int32_t* cache_rows, const int32_t* page_table, int num_pages,
+                              int page_size, int max_pages, const uint32_t* bro, const uint32_t* co,
+                              const int32_t* bl, int max_chunks, int B, uint32_t S, int32_t* status,
+                              cudaStream_t stream);
+
 struct UpprojArgs {
   void* k_nope;
   void* v;
@@ -49,13 +55,10 @@ struct UpprojArgs {
   float out_scale;
   int32_t* status;
   // A rows straight from the paged cache (kv_cache given): buffer row r of
-  // the chunk is the cache row of sequence b's context position
-  // cache_offsets[chunk][b] + r - buffer_row_offsets[chunk][b].
+  // the chunk is cache row cache_rows[r] (< num_cache_rows).
   const void* kv_cache = nullptr;
-  const int32_t* page_table = nullptr;
-  const uint32_t* bro = nullptr;
-  const uint32_t* co = nullptr;
-  int B = 0, num_pages = 0, page_size = 0, max_pages = 0;
+  const int32_t* cache_rows = nullptr;
+  int num_cache_rows = 0;
 };
 // The GEMM on two-SM pairs (cta_group::2 clusters, 256 x 256 tiles); an
 // error where the device cannot keep such a cluster resident.
@@ -70,9 +73,9 @@ struct AttnArgs {
   const void* k_nope;
   const void* v;
   const void* k_rope;           // [S][64] buffer, or null when k_rope comes from the paged cache
-  const void* kv_cache = nullptr;  // paged cache [num_pages][page_size][576] (k_rope = columns 512..575)
-  const int32_t* page_table = nullptr;  // [B][max_pages]
-  int num_pages = 0, page_size = 0, max_pages = 0;
+  const void* kv_cache = nullptr;      // paged cache rows [num_cache_rows][576] (k_rope = columns 512..575)
+  const int32_t* cache_rows = nullptr;  // the chunk's cache row of each buffer row
+  int num_cache_rows = 0;
   const uint32_t* iro;
   const uint32_t* cache_len;
   const uint32_t* bro;

@@ -198,6 +198,20 @@ __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// 16 bytes global -> shared without a register round trip, cached in L2
+// only.  These are generic-proxy writes: before a barrier that a tensor-core
+// reader waits on is signalled, the issuing thread waits for them
+// (cp_async_wait), fences (fence_async_smem) and then arrives.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until at most N of this thread's committed cp.async groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // ---------------------------------------------------------------- clusters
 // Rank of this CTA in its cluster, and the cluster-space address of the same
 // shared-memory offset in CTA `rank` of the cluster.

@@ -10,9 +10,13 @@
 //
 //   warp 0      TMA producer: own A rows and own B half per k-block, 6-stage ring.
 //               A comes from the chunk's c_kv buffer (one tile load), or
-//               straight from the paged cache: each lane locates four of the
-//               tile's 128 rows once per tile and loads them with one
-//               tile::gather4 per k-block.
+//               straight from the paged cache: the chunk's cache-row table
+//               gives the tile's 128 rows (read a tile ahead), and per
+//               k-block the warp copies the rows' 128-byte slices with
+//               16-byte cp.async into the swizzled layout the tile load
+//               would give.  A stage's
+//               A rows are counted on its barrier A_LAG stages later, once
+//               they have landed and been fenced into the async proxy.
 //   warp 1      both CTAs: TMEM allocation (512 columns, pair form).
 //               CTA 0: one elected lane issues the pair MMAs (M=256, N=256)
 //               into one of two 256-column accumulators and commits to the
@@ -54,48 +58,29 @@ static_assert(sizeof(PairGemmSmem) <= 256, "barrier block");
 
 // Where the A rows live when they are read from the paged cache.
 struct PagedA {
-  const uint32_t* bro;        // [max_chunks][B + 1]
-  const uint32_t* co;         // [max_chunks][B]
-  const int32_t* page_table;  // [B][max_pages], or null: A is the c_kv buffer
-  int B, page_size, max_pages, num_pages;
+  const uint8_t* cache;       // cache rows of row_bytes; c_kv = the first 512 * ELT bytes of a row
+  const int32_t* rows;        // the chunk's cache row of each buffer row, or null: A is the c_kv buffer
+  int num_rows, row_bytes;
 };
+// Stages between a stage's A copies and its arrival (cp.async groups left
+// pending): enough to cover the copies' latency at the tensor rate, fewer
+// than the ring's stages.
+constexpr int A_LAG = 4;
+static_assert(A_LAG < USTAGES, "the ring must hold the lagging stages");
 
-// Cache rows of the chunk's buffer rows r0 .. r0 + 3 (rows at or past `rows`
-// read row 0, and the epilogue zeroes their outputs).  The sequence of a row
-// is the last b with bro[chunk][b] <= row, found by bisection once and then
-// stepped forward.  A position outside the page table or a page id out of
-// range is reported and reads row 0.
-__device__ __forceinline__ void paged_a_rows(const PagedA& pa, int chunk, int r0, int rows, int32_t* status,
-                                             int (&y)[4]) {
-  const uint32_t* bro_c = pa.bro + static_cast<size_t>(chunk) * (pa.B + 1);
-  const uint32_t* co_c = pa.co + static_cast<size_t>(chunk) * pa.B;
-  int lo = 0, hi = pa.B - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(bro_c + mid) <= static_cast<uint32_t>(r0)) lo = mid;
-    else hi = mid - 1;
-  }
-  int b = lo;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int r = r0 + k;
-    y[k] = 0;
-    if (r >= rows) continue;
-    while (b + 1 < pa.B && __ldg(bro_c + b + 1) <= static_cast<uint32_t>(r)) ++b;
-    const long long pos = static_cast<long long>(__ldg(co_c + b)) + r - static_cast<long long>(__ldg(bro_c + b));
-    const long long pi = pos >= 0 ? pos / pa.page_size : -1;
-    const int page = pi >= 0 && pi < pa.max_pages
-                         ? __ldg(pa.page_table + static_cast<long long>(b) * pa.max_pages + pi)
-                         : -1;
-    if (page < 0 || page >= pa.num_pages) {
-      set_status(status, MLA_DEV_BAD_PAGE);
-      continue;
-    }
-    y[k] = static_cast<int>(static_cast<long long>(page) * pa.page_size + pos % pa.page_size);
-  }
+// Stage `bar`'s A copies have landed (all but the newest N cp.async groups
+// of the warp): fence them into the async proxy, count them on the barrier.
+template <int N>
+__device__ __forceinline__ void a_rows_landed(uint32_t bar) {
+  cp_async_wait<N>();
+  fence_async_smem();
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
-template <int ELT>
+// PAGED: A rows from the paged cache through the chunk's cache-row table (an
+// instantiation of its own, so that the buffered one carries no trace of it).
+template <int ELT, bool PAGED>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(U_THREADS, 1)
     upproj_pair_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap wk_map,
                        const __grid_constant__ CUtensorMap wuv_map,
@@ -122,7 +107,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(U_THREADS, 1)
   if (threadIdx.x == 0) {
     const uint32_t lead = rank == 0 ? 1u : 0u;
     for (int s = 0; s < USTAGES; ++s) {
-      mbar_init(smem_u32(&sh->full[s]), 1 + lead);
+      // own bytes (+ the paged A rows) + in CTA 0 the relay
+      mbar_init(smem_u32(&sh->full[s]), 1 + lead + (PAGED ? 1u : 0u));
       mbar_init(smem_u32(&sh->empty[s]), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -147,54 +133,146 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(U_THREADS, 1)
   volatile int* abort_flag = &sh->abort;
 
   if (warp == 0) {
-    // The whole warp runs the loop (paged A: every lane issues a gather).
-    const bool paged = pa.page_table != nullptr;
-    if (lane == 0) {
-      prefetch_tmap(&a_map);
-      prefetch_tmap(&wk_map);
-      prefetch_tmap(&wuv_map);
-    }
-    int stage = 0;
-    uint32_t phase = 0;
-    int last_ph[USTAGES];
-    for (int s = 0; s < USTAGES; ++s) last_ph[s] = -1;
-    for (int t = pair_id; t < num_tiles && !__any_sync(0xffffffffu, *abort_flag != 0); t += n_pairs) {
-      const int m0 = (t % num_m) * 2 * UBM + static_cast<int>(rank) * UBM;
-      const int nt = t / num_m;
-      const int hf = 2 * nt + static_cast<int>(rank);   // this CTA's 128-wide block of N
-      const CUtensorMap* wmap = hf < H ? &wk_map : &wuv_map;
-      int y[4];
-      if (paged) paged_a_rows(pa, chunk, m0 + 4 * lane, rows, status, y);
-      bool ok = true;
-      for (int kb = 0; kb < KB; ++kb) {
-        if (!(ok = mbar_wait_warp(smem_u32(&sh->empty[stage]), phase ^ 1, status, abort_flag))) break;
-        const uint32_t full = smem_u32(&sh->full[stage]);
-        const uint32_t adst = smem_u32(smem + U_SMEM_A + stage * UA_BYTES);
-        const int x = kb * (UBKB / ELT);
-        if (elect_one()) {
-          mbar_expect_tx(full, UA_BYTES + UB_BYTES);
-          if (!paged) tma_load_2d(adst, &a_map, full, x, m0);
-          tma_load_2d(smem_u32(smem + U_SMEM_B + stage * UB_BYTES), wmap, full, x, (hf % H) * 128);
+    if constexpr (!PAGED) {
+      // One lane issues both tile loads of every k-block.
+      if (lane == 0) {
+        prefetch_tmap(&a_map);
+        prefetch_tmap(&wk_map);
+        prefetch_tmap(&wuv_map);
+        int stage = 0;
+        uint32_t phase = 0;
+        int last_ph[USTAGES];
+        for (int s = 0; s < USTAGES; ++s) last_ph[s] = -1;
+        for (int t = pair_id; t < num_tiles && !*abort_flag; t += n_pairs) {
+          const int m0 = (t % num_m) * 2 * UBM + static_cast<int>(rank) * UBM;
+          const int nt = t / num_m;
+          const int hf = 2 * nt + static_cast<int>(rank);   // this CTA's 128-wide block of N
+          const CUtensorMap* wmap = hf < H ? &wk_map : &wuv_map;
+          bool ok = true;
+          for (int kb = 0; kb < KB; ++kb) {
+            if (!(ok = mbar_wait(smem_u32(&sh->empty[stage]), phase ^ 1, status, abort_flag))) break;
+            const uint32_t full = smem_u32(&sh->full[stage]);
+            mbar_expect_tx(full, UA_BYTES + UB_BYTES);
+            const int x = kb * (UBKB / ELT);
+            tma_load_2d(smem_u32(smem + U_SMEM_A + stage * UA_BYTES), &a_map, full, x, m0);
+            tma_load_2d(smem_u32(smem + U_SMEM_B + stage * UB_BYTES), wmap, full, x, (hf % H) * 128);
+            last_ph[stage] = int(phase);
+            if (++stage == USTAGES) { stage = 0; phase ^= 1; }
+          }
+          if (!ok) break;
         }
-        __syncwarp();
-        // Four 128-byte rows a lane, in tile row order (the swizzle follows
-        // the shared-memory address, as for the tile load).
-        if (paged) tma_gather4_2d(adst + lane * 4 * UBKB, &a_map, full, x, y[0], y[1], y[2], y[3]);
-        last_ph[stage] = int(phase);
-        if (++stage == USTAGES) { stage = 0; phase ^= 1; }
+        volatile int never = 0;
+        for (int s = 0; s < USTAGES; ++s)
+          if (last_ph[s] >= 0) mbar_wait(smem_u32(&sh->full[s]), uint32_t(last_ph[s]), status, &never);
+        // ... and every stage release the MMAs committed to this CTA has
+        // arrived: an asynchronous arrival must not reach a CTA that has left.
+        for (int s = 0; s < USTAGES; ++s)
+          if (last_ph[s] >= 0) mbar_wait(smem_u32(&sh->empty[s]), uint32_t(last_ph[s]), status, abort_flag);
       }
-      if (!ok) break;
+    } else {
+      // The whole warp runs the loop: every lane issues A copies.
+      if (lane == 0) {
+        prefetch_tmap(&a_map);
+        prefetch_tmap(&wk_map);
+        prefetch_tmap(&wuv_map);
+      }
+      int stage = 0;
+      uint32_t phase = 0;
+      int last_ph[USTAGES];
+      for (int s = 0; s < USTAGES; ++s) last_ph[s] = -1;
+      int issued = 0;   // stages whose A copies were issued (the last A_LAG not yet counted)
+      // Paged A: the cache rows of the tile's rows 4 lane .. 4 lane + 3, loaded
+      // a tile ahead of their use (0 past the chunk's rows).
+      int yn[4] = {0, 0, 0, 0};
+      auto fetch_rows = [&](int t) {
+        const int m0 = (t % num_m) * 2 * UBM + static_cast<int>(rank) * UBM;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int r = m0 + 4 * lane + k;
+          yn[k] = t < num_tiles && r < rows ? __ldg(pa.rows + r) : 0;
+        }
+      };
+      fetch_rows(pair_id);
+      for (int t = pair_id; t < num_tiles && !__any_sync(0xffffffffu, *abort_flag != 0); t += n_pairs) {
+        const int m0 = (t % num_m) * 2 * UBM + static_cast<int>(rank) * UBM;
+        const int nt = t / num_m;
+        const int hf = 2 * nt + static_cast<int>(rank);   // this CTA's 128-wide block of N
+        const CUtensorMap* wmap = hf < H ? &wk_map : &wuv_map;
+        // Paged A: lane l copies 16-byte chunk l % 8 of tile rows 4i + l / 8
+        // (i < 32); arow[i] is that row's cache row.  Row 4i + k is lane i's
+        // k-th row.  A row outside the cache is reported and read as row 0.
+        int arow[32];
+        {
+          int y[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) y[k] = yn[k];
+          fetch_rows(t + n_pairs);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            if (static_cast<unsigned>(y[k]) >= static_cast<unsigned>(pa.num_rows)) {
+              set_status(status, MLA_DEV_BAD_PAGE);
+              y[k] = 0;
+            }
+          }
+          const int k = lane >> 3;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int v0 = __shfl_sync(0xffffffffu, y[0], i), v1 = __shfl_sync(0xffffffffu, y[1], i);
+            const int v2 = __shfl_sync(0xffffffffu, y[2], i), v3 = __shfl_sync(0xffffffffu, y[3], i);
+            arow[i] = k == 0 ? v0 : k == 1 ? v1 : k == 2 ? v2 : v3;
+          }
+        }
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!(ok = mbar_wait_warp(smem_u32(&sh->empty[stage]), phase ^ 1, status, abort_flag))) break;
+          const uint32_t full = smem_u32(&sh->full[stage]);
+          const uint32_t adst = smem_u32(smem + U_SMEM_A + stage * UA_BYTES);
+          const int x = kb * (UBKB / ELT);
+          if (elect_one()) {
+            mbar_expect_tx(full, UB_BYTES);
+            tma_load_2d(smem_u32(smem + U_SMEM_B + stage * UB_BYTES), wmap, full, x, (hf % H) * 128);
+          }
+          __syncwarp();
+          {
+            const int c = lane & 7;
+            const uint8_t* src = pa.cache + kb * UBKB + c * 16;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int r = 4 * i + (lane >> 3);
+              cp_async16(adst + r * UBKB + ((c ^ (r & 7)) << 4), src + static_cast<size_t>(arow[i]) * pa.row_bytes);
+            }
+            cp_async_commit();
+            if (++issued > A_LAG) {
+              const int ls = (stage + USTAGES - A_LAG) % USTAGES;
+              a_rows_landed<A_LAG>(smem_u32(&sh->full[ls]));
+            }
+          }
+          last_ph[stage] = int(phase);
+          if (++stage == USTAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+      }
+      // The last stages' A rows (at most A_LAG), oldest first.
+      {
+        cp_async_wait<0>();
+        fence_async_smem();
+        __syncwarp();
+        const int n = issued < A_LAG ? issued : A_LAG;
+        if (lane == 0)
+          for (int j = n; j >= 1; --j) mbar_arrive(smem_u32(&sh->full[(stage + USTAGES - j) % USTAGES]));
+        __syncwarp();
+      }
+      if (lane == 0) {
+        volatile int never = 0;
+        for (int s = 0; s < USTAGES; ++s)
+          if (last_ph[s] >= 0) mbar_wait(smem_u32(&sh->full[s]), uint32_t(last_ph[s]), status, &never);
+        // ... and every stage release the MMAs committed to this CTA has
+        // arrived: an asynchronous arrival must not reach a CTA that has left.
+        for (int s = 0; s < USTAGES; ++s)
+          if (last_ph[s] >= 0) mbar_wait(smem_u32(&sh->empty[s]), uint32_t(last_ph[s]), status, abort_flag);
+      }
+      __syncwarp();
     }
-    if (lane == 0) {
-      volatile int never = 0;
-      for (int s = 0; s < USTAGES; ++s)
-        if (last_ph[s] >= 0) mbar_wait(smem_u32(&sh->full[s]), uint32_t(last_ph[s]), status, &never);
-      // ... and every stage release the MMAs committed to this CTA has
-      // arrived: an asynchronous arrival must not reach a CTA that has left.
-      for (int s = 0; s < USTAGES; ++s)
-        if (last_ph[s] >= 0) mbar_wait(smem_u32(&sh->empty[s]), uint32_t(last_ph[s]), status, abort_flag);
-    }
-    __syncwarp();
   } else if (warp == 1) {
     if (rank == 0) {
       // One elected lane runs the whole issue loop (no reconvergence while
@@ -344,7 +422,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(U_THREADS, 1)
   }
 }
 
-template <int ELT>
+template <int ELT, bool PAGED>
 int pair_gemm_clusters(int device) {
   static std::mutex mu;
   static int cached[64];
@@ -352,13 +430,13 @@ int pair_gemm_clusters(int device) {
   std::lock_guard<std::mutex> lock(mu);
   if (device < 0 || device >= 64) return 0;
   if (!done[device]) {
-    cudaFuncSetAttribute(upproj_pair_kernel<ELT>, cudaFuncAttributeMaxDynamicSharedMemorySize, U_SMEM_TOTAL);
+    cudaFuncSetAttribute(upproj_pair_kernel<ELT, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, U_SMEM_TOTAL);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2);
     cfg.blockDim = dim3(U_THREADS);
     cfg.dynamicSmemBytes = U_SMEM_TOTAL;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, upproj_pair_kernel<ELT>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, upproj_pair_kernel<ELT, PAGED>, &cfg) != cudaSuccess) {
       cudaGetLastError();
       n = 0;
     }
@@ -378,10 +456,12 @@ cudaError_t launch_upproject(const UpprojArgs& a, cudaStream_t stream) {
   const uint64_t HN = static_cast<uint64_t>(a.H) * 128;
   CUtensorMap a_map, wk_map, wuv_map, k_map, v_map;
   const bool paged = a.kv_cache != nullptr;
-  PagedA pa = {a.bro, a.co, paged ? a.page_table : nullptr, a.B, a.page_size, a.max_pages, a.num_pages};
+  PagedA pa = {static_cast<const uint8_t*>(a.kv_cache), paged ? a.cache_rows : nullptr, a.num_cache_rows,
+               576 * elt};
+  // (paged: a_map is not read; it is encoded over the cache rows to stay valid)
   const bool ok =
-      (paged ? encode_2d(&a_map, a.kv_cache, dt, 576, static_cast<uint64_t>(a.num_pages) * a.page_size,
-                         576ull * elt, box_k, 1, CU_TENSOR_MAP_SWIZZLE_128B)
+      (paged ? encode_2d(&a_map, a.kv_cache, dt, 576, static_cast<uint64_t>(a.num_cache_rows), 576ull * elt,
+                         box_k, 1, CU_TENSOR_MAP_SWIZZLE_128B)
              : encode_2d(&a_map, a.c_kv, dt, 512, a.S, 512ull * elt, box_k, UBM, CU_TENSOR_MAP_SWIZZLE_128B)) &&
       encode_2d(&wk_map, a.w_k, dt, 512, HN, 512ull * elt, box_k, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
       encode_2d(&wuv_map, a.w_uv, dt, 512, HN, 512ull * elt, box_k, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
@@ -392,19 +472,16 @@ cudaError_t launch_upproject(const UpprojArgs& a, cudaStream_t stream) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const int clusters = elt == 2 ? pair_gemm_clusters<2>(dev) : pair_gemm_clusters<1>(dev);
+  const int clusters = elt == 2 ? (paged ? pair_gemm_clusters<2, true>(dev) : pair_gemm_clusters<2, false>(dev))
+                                : (paged ? pair_gemm_clusters<1, true>(dev) : pair_gemm_clusters<1, false>(dev));
   if (clusters <= 0) return cudaErrorInvalidConfiguration;
   // Upper bound on pair tiles (the device reads the chunk's real row count).
   const long long max_tiles = static_cast<long long>((a.S + 2 * UBM - 1) / (2 * UBM)) * a.H;
   const int grid = 2 * static_cast<int>(max_tiles < clusters ? max_tiles : clusters);
-  if (elt == 2)
-    upproj_pair_kernel<2><<<grid, U_THREADS, U_SMEM_TOTAL, stream>>>(a_map, wk_map, wuv_map, k_map, v_map,
-                                                                    a.buffer_lengths, a.chunk, int(a.S), a.H,
-                                                                    a.out_scale, a.status, pa);
-  else
-    upproj_pair_kernel<1><<<grid, U_THREADS, U_SMEM_TOTAL, stream>>>(a_map, wk_map, wuv_map, k_map, v_map,
-                                                                    a.buffer_lengths, a.chunk, int(a.S), a.H,
-                                                                    a.out_scale, a.status, pa);
+  auto kernel = elt == 2 ? (paged ? upproj_pair_kernel<2, true> : upproj_pair_kernel<2, false>)
+                         : (paged ? upproj_pair_kernel<1, true> : upproj_pair_kernel<1, false>);
+  kernel<<<grid, U_THREADS, U_SMEM_TOTAL, stream>>>(a_map, wk_map, wuv_map, k_map, v_map, a.buffer_lengths, a.chunk,
+                                                    int(a.S), a.H, a.out_scale, a.status, pa);
   return cudaGetLastError();
 }
 

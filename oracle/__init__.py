@@ -7,7 +7,8 @@ import numpy as np
 
 from .mla_oracle import *  # noqa: F401,F403
 from .mla_oracle import (attention_over_chunks, attention_reference, attention_absorbed,  # noqa: F401
-                         context_latents, latent_cache_write, rms_norm, rope_rotate,
+                         chunk_cache_rows, context_latents, latent_cache_write, rms_norm,
+                         rope_rotate,
                          decode, gather_latent, merge_partials, mla_decode, mla_prefill,
                          mla_sparse_decode,
                          partial_attention, prefill_plan, upproject)

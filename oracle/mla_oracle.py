@@ -325,6 +325,36 @@ def gather_latent(kv_cache_codes, page_table, page_size: int, plan, chunk: int):
     return c_kv, k_rope, status
 
 
+def chunk_cache_rows(page_table, page_size: int, num_pages: int, plan, chunk: int,
+                     buffer_token_size: int):
+    """Where each buffer row of chunk ``chunk`` lives in the paged cache, the
+    cache seen as ``num_pages * page_size`` consecutive rows: the lookup of
+    ``gather_latent`` without the copy.  Buffer row ``buffer_row_offsets
+    [chunk, b] + t`` of sequence ``b`` is context position ``cache_offsets
+    [chunk, b] + t``, slot ``pos % page_size`` of page ``page_table[b, pos //
+    page_size]``, i.e. row ``page * page_size + pos % page_size``.  Entries
+    past the chunk's rows are 0, and so is the entry of a row whose page is
+    out of range (status BAD_PAGE).
+
+    Returns (rows [buffer_token_size] int64, status).
+    """
+    bro, co, bl, _ = plan
+    pt = np.asarray(page_table, dtype=np.int64)
+    rows = np.zeros(buffer_token_size, dtype=np.int64)
+    status = STATUS_OK
+    B = bro.shape[1] - 1
+    for b in range(B):
+        r0, r1 = int(bro[chunk, b]), int(bro[chunk, b + 1])
+        for t in range(r1 - r0):
+            pos = int(co[chunk, b]) + t
+            slot_page = pos // page_size
+            if slot_page >= pt.shape[1] or pt[b, slot_page] < 0 or pt[b, slot_page] >= num_pages:
+                status = STATUS_BAD_PAGE
+                continue
+            rows[r0 + t] = pt[b, slot_page] * page_size + pos % page_size
+    return rows, status
+
+
 def context_latents(kv_cache_codes, page_table, page_size: int, total_lens):
     """All context tokens of every sequence, in position order, straight from
     the paged cache (no plan): a list of [L_b, 576] code arrays."""

@@ -32,7 +32,9 @@ def lib():
 def test_header_declares_the_boundary():
     names = _declared()
     for n in ("mla_latent_cache_write", "mla_prefill_plan", "mla_gather_latent", "mla_upproject",
-              "mla_prefill_attention", "mla_prefill", "mla_prefill_workspace_bytes", "mla_status_string"):
+              "mla_prefill_attention", "mla_chunk_cache_rows", "mla_upproject_paged",
+              "mla_prefill_attention_paged", "mla_prefill", "mla_prefill_workspace_bytes",
+              "mla_status_string"):
         assert n in names
 
 
@@ -81,32 +83,54 @@ def test_host_argument_errors(lib):
     assert mla.mla_prefill_attention(*args, stream=s) == mla.MLA_ERR_ARG
 
 
-def test_paged_attention_host_argument_errors(lib):
-    s = 1
-    # out, lse, o_acc, lse_acc, q, k_nope, v, kv_cache, page_table, num_pages, page_size,
-    # max_pages, iro, cache_lengths, bro, co, bl, chunk, max_chunks, B, H, max_prompt_len, T, S, scale
-    ok = [16, None, None, None, 16, 16, 16, 16, 16, 4, 16, 2, 16, 16, 16, 16, 16, 0, 1, 1, 4, 16,
-          16, 8, 0.1]
-    names = ["out", "lse", "oacc", "lacc", "q", "kn", "v", "kv", "pt", "np", "ps", "mp", "iro", "cl",
-             "bro", "co", "bl", "ch", "mc", "B", "H", "mpl", "T", "S", "scale"]
-
+def _caller(fn, ok, names):
     def call(**change):
         a = list(ok)
         for k, v in change.items():
             a[names.index(k)] = v
-        return mla.mla_prefill_attention_paged(*a, stream=s)
+        return fn(*a, stream=1)   # any non-null handle: these calls fail before using it
+    return call
+
+
+def test_paged_attention_host_argument_errors(lib):
+    names = ["out", "lse", "oacc", "lacc", "q", "kn", "v", "kv", "rows", "ncr", "iro", "cl", "bro", "co",
+             "bl", "ch", "mc", "B", "H", "mpl", "T", "S", "scale"]
+    ok = [16, None, None, None, 16, 16, 16, 16, 16, 64, 16, 16, 16, 16, 16, 0, 1, 1, 4, 16, 16, 8, 0.1]
+    call = _caller(mla.mla_prefill_attention_paged, ok, names)
     assert call(kv=None) == mla.MLA_ERR_ARG
     assert call(kv=24) == mla.MLA_ERR_ARG              # misaligned cache
-    assert call(pt=None) == mla.MLA_ERR_ARG
-    assert call(np=0) == mla.MLA_ERR_ARG
-    assert call(ps=0) == mla.MLA_ERR_ARG
-    assert call(mp=0) == mla.MLA_ERR_ARG
-    assert call(np=1 << 20, ps=1 << 11) == mla.MLA_ERR_ARG   # 2^31 cache rows
+    assert call(rows=None) == mla.MLA_ERR_ARG
+    assert call(ncr=0) == mla.MLA_ERR_ARG
     assert call(H=0) == mla.MLA_ERR_GEOMETRY
     assert call(mc=2) == mla.MLA_ERR_ARG               # merge scratch missing
     # the buffered entry point still wants its k_rope buffer
     args = [16, None, None, None, 16, 16, 16, None] + [16] * 5 + [0, 1, 1, 4, 16, 16, 8, 0.1]
-    assert mla.mla_prefill_attention(*args, stream=s) == mla.MLA_ERR_ARG
+    assert mla.mla_prefill_attention(*args, stream=1) == mla.MLA_ERR_ARG
+
+
+def test_paged_upproject_host_argument_errors(lib):
+    names = ["kn", "v", "kv", "rows", "ncr", "bl", "ch", "S", "wk", "wuv", "H", "dt"]
+    ok = [16, 16, 16, 16, 64, 16, 0, 8, 16, 16, 2, mla.MLA_BF16]
+    call = _caller(mla.mla_upproject_paged, ok, names)
+    assert call(kv=None) == mla.MLA_ERR_ARG
+    assert call(kv=8) == mla.MLA_ERR_ARG
+    assert call(rows=None) == mla.MLA_ERR_ARG
+    assert call(bl=None) == mla.MLA_ERR_ARG
+    assert call(ncr=0) == mla.MLA_ERR_ARG
+    assert call(H=0) == mla.MLA_ERR_GEOMETRY
+    assert call(dt=5) == mla.MLA_ERR_DTYPE
+
+
+def test_chunk_cache_rows_host_argument_errors(lib):
+    names = ["rows", "pt", "np", "ps", "mp", "bro", "co", "bl", "mc", "B", "S"]
+    ok = [16, 16, 4, 16, 2, 16, 16, 16, 2, 1, 8]
+    call = _caller(mla.mla_chunk_cache_rows, ok, names)
+    for k in ("rows", "pt", "bro", "co", "bl"):
+        assert call(**{k: None}) == mla.MLA_ERR_ARG, k
+    for k in ("np", "ps", "mp", "mc", "B", "S"):
+        assert call(**{k: 0}) == mla.MLA_ERR_ARG, k
+    assert call(np=1 << 20, ps=1 << 11) == mla.MLA_ERR_ARG   # 2^31 cache rows
+    assert call(mc=1 << 16) == mla.MLA_ERR_ARG
 
 
 def test_selftest_host_argument_errors(lib):

@@ -454,12 +454,68 @@ def test_upproject(dtype, H, rows, S):
     assert np.all(gk[pad:] == 3.0) and np.all(gv[pad:] == 3.0)       # untouched beyond it
 
 
+def gpu_cache_rows(inp, tabs, S, mc, st=None, pt=None):
+    """mla_chunk_cache_rows for all chunks: [mc, S] int32 on the device."""
+    rows = torch.full((mc, S), -7, dtype=torch.int32, device=DEV)
+    pt = inp["page_table"].to(DEV) if pt is None else pt
+    mla.check(mla.mla_chunk_cache_rows(rows, pt, inp["num_pages"], inp["page_size"], inp["max_pages"],
+                                       *tabs, mc, inp["B"], S, st))
+    return rows
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("tiny_ragged", {}),
+    ("tiny_ragged", {"page_size": 1, "shuffle_pages": True}),
+    ("ragged_chunked_cache", {"H": 1, "B": 300, "buffer_token_size": 512, "max_chunks": 8,
+                              "new_range": (1, 5), "cache_range": (0, 4), "page_size": 3}),
+    ("ragged_chunked_cache", {}),
+    ("longctx_fp8", {}),
+])
+def test_chunk_cache_rows_bit_exact(name, kw):
+    """The table of every chunk equals the oracle's, entry for entry (entries
+    past a chunk's rows are 0), on the full-size workloads too."""
+    w = scaled(WORKLOADS[name], **kw) if kw else WORKLOADS[name]
+    inp = make_inputs(w)
+    c = {k: O.codes(inp[k]) for k in ("input_row_offsets", "cache_lengths", "page_table")}
+    S, mc = w.buffer_token_size, w.max_chunks
+    plan = O.prefill_plan(c["input_row_offsets"], c["cache_lengths"], S, mc)
+    g = gpu_plan(c["input_row_offsets"], c["cache_lengths"], S, mc)
+    tabs = [torch.as_tensor(x.astype(np.int32)).to(DEV) for x in g[:3]]
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    rows = gpu_cache_rows(inp, tabs, S, mc, st).cpu().numpy()
+    assert st.item() == 0
+    for ch in range(mc):
+        ref, ost = O.chunk_cache_rows(c["page_table"], inp["page_size"], inp["num_pages"], plan, ch, S)
+        assert ost == 0
+        np.testing.assert_array_equal(rows[ch], ref)
+
+
+def test_chunk_cache_rows_bad_page_reports_status():
+    w = scaled(WORKLOADS["tiny_ragged"], page_size=16)
+    inp = make_inputs(w)
+    c = {k: O.codes(inp[k]) for k in ("input_row_offsets", "cache_lengths", "page_table")}
+    S, mc = w.buffer_token_size, w.max_chunks
+    g = gpu_plan(c["input_row_offsets"], c["cache_lengths"], S, mc)
+    tabs = [torch.as_tensor(x.astype(np.int32)).to(DEV) for x in g[:3]]
+    pt = inp["page_table"].clone()
+    pt[inp["B"] - 1, 0] = inp["num_pages"]
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    rows = gpu_cache_rows(inp, tabs, S, mc, st, pt=pt.to(DEV))
+    torch.cuda.synchronize()
+    assert st.item() == mla.MLA_DEV_BAD_PAGE
+    plan = O.prefill_plan(c["input_row_offsets"], c["cache_lengths"], S, mc)
+    for ch in range(mc):
+        ref, _ = O.chunk_cache_rows(O.codes(pt), inp["page_size"], inp["num_pages"], plan, ch, S)
+        np.testing.assert_array_equal(rows[ch].cpu().numpy(), ref)
+
+
 def _paged_upproject_case(w, oracle=True, bad_page=False):
-    """mla_upproject_paged, c_kv rows read from the paged cache, every chunk:
-    (1) bit for bit equal to mla_gather_latent + mla_upproject over the whole
-    K and V buffers (the zeroed tile tail and the untouched rows past it
-    included), and (2) within rounding of the oracle's projection of the
-    oracle's gathered rows."""
+    """mla_upproject_paged, c_kv rows read from the paged cache through the
+    chunk's cache-row table, every chunk: (1) bit for bit equal to
+    mla_gather_latent + mla_upproject over the whole K and V buffers (the
+    zeroed tile tail and the untouched rows past it included), and (2) within
+    rounding of the oracle's projection of the oracle's gathered rows.  With
+    bad_page, one table entry points outside the cache: reported, no fault."""
     inp = make_inputs(w)
     dt = w.dtype
     c = {k: O.codes(inp[k]) for k in ("kv_cache", "page_table", "input_row_offsets", "cache_lengths",
@@ -469,11 +525,13 @@ def _paged_upproject_case(w, oracle=True, bad_page=False):
     g = gpu_plan(c["input_row_offsets"], c["cache_lengths"], S, mc)
     bro, co, bl = [torch.as_tensor(x.astype(np.int32)).to(DEV) for x in g[:3]]
     kv, pt = inp["kv_cache"].to(DEV), inp["page_table"].to(DEV)
-    if bad_page:
-        pt[B - 1] = inp["num_pages"]
     wk, wuv = inp["w_k"].to(DEV), inp["w_uv"].to(DEV)
     wsc = inp["w_scale"]
     paging = (inp["num_pages"], inp["page_size"], inp["max_pages"])
+    ncr = inp["num_pages"] * inp["page_size"]
+    rows_t = gpu_cache_rows(inp, [bro, co, bl], S, mc)
+    if bad_page:
+        rows_t[:, 5] = ncr + 7        # a table entry outside the cache
     vdt = torch.bfloat16 if dt == "bf16" else torch.float16
     st_bad = torch.zeros(1, dtype=torch.int32, device=DEV)
     for ch in range(mc):
@@ -488,8 +546,8 @@ def _paged_upproject_case(w, oracle=True, bad_page=False):
                 mla.check(mla.mla_gather_latent(ckv, kr, kv, pt, *paging, bro, co, bl, ch, B, S, _dt(w), st))
                 mla.check(mla.mla_upproject(kn, vv, ckv, wk, wuv, bl, ch, S, H, _dt(w), 1.0, wsc, 1.0, st))
             else:
-                mla.check(mla.mla_upproject_paged(kn, vv, kv, pt, *paging, bro, co, bl, ch, B, S, wk, wuv,
-                                                  H, _dt(w), 1.0, wsc, 1.0, st))
+                mla.check(mla.mla_upproject_paged(kn, vv, kv, rows_t[ch], ncr, bl, ch, S, wk, wuv, H, _dt(w),
+                                                  1.0, wsc, 1.0, st))
             torch.cuda.synchronize()
             res[mode] = (kn, vv, int(st.item()))
         if bad_page:
@@ -681,11 +739,13 @@ def test_head_split_equals_full_call_bit_for_bit():
 
 
 def _paged_attention_case(w, seed_base=41, oracle=True, bad_page=False):
-    """mla_prefill_attention_paged, k_rope read from the paged cache, chunk by
-    chunk: (1) bit for bit equal to mla_prefill_attention given the gathered
-    k_rope rows (the masked keys past a sequence read other rows in the two
-    calls and must change nothing), and (2) against the oracle, whose k_rope
-    for a key is the cache row of its context position."""
+    """mla_prefill_attention_paged, k_rope read from the paged cache through
+    the chunk's cache-row table, chunk by chunk: (1) bit for bit equal to
+    mla_prefill_attention given the gathered k_rope rows (the masked keys past
+    a sequence read other rows in the two calls and must change nothing), and
+    (2) against the oracle, whose k_rope for a key is the cache row of its
+    context position.  With bad_page, one table entry points outside the
+    cache: reported, no fault."""
     inp = make_inputs(w)
     dt = w.dtype
     c = {k: O.codes(inp[k]) for k in ("q", "input_row_offsets", "cache_lengths", "kv_cache",
@@ -695,11 +755,13 @@ def _paged_attention_case(w, seed_base=41, oracle=True, bad_page=False):
     g = gpu_plan(c["input_row_offsets"], c["cache_lengths"], S, mc)
     tabs = [torch.as_tensor(x.astype(np.int32)).to(DEV) for x in g[:3]]
     kv, pt = inp["kv_cache"].to(DEV), inp["page_table"].to(DEV)
-    if bad_page:
-        pt[B - 1, 0] = inp["num_pages"]
     q = inp["q"].to(DEV)
     iro, cl = inp["input_row_offsets"].to(DEV), inp["cache_lengths"].to(DEV)
     paging = (inp["num_pages"], inp["page_size"], inp["max_pages"])
+    ncr = inp["num_pages"] * inp["page_size"]
+    rows_t = gpu_cache_rows(inp, tabs, S, mc)
+    if bad_page:
+        rows_t[:, 3] = -2             # a table entry outside the cache
     res = {}
     for mode in ("paged",) if bad_page else ("buffer", "paged"):
         out = torch.full((T, H, 128), float("nan"), dtype=torch.bfloat16, device=DEV)
@@ -717,8 +779,8 @@ def _paged_attention_case(w, seed_base=41, oracle=True, bad_page=False):
                                                     ch, mc, B, H, inp["max_prompt_len"], T, S,
                                                     inp["scale"], dtype=_dt(w), d_status=st))
             else:
-                mla.check(mla.mla_prefill_attention_paged(out, lse, oacc, lacc, q, kn, vv, kv, pt,
-                                                          *paging, iro, cl, *tabs, ch, mc, B, H,
+                mla.check(mla.mla_prefill_attention_paged(out, lse, oacc, lacc, q, kn, vv, kv, rows_t[ch],
+                                                          ncr, iro, cl, *tabs, ch, mc, B, H,
                                                           inp["max_prompt_len"], T, S, inp["scale"],
                                                           dtype=_dt(w), d_status=st))
         torch.cuda.synchronize()

@@ -349,6 +349,56 @@ def test_gather_bad_page_status():
     assert O.gather_latent(kv, pt, 4, plan, 0)[2] == M.STATUS_BAD_PAGE
 
 
+def test_chunk_cache_rows_by_construction():
+    """Every element of the coded cache names its (sequence, position), so the
+    row a table entry points at must carry the code of the buffer row's own
+    token, taken from the token walk; entries past the chunk are 0."""
+    rng = np.random.default_rng(11)
+    for trial in range(30):
+        B = int(rng.integers(1, 5))
+        new = rng.integers(0, 30, size=B)
+        cache = rng.integers(0, 30, size=B)
+        ps = int(rng.integers(1, 9))
+        S = int(rng.integers(1, 40))
+        iro = np.concatenate([[0], np.cumsum(new)])
+        nc = max(1, -(-int((new + cache).sum()) // S))
+        kv, pt = _coded_cache(new, cache, ps, shuffle_seed=100 + trial)
+        flat = kv.reshape(-1, M.DC)
+        plan = O.prefill_plan(iro, cache, S, nc)
+        wbro, wco, wbl, _ = _token_walk(new, cache, S, nc)
+        for c in range(nc):
+            rows, st = O.chunk_cache_rows(pt, ps, kv.shape[0], plan, c, S)
+            assert st == 0 and rows.shape == (S,)
+            n = max(int(wbl[c]), 0)
+            assert np.all(rows[n:] == 0)
+            for b in range(B):
+                for t in range(wbro[c, b + 1] - wbro[c, b]):
+                    expect = (b * 1000 + wco[c, b] + t) * 1000
+                    assert flat[rows[wbro[c, b] + t], 0] == expect
+
+
+def test_chunk_cache_rows_identity_pages():
+    """One sequence on pages 0, 1, 2, ... in order: buffer row r of chunk c is
+    cache row c * S + r (the context positions themselves)."""
+    new, cache, ps, S = [37], [20], 8, 16
+    kv, pt = _coded_cache(new, cache, ps, None)
+    plan = O.prefill_plan([0, 37], cache, S, 4)
+    for c in range(4):
+        rows, st = O.chunk_cache_rows(pt, ps, kv.shape[0], plan, c, S)
+        n = min(S, 57 - c * S)
+        np.testing.assert_array_equal(rows[:n], c * S + np.arange(n))
+
+
+def test_chunk_cache_rows_bad_page_status():
+    kv, pt = _coded_cache([4], [4], 4)
+    plan = O.prefill_plan([0, 4], [4], 8, 1)
+    pt = pt.copy()
+    pt[0, 1] = kv.shape[0]          # out of range
+    rows, st = O.chunk_cache_rows(pt, 4, kv.shape[0], plan, 0, 8)
+    assert st == M.STATUS_BAD_PAGE
+    assert np.all(rows[4:] == 0) and np.array_equal(rows[:4], pt[0, 0] * 4 + np.arange(4))
+
+
 # ----------------------------------------------------------------------------
 # Up-projection
 # ----------------------------------------------------------------------------
