@@ -250,3 +250,23 @@ def test_causal_limit_on_sparse_lists_is_caught(monkeypatch):
     _plant(monkeypatch, "mla_sparse_decode", bad)
     _must_fail(P.test_sparse_decode_over_the_whole_context_equals_dense_decode,
                P.test_sparse_decode_is_a_set_and_ignores_entries_past_topk)
+
+
+def test_cache_row_table_slips_are_caught(monkeypatch):
+    """Two slips in the cache-row table: the page's first row for every slot
+    (the slot within the page dropped), and the buffer row's index used as
+    the context position (the chunk's cache offset dropped)."""
+    orig = M.chunk_cache_rows
+
+    def page_start_only(page_table, page_size, num_pages, plan, chunk, buffer_token_size):
+        rows, st = orig(page_table, page_size, num_pages, plan, chunk, buffer_token_size)
+        return rows - rows % page_size, st
+    _plant(monkeypatch, "chunk_cache_rows", page_start_only)
+    _must_fail(P.test_chunk_cache_rows_by_construction, P.test_chunk_cache_rows_identity_pages)
+
+    def no_cache_offset(page_table, page_size, num_pages, plan, chunk, buffer_token_size):
+        bro, co, bl, extra = plan
+        return orig(page_table, page_size, num_pages, (bro, np.zeros_like(co), bl, extra), chunk,
+                    buffer_token_size)
+    _plant(monkeypatch, "chunk_cache_rows", no_cache_offset)
+    _must_fail(P.test_chunk_cache_rows_by_construction, P.test_chunk_cache_rows_identity_pages)
