@@ -486,7 +486,8 @@ int32_t mla_decode_partitions(int32_t batch_size, int32_t num_heads, int32_t max
 
 /*
  * Workspace bytes mla_decode needs: the 576-wide query rows (bf16), every
- * partition's fp32 latent result and LSE, and the merged bf16 latent result.
+ * partition's latent result (bf16) and LSE (fp32), and the merged bf16 latent
+ * result.
  * The decode branch of "mla_prefill_decode_graph_bf16" (Args: w_uk, w_uv,
  * num_partitions_in) sizes no buffer, so this call has no counterpart on the
  * pages.  Host only; 0 for invalid sizes.

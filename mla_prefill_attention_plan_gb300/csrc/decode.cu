@@ -207,7 +207,10 @@ constexpr int D_SMEM_QR = D_SMEM_K + D_KSTAGES * D_KBYTES;
 constexpr int D_SMEM_XS = D_SMEM_QR + 2 * D_QR_BYTES;        // send buffers [slot][warp]
 constexpr int D_SMEM_XR = D_SMEM_XS + 2 * 4 * D_X_BYTES;     // receive buffers [slot][warp]
 constexpr int D_SMEM_BAR = D_SMEM_XR + 2 * 4 * D_X_BYTES;
-constexpr int D_SMEM_TOTAL = D_SMEM_BAR + 512 + 1024;
+constexpr int D_SMEM_LIST = D_SMEM_BAR + 512;                // this pair's work items
+constexpr int kDecodeListMax = 256;                          // items a pair can list
+constexpr int kDecodeCompactMax = 32768;                     // item indices worth compacting
+constexpr int D_SMEM_TOTAL = D_SMEM_LIST + 4 * kDecodeListMax + 1024;
 constexpr int D_THREADS = 320;                    // producer, MMA, 4 softmax warps, 4 exchange warps
 constexpr uint32_t D_TMEM_COLS = 512;
 constexpr uint32_t D_TM_S = 0, D_TM_O = 128, D_TM_Q = 384;   // S 2 x 64, O 256, Q 128 (bf16 pairs)
@@ -238,7 +241,7 @@ struct DecodeParams {
   const int32_t* page_table;
   const int32_t* indices;          // sparse form: [B][indices_stride] physical cache rows, or null
   const int32_t* topk;             // sparse form: [B] valid entries
-  float* o_part;                   // [parts][R][512]
+  __nv_bfloat16* o_part;           // [parts][R][512], each partition's normalised result
   float* lse_part;                 // [parts][R]
   int indices_stride;
   int num_pages, page_size, max_pages;
@@ -321,11 +324,59 @@ __device__ __forceinline__ bool decode_item(const DecodeParams& p, int idx, DIte
   return true;
 }
 
+// The items a pair works on: listed (n >= 0, the pair's share of the items
+// that exist, in order), or -- past the list's capacity -- every idx of the
+// pair's static stride, the empty ones skipped.
+struct DList {
+  const int* items;
+  int n;
+};
+
 __device__ __forceinline__ bool next_decode_item(const DecodeParams& p, int& idx, int stride, int total,
-                                                 DItem& it) {
+                                                 DItem& it, const DList& wl) {
+  if (wl.n >= 0) {
+    if (total <= 0) return false;   // a timeout seen at entry: no work
+    for (; idx < wl.n; ++idx)
+      if (decode_item(p, wl.items[idx], it)) return true;
+    return false;
+  }
   for (; idx < total; idx += stride)
     if (decode_item(p, idx, it)) return true;
   return false;
+}
+
+// Every thread of the CTA: rank the items that exist (idx order) and keep
+// those of rank pair_id, pair_id + n_pairs, ... in `mine`, so that the pairs
+// get the same number of items whatever the pattern of empty ones (a static
+// stride over all indices hands some pairs several times the work of
+// others).  Returns the pair's count, or -1 (walk the stride) when the index
+// space or the pair's share is too large.  `warp_cnt`: 32 ints of scratch.
+__device__ int decode_list(const DecodeParams& p, int total, int pair_id, int n_pairs, int* mine, int* warp_cnt) {
+  if (total > kDecodeCompactMax) return -1;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nwarps = static_cast<int>(blockDim.x) >> 5;
+  int base = 0;
+  for (int u0 = 0; u0 < total; u0 += static_cast<int>(blockDim.x)) {
+    const int u = u0 + tid;
+    DItem t;
+    const bool has = u < total && decode_item(p, u, t);
+    const uint32_t m = __ballot_sync(0xffffffffu, has);
+    if (lane == 0) warp_cnt[warp] = __popc(m);
+    __syncthreads();
+    int off = base, tot = 0;
+    for (int w = 0; w < nwarps; ++w) {
+      if (w < warp) off += warp_cnt[w];
+      tot += warp_cnt[w];
+    }
+    if (has) {
+      const int r = off + __popc(m & ((1u << lane) - 1u));
+      if (r % n_pairs == pair_id && r / n_pairs < kDecodeListMax) mine[r / n_pairs] = u;
+    }
+    base += tot;
+    __syncthreads();   // warp_cnt is rewritten by the next round
+  }
+  const int n = base > pair_id ? (base - pair_id + n_pairs - 1) / n_pairs : 0;
+  return n <= kDecodeListMax ? n : -1;
 }
 
 // Physical cache row of key `pos` of sequence b, or -1 (page out of range:
@@ -393,6 +444,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(D_THREADS, 1)
     tmem_alloc(smem_u32(&sh->tmem), D_TMEM_COLS);
     tmem_relinquish();
   }
+  // The pair's work list (both CTAs compute the same one); the send buffers,
+  // unused until the first exchange, hold the scan's scratch.
+  const DList wl{reinterpret_cast<const int*>(smem + D_SMEM_LIST),
+                 decode_list(p, total_items, pair_id, n_pairs, reinterpret_cast<int*>(smem + D_SMEM_LIST),
+                             reinterpret_cast<int*>(smem + D_SMEM_XS))};
+  const int istart = wl.n >= 0 ? 0 : pair_id;
+  const int istep = wl.n >= 0 ? 1 : n_pairs;
   tc_fence_before();
   cluster_sync();   // barriers of both CTAs initialised (the other CTA stores into them)
   tc_fence_after();
@@ -414,7 +472,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(D_THREADS, 1)
     DItem it;
     const int lat_x = 256 * static_cast<int>(rank);
     const int rope_x = 512 + 32 * static_cast<int>(rank);
-    for (int idx = pair_id; ok && next_decode_item(p, idx, n_pairs, total, it); idx += n_pairs) {
+    for (int idx = istart; ok && next_decode_item(p, idx, istep, total, it, wl); idx += istep) {
       const int qs = it_n & 1;
       if (it_n >= 2 &&
           !(ok = mbar_wait_warp(smem_u32(&sh->q_free[qs]), ((it_n >> 1) & 1) ^ 1, status, abort_flag)))
@@ -501,7 +559,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(D_THREADS, 1)
       uint32_t g = 0, it_n = 0;
       DItem it;
       bool ok = true;
-      for (int idx = pair_id; ok && next_decode_item(p, idx, n_pairs, total, it); idx += n_pairs) {
+      for (int idx = istart; ok && next_decode_item(p, idx, istep, total, it, wl); idx += istep) {
         const int qs = it_n & 1;
         if (!(ok = mbar_wait(smem_u32(&sh->q_ready), it_n & 1, status, abort_flag))) break;
         if (!(ok = mbar_wait(smem_u32(&sh->q_full[qs]), (it_n >> 1) & 1, status, abort_flag))) break;
@@ -578,7 +636,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(D_THREADS, 1)
     uint32_t g = 0;
     bool ok = true;
     DItem it;
-    for (int idx = pair_id; ok && next_decode_item(p, idx, n_pairs, total, it); idx += n_pairs) {
+    for (int idx = istart; ok && next_decode_item(p, idx, istep, total, it, wl); idx += istep) {
       for (int j = 0; j < it.n_kv; ++j) {
         const uint32_t gj = g + j;
         const uint32_t sb = gj & 1, use = gj >> 1;
@@ -646,9 +704,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(D_THREADS, 1)
       if (lane == 0) mbar_arrive(smem_u32(&sh->q_ready));
     };
 
-    int idx = pair_id;
+    int idx = istart;
     DItem it;
-    bool have = next_decode_item(p, idx, n_pairs, total, it);
+    bool have = next_decode_item(p, idx, istep, total, it, wl);
     if (have) stage_q(it);
     while (have && ok) {
       // This row's keys: [key0, hi) of the partition, causal for dense decode.
@@ -758,9 +816,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(D_THREADS, 1)
       }
       if (!ok) break;
       g += it.n_kv;
-      int nidx = idx + n_pairs;
+      int nidx = idx + istep;
       DItem nx;
-      const bool have_next = next_decode_item(p, nidx, n_pairs, total, nx);
+      const bool have_next = next_decode_item(p, nidx, istep, total, nx, wl);
       // Every S MMA of this item has completed (its last s_full): the next
       // item's Q may replace this one's in TMEM.
       if (have_next) stage_q(nx);
@@ -771,18 +829,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(D_THREADS, 1)
       const bool store = row < it.nrows;
       const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
       const long long grow = it.row0 + row;
-      float* dst = p.o_part + (static_cast<long long>(it.k) * p.R + grow) * 512 + 256 * rank;
+      __nv_bfloat16* dst = p.o_part + (static_cast<long long>(it.k) * p.R + grow) * 512 + 256 * rank;
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
         uint32_t r[32];
         tmem_ld32(tmem + lane_off + D_TM_O + c * 32, r);
         tmem_ld_wait();
         if (store) {
-          float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            d4[i] = make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
-                                __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
+          for (int i = 0; i < 4; ++i)
+            d4[i] = make_uint4(pack_bf16(__uint_as_float(r[8 * i]) * inv, __uint_as_float(r[8 * i + 1]) * inv),
+                               pack_bf16(__uint_as_float(r[8 * i + 2]) * inv, __uint_as_float(r[8 * i + 3]) * inv),
+                               pack_bf16(__uint_as_float(r[8 * i + 4]) * inv, __uint_as_float(r[8 * i + 5]) * inv),
+                               pack_bf16(__uint_as_float(r[8 * i + 6]) * inv, __uint_as_float(r[8 * i + 7]) * inv));
         }
       }
       tc_fence_before();
@@ -818,48 +878,84 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(D_THREADS, 1)
 // One row (token, head) per 128 threads, 4 latent columns a thread: merge the
 // partitions' (O, LSE) by LSE, add the attention sink (a logit with no value)
 // to the denominator when given, and round the latent result to bf16.
-__global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p, __nv_bfloat16* __restrict__ o_lat,
+// Each CTA merges a contiguous range of rows, two at a time (128 threads a
+// row, 4 latent columns a thread).  The sequence of a row is found once and
+// then followed as the token advances; four partitions' partial rows are
+// requested before any is used, and five CTAs fit on an SM.
+__global__ void __launch_bounds__(256, 5) decode_merge_kernel(const DecodeParams p, __nv_bfloat16* __restrict__ o_lat,
                                                            float* __restrict__ lse_out,
                                                            const float* __restrict__ sink) {
   if (timed_out_before(p.status)) return;
+  constexpr int KU = 4;                        // partitions loaded together
   const int sub = threadIdx.x >> 7;            // row within the CTA's pair of rows
   const int c = (threadIdx.x & 127) * 4;       // first latent column
-  for (long long grow = static_cast<long long>(blockIdx.x) * 2 + sub; grow < p.R;
-       grow += static_cast<long long>(gridDim.x) * 2) {
+  const long long per = ((p.R + gridDim.x - 1) / gridDim.x + 1) / 2 * 2;
+  const long long r_begin = static_cast<long long>(blockIdx.x) * per;
+  const long long r_end = min(static_cast<long long>(p.R), r_begin + per);
+  int b = -1;
+  uint32_t qa = 0, qe = 0;
+  for (long long grow = r_begin + sub; grow < r_end; grow += 2) {
     const int t = static_cast<int>(grow / p.H);
-    int lo = 0, hi_b = p.B;                    // largest b with iro[b] <= t
-    while (hi_b - lo > 1) {
-      const int mid = (lo + hi_b) >> 1;
-      if (p.iro[mid] <= static_cast<uint32_t>(t)) lo = mid; else hi_b = mid;
+    if (b < 0 || static_cast<uint32_t>(t) >= qe || static_cast<uint32_t>(t) < qa) {
+      int lo = 0, hi_b = p.B;                  // largest b with iro[b] <= t
+      while (hi_b - lo > 1) {
+        const int mid = (lo + hi_b) >> 1;
+        if (__ldg(p.iro + mid) <= static_cast<uint32_t>(t)) lo = mid; else hi_b = mid;
+      }
+      b = lo;
+      qa = __ldg(p.iro + b);
+      qe = __ldg(p.iro + b + 1);
     }
-    const int b = lo;
-    const uint32_t qa = p.iro[b], qe = p.iro[b + 1];
     if (!(qa <= static_cast<uint32_t>(t) && static_cast<uint32_t>(t) < qe)) {
       // A token outside every sequence: zeros, so the projection reads no garbage.
       *reinterpret_cast<uint2*>(o_lat + grow * 512 + c) = make_uint2(0u, 0u);
       if (lse_out != nullptr && c == 0) lse_out[grow] = kNegInfD;
+      b = -1;
       continue;
     }
-    const long long cb = p.cache_len[b];
+    const long long cb = __ldg(p.cache_len + b);
     const long long L = decode_keys(p, b, cb, static_cast<long long>(qe - qa));
     long long lim = L;
     if (p.indices == nullptr) lim = min(lim, cb + (t - static_cast<long long>(qa)) + 1);
     const int count = decode_part_count(p, L);
     const long long size = decode_part_size(L, count);
+    // Partitions holding keys the row sees: 0 .. used - 1.
+    const int used = static_cast<int>(min(static_cast<long long>(count), (lim + size - 1) / size));
+    // One pass: each group of KU partitions is loaded whole, then merged into
+    // the running (max, sum, O) by LSE.
     float mx = kNegInfD;
-    for (int k = 0; k < count; ++k)
-      if (static_cast<long long>(k) * size < lim) mx = fmaxf(mx, p.lse_part[static_cast<long long>(k) * p.R + grow]);
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
     float tot = 0.f;
-    if (mx != kNegInfD) {
-      for (int k = 0; k < count; ++k) {
-        if (static_cast<long long>(k) * size >= lim) continue;
-        const float lk = p.lse_part[static_cast<long long>(k) * p.R + grow];
-        const float wk = __expf(lk - mx);
-        tot += wk;
-        const float4 v = *reinterpret_cast<const float4*>(p.o_part + (static_cast<long long>(k) * p.R + grow) * 512 + c);
-        o.x += wk * v.x; o.y += wk * v.y; o.z += wk * v.z; o.w += wk * v.w;
+    for (int k0 = 0; k0 < used; k0 += KU) {
+      float4 v[KU];
+      float lk[KU];
+#pragma unroll
+      for (int i = 0; i < KU; ++i) {
+        const int k = k0 + i;
+        const long long at = static_cast<long long>(k) * p.R + grow;
+        lk[i] = k < used ? __ldg(p.lse_part + at) : kNegInfD;
+        if (k < used) {
+          const uint2 raw = __ldg(reinterpret_cast<const uint2*>(p.o_part + at * 512 + c));
+          v[i] = make_float4(bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y));
+        } else {
+          v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
+      float cm = lk[0];
+#pragma unroll
+      for (int i = 1; i < KU; ++i) cm = fmaxf(cm, lk[i]);
+      const float nm = fmaxf(mx, cm);
+      if (nm == kNegInfD) continue;
+      const float r = mx == kNegInfD ? 0.f : __expf(mx - nm);
+      tot *= r;
+      o.x *= r; o.y *= r; o.z *= r; o.w *= r;
+#pragma unroll
+      for (int i = 0; i < KU; ++i) {
+        const float w = lk[i] == kNegInfD ? 0.f : __expf(lk[i] - nm);
+        tot += w;
+        o.x += w * v[i].x; o.y += w * v[i].y; o.z += w * v[i].z; o.w += w * v[i].w;
+      }
+      mx = nm;
     }
     float lse = tot > 0.f ? mx + __logf(tot) : kNegInfD;
     float w = tot > 0.f ? 1.0f / tot : 0.f;
@@ -932,7 +1028,7 @@ DecodeLayout decode_layout(int T, int H, int parts) {
     return at;
   };
   L.q_full = take(R * 576 * 2);
-  L.o_part = take(static_cast<size_t>(parts) * R * 512 * 4);
+  L.o_part = take(static_cast<size_t>(parts) * R * 512 * 2);
   L.lse_part = take(static_cast<size_t>(parts) * R * 4);
   L.o_lat = take(R * 512 * 2);
   L.total = off;
@@ -960,7 +1056,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   const DecodeLayout L = decode_layout(T, H, a.parts);
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   __nv_bfloat16* q_full = reinterpret_cast<__nv_bfloat16*>(ws + L.q_full);
-  float* o_part = reinterpret_cast<float*>(ws + L.o_part);
+  __nv_bfloat16* o_part = reinterpret_cast<__nv_bfloat16*>(ws + L.o_part);
   float* lse_part = reinterpret_cast<float*>(ws + L.lse_part);
   __nv_bfloat16* o_lat = reinterpret_cast<__nv_bfloat16*>(ws + L.o_lat);
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
