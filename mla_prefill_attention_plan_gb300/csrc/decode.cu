@@ -400,10 +400,50 @@ __device__ __forceinline__ int decode_phys_row(const DecodeParams& p, int b, lon
   return static_cast<int>(static_cast<long long>(page) * p.page_size + pos % p.page_size);
 }
 
+// 64 key rows of a stage from the cache, 16 bytes per cp.async: lane l holds
+// the cache rows of keys l (ra) and l + 32 (rb); each warp instruction copies
+// 32 / CH whole rows (CH = 16-byte chunks a row), chunk l % CH of row
+// RPI * i + l / CH, into the swizzled layout a tensor-map tile load would give
+// (SW128 for 128-byte rows, SW64 for 64-byte rows).  `col0` points at the
+// columns to copy in cache row 0.
+template <int ROW_BYTES>
+__device__ __forceinline__ void key_rows_cp_async(uint32_t dst, const uint8_t* col0, int ra, int rb) {
+  constexpr int CH = ROW_BYTES / 16;
+  constexpr int RPI = 32 / CH;
+  constexpr int ITERS = 64 / RPI;
+  const int lane = threadIdx.x & 31;
+  const int c = lane % CH;
+  const uint8_t* src = col0 + c * 16;
+#pragma unroll
+  for (int i = 0; i < ITERS; ++i) {
+    const int r = RPI * i + lane / CH;
+    const int row = __shfl_sync(0xffffffffu, i < ITERS / 2 ? ra : rb, r & 31);
+    const int sw = ROW_BYTES == 128 ? (r & 7) : ((r >> 1) & 3);
+    cp_async16(dst + r * ROW_BYTES + ((c ^ sw) << 4), src + static_cast<size_t>(row) * 1152);
+  }
+}
+
+// A stage's cp.async rows have landed (all but the newest N groups of the
+// warp): fence them into the async proxy the MMAs read through, then arrive
+// on the stage's barrier.
+template <int N>
+__device__ __forceinline__ void key_rows_landed(uint32_t bar) {
+  cp_async_wait<N>();
+  fence_async_smem();
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
+// DENSE: every 64-key tile is 64 consecutive rows of one page, loaded as
+// rectangular tiles; otherwise (page size not a multiple of 64, or sparse
+// lists) the rows are copied one by one with cp.async.  Two instantiations,
+// so that the dense one carries no trace of the other path.
+template <bool DENSE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(D_THREADS, 1)
     decode_attn_kernel(const __grid_constant__ CUtensorMap qr_map, const __grid_constant__ CUtensorMap kl_map,
                        const __grid_constant__ CUtensorMap kr_map, const __grid_constant__ CUtensorMap kl1_map,
-                       const __grid_constant__ CUtensorMap kr1_map, const DecodeParams p, int total_items) {
+                       const __grid_constant__ CUtensorMap kr1_map, const DecodeParams p, int total_items,
+                       const uint8_t* __restrict__ cache_rows) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   DecodeSmem* sh = reinterpret_cast<DecodeSmem*>(smem + D_SMEM_BAR);
@@ -462,12 +502,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(D_THREADS, 1)
     // ------------------------------------------------------------ producer
     if (elect_one()) {
       prefetch_tmap(&qr_map);
-      prefetch_tmap(p.dense_tiles ? &kl_map : &kl1_map);
-      prefetch_tmap(p.dense_tiles ? &kr_map : &kr1_map);
+      prefetch_tmap(DENSE ? &kl_map : &kl1_map);
+      prefetch_tmap(DENSE ? &kr_map : &kr1_map);
     }
     __syncwarp();
     uint32_t g = 0, it_n = 0;
     uint32_t q_issued = 0, k_issued = 0;   // Q-rope and K-tile loads issued
+    int k_pend = -1;                       // stage whose cp.async rows are in flight
     bool ok = true;
     DItem it;
     const int lat_x = 256 * static_cast<int>(rank);
@@ -491,7 +532,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(D_THREADS, 1)
         // The tile's cache rows (a page-table or index read) before waiting for
         // its stage, so that the read's latency overlaps the wait.
         int ra, rb;
-        if (p.dense_tiles) {
+        if constexpr (DENSE) {
           // 64 consecutive positions, all in one page.
           ra = decode_phys_row(p, it.b, pos0);
           if (ra < 0) ra = p.num_pages * p.page_size;   // past the end: reads zeros
@@ -508,7 +549,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(D_THREADS, 1)
           break;
         const uint32_t kf = smem_u32(&sh->k_full[st]);
         const uint32_t kd = smem_u32(smem + D_SMEM_K + st * D_KBYTES);
-        if (p.dense_tiles) {
+        if constexpr (DENSE) {
           if (elect_one()) {
             mbar_expect_tx(kf, D_KBYTES);
 #pragma unroll
@@ -516,29 +557,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(D_THREADS, 1)
             tma_load_2d(kd + D_KLAT, &kr_map, kf, rope_x, ra);
           }
         } else {
-          // Any rows: four at a time (tile::gather4), 16 lanes each one group.
-          int y[4];
+          // Any rows, 16 bytes per cp.async (one-row TMA gathers cost far
+          // more per byte); the previous stage is counted once its rows land.
+          const uint8_t* cache = cache_rows;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int key = 4 * (lane & 15) + k;
-            const int va = __shfl_sync(0xffffffffu, ra, key & 31);
-            const int vb = __shfl_sync(0xffffffffu, rb, key & 31);
-            y[k] = key < 32 ? va : vb;
-          }
-          if (lane == 0) mbar_expect_tx(kf, D_KBYTES);
-          __syncwarp();
-          if (lane < 16) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-              tma_gather4_2d(kd + c * D_KBLK + lane * 512, &kl1_map, kf, lat_x + 64 * c, y[0], y[1], y[2], y[3]);
-            tma_gather4_2d(kd + D_KLAT + lane * 256, &kr1_map, kf, rope_x, y[0], y[1], y[2], y[3]);
-          }
+          for (int c = 0; c < 4; ++c) key_rows_cp_async<128>(kd + c * D_KBLK, cache + (lat_x + 64 * c) * 2, ra, rb);
+          key_rows_cp_async<64>(kd + D_KLAT, cache + rope_x * 2, ra, rb);
+          cp_async_commit();
+          if (k_pend >= 0) key_rows_landed<1>(smem_u32(&sh->k_full[k_pend]));
+          k_pend = st;
         }
         __syncwarp();
         ++k_issued;
       }
+      if constexpr (!DENSE) {   // the item's last stage, before any other wait
+        if (k_pend >= 0) key_rows_landed<0>(smem_u32(&sh->k_full[k_pend]));
+        k_pend = -1;
+      }
       g += it.n_kv;
       ++it_n;
+    }
+    if constexpr (!DENSE) {
+      if (k_pend >= 0) key_rows_landed<0>(smem_u32(&sh->k_full[k_pend]));
     }
     // Every issued load lands before the CTA leaves: the last phase of each
     // slot and stage that a load used.
@@ -978,6 +1018,7 @@ __global__ void __launch_bounds__(256, 5) decode_merge_kernel(const DecodeParams
 
 // Two-CTA clusters of the attention kernel the current device can keep
 // resident, or 0.
+template <bool DENSE>
 int decode_clusters(int device) {
   static std::mutex mu;
   static int cached[64];
@@ -985,13 +1026,13 @@ int decode_clusters(int device) {
   std::lock_guard<std::mutex> lock(mu);
   if (device < 0 || device >= 64) return 0;
   if (!done[device]) {
-    cudaFuncSetAttribute(decode_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, D_SMEM_TOTAL);
+    cudaFuncSetAttribute(decode_attn_kernel<DENSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, D_SMEM_TOTAL);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2);
     cfg.blockDim = dim3(D_THREADS);
     cfg.dynamicSmemBytes = D_SMEM_TOTAL;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, decode_attn_kernel, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, decode_attn_kernel<DENSE>, &cfg) != cudaSuccess) {
       cudaGetLastError();
       n = 0;
     }
@@ -1108,11 +1149,18 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   if (total > 0) {
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    const int clusters = decode_clusters(dev);
+    const bool dense = p.dense_tiles != 0;
+    const int clusters = dense ? decode_clusters<true>(dev) : decode_clusters<false>(dev);
     if (clusters <= 0) return cudaErrorInvalidConfiguration;
     const int grid = 2 * static_cast<int>(std::min<long long>(total, clusters));
-    decode_attn_kernel<<<grid, D_THREADS, D_SMEM_TOTAL, stream>>>(qr_map, kl_map, kr_map, kl1_map, kr1_map, p,
-                                                                  static_cast<int>(total));
+    if (dense)
+      decode_attn_kernel<true><<<grid, D_THREADS, D_SMEM_TOTAL, stream>>>(qr_map, kl_map, kr_map, kl1_map, kr1_map,
+                                                                          p, static_cast<int>(total),
+                                                                          static_cast<const uint8_t*>(a.kv_cache));
+    else
+      decode_attn_kernel<false><<<grid, D_THREADS, D_SMEM_TOTAL, stream>>>(qr_map, kl_map, kr_map, kl1_map,
+                                                                           kr1_map, p, static_cast<int>(total),
+                                                                           static_cast<const uint8_t*>(a.kv_cache));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
 
