@@ -474,7 +474,7 @@ mla_status_t mla_prefill(void* out, float* lse, const void* q, const uint32_t* i
  * Partitions per sequence the library uses for mla_decode when num_partitions
  * is 0 (size the workspace with it).  It cuts every sequence's keys into
  * pieces of about the same size -- between 256 and 2048 keys, chosen from the
- * batch's sizes for about four waves of work on the GPU's SM pairs -- so that
+ * batch's sizes for about two waves of work on the GPU's SM pairs -- so that
  * short and long sequences make items of equal cost; this returns the most
  * pieces a sequence can get.  max_keys: max_seq_len for dense decode (the
  * longest context, new tokens included), the list stride for sparse decode.
@@ -524,7 +524,8 @@ size_t mla_decode_workspace_bytes(int32_t num_heads, int32_t total_q_tokens, int
  * num_partitions > 0 splits every sequence into that many ranges; 0 lets the
  * library pick ranges of equal size (mla_decode_partitions).
  * q_lat and the merged latent result are rounded to bf16 for the tensor-core
- * projections; scores, softmax and the merge run in fp32.
+ * projections, and each partition's normalised latent result is stored as
+ * bf16; scores, softmax, LSE and the merge arithmetic run in fp32.
  *
  * out:      [total_q_tokens][num_heads][128] bf16, output
  * lse:      [total_q_tokens][num_heads] fp32 output (natural log), or NULL
