@@ -10,7 +10,7 @@
 // back per head.  Four launches:
 //
 //   1. head_gemm_kernel  q_lat[t, h] = w_uk[h] q_nope[t, h]      (tcgen05 GEMM,
-//      M = tokens, N = 512, K = 128 per head), written with q's rope part as
+//      M = tokens, N = 512 in four CTAs, K = 128 per head), written with q's rope part as
 //      the 576-wide query rows q_full [T*H, 576] bf16.
 //   2. decode_attn_kernel  the latent attention over key partitions, on pairs
 //      of SMs.  A work item is (sequence, 128 query rows, key partition); the
@@ -67,7 +67,9 @@ struct HeadGemm {
   static_assert(K % 64 == 0 && N % NB == 0, "shape");
 };
 
-template <int N, int K, int STAGES>
+// SPLIT > 1: the head's N * SPLIT output columns are shared by SPLIT CTAs
+// (grid.y = H * SPLIT), N each, so that a small M still fills the GPU.
+template <int N, int K, int STAGES, int SPLIT>
 __global__ void __launch_bounds__(192, 1)
     head_gemm_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap b_map,
                      int a_col0, int a_hstride, __nv_bfloat16* __restrict__ out, long long out_ld,
@@ -83,7 +85,8 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* sh = reinterpret_cast<Bars*>(smem + C::SMEM_BAR);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.y;
+  const int h = blockIdx.y / SPLIT;
+  const int nc = blockIdx.y % SPLIT;   // this CTA's N-column block of the head
   const int m0 = blockIdx.x * 128;
   if (timed_out_before(status)) return;   // an earlier kernel timed out: no work
 
@@ -122,7 +125,7 @@ __global__ void __launch_bounds__(192, 1)
         tma_load_2d(a, &a_map, full, a_col0 + h * a_hstride + kb * 64, m0);
 #pragma unroll
         for (int nb = 0; nb < N; nb += C::NB)
-          tma_load_2d(a + C::A_BYTES + nb * 128, &b_map, full, kb * 64, h * N + nb);
+          tma_load_2d(a + C::A_BYTES + nb * 128, &b_map, full, kb * 64, (h * SPLIT + nc) * N + nb);
         last[s] = (kb / STAGES) & 1;
       }
       volatile int never = 0;
@@ -161,7 +164,8 @@ __global__ void __launch_bounds__(192, 1)
     if (mbar_wait_warp(smem_u32(&sh->done), 0, status, abort_flag)) {
       tc_fence_after();
       const bool row_ok = m0 + row < M;
-      __nv_bfloat16* dst = out + static_cast<long long>(m0 + row) * out_ld + static_cast<long long>(h) * out_hstride;
+      __nv_bfloat16* dst =
+          out + static_cast<long long>(m0 + row) * out_ld + static_cast<long long>(h) * out_hstride + nc * N;
 #pragma unroll 1
       for (int c = 0; c < N / 32; ++c) {
         uint32_t r[32];
@@ -176,7 +180,7 @@ __global__ void __launch_bounds__(192, 1)
           for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
         }
       }
-      if (rope_src != nullptr && row_ok) {
+      if (rope_src != nullptr && row_ok && nc == SPLIT - 1) {
         const uint4* s4 = reinterpret_cast<const uint4*>(rope_src + static_cast<long long>(m0 + row) * rope_ld +
                                                          static_cast<long long>(h) * rope_hstride);
         uint4* d4 = reinterpret_cast<uint4*>(dst + N);
@@ -1042,17 +1046,17 @@ int decode_clusters(int device) {
   return cached[device];
 }
 
-template <int N, int K, int STAGES>
+template <int N, int K, int STAGES, int SPLIT = 1>
 cudaError_t launch_head_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, int a_col0, int a_hstride,
                              __nv_bfloat16* out, long long out_ld, int out_hstride, const __nv_bfloat16* rope_src,
                              long long rope_ld, int rope_hstride, int M, int H, int32_t* status,
                              cudaStream_t stream) {
   using C = HeadGemm<N, K, STAGES>;
-  cudaError_t e = cudaFuncSetAttribute(head_gemm_kernel<N, K, STAGES>,
+  cudaError_t e = cudaFuncSetAttribute(head_gemm_kernel<N, K, STAGES, SPLIT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_TOTAL);
   if (e != cudaSuccess) return e;
-  const dim3 grid((M + 127) / 128, H);
-  head_gemm_kernel<N, K, STAGES><<<grid, 192, C::SMEM_TOTAL, stream>>>(
+  const dim3 grid((M + 127) / 128, H * SPLIT);
+  head_gemm_kernel<N, K, STAGES, SPLIT><<<grid, 192, C::SMEM_TOTAL, stream>>>(
       a_map, b_map, a_col0, a_hstride, out, out_ld, out_hstride, rope_src, rope_ld, rope_hstride, M, status);
   return cudaGetLastError();
 }
@@ -1108,12 +1112,14 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   CUtensorMap qa_map, wuk_map;
   if (!encode_2d(&qa_map, a.q, bf, static_cast<uint64_t>(H) * 192, T, static_cast<uint64_t>(H) * 384, 64, 128,
                  CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_2d(&wuk_map, a.w_uk, bf, 128, static_cast<uint64_t>(H) * 512, 256, 64, 256,
+      !encode_2d(&wuk_map, a.w_uk, bf, 128, static_cast<uint64_t>(H) * 512, 256, 64, 128,
                  CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  cudaError_t e = launch_head_gemm<512, 128, 2>(qa_map, wuk_map, 0, 192, q_full, static_cast<long long>(H) * 576,
-                                                576, static_cast<const __nv_bfloat16*>(a.q) + 128,
-                                                static_cast<long long>(H) * 192, 192, T, H, a.status, stream);
+  // Four CTAs a head, 128 latent columns each: a decode batch has few rows.
+  cudaError_t e = launch_head_gemm<128, 128, 2, 4>(qa_map, wuk_map, 0, 192, q_full,
+                                                   static_cast<long long>(H) * 576, 576,
+                                                   static_cast<const __nv_bfloat16*>(a.q) + 128,
+                                                   static_cast<long long>(H) * 192, 192, T, H, a.status, stream);
   if (e != cudaSuccess) return e;
 
   // 2. Latent attention over the key partitions.
