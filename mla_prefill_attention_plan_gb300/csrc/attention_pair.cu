@@ -396,11 +396,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
           auto issue_pv = [&](int j) -> bool {
             const uint32_t gp = g + j;
             const int vs = gp % PNV;
-            if (!mbar_wait_cluster(smem_u32(&sh->p_full[gp & 1]), (gp >> 1) & 1, status, abort_flag)) return false;
+            // V and the free O first: they are ready long before P as a rule,
+            // and checking them after P would add their barrier round trips to
+            // the hand-off from the softmax to P*V.
             if (!mbar_wait_cluster(smem_u32(&sh->v_full[vs]), (gp / PNV) & 1, status, abort_flag)) return false;
             if (j == 0 && it_n >= 1 &&
                 !mbar_wait_cluster(smem_u32(&sh->o_free), (it_n - 1) & 1, status, abort_flag))
               return false;
+            if (!mbar_wait_cluster(smem_u32(&sh->p_full[gp & 1]), (gp >> 1) & 1, status, abort_flag)) return false;
             tc_fence_after();
             const uint32_t v_s = smem_u32(smem + P_SMEM_V + vs * PV_BYTES);
             const uint32_t pa = tmem + P_TM_S + (gp & 1) * 128;
@@ -880,11 +883,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
           auto issue_pv = [&](int j) -> bool {
             const uint32_t gp = g + j;
             const int vs = gp % PNV;
-            if (!mbar_wait_cluster(smem_u32(&sh->p_full[gp & 1]), (gp >> 1) & 1, status, abort_flag)) return false;
+            // V and the free O first: they are ready long before P as a rule,
+            // and checking them after P would add their barrier round trips to
+            // the hand-off from the softmax to P*V.
             if (!mbar_wait_cluster(smem_u32(&sh->v_full[vs]), (gp / PNV) & 1, status, abort_flag)) return false;
             if (j == 0 && it_n >= 1 &&
                 !mbar_wait_cluster(smem_u32(&sh->o_free), (it_n - 1) & 1, status, abort_flag))
               return false;
+            if (!mbar_wait_cluster(smem_u32(&sh->p_full[gp & 1]), (gp >> 1) & 1, status, abort_flag)) return false;
             tc_fence_after();
             const uint32_t v_s = smem_u32(smem + E_SMEM_V + vs * PV_BYTES);
             const uint32_t pa = tmem + P_TM_S + (gp & 1) * 128;
