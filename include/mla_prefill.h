@@ -28,7 +28,11 @@
  *     stated otherwise.  The library allocates no memory.
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
  *     legacy default stream) and never synchronises.  A host return of
- *     MLA_OK means the work was enqueued.
+ *     MLA_OK means the work was enqueued.  The kernels of the plan, gather,
+ *     projection, attention and decode entry points are programmatic
+ *     dependent launches: each may start launching while the kernel before
+ *     it on the stream finishes, and waits for that kernel to complete before
+ *     it touches memory, so stream order is unchanged.
  *   - Tensors are dense row-major with the leading dimensions written in the
  *     comments.  Integer tables are uint32/int32 as on the pages.
  *   - Geometry is fixed by the pages: q_depth 192 = 128 nope + 64 rope,

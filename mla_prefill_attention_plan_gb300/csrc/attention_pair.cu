@@ -207,6 +207,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
   const int pair_id = blockIdx.x >> 1;
   const int n_pairs = gridDim.x >> 1;
 
+  pdl_enter();
   // Both CTAs of a pair see the same chunk length, so they return together.
   if (p.bl[p.chunk] <= 0) return;
 
@@ -684,6 +685,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
   const int pair_id = blockIdx.x >> 1;
   const int n_pairs = gridDim.x >> 1;
 
+  pdl_enter();
   // Both CTAs of a pair see the same chunk length, so they return together.
   if (p.bl[p.chunk] <= 0) return;
 
@@ -1198,11 +1200,11 @@ cudaError_t launch_attention_pair(const AttnArgs& a, cudaStream_t stream) {
   const int grid = 2 * static_cast<int>(total < clusters ? total : clusters);
   const int smem = pair_smem_bytes(P_SMEM_UNITS, p);
   if (paged)
-    attn_pair_kernel<true><<<grid, P_THREADS, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], p,
-                                                              static_cast<int>(total), pr);
+    return launch_pdl(attn_pair_kernel<true>, dim3(grid), dim3(P_THREADS), smem, stream, maps[0], maps[1], maps[2],
+                      maps[3], p, static_cast<int>(total), pr);
   else
-    attn_pair_kernel<false><<<grid, P_THREADS, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], p,
-                                                               static_cast<int>(total), pr);
+    return launch_pdl(attn_pair_kernel<false>, dim3(grid), dim3(P_THREADS), smem, stream, maps[0], maps[1],
+                      maps[2], maps[3], p, static_cast<int>(total), pr);
   return cudaGetLastError();
 }
 
@@ -1256,11 +1258,11 @@ cudaError_t launch_attention_pair_e4m3(const AttnArgs& a, cudaStream_t stream) {
   const int grid = 2 * static_cast<int>(total < clusters ? total : clusters);
   const int smem = pair_smem_bytes(E_SMEM_UNITS, p);
   if (paged)
-    attn_pair_kernel_e4m3<true><<<grid, P_THREADS, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4],
-                                                                   p, static_cast<int>(total), pr);
+    return launch_pdl(attn_pair_kernel_e4m3<true>, dim3(grid), dim3(P_THREADS), smem, stream, maps[0], maps[1],
+                      maps[2], maps[3], maps[4], p, static_cast<int>(total), pr);
   else
-    attn_pair_kernel_e4m3<false><<<grid, P_THREADS, smem, stream>>>(maps[0], maps[1], maps[2], maps[3],
-                                                                    maps[4], p, static_cast<int>(total), pr);
+    return launch_pdl(attn_pair_kernel_e4m3<false>, dim3(grid), dim3(P_THREADS), smem, stream, maps[0], maps[1],
+                      maps[2], maps[3], maps[4], p, static_cast<int>(total), pr);
   return cudaGetLastError();
 }
 

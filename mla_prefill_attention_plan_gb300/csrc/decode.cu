@@ -88,6 +88,7 @@ __global__ void __launch_bounds__(192, 1)
   const int h = blockIdx.y / SPLIT;
   const int nc = blockIdx.y % SPLIT;   // this CTA's N-column block of the head
   const int m0 = blockIdx.x * 128;
+  pdl_enter();
   if (timed_out_before(status)) return;   // an earlier kernel timed out: no work
 
   if (threadIdx.x == 0) {
@@ -457,6 +458,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(D_THREADS, 1)
   const int pair_id = blockIdx.x >> 1;
   const int n_pairs = gridDim.x >> 1;
   int32_t* status = p.status;
+  pdl_enter();
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -929,6 +931,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(D_THREADS, 1)
 __global__ void __launch_bounds__(256, 5) decode_merge_kernel(const DecodeParams p, __nv_bfloat16* __restrict__ o_lat,
                                                            float* __restrict__ lse_out,
                                                            const float* __restrict__ sink) {
+  pdl_enter();
   if (timed_out_before(p.status)) return;
   constexpr int KU = 4;                        // partitions loaded together
   const int sub = threadIdx.x >> 7;            // row within the CTA's pair of rows
@@ -1056,9 +1059,8 @@ cudaError_t launch_head_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_TOTAL);
   if (e != cudaSuccess) return e;
   const dim3 grid((M + 127) / 128, H * SPLIT);
-  head_gemm_kernel<N, K, STAGES, SPLIT><<<grid, 192, C::SMEM_TOTAL, stream>>>(
-      a_map, b_map, a_col0, a_hstride, out, out_ld, out_hstride, rope_src, rope_ld, rope_hstride, M, status);
-  return cudaGetLastError();
+  return launch_pdl(head_gemm_kernel<N, K, STAGES, SPLIT>, grid, dim3(192), C::SMEM_TOTAL, stream, a_map, b_map,
+                    a_col0, a_hstride, out, out_ld, out_hstride, rope_src, rope_ld, rope_hstride, M, status);
 }
 
 }  // namespace
@@ -1162,20 +1164,19 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     if (clusters <= 0) return cudaErrorInvalidConfiguration;
     const int grid = 2 * static_cast<int>(std::min<long long>(total, clusters));
     if (dense)
-      decode_attn_kernel<true><<<grid, D_THREADS, D_SMEM_TOTAL, stream>>>(qr_map, kl_map, kr_map, kl1_map, kr1_map,
-                                                                          p, static_cast<int>(total),
-                                                                          static_cast<const uint8_t*>(a.kv_cache));
+      e = launch_pdl(decode_attn_kernel<true>, dim3(grid), dim3(D_THREADS), D_SMEM_TOTAL, stream, qr_map, kl_map,
+                     kr_map, kl1_map, kr1_map, p, static_cast<int>(total), static_cast<const uint8_t*>(a.kv_cache));
     else
-      decode_attn_kernel<false><<<grid, D_THREADS, D_SMEM_TOTAL, stream>>>(qr_map, kl_map, kr_map, kl1_map,
-                                                                           kr1_map, p, static_cast<int>(total),
-                                                                           static_cast<const uint8_t*>(a.kv_cache));
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      e = launch_pdl(decode_attn_kernel<false>, dim3(grid), dim3(D_THREADS), D_SMEM_TOTAL, stream, qr_map, kl_map,
+                     kr_map, kl1_map, kr1_map, p, static_cast<int>(total), static_cast<const uint8_t*>(a.kv_cache));
+    if (e != cudaSuccess) return e;
   }
 
   // 3. Merge the partitions (and the sink) into the bf16 latent result.
   const long long blocks = std::min<long long>((R + 1) / 2, 8ll * sm_count());
-  decode_merge_kernel<<<static_cast<unsigned>(std::max(1ll, blocks)), 256, 0, stream>>>(p, o_lat, a.lse, a.sink);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_pdl(decode_merge_kernel, dim3(static_cast<unsigned>(std::max(1ll, blocks))), dim3(256), 0, stream,
+                      p, o_lat, a.lse, a.sink)) != cudaSuccess)
+    return e;
 
   // 4. out = w_uv[h] o_lat.
   CUtensorMap ol_map, wuv_map;

@@ -39,6 +39,7 @@ __global__ void __launch_bounds__(kThreads)
   constexpr int kPerThread = (kVecs + kThreads - 1) / kThreads;
 
   __shared__ const uint8_t* src_row[kRows];
+  pdl_enter();
   if (timed_out_before(status)) return;   // an earlier kernel timed out: no work
   const int n = min(bl[chunk], S);        // never past the buffers, whatever the table says
   const int r0 = blockIdx.x * kRows;
@@ -144,16 +145,12 @@ cudaError_t launch_gather(void* c_kv_buf, void* k_rope_buf, const void* kv_cache
                           int B, uint32_t S, int elt_bytes, int32_t* status, cudaStream_t stream) {
   const unsigned grid = static_cast<unsigned>((static_cast<uint64_t>(S) + kRows - 1) / kRows);
   if (elt_bytes == 2)
-    gather_kernel<2><<<grid, kThreads, 0, stream>>>(
-        static_cast<uint8_t*>(c_kv_buf), static_cast<uint8_t*>(k_rope_buf),
-        static_cast<const uint8_t*>(kv_cache), page_table, num_pages, page_size, max_pages, bro,
-        co, bl, chunk, B, static_cast<int>(S), status);
-  else
-    gather_kernel<1><<<grid, kThreads, 0, stream>>>(
-        static_cast<uint8_t*>(c_kv_buf), static_cast<uint8_t*>(k_rope_buf),
-        static_cast<const uint8_t*>(kv_cache), page_table, num_pages, page_size, max_pages, bro,
-        co, bl, chunk, B, static_cast<int>(S), status);
-  return cudaGetLastError();
+    return launch_pdl(gather_kernel<2>, dim3(grid), dim3(kThreads), 0, stream, static_cast<uint8_t*>(c_kv_buf),
+                      static_cast<uint8_t*>(k_rope_buf), static_cast<const uint8_t*>(kv_cache), page_table,
+                      num_pages, page_size, max_pages, bro, co, bl, chunk, B, static_cast<int>(S), status);
+  return launch_pdl(gather_kernel<1>, dim3(grid), dim3(kThreads), 0, stream, static_cast<uint8_t*>(c_kv_buf),
+                    static_cast<uint8_t*>(k_rope_buf), static_cast<const uint8_t*>(kv_cache), page_table,
+                    num_pages, page_size, max_pages, bro, co, bl, chunk, B, static_cast<int>(S), status);
 }
 
 }  // namespace mla

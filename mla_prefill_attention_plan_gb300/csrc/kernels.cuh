@@ -10,6 +10,25 @@
 
 namespace mla {
 
+// Launch with programmatic stream serialization: the kernel may begin while
+// the previous kernel of the stream finishes; it calls pdl_enter() before it
+// touches global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 cudaError_t launch_plan(uint32_t* bro, uint32_t* co, int32_t* bl, const uint32_t* iro,
                         const uint32_t* cache_len, int B, int max_chunks, uint32_t S,
                         int32_t* status, cudaStream_t stream);

@@ -98,6 +98,7 @@ __global__ void __launch_bounds__(kThreads) plan_one_cta(uint32_t* bro, uint32_t
                                                          int32_t* status) {
   __shared__ uint64_t warp_tot[32];
   __shared__ int s_bad;
+  pdl_enter();
   if (timed_out_before(status)) return;   // an earlier kernel timed out: no work
   if (threadIdx.x == 0) s_bad = (B >= 0 && iro[0] != 0) ? 1 : 0;
   __syncthreads();
@@ -163,8 +164,9 @@ __global__ void __launch_bounds__(kSThreads) plan_tile_totals(uint32_t* co, cons
                                                               const uint32_t* cache_len, int B,
                                                               const int32_t* status) {
   __shared__ uint64_t red[kSWarps];
-  // Let pass B's CTAs start their own loads while this pass runs.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // After the previous kernel of the stream, let pass B's CTAs start their
+  // own loads while this pass runs.
+  pdl_enter();
   if (timed_out_before(status)) return;   // pass B returns too
   const int t = blockIdx.x;
   const int base = t * kSTile;
@@ -306,12 +308,12 @@ cudaError_t launch_plan(uint32_t* bro, uint32_t* co, int32_t* bl, const uint32_t
                         const uint32_t* cache_len, int B, int max_chunks, uint32_t S,
                         int32_t* status, cudaStream_t stream) {
   if (B <= kOneCtaMax) {
-    plan_one_cta<<<1, kThreads, 0, stream>>>(bro, co, bl, iro, cache_len, B, max_chunks, S, status);
-    return cudaGetLastError();
+    return launch_pdl(plan_one_cta, dim3(1), dim3(kThreads), 0, stream, bro, co, bl, iro, cache_len, B, max_chunks,
+                      S, status);
   }
   const int ntiles = (B + kSTile - 1) / kSTile;
-  plan_tile_totals<<<ntiles, kSThreads, 0, stream>>>(co, iro, cache_len, B, status);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_pdl(plan_tile_totals, dim3(ntiles), dim3(kSThreads), 0, stream, co, iro, cache_len, B,
+                               static_cast<const int32_t*>(status));
   if (err != cudaSuccess) return err;
   // Pass B as a programmatic dependent launch of pass A.
   cudaLaunchConfig_t cfg = {};

@@ -58,6 +58,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return done != 0;
 }
+// Programmatic dependent launch: wait until the grids this one depends on
+// have completed and their writes are visible (a no-op for a launch without
+// the attribute), then let the next grid of the stream begin launching (its
+// blocks run up to their own wait, which orders them after this grid).
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 __device__ __forceinline__ uint32_t cluster_size() {
   uint32_t n;
   asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));

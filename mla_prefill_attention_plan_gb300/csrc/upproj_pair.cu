@@ -95,6 +95,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(U_THREADS, 1)
   const int pair_id = blockIdx.x >> 1;
   const int n_pairs = gridDim.x >> 1;
 
+  pdl_enter();
   // Both CTAs of a pair read the same row count, so they return together.
   int rows = buffer_lengths ? buffer_lengths[chunk] : S;
   if (rows <= 0) return;
@@ -480,9 +481,8 @@ cudaError_t launch_upproject(const UpprojArgs& a, cudaStream_t stream) {
   const int grid = 2 * static_cast<int>(max_tiles < clusters ? max_tiles : clusters);
   auto kernel = elt == 2 ? (paged ? upproj_pair_kernel<2, true> : upproj_pair_kernel<2, false>)
                          : (paged ? upproj_pair_kernel<1, true> : upproj_pair_kernel<1, false>);
-  kernel<<<grid, U_THREADS, U_SMEM_TOTAL, stream>>>(a_map, wk_map, wuv_map, k_map, v_map, a.buffer_lengths, a.chunk,
-                                                    int(a.S), a.H, a.out_scale, a.status, pa);
-  return cudaGetLastError();
+  return launch_pdl(kernel, dim3(grid), dim3(U_THREADS), U_SMEM_TOTAL, stream, a_map, wk_map, wuv_map, k_map, v_map,
+                    a.buffer_lengths, a.chunk, int(a.S), a.H, a.out_scale, a.status, pa);
 }
 
 }  // namespace mla
