@@ -529,9 +529,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx8[i] = fmax3(x[i], x[8 + i], x[16 + i]);
 #pragma unroll
-        for (int k = 24; k < BN; k += 16)
+        for (int k = 24; k + 16 <= BN; k += 16)
 #pragma unroll
           for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], x[k + i], x[k + 8 + i]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], x[BN - 8 + i]);
         const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
                                fmaxf(mx8[6], mx8[7]));
         const float m_new = fmaxf(m_run, mx * sl2);
@@ -1003,9 +1005,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx8[i] = fmax3(x[i], x[8 + i], x[16 + i]);
 #pragma unroll
-        for (int k = 24; k < BN; k += 16)
+        for (int k = 24; k + 16 <= BN; k += 16)
 #pragma unroll
           for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], x[k + i], x[k + 8 + i]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], x[BN - 8 + i]);
         const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
                                fmaxf(mx8[6], mx8[7]));
         const float m_new = fmaxf(m_run, mx * sl2);

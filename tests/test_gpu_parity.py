@@ -672,6 +672,41 @@ def test_attention_stage_multi_chunk(bf16_kernel):
     _attention_stage(WORKLOADS["tiny_ragged"])
 
 
+def test_attention_strongly_negative_scores(bf16_kernel):
+    """Every score of every row near -150 (about -210 in log2 units, far below
+    the fp32 exponent range once shifted by anything but the row's own
+    maximum): the output is right only if each tile's maximum is taken over
+    exactly its own scores.  q_nope = 4, k_nope = -4 plus a seeded multiple of
+    1/32 (exact in bf16), rope parts zero, two sequences with two and one key
+    tiles."""
+    rng = np.random.default_rng(5)
+    new, cache = np.array([150, 60]), np.array([0, 40])
+    B, H, S = 2, 2, 256
+    iro = np.concatenate([[0], np.cumsum(new)]).astype(np.int64)
+    T = int(iro[-1])
+    plan = O.prefill_plan(iro, cache, S, 1)
+    g = gpu_plan(iro, cache, S, 1)
+    tabs = [torch.as_tensor(x.astype(np.int32)).to(DEV) for x in g[:3]]
+    q = torch.zeros(T, H, 192, dtype=torch.bfloat16)
+    q[:, :, :128] = 4.0
+    kn = (-4.0 + rng.integers(0, 3, size=(S, H, 128)) / 32.0).astype(np.float32)
+    kn = torch.as_tensor(kn).to(torch.bfloat16)
+    kr = torch.zeros(S, 64, dtype=torch.bfloat16)
+    vv = torch.as_tensor(rng.standard_normal((S, H, 128)).astype(np.float32)).to(torch.bfloat16)
+    scale = 1.0 / math.sqrt(192.0)
+    out = torch.full((T, H, 128), float("nan"), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(T, H, dtype=torch.float32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    mla.check(mla.mla_prefill_attention(out, lse, None, None, q.to(DEV), kn.to(DEV), vv.to(DEV), kr.to(DEV),
+                                        _i32(iro).to(DEV), _i32(cache).to(DEV), *tabs, 0, 1, B, H,
+                                        int(new.max()), T, S, scale, d_status=st))
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    dec = lambda t: O.decode(O.codes(t), "bf16")
+    ref = O.attention_over_chunks(dec(q), lambda ch: (dec(kn), dec(kr), dec(vv)), plan, iro, cache, scale)
+    _compare(out, ref, "bf16", lse)
+
+
 def test_attention_offsets_past_total_q_tokens():
     """input_row_offsets[B] beyond total_q_tokens: the device reports bad
     offsets, leaves that sequence out and writes no row at or past
