@@ -567,8 +567,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
           }
           fence_async_smem();
         }
-        tmem_st32(tmem + lane_off + P_TM_S + sb * 128, pk);
-        tmem_st32(tmem + lane_off + P_TM_S + sb * 128 + 32, pk + 32);
+        tmem_st64(tmem + lane_off + P_TM_S + sb * 128, pk);
         if (j > 0 && __any_sync(0xffffffffu, need)) {
           // Rescale O only when the row maximum grew by more than 2^8, once P*V
           // of the previous tile has completed.
@@ -1043,8 +1042,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
           }
           fence_async_smem();
         }
-        tmem_st32(tmem + lane_off + P_TM_S + sb * 128, pk);
-        tmem_st32(tmem + lane_off + P_TM_S + sb * 128 + 32, pk + 32);
+        tmem_st64(tmem + lane_off + P_TM_S + sb * 128, pk);
         if (j > 0 && __any_sync(0xffffffffu, need)) {
           // Rescale O only when the row maximum grew by more than 2^8, once P*V
           // of the previous tile has completed.
