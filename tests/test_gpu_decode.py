@@ -114,6 +114,49 @@ def test_decode_page128_tiles(parts):
     _compare(out, lse, oracle_decode(inp, heads=[0, 1, 63, 64, 127]))
 
 
+def test_decode_replays_in_a_cuda_graph():
+    """The four launches of a decode call (programmatic dependent launches)
+    captured in a CUDA graph: two replays give the eager call's output and LSE
+    bit for bit."""
+    w = _decode_workload(3, 16, [1, 2, 1], [300, 1000, 77])
+    inp = make_inputs(w, with_w_uk=True)
+    ref_out, ref_lse = run_decode(inp)
+    B, H, T = inp["B"], w.H, inp["T_q"]
+    max_new = int(inp["new_lens"].max())
+    max_seq = int((inp["new_lens"] + inp["cache_lens"]).max())
+    nparts = mla.mla_decode_partitions(B, H, max_new, max_seq)
+    nbytes = mla.mla_decode_workspace_bytes(H, T, nparts)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    out = torch.full((T, H, 128), float("nan"), dtype=torch.bfloat16, device=DEV)
+    lse = torch.full((T, H), float("nan"), dtype=torch.float32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    d = {k: inp[k].to(DEV) for k in ("q", "input_row_offsets", "cache_lengths", "kv_cache", "page_table",
+                                     "w_uk", "w_uv")}
+
+    def call():
+        mla.check(mla.mla_decode(out, lse, d["q"], d["input_row_offsets"], d["cache_lengths"], d["kv_cache"],
+                                 d["page_table"], inp["num_pages"], inp["page_size"], inp["max_pages"],
+                                 d["w_uk"], d["w_uv"], B, H, T, max_new, max_seq, 0, inp["scale"],
+                                 workspace=ws, workspace_bytes=nbytes, d_status=st))
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    for _ in range(2):
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0, mla.status_string(int(st.item()))
+        assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+        assert torch.equal(lse, ref_lse)
+
+
 def test_decode_small_heads_many_tokens():
     """16 heads: one 128-row tile holds 8 tokens of a sequence; a sequence of
     20 new tokens spans three tiles, each with its own causal limit."""

@@ -907,6 +907,49 @@ def run_fused(inp, S=None, max_chunks=None, lse=True):
     return out, lse_t
 
 
+@pytest.mark.parametrize("name,heads", [("tiny_ragged", 4), ("ragged_chunked_cache", 4)])
+def test_fused_call_replays_in_a_cuda_graph(name, heads, bf16_kernel):
+    """The fused call (the plan, then per chunk the gather, projection and
+    attention, every kernel a programmatic dependent launch) captured in a CUDA
+    graph: two replays give the eager call's output and LSE bit for bit."""
+    w = scaled(WORKLOADS[name], H=heads)
+    inp = make_inputs(w)
+    ref_out, ref_lse = run_fused(inp)
+    S, mc, B, H, T = w.buffer_token_size, w.max_chunks, inp["B"], w.H, inp["T_q"]
+    dt = _dt(w)
+    dev_in = {k: inp[k].to(DEV) for k in ("q", "input_row_offsets", "cache_lengths", "kv_cache",
+                                           "page_table", "w_k", "w_uv")}
+    out = torch.full((T, H, 128), float("nan"), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(T, H, dtype=torch.float32, device=DEV)
+    nbytes = mla.mla_prefill_workspace_bytes(B, H, T, mc, S, dt)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+
+    def call():
+        mla.check(mla.mla_prefill(out, lse, dev_in["q"], dev_in["input_row_offsets"],
+                                  dev_in["cache_lengths"], dev_in["kv_cache"], dev_in["page_table"],
+                                  inp["num_pages"], inp["page_size"], inp["max_pages"], dev_in["w_k"],
+                                  dev_in["w_uv"], B, H, T, inp["max_prompt_len"], S, mc, inp["scale"],
+                                  inp["q_scale"], inp["ckv_scale"], inp["w_scale"], dt, ws, nbytes, st))
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call()   # warm-up outside the capture (first-use set-up of the kernels)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    for _ in range(2):
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert st.item() == 0, mla.status_string(int(st.item()))
+        assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+        assert torch.equal(lse, ref_lse)
+
+
 def oracle_fused(inp, S=None, max_chunks=None, heads=None, rows=None):
     w = inp["workload"]
     c = {k: O.codes(inp[k]) for k in ("q", "kv_cache", "page_table", "w_k", "w_uv",
