@@ -928,20 +928,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(D_THREADS, 1)
 // row, 4 latent columns a thread).  The sequence of a row is found once and
 // then followed as the token advances; four partitions' partial rows are
 // requested before any is used, and five CTAs fit on an SM.
-__global__ void __launch_bounds__(256, 5) decode_merge_kernel(const DecodeParams p, __nv_bfloat16* __restrict__ o_lat,
+__global__ void __launch_bounds__(256, 4) decode_merge_kernel(const DecodeParams p, __nv_bfloat16* __restrict__ o_lat,
                                                            float* __restrict__ lse_out,
                                                            const float* __restrict__ sink) {
   pdl_enter();
   if (timed_out_before(p.status)) return;
   constexpr int KU = 4;                        // partitions loaded together
-  const int sub = threadIdx.x >> 7;            // row within the CTA's pair of rows
-  const int c = (threadIdx.x & 127) * 4;       // first latent column
-  const long long per = ((p.R + gridDim.x - 1) / gridDim.x + 1) / 2 * 2;
+  constexpr int RPP = 4;                       // rows per pass of the CTA (64 threads a row)
+  const int sub = threadIdx.x >> 6;            // row within the CTA's group of rows
+  const int c = (threadIdx.x & 63) * 8;        // first latent column (16 bytes of bf16)
+  const long long per = ((p.R + gridDim.x - 1) / gridDim.x + RPP - 1) / RPP * RPP;
   const long long r_begin = static_cast<long long>(blockIdx.x) * per;
   const long long r_end = min(static_cast<long long>(p.R), r_begin + per);
   int b = -1;
   uint32_t qa = 0, qe = 0;
-  for (long long grow = r_begin + sub; grow < r_end; grow += 2) {
+  for (long long grow = r_begin + sub; grow < r_end; grow += RPP) {
     const int t = static_cast<int>(grow / p.H);
     if (b < 0 || static_cast<uint32_t>(t) >= qe || static_cast<uint32_t>(t) < qa) {
       int lo = 0, hi_b = p.B;                  // largest b with iro[b] <= t
@@ -955,7 +956,7 @@ __global__ void __launch_bounds__(256, 5) decode_merge_kernel(const DecodeParams
     }
     if (!(qa <= static_cast<uint32_t>(t) && static_cast<uint32_t>(t) < qe)) {
       // A token outside every sequence: zeros, so the projection reads no garbage.
-      *reinterpret_cast<uint2*>(o_lat + grow * 512 + c) = make_uint2(0u, 0u);
+      *reinterpret_cast<uint4*>(o_lat + grow * 512 + c) = make_uint4(0u, 0u, 0u, 0u);
       if (lse_out != nullptr && c == 0) lse_out[grow] = kNegInfD;
       b = -1;
       continue;
@@ -971,22 +972,18 @@ __global__ void __launch_bounds__(256, 5) decode_merge_kernel(const DecodeParams
     // One pass: each group of KU partitions is loaded whole, then merged into
     // the running (max, sum, O) by LSE.
     float mx = kNegInfD;
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     float tot = 0.f;
     for (int k0 = 0; k0 < used; k0 += KU) {
-      float4 v[KU];
+      uint4 raw[KU];
       float lk[KU];
 #pragma unroll
       for (int i = 0; i < KU; ++i) {
         const int k = k0 + i;
         const long long at = static_cast<long long>(k) * p.R + grow;
         lk[i] = k < used ? __ldg(p.lse_part + at) : kNegInfD;
-        if (k < used) {
-          const uint2 raw = __ldg(reinterpret_cast<const uint2*>(p.o_part + at * 512 + c));
-          v[i] = make_float4(bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y));
-        } else {
-          v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+        raw[i] = k < used ? __ldg(reinterpret_cast<const uint4*>(p.o_part + at * 512 + c))
+                          : make_uint4(0u, 0u, 0u, 0u);
       }
       float cm = lk[0];
 #pragma unroll
@@ -995,12 +992,18 @@ __global__ void __launch_bounds__(256, 5) decode_merge_kernel(const DecodeParams
       if (nm == kNegInfD) continue;
       const float r = mx == kNegInfD ? 0.f : __expf(mx - nm);
       tot *= r;
-      o.x *= r; o.y *= r; o.z *= r; o.w *= r;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) o[j] *= r;
 #pragma unroll
       for (int i = 0; i < KU; ++i) {
         const float w = lk[i] == kNegInfD ? 0.f : __expf(lk[i] - nm);
         tot += w;
-        o.x += w * v[i].x; o.y += w * v[i].y; o.z += w * v[i].z; o.w += w * v[i].w;
+        const uint32_t u[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          o[2 * j] += w * bf16_lo(u[j]);
+          o[2 * j + 1] += w * bf16_hi(u[j]);
+        }
       }
       mx = nm;
     }
@@ -1015,10 +1018,9 @@ __global__ void __launch_bounds__(256, 5) decode_merge_kernel(const DecodeParams
       w *= lse == kNegInfD ? 0.f : __expf(lse - lse2);
       lse = lse2;
     }
-    uint2 pk;
-    pk.x = pack_bf16(o.x * w, o.y * w);
-    pk.y = pack_bf16(o.z * w, o.w * w);
-    *reinterpret_cast<uint2*>(o_lat + grow * 512 + c) = pk;
+    *reinterpret_cast<uint4*>(o_lat + grow * 512 + c) =
+        make_uint4(pack_bf16(o[0] * w, o[1] * w), pack_bf16(o[2] * w, o[3] * w), pack_bf16(o[4] * w, o[5] * w),
+                   pack_bf16(o[6] * w, o[7] * w));
     if (lse_out != nullptr && c == 0) lse_out[grow] = lse;
   }
 }
@@ -1173,7 +1175,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   }
 
   // 3. Merge the partitions (and the sink) into the bf16 latent result.
-  const long long blocks = std::min<long long>((R + 1) / 2, 8ll * sm_count());
+  const long long blocks = std::min<long long>((R + 3) / 4, 4ll * sm_count());
   if ((e = launch_pdl(decode_merge_kernel, dim3(static_cast<unsigned>(std::max(1ll, blocks))), dim3(256), 0, stream,
                       p, o_lat, a.lse, a.sink)) != cudaSuccess)
     return e;
