@@ -921,13 +921,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(D_THREADS, 1)
 }
 
 // ============================================================ partition merge
-// One row (token, head) per 128 threads, 4 latent columns a thread: merge the
-// partitions' (O, LSE) by LSE, add the attention sink (a logit with no value)
-// to the denominator when given, and round the latent result to bf16.
-// Each CTA merges a contiguous range of rows, two at a time (128 threads a
-// row, 4 latent columns a thread).  The sequence of a row is found once and
-// then followed as the token advances; four partitions' partial rows are
-// requested before any is used, and five CTAs fit on an SM.
+// One row (token, head) per 64 threads, 8 latent columns (one 16-byte load) a
+// thread: merge the partitions' (O, LSE) by LSE, add the attention sink (a
+// logit with no value) to the denominator when given, and round the latent
+// result to bf16.  Each CTA merges a contiguous range of rows, four at a time.
+// The sequence of a row is found once and then followed as the token
+// advances; four partitions' partial rows are requested before any is used,
+// and the grid is one wave of four CTAs per SM.
 __global__ void __launch_bounds__(256, 4) decode_merge_kernel(const DecodeParams p, __nv_bfloat16* __restrict__ o_lat,
                                                            float* __restrict__ lse_out,
                                                            const float* __restrict__ sink) {
