@@ -166,6 +166,15 @@ def test_decode_small_heads_many_tokens():
     _compare(out, lse, oracle_decode(inp))
 
 
+def test_decode_one_head():
+    """One head: a 128-row tile holds 128 tokens of a sequence, so a sequence
+    of 150 new tokens spans two tiles with different causal limits."""
+    w = _decode_workload(2, 1, (150, 2), (300, 1000))
+    inp = make_inputs(w, with_w_uk=True)
+    out, lse = run_decode(inp, 3)
+    _compare(out, lse, oracle_decode(inp))
+
+
 def test_decode_partition_count_invariance():
     w = _decode_workload(3, 8, (2, 1, 1), (700, 2000, 1))
     inp = make_inputs(w, with_w_uk=True)

@@ -988,6 +988,16 @@ def test_fused_tiny_ragged_all_rows(bf16_kernel):
     _compare(out, oracle_fused(inp), "bf16", lse)
 
 
+@pytest.mark.parametrize("H", [1, 2])
+def test_fused_one_and_two_heads(H, bf16_kernel):
+    """One or two heads: a projection tile of 256 columns holds a single
+    head's K (and a V tile the same head's V), and a head group is the whole
+    head count; every row of the multi-chunk tiny workload is checked."""
+    inp = make_inputs(scaled(WORKLOADS["tiny_ragged"], H=H))
+    out, lse = run_fused(inp)
+    _compare(out, oracle_fused(inp), "bf16", lse)
+
+
 @pytest.mark.parametrize("S", [7, 64, 200])
 def test_fused_buffer_size_invariance(S, bf16_kernel):
     """Different buffer sizes cut the context differently; the result is the same."""
