@@ -672,13 +672,14 @@ def test_attention_stage_multi_chunk(bf16_kernel):
     _attention_stage(WORKLOADS["tiny_ragged"])
 
 
-def test_attention_strongly_negative_scores(bf16_kernel):
-    """Every score of every row near -150 (about -210 in log2 units, far below
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
+def test_attention_strongly_negative_scores(dtype):
+    """Every score of every row near -140 (about -200 in log2 units, far below
     the fp32 exponent range once shifted by anything but the row's own
     maximum): the output is right only if each tile's maximum is taken over
     exactly its own scores.  q_nope = 4, k_nope = -4 plus a seeded multiple of
-    1/32 (exact in bf16), rope parts zero, two sequences with two and one key
-    tiles."""
+    1/4 (exact in bf16 and e4m3), rope parts zero, two sequences with two and
+    one key tiles."""
     rng = np.random.default_rng(5)
     new, cache = np.array([150, 60]), np.array([0, 40])
     B, H, S = 2, 2, 256
@@ -687,24 +688,28 @@ def test_attention_strongly_negative_scores(bf16_kernel):
     plan = O.prefill_plan(iro, cache, S, 1)
     g = gpu_plan(iro, cache, S, 1)
     tabs = [torch.as_tensor(x.astype(np.int32)).to(DEV) for x in g[:3]]
-    q = torch.zeros(T, H, 192, dtype=torch.bfloat16)
+    store = torch.bfloat16 if dtype == "bf16" else torch.float8_e4m3fn
+    q = torch.zeros(T, H, 192, dtype=torch.float32)
     q[:, :, :128] = 4.0
-    kn = (-4.0 + rng.integers(0, 3, size=(S, H, 128)) / 32.0).astype(np.float32)
-    kn = torch.as_tensor(kn).to(torch.bfloat16)
-    kr = torch.zeros(S, 64, dtype=torch.bfloat16)
-    vv = torch.as_tensor(rng.standard_normal((S, H, 128)).astype(np.float32)).to(torch.bfloat16)
+    q = q.to(store)
+    kn = torch.as_tensor((-4.0 + rng.integers(0, 3, size=(S, H, 128)) / 4.0).astype(np.float32)).to(store)
+    kr = torch.zeros(S, 64, dtype=torch.float32).to(store)
+    vv = torch.as_tensor(rng.standard_normal((S, H, 128)).astype(np.float32)).to(store)
+    if dtype == "e4m3":
+        vv = vv.to(torch.float16)   # V of the e4m3 path: float16 holding e4m3 values
     scale = 1.0 / math.sqrt(192.0)
     out = torch.full((T, H, 128), float("nan"), dtype=torch.bfloat16, device=DEV)
     lse = torch.empty(T, H, dtype=torch.float32, device=DEV)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
     mla.check(mla.mla_prefill_attention(out, lse, None, None, q.to(DEV), kn.to(DEV), vv.to(DEV), kr.to(DEV),
-                                        _i32(iro).to(DEV), _i32(cache).to(DEV), *tabs, 0, 1, B, H,
-                                        int(new.max()), T, S, scale, d_status=st))
+                                        _i32(iro), _i32(cache), *tabs, 0, 1, B, H, int(new.max()), T, S, scale,
+                                        dtype=mla.MLA_BF16 if dtype == "bf16" else mla.MLA_E4M3, d_status=st))
     torch.cuda.synchronize()
     assert st.item() == 0
-    dec = lambda t: O.decode(O.codes(t), "bf16")
-    ref = O.attention_over_chunks(dec(q), lambda ch: (dec(kn), dec(kr), dec(vv)), plan, iro, cache, scale)
-    _compare(out, ref, "bf16", lse)
+    dec = lambda t: O.decode(O.codes(t), dtype)
+    v64 = vv.double().numpy() if dtype == "e4m3" else dec(vv)
+    ref = O.attention_over_chunks(dec(q), lambda ch: (dec(kn), dec(kr), v64), plan, iro, cache, scale)
+    _compare(out, ref, dtype, lse)
 
 
 def test_attention_offsets_past_total_q_tokens():
