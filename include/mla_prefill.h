@@ -478,7 +478,7 @@ mla_status_t mla_prefill(void* out, float* lse, const void* q, const uint32_t* i
  * Partitions per sequence the library uses for mla_decode when num_partitions
  * is 0 (size the workspace with it).  It cuts every sequence's keys into
  * pieces of about the same size -- between 256 and 2048 keys, chosen from the
- * batch's sizes for about two waves of work on the GPU's SM pairs -- so that
+ * batch's sizes for about one item per SM pair of the GPU -- so that
  * short and long sequences make items of equal cost; this returns the most
  * pieces a sequence can get.  max_keys: max_seq_len for dense decode (the
  * longest context, new tokens included), the list stride for sparse decode.

@@ -1085,14 +1085,15 @@ DecodeLayout decode_layout(int T, int H, int parts) {
 }
 
 DecodePartitioning decode_partitioning(int B, int H, int max_new, int max_keys) {
-  // Items of about the same size, enough of them for about two waves of SM
-  // pairs (each pair gets an equal share of the items, so more waves buy no
-  // balance, only more partial results to merge), each between 256 and 2048
-  // keys; at most kDecodeMaxParts a sequence.
+  // Items of about the same size, about one per SM pair (each pair gets an
+  // equal share of the items, so more items buy no balance, only more partial
+  // results to merge: two per pair measured 3 % slower on the top-2048 sparse
+  // decode), each between 256 and 2048 keys; at most kDecodeMaxParts a
+  // sequence.
   const long long pairs = std::max(1, sm_count() / 2);
   const long long m_tiles = (static_cast<long long>(std::max(1, max_new)) * H + 127) / 128;
   const long long keys = std::max(1, max_keys);
-  long long pk = static_cast<long long>(B) * m_tiles * keys / (2 * pairs);
+  long long pk = static_cast<long long>(B) * m_tiles * keys / pairs;
   pk = std::min<long long>(2048, std::max<long long>(256, (pk + 63) / 64 * 64));
   DecodePartitioning d;
   d.part_keys = static_cast<int>(pk);
