@@ -37,7 +37,7 @@ sys.path.insert(0, ROOT)
 # DRAM bytes (read + write) per attention launch from one ncu capture of the
 # current kernel (dram__bytes_read.sum + dram__bytes_write.sum), keyed by
 # (workload, kernel); absent where the kernel has changed since its capture.
-ATTN_DRAM_BYTES_PER_LAUNCH = {("v3_prefill", "attn_pair_kernel"): 481_545_216 + 118_875_136}
+ATTN_DRAM_BYTES_PER_LAUNCH = {("v3_prefill", "attn_pair_kernel"): 474_251_776 + 118_507_520}
 # CUDA kernel name of each attention variant the library reports.
 ATTN_KERNEL_NAMES = {"pair": "attn_pair_kernel", "e4m3": "attn_pair_kernel_e4m3"}
 
